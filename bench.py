@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""Benchmark of the speculative-KV-coding hot path on GB300.
+
+One step = the whole path over one synthetic cache: encode (rank, model CDF,
+interleaved rANS, size scan, compaction into the container), decode (search,
+rANS update, stream reads, output) and the ideal-bits reduction.  The default
+workload is the Qwen3-0.6B-shaped bf16 cache (28 layers x {K,V} x 8 heads x
+4096 tokens x 128 = 234.9M scalars).  ``value`` is raw-KV bytes per second of
+the whole step (2 bytes per bf16 scalar), inputs resident in HBM.
+
+``--impl reference`` times the oracle (plain single-threaded C) on the host
+cores on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "raw-KV encode & decode GB/s on 1 GB300 (% of roofline); bits/scalar vs ideal"
+DEFAULT_WORKLOAD = "qwen3-0.6b-bf16"
+# launches of our kernels per step: encode (prep, encode, 2 scans, compact),
+# decode (prep, header check, decode), ideal bits (prep, bits, final sum)
+LAUNCHES_PER_STEP = 11
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Maximum of a host float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def rank_seed(rank: int) -> int:
+    """Weak scaling: every rank codes its own cache, drawn with its own seed."""
+    return rank
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def load_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(kernel, {}).get(workload)
+    if not ent:
+        return None
+    import lossless_kv_cache_fixed_gb300.build as B
+    if ent.get("source_digest") != B.source_digest():
+        return None
+    return ent.get("bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------
+# oracle timing (cpu_baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_sample_step(O, m, kv, mu, chunks):
+    """Encode, decode and ideal bits of the listed chunks, single-threaded."""
+    s = m.s
+    D, T, Tb = s.D, s.T, s.Tb
+    ntb = (T + Tb - 1) // Tb
+    dec = _scratch_for(kv)
+    scalars = 0
+    for c in chunks:
+        words = O._encode_chunk_raw(m, kv, mu, c)
+        rc = O.decode_chunk(m, words, mu, c, dec)
+        if rc != 0:
+            raise RuntimeError("oracle decode failed rc=%d" % rc)
+        row, tb = divmod(c, ntb)
+        t0 = tb * Tb
+        tn = min(Tb, T - t0)
+        base = row * T * D + t0 * D
+        O.ideal_bits(m, kv, mu, base, base + tn * D)
+        scalars += tn * D
+    return scalars
+
+
+_SCRATCH = {}
+
+
+def _scratch_for(kv):
+    key = (kv.dtype.str, kv.size)
+    if key not in _SCRATCH:
+        import numpy as np
+        _SCRATCH[key] = np.empty_like(kv)
+    return _SCRATCH[key]
+
+
+def oracle_setup(workload_name, seed, device):
+    import oracle as O
+    import synth
+    O.build()
+    w = synth.make(workload_name, device=device, seed=seed)
+    kv, mu, sigma, counts = synth.to_numpy(w)
+    s = w.spec
+    m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sigma, counts=counts)
+    return O, w, m, kv.reshape(-1), mu.reshape(-1)
+
+
+def time_oracle(O, m, kv, mu, nchunks_total, budget_chunks):
+    """Time the oracle on an evenly spread, deterministic sample of chunks."""
+    step = max(1, nchunks_total // budget_chunks)
+    chunks = list(range(0, nchunks_total, step))[:budget_chunks]
+    t0 = time.perf_counter()
+    scalars = oracle_sample_step(O, m, kv, mu, chunks)
+    dt = time.perf_counter() - t0
+    return scalars, dt, chunks
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import synth
+    import lossless_kv_cache_fixed_gb300 as P
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    _init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    P.build()
+
+    w = synth.make(args.workload, device=dev, seed=rank_seed(rank))
+    s = w.spec
+    bps = 2 if s.dtype == synth.BF16 else 1
+    ecdf = phat = None
+    if s.dtype == synth.BF16:
+        E, ph = P.skv_build_ecdf(w.counts.cpu().numpy().astype(np.uint64))
+        ecdf = torch.from_numpy(E.view(np.int32)).to(dev)
+        phat = torch.from_numpy(ph).to(dev)
+    codec = P.Codec(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, w.sigma.to(dev), ecdf, phat)
+    kv = (w.kv.view(torch.int16) if s.dtype == synth.BF16 else w.kv).reshape(-1)
+    mu = w.mu.view(torch.int16).reshape(-1)
+    n = s.n
+    raw = n * bps
+    out = torch.empty(codec.max_bytes, dtype=torch.uint8, device=dev)
+    dec = torch.empty_like(kv)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        _, nb = codec.encode(kv, mu, out=out)
+        if ev:
+            ev[1].record(stream)
+        codec.decode(out, nb, mu, out=dec)
+        if ev:
+            ev[2].record(stream)
+        bits = codec.ideal_bits(kv, mu)
+        if ev:
+            ev[3].record(stream)
+        return nb, bits
+
+    for _ in range(args.warmup):
+        nb, bits = step()
+    torch.cuda.synchronize()
+    if not torch.equal(dec, kv):
+        raise RuntimeError("decode mismatch in warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            nb, bits = step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(stop)
+    t_enc = [e[0].elapsed_time(e[1]) for e in evs]
+    t_dec = [e[1].elapsed_time(e[2]) for e in evs]
+    t_bits = [e[2].elapsed_time(e[3]) for e in evs]
+    ms = max_over_ranks(ms, world, dev)
+    ms_step = ms / args.steps
+    value = world * raw / (ms_step * 1e-3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers ----
+    kv_h = kv.cpu().pin_memory()
+    mu_h = mu.cpu().pin_memory()
+    box_h = torch.empty(codec.max_bytes, dtype=torch.uint8).pin_memory()
+    kv_back = torch.empty_like(kv_h).pin_memory()
+    kv_d = torch.empty_like(kv)
+    mu_d = torch.empty_like(mu)
+    box_d = torch.empty_like(out)
+
+    def e2e_step():
+        kv_d.copy_(kv_h, non_blocking=True)
+        mu_d.copy_(mu_h, non_blocking=True)
+        _, nb2 = codec.encode(kv_d, mu_d, out=box_d)
+        box_h[:nb2].copy_(box_d[:nb2], non_blocking=True)
+        box_d[:nb2].copy_(box_h[:nb2], non_blocking=True)
+        codec.decode(box_d, nb2, mu_d, out=kv_d)
+        kv_back.copy_(kv_d, non_blocking=True)
+        tot = codec.ideal_bits(kv_d, mu_d)
+        torch.cuda.synchronize()
+        return nb2, tot
+
+    for _ in range(max(1, args.warmup)):
+        nb2, _ = e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        nb2, _ = e2e_step()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world, dev)
+    if not torch.equal(kv_back, kv_h):
+        raise RuntimeError("end-to-end round trip mismatch")
+    h2d = raw + 2 * n + nb2
+    d2h = nb2 + raw + 8 + 3 * 32  # container, cache, total, three status reads
+
+    if rank != 0:
+        return None
+
+    # ---- roofline of the dominant kernel ----
+    med = {"encode": statistics.median(t_enc), "decode": statistics.median(t_dec),
+           "ideal_bits": statistics.median(t_bits)}
+    top = max(med, key=med.get)
+    cb = nb / n  # container bytes per scalar
+    alg = {"encode": bps + 2 + cb, "decode": cb + 2 + bps, "ideal_bits": bps + 2}
+    peak, peak_kind = measured_peaks()
+    achieved = alg[top] * n / (med[top] * 1e-3) / 1e9
+    kname = {"encode": "k_encode", "decode": "k_decode", "ideal_bits": "k_ideal"}[top]
+    roof = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": load_traffic(kname, args.workload),
+            "algorithmic_bytes_per_scalar": round(alg[top], 4),
+            "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+            else "fallback 6.8 TB/s"}
+
+    # ---- oracle on the host cores, bounded sample ----
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle as O
+        kvn, mun, sig, cnt = synth.to_numpy(w)
+        m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sig, counts=cnt)
+        nch = m.num_chunks()
+        sc, dt, chunks = time_oracle(O, m, kvn.reshape(-1), mun.reshape(-1), nch,
+                                     args.cpu_sample_chunks)
+        cpu = {"value": round(sc * bps / dt / 1e9, 6), "unit": "GB/s", "cores": 1,
+               "kind": "oracle",
+               "sample": "%d of %d chunks (%d scalars, every %d-th chunk): encode + decode + "
+                         "ideal bits, single-threaded C, %.1f s" % (len(chunks), nch, sc,
+                                                                      max(1, nch // args.cpu_sample_chunks), dt)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "symbols": "bf16" if bps == 2 else "e4m3",
+                   "layers": s.L, "heads": s.H, "tokens": s.T, "head_dim": s.D,
+                   "scalars_per_gpu": n, "token_block": s.Tb, "lanes": s.G,
+                   "parallelism": "dp%d (independent caches)" % world,
+                   "l2": "inputs larger than L2: %.0f MB KV + %.0f MB mu per step" % (
+                       raw / 1e6, 2 * n / 1e6)},
+        "encode_gbs": round(raw / (med["encode"] * 1e-3) / 1e9, 2),
+        "decode_gbs": round(raw / (med["decode"] * 1e-3) / 1e9, 2),
+        "ideal_bits_gbs": round(raw / (med["ideal_bits"] * 1e-3) / 1e9, 2),
+        "bits_per_scalar": round(8.0 * nb / n, 5),
+        "ideal_bits_per_scalar": round(bits / n, 5),
+        "overhead_pct": round(100.0 * (8.0 * nb / bits - 1.0), 3),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * raw / e2e_s / 1e9, 3), "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clk.summary(),
+    }
+    return line
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on the host cores of this machine."""
+    rank, world, local = _dist()
+    if rank != 0:
+        return None
+    import torch
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    O, w, m, kv, mu = oracle_setup(args.workload, 0, device)
+    s = w.spec
+    bps = 2 if s.dtype == 0 else 1
+    nch = m.num_chunks()
+    per_step = max(1, args.ref_chunks_per_step)
+    stride = max(1, nch // (per_step * max(1, args.steps + args.warmup)))
+    order = list(range(0, nch, stride))
+    k = 0
+
+    def step():
+        nonlocal k
+        chunks = [order[(k + i) % len(order)] for i in range(per_step)]
+        k += per_step
+        return oracle_sample_step(O, m, kv, mu, chunks)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    sc = 0
+    for _ in range(args.steps):
+        sc += step()
+    dt = time.perf_counter() - t0
+    v = sc * bps / dt / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * dt / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+        "config": {"workload": args.workload, "scalars_per_gpu": s.n, "token_block": s.Tb,
+                   "lanes": s.G},
+        "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d chunks per step of %d scalars each (every %d-th chunk), "
+                                   "encode + decode + ideal bits" % (per_step, s.Tb * s.D, stride)},
+        "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["skv", "reference"], default="skv")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--cpu-sample-chunks", type=int, default=384)
+    ap.add_argument("--ref-chunks-per-step", type=int, default=24)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "skv":
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    rank, world, _ = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

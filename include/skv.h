@@ -1,0 +1,178 @@
+/*
+ * skv.h -- C ABI of the GB300 speculative-KV-coding library (libskv.so).
+ *
+ * What it computes.  Page "推测式 KV 编码无损压缩 KV 缓存最高可达约 4 倍"
+ * (Speculative KV coding, lpnh.cn/news/878951):
+ *   - section "什么能预测 KV 缓存" (what can predict the KV cache): an
+ *     arithmetic coder turns (KV_full, mu, sigma) into a bitstream on the
+ *     encoding side and (bits, mu, sigma) back into KV_full on the decoding side;
+ *   - section "q 应是什么样的" (what q should look like): each scalar is coded
+ *     under a Gaussian centred on its prediction mu with calibrated sigma^2;
+ *   - section "早期结果" (early results): bf16 caches use the mixture
+ *     q = 0.95 N(mu, sigma^2) + 0.03 N(mu, (3 sigma)^2) + 0.02 p-hat_bf16,
+ *     with sigma per (kv, head, channel) and p-hat the empirical bf16 symbol
+ *     distribution measured on calibration data;
+ *   - section "原生 FP8 KV 缓存" (native FP8 cache): e4m3 caches use the
+ *     bin-integrated N(mu, sigma^2);
+ *   - section "下一步计划" (next steps): both ends must derive bit-identical
+ *     probabilities, so the model is evaluated in integer fixed point.
+ *   - section "KV 缓存并非真正随机" (the cache is not random): the coded size
+ *     is the cross-entropy -sum log2 q(x); skv_ideal_bits reports it.
+ *
+ * Format (spec v1; the pages fix no coder details).  Every symbol r (its rank
+ * in value order) gets cum(r) = floor((2^M - |S|) F(lo(r))) + r, M = 28 for
+ * bf16 (|S| = 65282 non-NaN patterns) and 16 for e4m3 (|S| = 254), where lo(r)
+ * is the lower edge of the symbol's round-to-nearest bin and F the model CDF
+ * built from an integer-interpolated Phi table and the integer p-hat prefix
+ * table.  The coder is interleaved rANS with a 64-bit state, L = 2^31 and
+ * 32-bit words.  A chunk is one (layer, kv, head, token block); scalar p of a
+ * chunk belongs to lane (p / 8) mod G.  The container is a 64-byte header,
+ * u64 offsets[num_chunks + 1] and the chunk payloads; see skv_encode.
+ *
+ * Conventions for every call below.
+ *   - Pointers are DEVICE pointers unless marked "host".  The caller owns every
+ *     buffer; no call allocates memory.
+ *   - Tensors are row-major [layers][2][heads][tokens][head_dim]: KV is bf16
+ *     bit patterns (uint16) or e4m3 codes (uint8); mu is always bf16.
+ *   - Work is issued on `stream` (a cudaStream_t; NULL = legacy default).
+ *     Calls that return a status or a host value synchronize that stream.
+ *   - Return value: SKV_OK (0) or a negative skv_status.  Kernel-side errors
+ *     (bad symbols, parameters or streams) are gathered in a device flag in
+ *     the workspace and reported at the end of the call; the library never
+ *     traps the GPU.
+ *   - The first call on a device uploads the model constants to that device
+ *     (a synchronous copy), so make one call before any stream capture.
+ *   - Calls on different streams must use different workspaces.
+ */
+#ifndef SKV_H
+#define SKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *skv_stream_t; /* cudaStream_t */
+
+typedef enum { SKV_BF16 = 0, SKV_E4M3 = 1 } skv_dtype;
+
+typedef enum {
+  SKV_OK = 0,
+  SKV_ERR_ARG = -1,       /* bad shape, token block, lanes, or a NULL pointer */
+  SKV_ERR_CAPACITY = -2,  /* output buffer or workspace too small */
+  SKV_ERR_SYMBOL = -3,    /* a NaN bit pattern in the KV input */
+  SKV_ERR_PARAM = -4,     /* invalid sigma (not finite, < FLT_MIN, 3 sigma overflows),
+                             non-finite mu, or an ill-formed p-hat table */
+  SKV_ERR_CORRUPT = -5,   /* bad header, offsets, model fingerprint, stream overrun,
+                             or a lane that does not end in the initial state */
+  SKV_ERR_CUDA = -6       /* a CUDA runtime error */
+} skv_status;
+
+typedef enum { SKV_OP_ENCODE = 0, SKV_OP_DECODE = 1, SKV_OP_IDEAL_BITS = 2 } skv_op;
+
+/* Tensor shape.  kv must be 2 (keys and values); head_dim a multiple of 8. */
+typedef struct {
+  int32_t layers, kv, heads, tokens, head_dim;
+} skv_shape;
+
+/* Coding model and chunking.
+ *   dtype        SKV_BF16 or SKV_E4M3.
+ *   token_block  tokens per chunk (Tb >= 1); chunk = Tb * head_dim scalars.
+ *   lanes        rANS lanes per chunk, G in {1, 2, 4, 8, 16, 32}.
+ *   sigma        device, fp32 [layers][2][heads][head_dim]; per (layer, kv,
+ *                head, channel) standard deviation of the narrow component.
+ *   ecdf         device, bf16 only: u32 E_q[0..65282], E_q[r] =
+ *                floor(2^26 S[r] / S_tot), S[r] = sum over ranks j < r of
+ *                (count_j + 1); built by skv_build_ecdf.  Unused for e4m3.
+ *   phat         device, bf16 only: fp32 p-hat[0..65281] by rank, the
+ *                smoothed empirical probability (count + 1) / S_tot.  Read by
+ *                skv_ideal_bits only; NULL is allowed for encode and decode.
+ */
+typedef struct {
+  int32_t dtype;
+  int32_t token_block;
+  int32_t lanes;
+  int32_t reserved; /* must be 0 */
+  const float *sigma;
+  const uint32_t *ecdf;
+  const float *phat;
+} skv_params;
+
+/* Upper bound on the container size in bytes for this shape (worst case:
+ * every symbol costs one 32-bit word).  Returns 0 if the arguments are invalid. */
+size_t skv_max_encoded_bytes(const skv_params *params, const skv_shape *shape);
+
+/* Workspace bytes needed by `op` (an skv_op) for this shape; 0 if invalid.
+ * The encoder's workspace holds one word stack per chunk (about M/8 bytes per
+ * scalar), the chunk sizes and offsets, the per-channel reciprocals and the
+ * error flags; decode and ideal-bits need only small tables.  The workspace
+ * must be 256-byte aligned (cudaMalloc memory is). */
+size_t skv_workspace_bytes(const skv_params *params, const skv_shape *shape, int op);
+
+/* Encode a whole cache into one container.
+ *   kv, mu        device inputs as above.
+ *   out           device output, out_capacity bytes (skv_max_encoded_bytes is
+ *                 always enough).
+ *   out_bytes     host; receives the container size.
+ * Container v1 (little-endian): a 64-byte header {u32 magic "SKV1", u16 version
+ * 1, u8 dtype, u8 M, u32 layers, u32 2, u32 heads, u32 tokens, u32 head_dim,
+ * u32 token_block, u16 lanes, u8 8, u8 9, u16 8, u16 0, u64 num_chunks, u64
+ * payload_bytes, u64 model fingerprint of sigma (and E_q for bf16)}, then u64
+ * offsets[num_chunks + 1] (byte offsets from the payload start), then the
+ * payload: chunk c (index ((l*2 + kv)*heads + h)*ceil(tokens/Tb) + tb) is u32
+ * words in decoder order -- lane states (lo, hi) for lanes 0..G-1, then the
+ * renormalisation words.  Errors: SKV_ERR_ARG, SKV_ERR_CAPACITY (out or
+ * workspace too small; nothing useful is written), SKV_ERR_SYMBOL,
+ * SKV_ERR_PARAM, SKV_ERR_CUDA.  Synchronizes `stream`. */
+int skv_encode(const skv_params *params, const skv_shape *shape, const void *kv,
+               const uint16_t *mu, void *out, size_t out_capacity, size_t *out_bytes,
+               void *workspace, size_t workspace_bytes, skv_stream_t stream);
+
+/* Decode a container produced by skv_encode with the same params, shape and mu.
+ *   in, in_bytes  device container and its exact size.
+ *   kv_out        device output tensor (2 or 1 bytes per scalar).
+ * The header must match params and shape, and its model fingerprint must match
+ * sigma (and E_q); every offset, every stream read and every lane's final
+ * state are checked.  Errors: SKV_ERR_ARG, SKV_ERR_CAPACITY (workspace),
+ * SKV_ERR_PARAM, SKV_ERR_CORRUPT (kv_out is then unspecified), SKV_ERR_CUDA.
+ * Synchronizes `stream`. */
+int skv_decode(const skv_params *params, const skv_shape *shape, const void *in,
+               size_t in_bytes, const uint16_t *mu, void *kv_out, void *workspace,
+               size_t workspace_bytes, skv_stream_t stream);
+
+/* Ideal code length: the cross-entropy -log2 q(x) of every scalar under the
+ * continuous model (bin mass of the mixture, or of N(mu, sigma^2) for e4m3),
+ * evaluated in tail-safe fp32 and summed in fp64 in a fixed order.
+ *   per_scalar    device fp32 [N] output, or NULL.
+ *   total         host; receives the sum in bits.
+ * Requires params->phat for bf16.  Errors: SKV_ERR_ARG, SKV_ERR_CAPACITY
+ * (workspace), SKV_ERR_SYMBOL, SKV_ERR_PARAM, SKV_ERR_CUDA.  Synchronizes. */
+int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void *kv,
+                   const uint16_t *mu, float *per_scalar, double *total, void *workspace,
+                   size_t workspace_bytes, skv_stream_t stream);
+
+/* Host helper: p-hat tables from a calibration histogram.
+ *   counts   host, u64[65536], occurrences of each bf16 bit pattern (NaN
+ *            patterns are ignored).
+ *   ecdf     host output, u32[65283] (E_q, see skv_params).
+ *   phat     host output, fp32[65282] by rank, or NULL.
+ * Add-one smoothing over the 65282 non-NaN symbols.  Errors: SKV_ERR_ARG
+ * (NULL pointer, or a total count >= 2^37). */
+int skv_build_ecdf(const uint64_t *counts, uint32_t *ecdf, float *phat);
+
+/* Host helper: the Phi table of the model, u32[8193] with
+ * T[i] = RNE(2^26 Phi(-8 + i/512)), T[0] = 0, T[8192] = 2^26. */
+int skv_phi_table(uint32_t *table);
+
+/* Static description of a status code. */
+const char *skv_strerror(int status);
+
+/* Library format version (1). */
+int skv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SKV_H */

@@ -1,0 +1,208 @@
+"""Speculative KV coding on GB300 -- Python binding of libskv.so.
+
+The functions named ``skv_*`` mirror the C ABI in ``include/skv.h`` one to one
+and only marshal arguments (ctypes structs, raw device pointers, the current
+CUDA stream).  ``Codec`` is a convenience wrapper that owns the workspace and
+output buffers as torch tensors; every step of the coder runs in the CUDA
+kernels of ``csrc/``.  There is no fallback: if the library is missing, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+from .build import LIB, build  # noqa: F401
+
+SKV_BF16, SKV_E4M3 = 0, 1
+SKV_OP_ENCODE, SKV_OP_DECODE, SKV_OP_IDEAL_BITS = 0, 1, 2
+SKV_OK, SKV_ERR_ARG, SKV_ERR_CAPACITY, SKV_ERR_SYMBOL = 0, -1, -2, -3
+SKV_ERR_PARAM, SKV_ERR_CORRUPT, SKV_ERR_CUDA = -4, -5, -6
+NSYM = {SKV_BF16: 65282, SKV_E4M3: 254}
+
+EXPORTS = ("skv_max_encoded_bytes", "skv_workspace_bytes", "skv_encode", "skv_decode",
+           "skv_ideal_bits", "skv_build_ecdf", "skv_phi_table", "skv_strerror", "skv_version")
+
+
+class SkvParams(C.Structure):
+    _fields_ = [("dtype", C.c_int32), ("token_block", C.c_int32), ("lanes", C.c_int32),
+                ("reserved", C.c_int32), ("sigma", C.c_void_p), ("ecdf", C.c_void_p),
+                ("phat", C.c_void_p)]
+
+
+class SkvShape(C.Structure):
+    _fields_ = [("layers", C.c_int32), ("kv", C.c_int32), ("heads", C.c_int32),
+                ("tokens", C.c_int32), ("head_dim", C.c_int32)]
+
+
+class SkvError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__("%s: %s (%d)" % (what or "skv", skv_strerror(status), status))
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libskv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError("libskv.so is not built (%s); run __graft_entry__.build()" % LIB)
+        L = C.CDLL(LIB)
+        P, S = C.POINTER(SkvParams), C.POINTER(SkvShape)
+        vp, sz = C.c_void_p, C.c_size_t
+        sig = {
+            "skv_max_encoded_bytes": (sz, [P, S]),
+            "skv_workspace_bytes": (sz, [P, S, C.c_int]),
+            "skv_encode": (C.c_int, [P, S, vp, vp, vp, sz, C.POINTER(sz), vp, sz, vp]),
+            "skv_decode": (C.c_int, [P, S, vp, sz, vp, vp, vp, sz, vp]),
+            "skv_ideal_bits": (C.c_int, [P, S, vp, vp, vp, C.POINTER(C.c_double), vp, sz, vp]),
+            "skv_build_ecdf": (C.c_int, [vp, vp, vp]),
+            "skv_phi_table": (C.c_int, [vp]),
+            "skv_strerror": (C.c_char_p, [C.c_int]),
+            "skv_version": (C.c_int, []),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+# ---- one-to-one wrappers of the C ABI ----
+
+def skv_max_encoded_bytes(params: SkvParams, shape: SkvShape) -> int:
+    return int(lib().skv_max_encoded_bytes(C.byref(params), C.byref(shape)))
+
+
+def skv_workspace_bytes(params: SkvParams, shape: SkvShape, op: int) -> int:
+    return int(lib().skv_workspace_bytes(C.byref(params), C.byref(shape), op))
+
+
+def skv_encode(params, shape, kv_ptr, mu_ptr, out_ptr, out_capacity, ws_ptr, ws_bytes, stream):
+    """Returns (status, container bytes)."""
+    nb = C.c_size_t(0)
+    rc = lib().skv_encode(C.byref(params), C.byref(shape), kv_ptr, mu_ptr, out_ptr, out_capacity,
+                          C.byref(nb), ws_ptr, ws_bytes, stream)
+    return rc, nb.value
+
+
+def skv_decode(params, shape, in_ptr, in_bytes, mu_ptr, kv_out_ptr, ws_ptr, ws_bytes, stream):
+    return lib().skv_decode(C.byref(params), C.byref(shape), in_ptr, in_bytes, mu_ptr, kv_out_ptr,
+                            ws_ptr, ws_bytes, stream)
+
+
+def skv_ideal_bits(params, shape, kv_ptr, mu_ptr, per_scalar_ptr, ws_ptr, ws_bytes, stream):
+    """Returns (status, total bits)."""
+    tot = C.c_double(0)
+    rc = lib().skv_ideal_bits(C.byref(params), C.byref(shape), kv_ptr, mu_ptr, per_scalar_ptr,
+                              C.byref(tot), ws_ptr, ws_bytes, stream)
+    return rc, tot.value
+
+
+def skv_build_ecdf(counts):
+    """counts: numpy uint64[65536] by bf16 pattern -> (E_q uint32[65283], p-hat float32[65282])."""
+    import numpy as np
+    counts = np.ascontiguousarray(counts, dtype=np.uint64)
+    if counts.size != 65536:
+        raise ValueError("counts must have 65536 entries")
+    E = np.zeros(65283, dtype=np.uint32)
+    ph = np.zeros(65282, dtype=np.float32)
+    rc = lib().skv_build_ecdf(counts.ctypes.data, E.ctypes.data, ph.ctypes.data)
+    if rc:
+        raise SkvError(rc, "skv_build_ecdf")
+    return E, ph
+
+
+def skv_phi_table():
+    import numpy as np
+    T = np.zeros(8193, dtype=np.uint32)
+    rc = lib().skv_phi_table(T.ctypes.data)
+    if rc:
+        raise SkvError(rc, "skv_phi_table")
+    return T
+
+
+def skv_strerror(status: int) -> str:
+    return lib().skv_strerror(int(status)).decode()
+
+
+def skv_version() -> int:
+    return int(lib().skv_version())
+
+
+# ---- torch convenience wrapper (buffers only) ----
+
+def _stream_handle(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+class Codec:
+    """Owns device buffers for one (model, shape) and calls the C ABI.
+
+    sigma: float32 [L, 2, H, D] on the device; ecdf: int32/uint32 [65283]
+    (bf16); phat: float32 [65282] (bf16, ideal bits only).
+    """
+
+    def __init__(self, dtype, L, H, T, D, token_block, lanes, sigma, ecdf=None, phat=None):
+        import torch
+        self.dtype = dtype
+        self.sigma, self.ecdf, self.phat = sigma.contiguous(), ecdf, phat
+        self.params = SkvParams(dtype, token_block, lanes, 0, self.sigma.data_ptr(),
+                                ecdf.data_ptr() if ecdf is not None else None,
+                                phat.data_ptr() if phat is not None else None)
+        self.shape = SkvShape(L, 2, H, T, D)
+        self.n = L * 2 * H * T * D
+        self.device = sigma.device
+        self._ws = {}
+        self.max_bytes = skv_max_encoded_bytes(self.params, self.shape)
+        if self.max_bytes == 0:
+            raise SkvError(SKV_ERR_ARG, "Codec")
+        self.torch = torch
+
+    def workspace(self, op):
+        if op not in self._ws:
+            nb = skv_workspace_bytes(self.params, self.shape, op)
+            self._ws[op] = self.torch.empty(max(nb, 256), dtype=self.torch.uint8,
+                                            device=self.device)
+        return self._ws[op]
+
+    def kv_dtype(self):
+        return self.torch.int16 if self.dtype == SKV_BF16 else self.torch.uint8
+
+    def encode(self, kv, mu, out=None, stream=None):
+        """Returns (container uint8 tensor, size in bytes)."""
+        if out is None:
+            out = self.torch.empty(self.max_bytes, dtype=self.torch.uint8, device=self.device)
+        ws = self.workspace(SKV_OP_ENCODE)
+        rc, nb = skv_encode(self.params, self.shape, kv.data_ptr(), mu.data_ptr(), out.data_ptr(),
+                            out.numel(), ws.data_ptr(), ws.numel(), _stream_handle(stream))
+        if rc:
+            raise SkvError(rc, "skv_encode")
+        return out, nb
+
+    def decode(self, buf, nbytes, mu, out=None, stream=None):
+        if out is None:
+            out = self.torch.empty(self.n, dtype=self.kv_dtype(), device=self.device)
+        ws = self.workspace(SKV_OP_DECODE)
+        rc = skv_decode(self.params, self.shape, buf.data_ptr(), nbytes, mu.data_ptr(),
+                        out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream))
+        if rc:
+            raise SkvError(rc, "skv_decode")
+        return out
+
+    def ideal_bits(self, kv, mu, per_scalar=False, stream=None):
+        ws = self.workspace(SKV_OP_IDEAL_BITS)
+        ps = None
+        if per_scalar:
+            ps = self.torch.empty(self.n, dtype=self.torch.float32, device=self.device)
+        rc, tot = skv_ideal_bits(self.params, self.shape, kv.data_ptr(), mu.data_ptr(),
+                                 ps.data_ptr() if ps is not None else None, ws.data_ptr(),
+                                 ws.numel(), _stream_handle(stream))
+        if rc:
+            raise SkvError(rc, "skv_ideal_bits")
+        return (tot, ps) if per_scalar else tot

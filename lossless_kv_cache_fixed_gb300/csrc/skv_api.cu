@@ -1,0 +1,353 @@
+// skv_api.cu -- the C ABI declared in include/skv.h: argument checks, workspace
+// layout, the host-built model constants, launches and status readback.
+//
+// Page "推测式 KV 编码无损压缩 KV 缓存最高可达约 4 倍" (Speculative KV coding):
+// section "什么能预测 KV 缓存" defines the encode (KV, mu, sigma) -> bits and
+// decode (bits, mu, sigma) -> KV operations; section "早期结果" the mixture with
+// the empirical bf16 distribution that skv_build_ecdf tabulates.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/skv.h"
+#include "skv_internal.h"
+#include "skv_model.cuh"
+
+using namespace skv;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// ---- host-built model constants ----
+
+uint32_t g_phi_host[kPhiKnots];
+float g_lo8_host[256];
+std::once_flag g_const_once;
+
+double e4m3_value_host(uint32_t u) {
+  uint32_t e = (u >> 3) & 15u, m = u & 7u;
+  double v = e ? std::ldexp(1.0 + m / 8.0, (int)e - 7) : std::ldexp(m / 8.0, -6);
+  return (u & 0x80u) ? -v : v;
+}
+
+uint32_t e4m3_bits_host(int r) { return r >= 127 ? (uint32_t)(r - 127) : (0x80u | (uint32_t)(126 - r)); }
+
+void build_constants() {
+  // T[i] = RNE(2^26 Phi(-8 + i/512)), Phi(z) = erfc(-z/sqrt 2)/2.  The nearest
+  // tie of 2^26 Phi over these knots is 2.3e-4 units away, far beyond the
+  // error of any binary64 erfc, so the table is the same on every host.
+  for (int i = 0; i < kPhiKnots; ++i) {
+    double z = -8.0 + (double)i / 512.0;
+    g_phi_host[i] = (uint32_t)std::nearbyint(std::ldexp(0.5 * std::erfc(-z / std::sqrt(2.0)), 26));
+  }
+  g_phi_host[0] = 0;
+  g_phi_host[kPhiKnots - 1] = kPhiOne;
+  // e4m3 bin lower edges by rank: midpoints, with the +-448 bins open-ended
+  g_lo8_host[0] = -INFINITY;
+  for (int r = 1; r < kNsymE4m3; ++r)
+    g_lo8_host[r] = (float)(0.5 * (e4m3_value_host(e4m3_bits_host(r - 1)) +
+                                   e4m3_value_host(e4m3_bits_host(r))));
+  g_lo8_host[kNsymE4m3] = INFINITY;
+  g_lo8_host[255] = INFINITY;
+}
+
+std::mutex g_dev_mu;
+bool g_dev_ready[1024];
+
+int ensure_device_tables() {
+  std::call_once(g_const_once, build_constants);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
+  if (dev < 0 || dev >= 1024) return SKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_dev_ready[dev]) {
+    if (upload_tables(g_phi_host, g_lo8_host) != cudaSuccess) return SKV_ERR_CUDA;
+    g_dev_ready[dev] = true;
+  }
+  return SKV_OK;
+}
+
+struct Plan {
+  Geo geo;
+  int dtype;
+  int64_t nsig;
+  // workspace layout (byte offsets)
+  size_t off_inv, off_sizes, off_starts, off_partials, off_scratch, off_bits, total;
+  int64_t stride;  // words per chunk stack
+  int bits_blocks;
+};
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
+  if (!p || !s || !out) return SKV_ERR_ARG;
+  if (p->dtype != SKV_BF16 && p->dtype != SKV_E4M3) return SKV_ERR_ARG;
+  if (p->reserved != 0) return SKV_ERR_ARG;
+  if (s->kv != 2 || s->layers <= 0 || s->heads <= 0 || s->tokens <= 0 || s->head_dim <= 0)
+    return SKV_ERR_ARG;
+  if (s->head_dim % 8) return SKV_ERR_ARG;
+  const int G = p->lanes;
+  if (G < 1 || G > 32 || (G & (G - 1))) return SKV_ERR_ARG;
+  if (p->token_block <= 0) return SKV_ERR_ARG;
+  Plan pl;
+  pl.dtype = p->dtype;
+  pl.geo.L = s->layers;
+  pl.geo.H = s->heads;
+  pl.geo.T = s->tokens;
+  pl.geo.D = s->head_dim;
+  pl.geo.Tb = p->token_block;
+  const int64_t tb_eff = p->token_block < s->tokens ? p->token_block : s->tokens;
+  pl.geo.G = G;
+  pl.geo.ntb = ((int64_t)s->tokens + pl.geo.Tb - 1) / pl.geo.Tb;
+  const int64_t rows = (int64_t)s->layers * 2 * s->heads;
+  pl.geo.nchunks = rows * pl.geo.ntb;
+  pl.geo.n = rows * (int64_t)s->tokens * s->head_dim;
+  // a chunk's scalar offsets are 32-bit inside the kernels
+  if (tb_eff * s->head_dim >= (1ll << 31)) return SKV_ERR_ARG;
+  pl.nsig = rows * s->head_dim;
+  // worst case words of one full chunk: every lane emits at most one word per
+  // symbol and, since a symbol adds at most M + log2(1 + 2^(M-31)) < M + 1
+  // bits of state, at most ceil(n (M + 1) / 32) words; plus 2 flush words.
+  const int M = p->dtype == SKV_BF16 ? kMBf16 : kME4m3;
+  const int64_t ngroup = tb_eff * s->head_dim / 8;
+  const int64_t nlane = 8 * ((ngroup + G - 1) / G);
+  int64_t wl = (nlane * (M + 1) + 31) / 32;
+  if (wl > nlane) wl = nlane;
+  pl.stride = ((G * (wl + 2)) + 3) / 4 * 4;
+  size_t off = align_up(sizeof(WsHead));
+  pl.off_inv = off;
+  off = align_up(off + sizeof(float2) * (size_t)pl.nsig);
+  pl.off_sizes = off;
+  off = align_up(off + sizeof(uint64_t) * (size_t)(pl.geo.nchunks + 1));
+  pl.off_starts = off;
+  off = align_up(off + sizeof(uint32_t) * (size_t)pl.geo.nchunks);
+  pl.off_partials = off;
+  off = align_up(off + sizeof(uint64_t) * (size_t)((pl.geo.nchunks + kScanBlock - 1) / kScanBlock + 1));
+  pl.off_scratch = off;
+  off = align_up(off + sizeof(uint32_t) * (size_t)pl.stride * (size_t)pl.geo.nchunks);
+  pl.total = off;
+  int64_t n8 = pl.geo.n / 8;
+  int64_t nb = (n8 + 255) / 256;
+  pl.bits_blocks = (int)(nb < 4096 ? (nb > 0 ? nb : 1) : 4096);
+  pl.off_bits = align_up(pl.off_inv + sizeof(float2) * (size_t)pl.nsig);
+  *out = pl;
+  return SKV_OK;
+}
+
+size_t ws_bytes_for(const Plan &pl, int op) {
+  if (op == SKV_OP_ENCODE) return pl.total;
+  if (op == SKV_OP_DECODE) return pl.off_sizes;
+  return align_up(pl.off_bits + sizeof(double) * (size_t)pl.bits_blocks);
+}
+
+uint64_t hash_words(const Plan &pl) {
+  return (uint64_t)pl.nsig + (pl.dtype == SKV_BF16 ? (uint64_t)kNsymBf16 + 1 : 0);
+}
+
+int status_from_flags(uint32_t f) {
+  if (f & kFlagSymbol) return SKV_ERR_SYMBOL;
+  if (f & kFlagParam) return SKV_ERR_PARAM;
+  if (f & kFlagCorrupt) return SKV_ERR_CORRUPT;
+  if (f & kFlagCapacity) return SKV_ERR_CAPACITY;
+  if (f & kFlagOverflow) return SKV_ERR_CUDA;  // an internal bound was broken
+  return SKV_OK;
+}
+
+// Reads the workspace head back (a synchronising copy).
+int read_head(WsHead *dev, WsHead *host, cudaStream_t st) {
+  if (cudaMemcpyAsync(host, dev, sizeof(WsHead), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SKV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SKV_ERR_CUDA;
+  return SKV_OK;
+}
+
+int common_inputs(const skv_params *p, const Plan &pl, const void *kv, const uint16_t *mu) {
+  if (!kv || !mu || !p->sigma) return SKV_ERR_ARG;
+  if (!aligned(kv, 16) || !aligned(mu, 16) || !aligned(p->sigma, 4)) return SKV_ERR_ARG;
+  if (pl.dtype == SKV_BF16 && (!p->ecdf || !aligned(p->ecdf, 4))) return SKV_ERR_ARG;
+  return SKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t skv_max_encoded_bytes(const skv_params *params, const skv_shape *shape) {
+  Plan pl;
+  if (make_plan(params, shape, &pl) != SKV_OK) return 0;
+  return 64 + 8 * (size_t)(pl.geo.nchunks + 1) +
+         4 * ((size_t)pl.geo.n + 2 * (size_t)pl.geo.G * (size_t)pl.geo.nchunks);
+}
+
+size_t skv_workspace_bytes(const skv_params *params, const skv_shape *shape, int op) {
+  Plan pl;
+  if (make_plan(params, shape, &pl) != SKV_OK) return 0;
+  if (op < SKV_OP_ENCODE || op > SKV_OP_IDEAL_BITS) return 0;
+  return ws_bytes_for(pl, op);
+}
+
+int skv_encode(const skv_params *params, const skv_shape *shape, const void *kv,
+               const uint16_t *mu, void *out, size_t out_capacity, size_t *out_bytes,
+               void *workspace, size_t workspace_bytes, skv_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  if ((rc = common_inputs(params, pl, kv, mu))) return rc;
+  if (!out || !out_bytes || !workspace || !aligned(out, 8) || !aligned(workspace, kAlign))
+    return SKV_ERR_ARG;
+  if (workspace_bytes < ws_bytes_for(pl, SKV_OP_ENCODE)) return SKV_ERR_CAPACITY;
+  if ((rc = ensure_device_tables())) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  WsHead *head = reinterpret_cast<WsHead *>(ws);
+  if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
+  float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
+  const uint32_t *ecdf = pl.dtype == SKV_BF16 ? params->ecdf : nullptr;
+  if (launch_prep(params->sigma, pl.nsig, ecdf, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
+  EncodeLaunch a;
+  a.geo = pl.geo;
+  a.dtype = pl.dtype;
+  a.kv = kv;
+  a.mu = mu;
+  a.inv = inv;
+  a.ecdf = ecdf;
+  a.scratch = reinterpret_cast<uint32_t *>(ws + pl.off_scratch);
+  a.stride = pl.stride;
+  a.sizes = reinterpret_cast<uint64_t *>(ws + pl.off_sizes);
+  a.starts = reinterpret_cast<uint32_t *>(ws + pl.off_starts);
+  a.partials = reinterpret_cast<uint64_t *>(ws + pl.off_partials);
+  a.head = head;
+  a.out = static_cast<uint8_t *>(out);
+  a.capacity = out_capacity;
+  a.hash_words = hash_words(pl);
+  if (launch_encode(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  WsHead h;
+  if ((rc = read_head(head, &h, st))) return rc;
+  if ((rc = status_from_flags(h.flags))) return rc;
+  *out_bytes = 64 + 8 * (size_t)(pl.geo.nchunks + 1) + (size_t)h.total;
+  return SKV_OK;
+}
+
+int skv_decode(const skv_params *params, const skv_shape *shape, const void *in, size_t in_bytes,
+               const uint16_t *mu, void *kv_out, void *workspace, size_t workspace_bytes,
+               skv_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  if ((rc = common_inputs(params, pl, kv_out, mu))) return rc;
+  if (!in || !aligned(in, 8) || !workspace || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
+  if (workspace_bytes < ws_bytes_for(pl, SKV_OP_DECODE)) return SKV_ERR_CAPACITY;
+  if (in_bytes < 64 + 8 * (size_t)(pl.geo.nchunks + 1)) return SKV_ERR_CORRUPT;
+  if ((rc = ensure_device_tables())) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  WsHead *head = reinterpret_cast<WsHead *>(ws);
+  if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
+  float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
+  const uint32_t *ecdf = pl.dtype == SKV_BF16 ? params->ecdf : nullptr;
+  if (launch_prep(params->sigma, pl.nsig, ecdf, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
+  DecodeLaunch a;
+  a.geo = pl.geo;
+  a.dtype = pl.dtype;
+  a.in = static_cast<const uint8_t *>(in);
+  a.in_bytes = in_bytes;
+  a.mu = mu;
+  a.inv = inv;
+  a.ecdf = ecdf;
+  a.kv_out = kv_out;
+  a.head = head;
+  a.hash_words = hash_words(pl);
+  if (launch_decode(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  WsHead h;
+  if ((rc = read_head(head, &h, st))) return rc;
+  return status_from_flags(h.flags);
+}
+
+int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void *kv,
+                   const uint16_t *mu, float *per_scalar, double *total, void *workspace,
+                   size_t workspace_bytes, skv_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  if ((rc = common_inputs(params, pl, kv, mu))) return rc;
+  if (!total || !workspace || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
+  if (per_scalar && !aligned(per_scalar, 16)) return SKV_ERR_ARG;
+  if (pl.dtype == SKV_BF16 && (!params->phat || !aligned(params->phat, 4))) return SKV_ERR_ARG;
+  if (workspace_bytes < ws_bytes_for(pl, SKV_OP_IDEAL_BITS)) return SKV_ERR_CAPACITY;
+  if ((rc = ensure_device_tables())) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  WsHead *head = reinterpret_cast<WsHead *>(ws);
+  if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
+  float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
+  // sigma validity only: the p-hat table enters through `phat`
+  if (launch_prep(params->sigma, pl.nsig, nullptr, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
+  IdealLaunch a;
+  a.geo = pl.geo;
+  a.dtype = pl.dtype;
+  a.kv = kv;
+  a.mu = mu;
+  a.sigma = params->sigma;
+  a.phat = params->phat;
+  a.per_scalar = per_scalar;
+  a.partials = reinterpret_cast<double *>(ws + pl.off_bits);
+  a.nblocks = pl.bits_blocks;
+  a.head = head;
+  if (launch_ideal(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  WsHead h;
+  if ((rc = read_head(head, &h, st))) return rc;
+  if ((rc = status_from_flags(h.flags))) return rc;
+  *total = h.bits;
+  return SKV_OK;
+}
+
+int skv_build_ecdf(const uint64_t *counts, uint32_t *ecdf, float *phat) {
+  if (!counts || !ecdf) return SKV_ERR_ARG;
+  // ranks in value order: negatives from -inf up to -0, then +0 up to +inf
+  auto pattern = [](int r) -> uint32_t {
+    uint32_t key = (uint32_t)(r + 127);
+    return (key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu);
+  };
+  unsigned __int128 tot = 0;
+  for (int r = 0; r < kNsymBf16; ++r) tot += (unsigned __int128)counts[pattern(r)] + 1;
+  if (tot >= ((unsigned __int128)1 << 37)) return SKV_ERR_ARG;
+  const uint64_t S_tot = (uint64_t)tot;
+  uint64_t S = 0;
+  for (int r = 0; r <= kNsymBf16; ++r) {
+    ecdf[r] = (uint32_t)(((unsigned __int128)S << 26) / S_tot);
+    if (r < kNsymBf16) {
+      const uint64_t c = counts[pattern(r)] + 1;
+      if (phat) phat[r] = (float)((double)c / (double)S_tot);
+      S += c;
+    }
+  }
+  return SKV_OK;
+}
+
+int skv_phi_table(uint32_t *table) {
+  if (!table) return SKV_ERR_ARG;
+  std::call_once(g_const_once, build_constants);
+  std::memcpy(table, g_phi_host, sizeof(g_phi_host));
+  return SKV_OK;
+}
+
+const char *skv_strerror(int status) {
+  switch (status) {
+    case SKV_OK: return "ok";
+    case SKV_ERR_ARG: return "invalid argument";
+    case SKV_ERR_CAPACITY: return "output buffer or workspace too small";
+    case SKV_ERR_SYMBOL: return "NaN symbol in the KV input";
+    case SKV_ERR_PARAM: return "invalid sigma, mu or p-hat table";
+    case SKV_ERR_CORRUPT: return "corrupt or mismatched container";
+    case SKV_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+int skv_version(void) { return 1; }
+
+}  // extern "C"

@@ -1,0 +1,582 @@
+// skv_code.cu -- encode, size scan, compaction, header check and decode kernels.
+//
+// Page "推测式 KV 编码无损压缩 KV 缓存最高可达约 4 倍" (Speculative KV coding),
+// section "什么能预测 KV 缓存": an arithmetic coder maps (KV_full, mu, sigma) to
+// bits and (bits, mu, sigma) back to KV_full.  Here the coder is interleaved
+// rANS (64-bit state x in [2^31, 2^63), 32-bit words) over the fixed-point
+// model of skv_model.cuh.
+//
+// GPU mapping.  One thread is one rANS lane; the G lanes of a chunk sit in
+// consecutive threads of one warp (32/G chunks per warp), so the order in which
+// lanes emit or consume renormalisation words inside a round comes from one
+// ballot plus a prefix popcount.  A lane's symbols are 8-scalar groups, so KV
+// and mu move as 16-byte vectors (8-byte for e4m3 KV).  Warps loop over 32-lane
+// tasks; the grid is a whole number of blocks per SM.  The Phi knot table
+// (64 KiB) and the e4m3 bin edges sit in shared memory.
+#include <cuda_runtime.h>
+
+#include "skv_internal.h"
+#include "skv_model.cuh"
+
+namespace skv {
+
+__device__ uint2 g_phi[kPhiKnots];
+__device__ float g_lo8[256];
+
+constexpr int kCodeThreads = 128;
+constexpr size_t kCodeSmem = sizeof(uint2) * kPhiKnots + sizeof(float) * 256;
+
+cudaError_t upload_tables(const uint32_t *T, const float *lo8) {
+  uint2 pairs[kPhiKnots];
+  for (int i = 0; i < kPhiKnots; ++i) {
+    pairs[i].x = T[i];
+    pairs[i].y = i + 1 < kPhiKnots ? T[i + 1] - T[i] : 0u;
+  }
+  cudaError_t e = cudaMemcpyToSymbol(g_phi, pairs, sizeof(pairs));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_lo8, lo8, sizeof(float) * 256);
+}
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  return n > 0 ? n : 1;
+}
+
+// SplitMix64 output function (Steele, Lea, Flood, OOPSLA 2014): the model
+// fingerprint is sum_k mix64(k << 32 | word_k) mod 2^64, then mix64(sum ^ nwords).
+__device__ __forceinline__ uint64_t mix64(uint64_t z) {
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+__device__ __forceinline__ void stage_tables(uint2 *s_phi, float *s_lo8) {
+  for (int i = threadIdx.x; i < kPhiKnots; i += blockDim.x) s_phi[i] = g_phi[i];
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) s_lo8[i] = g_lo8[i];
+  __syncthreads();
+}
+
+struct ChunkGeo {
+  uint64_t base;    // first scalar
+  uint64_t srow;    // first sigma entry of the (l, kv, h) row
+  uint32_t ngroup;  // 8-scalar groups in the chunk
+};
+
+__device__ __forceinline__ ChunkGeo chunk_geo(const Geo &g, int64_t c) {
+  int64_t row = c / g.ntb, tb = c - row * g.ntb;
+  int64_t t0 = tb * g.Tb;
+  int64_t tn = (int64_t)g.T - t0;
+  if (tn > g.Tb) tn = g.Tb;
+  ChunkGeo r;
+  r.base = (uint64_t)row * (uint64_t)g.T * (uint64_t)g.D + (uint64_t)t0 * (uint64_t)g.D;
+  r.srow = (uint64_t)row * (uint64_t)g.D;
+  r.ngroup = (uint32_t)(tn * g.D / 8);
+  return r;
+}
+
+// 8 consecutive symbols of a group (bf16 patterns or e4m3 codes)
+template <int DT>
+__device__ __forceinline__ void load_syms(const void *kv, uint64_t at, uint32_t (&s)[8]) {
+  if (DT == 0) {
+    uint4 v = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(kv) + at));
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s[k] = (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+  } else {
+    uint2 v = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint8_t *>(kv) + at));
+    uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s[k] = (w[k >> 2] >> (8 * (k & 3))) & 0xFFu;
+  }
+}
+
+__device__ __forceinline__ void load_mu(const uint16_t *mu, uint64_t at, uint32_t (&m)[8]) {
+  uint4 v = __ldg(reinterpret_cast<const uint4 *>(mu + at));
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+}
+
+__device__ __forceinline__ void load_inv(const float2 *inv, uint64_t at, ChanInv (&c)[8]) {
+  const float4 *p = reinterpret_cast<const float4 *>(inv + at);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float4 v = __ldg(p + k);
+    c[2 * k].s = v.x;
+    c[2 * k].s3 = v.y;
+    c[2 * k + 1].s = v.z;
+    c[2 * k + 1].s3 = v.w;
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t cum_of(int32_t r, float mu, ChanInv inv, const uint2 *phi,
+                                           const float *lo8, const uint32_t *ecdf) {
+  if (DT == 0) return cum_bf16(r, mu, inv, phi, ecdf);
+  return cum_e4m3(r, mu, inv.s, phi, lo8);
+}
+
+// ------------------------------------------------------------------------
+// Model preparation
+// ------------------------------------------------------------------------
+
+__global__ void k_prep(const float *__restrict__ sigma, int64_t nsig,
+                       const uint32_t *__restrict__ ecdf, float2 *__restrict__ inv,
+                       WsHead *head) {
+  uint64_t h = 0;
+  uint32_t bad = 0;
+  const int64_t nE = ecdf ? (int64_t)kNsymBf16 + 1 : 0;
+  for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < nsig + nE;
+       k += (int64_t)gridDim.x * blockDim.x) {
+    uint32_t w;
+    if (k < nsig) {
+      float s = sigma[k];
+      if (!sigma_valid(s)) {
+        bad = 1;
+        s = 1.0f;
+      }
+      ChanInv c = chan_inv(s);
+      inv[k] = make_float2(c.s, c.s3);
+      w = __float_as_uint(sigma[k]);
+    } else {
+      int64_t r = k - nsig;
+      w = ecdf[r];
+      if (r == 0 && w != 0u) bad = 1;
+      if (r == kNsymBf16 && w != kPhiOne) bad = 1;
+      if (r > 0 && w < ecdf[r - 1]) bad = 1;
+    }
+    h += mix64(((uint64_t)k << 32) | w);
+  }
+  if (bad) atomicOr(&head->flags, kFlagParam);
+  for (int o = 16; o; o >>= 1) h += __shfl_xor_sync(0xFFFFFFFFu, h, o);
+  if ((threadIdx.x & 31) == 0) atomicAdd(&head->hash_acc, (unsigned long long)h);
+}
+
+cudaError_t launch_prep(const float *sigma, int64_t nsig, const uint32_t *ecdf, float2 *inv,
+                        WsHead *head, cudaStream_t s) {
+  int64_t n = nsig + (ecdf ? kNsymBf16 + 1 : 0);
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 1024) blocks = 1024;
+  k_prep<<<blocks, 256, 0, s>>>(sigma, nsig, ecdf, inv, head);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------
+// Encode: one thread per lane, rounds descending, lanes descending.
+// ------------------------------------------------------------------------
+
+template <int DT>
+__global__ void __launch_bounds__(kCodeThreads) k_encode(EncodeLaunch a) {
+  extern __shared__ uint2 s_phi[];
+  float *s_lo8 = reinterpret_cast<float *>(s_phi + kPhiKnots);
+  stage_tables(s_phi, s_lo8);
+
+  constexpr int M = DT == 0 ? kMBf16 : kME4m3;
+  constexpr int32_t NS = DT == 0 ? kNsymBf16 : kNsymE4m3;
+  const int G = a.geo.G;
+  const int lane = threadIdx.x & 31;
+  const int ell = lane & (G - 1);
+  const uint32_t seg = G == 32 ? 0xFFFFFFFFu : (((1u << G) - 1u) << (lane & ~(G - 1)));
+  const uint32_t lt = seg & ((1u << lane) - 1u);
+  const int64_t ntasks = (a.geo.nchunks * G + 31) / 32;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const uint32_t D = (uint32_t)a.geo.D;
+
+  for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks;
+       task += nwarps) {
+    const int64_t c = (task * 32 + lane) / G;
+    const bool live = c < a.geo.nchunks;
+    ChunkGeo cg = chunk_geo(a.geo, live ? c : 0);
+    const uint32_t my_groups =
+        (live && (uint32_t)ell < cg.ngroup) ? (cg.ngroup - ell + G - 1) / G : 0u;
+    const uint32_t max_groups = __reduce_max_sync(0xFFFFFFFFu, my_groups);
+    uint32_t *region = a.scratch + (live ? c : 0) * a.stride;
+    int64_t sp = a.stride;
+    uint64_t x = kStateL;
+    uint32_t flags = 0;
+
+    for (int64_t gi = (int64_t)max_groups - 1; gi >= 0; --gi) {
+      const bool has = (uint32_t)gi < my_groups;
+      const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * (uint32_t)gi);
+      uint32_t sym[8], mub[8];
+      ChanInv inv[8];
+      if (has) {
+        load_syms<DT>(a.kv, cg.base + p0, sym);
+        load_mu(a.mu, cg.base + p0, mub);
+        load_inv(a.inv, cg.srow + p0 % D, inv);
+      }
+#pragma unroll
+      for (int k = 7; k >= 0; --k) {
+        uint32_t cst = 0, f = 1;
+        bool emit = false;
+        if (has) {
+          int32_t r = DT == 0 ? rank_bf16(sym[k]) : rank_e4m3(sym[k]);
+          if (r < 0 || r >= NS) {
+            flags |= kFlagSymbol;
+            r = 0;
+          }
+          if (!mu_valid(mub[k])) {
+            flags |= kFlagParam;
+            mub[k] = 0;
+          }
+          const float muf = bf16_to_f32(mub[k]);
+          cst = cum_of<DT>(r, muf, inv[k], s_phi, s_lo8, a.ecdf);
+          f = cum_of<DT>(r + 1, muf, inv[k], s_phi, s_lo8, a.ecdf) - cst;
+          emit = x >= ((uint64_t)f << (63 - M));
+        }
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, emit) & seg;
+        const int n = __popc(m);
+        if (emit) {
+          const int64_t idx = sp - n + __popc(m & lt);
+          if (idx >= 0) region[idx] = (uint32_t)x;
+          else flags |= kFlagOverflow;
+          x >>= 32;
+        }
+        sp -= n;
+        if (has) {
+          const uint64_t q = x / f;
+          x = (q << M) + (x - q * f) + cst;
+        }
+      }
+    }
+    if (live) {
+      const int64_t at = sp - 2 * G + 2 * ell;
+      if (at >= 0) {
+        region[at] = (uint32_t)x;
+        region[at + 1] = (uint32_t)(x >> 32);
+      } else {
+        flags |= kFlagOverflow;
+      }
+      if (ell == 0) {
+        const int64_t start = sp - 2 * G < 0 ? 0 : sp - 2 * G;
+        a.starts[c] = (uint32_t)start;
+        a.sizes[c] = 4ull * (uint64_t)(a.stride - start);
+      }
+    }
+    if (flags) atomicOr(&a.head->flags, flags);
+  }
+}
+
+// ------------------------------------------------------------------------
+// Exclusive scan of chunk sizes: block-local scans, then the block totals.
+// ------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(256) k_scan_local(uint64_t *sizes, int64_t n,
+                                                    uint64_t *partials) {
+  __shared__ uint64_t s[256];
+  const int64_t b0 = (int64_t)blockIdx.x * kScanBlock + threadIdx.x * 8;
+  uint64_t v[8], sum = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    v[k] = b0 + k < n ? sizes[b0 + k] : 0;
+    sum += v[k];
+  }
+  s[threadIdx.x] = sum;
+  __syncthreads();
+  for (int off = 1; off < 256; off <<= 1) {
+    uint64_t t = threadIdx.x >= off ? s[threadIdx.x - off] : 0;
+    __syncthreads();
+    s[threadIdx.x] += t;
+    __syncthreads();
+  }
+  uint64_t excl = s[threadIdx.x] - sum;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (b0 + k < n) sizes[b0 + k] = excl;  // in place: block-local exclusive offset
+    excl += v[k];
+  }
+  if (threadIdx.x == 255) partials[blockIdx.x] = s[255];
+}
+
+__global__ void __launch_bounds__(1024) k_scan_partials(uint64_t *partials, int64_t nb,
+                                                        WsHead *head) {
+  __shared__ uint64_t s[1024];
+  uint64_t carry = 0;
+  for (int64_t b0 = 0; b0 < nb; b0 += 1024) {
+    const int64_t i = b0 + threadIdx.x;
+    const uint64_t v = i < nb ? partials[i] : 0;
+    s[threadIdx.x] = v;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+      uint64_t t = threadIdx.x >= off ? s[threadIdx.x - off] : 0;
+      __syncthreads();
+      s[threadIdx.x] += t;
+      __syncthreads();
+    }
+    if (i < nb) partials[i] = carry + s[threadIdx.x] - v;
+    carry += s[1023];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) head->total = carry;
+}
+
+// ------------------------------------------------------------------------
+// Compaction into the container: header | offsets | payload.
+// ------------------------------------------------------------------------
+
+__device__ __forceinline__ void put_u16(uint8_t *p, uint32_t v) {
+  p[0] = (uint8_t)v;
+  p[1] = (uint8_t)(v >> 8);
+}
+__device__ __forceinline__ void put_u32(uint8_t *p, uint32_t v) {
+  for (int i = 0; i < 4; ++i) p[i] = (uint8_t)(v >> (8 * i));
+}
+__device__ __forceinline__ void put_u64(uint8_t *p, uint64_t v) {
+  for (int i = 0; i < 8; ++i) p[i] = (uint8_t)(v >> (8 * i));
+}
+
+// The 64-byte container header for this geometry (see skv.h).
+__device__ void make_header(uint8_t *h, const Geo &g, int dtype, uint64_t payload,
+                            uint64_t hash) {
+  for (int i = 0; i < 64; ++i) h[i] = 0;
+  put_u32(h + 0, 0x31564B53u);
+  put_u16(h + 4, 1);
+  h[6] = (uint8_t)dtype;
+  h[7] = (uint8_t)(dtype == 0 ? kMBf16 : kME4m3);
+  put_u32(h + 8, (uint32_t)g.L);
+  put_u32(h + 12, 2);
+  put_u32(h + 16, (uint32_t)g.H);
+  put_u32(h + 20, (uint32_t)g.T);
+  put_u32(h + 24, (uint32_t)g.D);
+  put_u32(h + 28, (uint32_t)g.Tb);
+  put_u16(h + 32, (uint32_t)g.G);
+  h[34] = 8;
+  h[35] = 9;
+  put_u16(h + 36, 8);
+  put_u64(h + 40, (uint64_t)g.nchunks);
+  put_u64(h + 48, payload);
+  put_u64(h + 56, hash);
+}
+
+__global__ void __launch_bounds__(256) k_compact(EncodeLaunch a) {
+  const uint64_t total = a.head->total;
+  const int64_t nc = a.geo.nchunks;
+  const uint64_t hbytes = 64 + 8 * (uint64_t)(nc + 1);
+  if (hbytes + total > a.capacity) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(&a.head->flags, kFlagCapacity);
+    return;
+  }
+  uint64_t *offs = reinterpret_cast<uint64_t *>(a.out + 64);
+  uint32_t *payload = reinterpret_cast<uint32_t *>(a.out + hbytes);
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t c = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); c < nc;
+       c += nwarps) {
+    const uint64_t off = a.sizes[c] + a.partials[c / kScanBlock];
+    const int64_t start = a.starts[c];
+    const int64_t nw = a.stride - start;
+    const uint32_t *src = a.scratch + c * a.stride + start;
+    uint32_t *dst = payload + off / 4;
+    for (int64_t i = lane; i < nw; i += 32) dst[i] = src[i];
+    if (lane == 0) offs[c] = off;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    offs[nc] = total;
+    uint8_t h[64];
+    make_header(h, a.geo, a.dtype, total, mix64(a.head->hash_acc ^ a.hash_words));
+    for (int i = 0; i < 64; ++i) a.out[i] = h[i];
+  }
+}
+
+static int code_blocks(int64_t ntasks) {
+  // whole blocks per SM: 3 blocks of 4 warps fit next to the 66 KiB table
+  const int64_t warps_per_block = kCodeThreads / 32;
+  int64_t want = (ntasks + warps_per_block - 1) / warps_per_block;
+  int64_t cap = (int64_t)device_sm_count() * 3;
+  return (int)(want < cap ? want : cap);
+}
+
+cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s) {
+  const int64_t ntasks = (a.geo.nchunks * a.geo.G + 31) / 32;
+  const int blocks = code_blocks(ntasks);
+  cudaError_t e;
+  if (a.dtype == 0) {
+    e = cudaFuncSetAttribute(k_encode<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCodeSmem);
+    if (e != cudaSuccess) return e;
+    k_encode<0><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
+  } else {
+    e = cudaFuncSetAttribute(k_encode<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCodeSmem);
+    if (e != cudaSuccess) return e;
+    k_encode<1><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
+  }
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int64_t nb = (a.geo.nchunks + kScanBlock - 1) / kScanBlock;
+  k_scan_local<<<(unsigned)nb, 256, 0, s>>>(a.sizes, a.geo.nchunks, a.partials);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  k_scan_partials<<<1, 1024, 0, s>>>(a.partials, nb, a.head);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  int64_t cblocks = (a.geo.nchunks + 7) / 8;
+  if (cblocks > (int64_t)device_sm_count() * 16) cblocks = (int64_t)device_sm_count() * 16;
+  k_compact<<<(unsigned)cblocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------
+// Decode
+// ------------------------------------------------------------------------
+
+__device__ __forceinline__ uint64_t get_u64(const uint8_t *p) {
+  uint64_t v = 0;
+  for (int i = 7; i >= 0; --i) v = (v << 8) | p[i];
+  return v;
+}
+
+// Header, fingerprint and offset-table ends; per-chunk offsets are checked by
+// the decode kernel itself.
+__global__ void k_check_header(DecodeLaunch a) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const int64_t nc = a.geo.nchunks;
+  const uint64_t hbytes = 64 + 8 * (uint64_t)(nc + 1);
+  const uint64_t payload = a.in_bytes - hbytes;
+  uint8_t want[64];
+  make_header(want, a.geo, a.dtype, payload, mix64(a.head->hash_acc ^ a.hash_words));
+  bool ok = true;
+  for (int i = 0; i < 64; ++i) ok &= a.in[i] == want[i];
+  ok &= get_u64(a.in + 64) == 0;
+  ok &= get_u64(a.in + 64 + 8 * (uint64_t)nc) == payload;
+  if (!ok) atomicOr(&a.head->flags, kFlagCorrupt);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kCodeThreads) k_decode(DecodeLaunch a) {
+  extern __shared__ uint2 s_phi[];
+  float *s_lo8 = reinterpret_cast<float *>(s_phi + kPhiKnots);
+  stage_tables(s_phi, s_lo8);
+
+  constexpr int M = DT == 0 ? kMBf16 : kME4m3;
+  constexpr int32_t NS = DT == 0 ? kNsymBf16 : kNsymE4m3;
+  constexpr uint32_t kMask = (1u << M) - 1u;
+  const int G = a.geo.G;
+  const int lane = threadIdx.x & 31;
+  const int ell = lane & (G - 1);
+  const uint32_t seg = G == 32 ? 0xFFFFFFFFu : (((1u << G) - 1u) << (lane & ~(G - 1)));
+  const uint32_t lt = seg & ((1u << lane) - 1u);
+  const int64_t ntasks = (a.geo.nchunks * G + 31) / 32;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const uint32_t D = (uint32_t)a.geo.D;
+  const int64_t nc = a.geo.nchunks;
+  const uint64_t hbytes = 64 + 8 * (uint64_t)(nc + 1);
+  const uint64_t payload_bytes = a.in_bytes - hbytes;
+  const uint8_t *payload = a.in + hbytes;
+
+  for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks;
+       task += nwarps) {
+    const int64_t c = (task * 32 + lane) / G;
+    const bool live = c < nc;
+    uint32_t flags = 0;
+    uint64_t off_a = 0, off_b = 0;
+    if (live) {
+      const uint64_t *offs = reinterpret_cast<const uint64_t *>(a.in + 64);
+      off_a = offs[c];
+      off_b = offs[c + 1];
+    }
+    const bool ok = live && off_a <= off_b && off_b <= payload_bytes && ((off_b - off_a) & 3) == 0 &&
+                    (off_b - off_a) / 4 >= 2ull * G;
+    if (live && !ok) flags |= kFlagCorrupt;
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(payload + (ok ? off_a : 0));
+    const uint64_t nw = ok ? (off_b - off_a) / 4 : 0;
+    ChunkGeo cg = chunk_geo(a.geo, live ? c : 0);
+    const uint32_t my_groups =
+        (ok && (uint32_t)ell < cg.ngroup) ? (cg.ngroup - ell + G - 1) / G : 0u;
+    const uint32_t max_groups = __reduce_max_sync(0xFFFFFFFFu, my_groups);
+    uint64_t x = ok ? ((uint64_t)w[2 * ell] | ((uint64_t)w[2 * ell + 1] << 32)) : kStateL;
+    uint64_t cur = 2ull * G;
+
+    for (uint32_t gi = 0; gi < max_groups; ++gi) {
+      const bool has = gi < my_groups;
+      const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * gi);
+      uint32_t mub[8], out[8];
+      ChanInv inv[8];
+      if (has) {
+        load_mu(a.mu, cg.base + p0, mub);
+        load_inv(a.inv, cg.srow + p0 % D, inv);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        bool need = false;
+        out[k] = 0;
+        if (has) {
+          if (!mu_valid(mub[k])) {
+            flags |= kFlagParam;
+            mub[k] = 0;
+          }
+          const float muf = bf16_to_f32(mub[k]);
+          const uint32_t slot = (uint32_t)x & kMask;
+          // largest r with cum(r) <= slot; clo = cum(r), chi = cum(r + 1)
+          int32_t r = 0;
+          uint32_t clo = 0, chi = 1u << M;
+#pragma unroll
+          for (int step = DT == 0 ? (1 << 15) : (1 << 7); step >= 1; step >>= 1) {
+            const int32_t cand = r + step;
+            if (cand < NS) {
+              const uint32_t cv = cum_of<DT>(cand, muf, inv[k], s_phi, s_lo8, a.ecdf);
+              if (cv <= slot) {
+                r = cand;
+                clo = cv;
+              } else {
+                chi = cv;
+              }
+            }
+          }
+          x = (uint64_t)(chi - clo) * (x >> M) + (slot - clo);
+          need = x < kStateL;
+          out[k] = DT == 0 ? bits_bf16(r) : bits_e4m3(r);
+        }
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, need) & seg;
+        if (need) {
+          const uint64_t pos = cur + __popc(m & lt);
+          if (pos < nw) {
+            x = (x << 32) | w[pos];
+          } else {
+            flags |= kFlagCorrupt;
+            x = kStateL;
+          }
+        }
+        cur += __popc(m);
+      }
+      if (has) {
+        if (DT == 0) {
+          uint4 v;
+          v.x = out[0] | (out[1] << 16);
+          v.y = out[2] | (out[3] << 16);
+          v.z = out[4] | (out[5] << 16);
+          v.w = out[6] | (out[7] << 16);
+          *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.kv_out) + cg.base + p0) = v;
+        } else {
+          uint2 v;
+          v.x = out[0] | (out[1] << 8) | (out[2] << 16) | (out[3] << 24);
+          v.y = out[4] | (out[5] << 8) | (out[6] << 16) | (out[7] << 24);
+          *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.kv_out) + cg.base + p0) = v;
+        }
+      }
+    }
+    if (ok) {
+      if (x != kStateL) flags |= kFlagCorrupt;
+      if (ell == 0 && cur != nw) flags |= kFlagCorrupt;
+    }
+    if (flags) atomicOr(&a.head->flags, flags);
+  }
+}
+
+cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s) {
+  k_check_header<<<1, 32, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t ntasks = (a.geo.nchunks * a.geo.G + 31) / 32;
+  const int blocks = code_blocks(ntasks);
+  if (a.dtype == 0) {
+    e = cudaFuncSetAttribute(k_decode<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCodeSmem);
+    if (e != cudaSuccess) return e;
+    k_decode<0><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
+  } else {
+    e = cudaFuncSetAttribute(k_decode<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCodeSmem);
+    if (e != cudaSuccess) return e;
+    k_decode<1><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace skv

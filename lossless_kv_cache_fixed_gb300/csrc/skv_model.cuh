@@ -1,0 +1,134 @@
+// skv_model.cuh -- the fixed-point probability model on the device.
+//
+// Page "推测式 KV 编码无损压缩 KV 缓存最高可达约 4 倍" (Speculative KV coding):
+//   section "q 应是什么样的": Gaussian q(x) = N(x; mu, sigma^2) around the
+//     per-scalar prediction;
+//   section "早期结果": bf16 symbols use 0.95 N(mu, sigma^2) + 0.03 N(mu, (3 sigma)^2)
+//     + 0.02 p-hat_bf16;
+//   section "原生 FP8 KV 缓存": e4m3 symbols use the bin-integrated N(mu, sigma^2);
+//   section "下一步计划": both ends must obtain bit-identical probabilities.
+//
+// Every function below is exact integer or IEEE round-to-nearest fp32
+// arithmetic through explicit intrinsics (never contracted into FMAs), so the
+// frequencies are the same on every GPU and on any IEEE CPU.
+#pragma once
+#include <cstdint>
+
+namespace skv {
+
+constexpr int kNsymBf16 = 65282;            // non-NaN bf16 patterns
+constexpr int kNsymE4m3 = 254;              // non-NaN e4m3 codes
+constexpr uint32_t kPhiOne = 1u << 26;      // Phi_q scale
+constexpr int kPhiKnots = 8193;             // z = -8 + i/512, i = 0..8192
+constexpr uint64_t kStateL = 1ull << 31;    // rANS lower bound
+constexpr int kMBf16 = 28, kME4m3 = 16;     // frequency precision
+constexpr uint32_t kKBf16 = (1u << 28) - kNsymBf16;  // 2^M - |S|
+constexpr uint32_t kKE4m3 = (1u << 16) - kNsymE4m3;
+
+// ---- symbol <-> rank (monotone value order, -0 before +0) ----
+
+// bf16: the IEEE totalOrder key of a pattern is (u | 0x8000) for a clear sign
+// bit and (~u & 0xFFFF) otherwise; the 127 NaNs below -inf are skipped.
+// Valid iff 0 <= result < kNsymBf16.
+__device__ __forceinline__ int32_t rank_bf16(uint32_t u) {
+  uint32_t key = (u & 0x8000u) ? (~u & 0xFFFFu) : (u | 0x8000u);
+  return (int32_t)key - 127;
+}
+
+__device__ __forceinline__ uint32_t bits_bf16(int32_t r) {
+  uint32_t key = (uint32_t)(r + 127);
+  return (key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu);
+}
+
+// e4m3: magnitude 0x7F is NaN; negatives are ranks 0..126 (-448 .. -0).
+__device__ __forceinline__ int32_t rank_e4m3(uint32_t u) {
+  uint32_t mag = u & 0x7Fu;
+  int32_t r = (u & 0x80u) ? 126 - (int32_t)mag : 127 + (int32_t)mag;
+  return mag == 0x7Fu ? -1 : r;
+}
+
+__device__ __forceinline__ uint32_t bits_e4m3(int32_t r) {
+  return r >= 127 ? (uint32_t)(r - 127) : (0x80u | (uint32_t)(126 - r));
+}
+
+// Lower edge of bf16 symbol r's round-to-nearest bin, as fp32 bits.  The edge
+// between two neighbours is their midpoint: the smaller magnitude's pattern
+// followed by a half-ulp bit.  Ranks 0, 1 (-inf, -max) start at -inf, ranks
+// 65281, 65282 (+inf, end) at +inf, and -0 | +0 split at 0.
+__device__ __forceinline__ float lo_bf16(int32_t r) {
+  uint32_t pos = ((uint32_t)(r + 126 - 32768) << 16) | 0x8000u;           // r >= 32642
+  uint32_t neg = 0x80000000u | ((uint32_t)(32640 - r) << 16) | 0x8000u;   // r <= 32640
+  uint32_t b = r >= 32642 ? pos : neg;
+  b = r == 32641 ? 0u : b;
+  b = r <= 1 ? 0xFF800000u : b;
+  b = r >= 65281 ? 0x7F800000u : b;
+  return __uint_as_float(b);
+}
+
+// ---- Phi_q: 2^26 Phi(z) by integer interpolation of the knot table ----
+// With t = 512 z: Phi_q = 0 for t <= -4096, 2^26 for t >= 4096, else
+// T[i] + ((T[i+1] - T[i]) fr >> 16) with i = floor(t) + 4096 and
+// fr = floor(65536 (t - floor t)).  Both come out of one integer,
+// q = floor(2^25 z) = 65536 floor(t) + fr: i = (q >> 16) + 4096, fr = q & 0xFFFF.
+// 2^25 z is an exact scaling (or +-inf, which the clamps map to the ends).
+// `phi` holds (T[i], T[i+1] - T[i]) pairs; the last pair is (2^26, 0).
+__device__ __forceinline__ uint32_t phi_q(float z, const uint2 *phi) {
+  int32_t q = __float2int_rd(__fmul_rn(z, 33554432.0f));
+  q = max(q, -(1 << 28));
+  q = min(q, 1 << 28);
+  uint2 e = phi[(q >> 16) + 4096];
+  return e.x + ((e.y * ((uint32_t)q & 0xFFFFu)) >> 16);
+}
+
+// Per-channel reciprocals: IEEE round-to-nearest 1/sigma and 1/(3 sigma).
+struct ChanInv {
+  float s, s3;
+};
+
+__device__ __forceinline__ bool sigma_valid(float s) {
+  // finite and >= FLT_MIN, with 3 sigma finite (NaN fails the first test)
+  return s >= 1.17549435e-38f && __fmul_rn(3.0f, s) <= 3.40282347e38f;
+}
+
+__device__ __forceinline__ ChanInv chan_inv(float sigma) {
+  ChanInv c;
+  c.s = __frcp_rn(sigma);
+  c.s3 = __frcp_rn(__fmul_rn(3.0f, sigma));
+  return c;
+}
+
+// cum(r) for bf16: floor(K (95 Phi_q(z1) + 3 Phi_q(z3) + 2 E_q[r]) / (100 2^26)) + r,
+// z1 = (lo - mu) / sigma, z3 = (lo - mu) / (3 sigma), each product rounded.
+__device__ __forceinline__ uint32_t cum_bf16(int32_t r, float mu, ChanInv inv, const uint2 *phi,
+                                             const uint32_t *__restrict__ ecdf) {
+  float d = __fsub_rn(lo_bf16(r), mu);
+  uint32_t p1 = phi_q(__fmul_rn(d, inv.s), phi);
+  uint32_t p3 = phi_q(__fmul_rn(d, inv.s3), phi);
+  uint32_t e = __ldg(ecdf + r);
+  uint64_t F = 95ull * p1 + 3ull * p3 + 2ull * e;
+  uint64_t v = ((uint64_t)kKBf16 * F) >> 26;
+  return (uint32_t)(v / 100u) + (uint32_t)r;
+}
+
+// cum(r) for e4m3: floor(K Phi_q(z1) / 2^26) + r.
+__device__ __forceinline__ uint32_t cum_e4m3(int32_t r, float mu, float inv_s, const uint2 *phi,
+                                             const float *lo8) {
+  float d = __fsub_rn(lo8[r], mu);
+  uint32_t p = phi_q(__fmul_rn(d, inv_s), phi);
+  return (uint32_t)(((uint64_t)kKE4m3 * p) >> 26) + (uint32_t)r;
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t u) { return __uint_as_float(u << 16); }
+
+__device__ __forceinline__ bool mu_valid(uint32_t mu_bits) { return (mu_bits & 0x7F80u) != 0x7F80u; }
+
+// Error flag bits gathered in the workspace.
+enum : uint32_t {
+  kFlagSymbol = 1u,
+  kFlagParam = 2u,
+  kFlagCorrupt = 4u,
+  kFlagOverflow = 8u,
+  kFlagCapacity = 16u,
+};
+
+}  // namespace skv

@@ -1,0 +1,52 @@
+"""Shared set-up for the GPU tests: one synthetic workload, fed identically to the
+CUDA library (through the C ABI) and to the oracle."""
+import numpy as np
+import torch
+
+import synth
+
+
+def skv():
+    import lossless_kv_cache_fixed_gb300 as P
+    P.build()
+    return P
+
+
+def gpu_codec(w: synth.Workload, Tb=None, G=None):
+    P = skv()
+    s = w.spec
+    dev = torch.device("cuda")
+    ecdf = phat = None
+    if s.dtype == synth.BF16:
+        E, ph = P.skv_build_ecdf(w.counts.cpu().numpy().astype(np.uint64))
+        ecdf = torch.from_numpy(E.view(np.int32)).to(dev)
+        phat = torch.from_numpy(ph).to(dev)
+    return P.Codec(s.dtype, s.L, s.H, s.T, s.D, Tb or s.Tb, G or s.G, w.sigma.to(dev), ecdf, phat)
+
+
+def oracle_model(O, w: synth.Workload, Tb=None, G=None):
+    s = w.spec
+    sigma = w.sigma.cpu().numpy().astype(np.float32)
+    counts = None if w.counts is None else w.counts.cpu().numpy().astype(np.uint64)
+    return O.Model(s.dtype, s.L, s.H, s.T, s.D, Tb or s.Tb, G or s.G, sigma, counts=counts)
+
+
+def host_views(w: synth.Workload):
+    kv, mu, _, _ = synth.to_numpy(w)
+    return kv.reshape(-1), mu.reshape(-1)
+
+
+def device_views(w: synth.Workload):
+    dev = torch.device("cuda")
+    if w.spec.dtype == synth.BF16:
+        kv = w.kv.view(torch.int16).to(dev).reshape(-1)
+    else:
+        kv = w.kv.to(dev).reshape(-1)
+    mu = w.mu.view(torch.int16).to(dev).reshape(-1)
+    return kv, mu
+
+
+def container_chunk(buf_host: np.ndarray, nchunks: int, c: int) -> np.ndarray:
+    head = 64 + 8 * (nchunks + 1)
+    offs = buf_host[64:head].view(np.uint64)
+    return buf_host[head + int(offs[c]): head + int(offs[c + 1])].view(np.uint32)

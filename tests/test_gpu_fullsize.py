@@ -1,0 +1,87 @@
+"""GPU parity at the full workload sizes, in the launch configuration bench.py
+times: the whole cache round-trips exactly on the device; an evenly spread
+sample of chunks is byte-identical to the oracle's encoding of those chunks;
+ideal bits match the oracle per scalar on the sampled chunks; the coded size is
+at most 1% over the summed ideal (except at 1K-scalar chunks, where the 32-64
+bit rANS flush per lane alone is ~2% of ~2.3 bits/scalar: reported, not a
+failure).
+
+Workloads (seeded, synthetic, Qwen3 shapes):
+  qwen3-0.6b-bf16  28 x 2 x 8 x 4096 x 128   bf16, 234.9M scalars
+  qwen3-32b-bf16   64 x 2 x 8 x 8192 x 128   bf16, 1.07G scalars, calibrated sigma
+  qwen3-8b-e4m3    36 x 2 x 8 x 16384 x 128  e4m3, 1.21G scalars
+  long-32k-e4m3    64 x 2 x 8 x 32768 x 128  e4m3, 2^32 scalars, chunk sweep 1K/4K/16K
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_helpers import container_chunk, gpu_codec, oracle_model
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _check(O, w, Tb=None, G=None, nsample=32, max_overhead=0.01):
+    s = w.spec
+    codec = gpu_codec(w, Tb, G)
+    kv_d = (w.kv.view(torch.int16) if s.dtype == synth.BF16 else w.kv).reshape(-1)
+    mu_d = w.mu.view(torch.int16).reshape(-1)
+    buf, nb = codec.encode(kv_d, mu_d)
+    dec = codec.decode(buf, nb, mu_d)
+    assert torch.equal(dec, kv_d)
+    del dec
+    tot, ps = codec.ideal_bits(kv_d, mu_d, per_scalar=True)
+    assert abs(tot - ps.double().sum().item()) <= 1e-9 * tot
+    m = oracle_model(O, w, Tb, G)
+    nc = m.num_chunks()
+    host = buf[:nb].cpu().numpy()
+    del buf
+    assert O.check_header(m, host) == 0
+    chunks = sorted(set(np.linspace(0, nc - 1, nsample).astype(np.int64).tolist()))
+    kv_h = kv_d.cpu().numpy()
+    kv_h = kv_h.view(np.uint16) if s.dtype == synth.BF16 else kv_h.view(np.uint8)
+    mu_h = mu_d.cpu().numpy().view(np.uint16)
+    want = O.encode_chunks(m, kv_h, mu_h, chunks)
+    Tbe = Tb or s.Tb
+    ntb = (s.T + Tbe - 1) // Tbe
+    for c, ww in zip(chunks, want):
+        assert np.array_equal(container_chunk(host, nc, c), ww), c
+        row, tb = divmod(c, ntb)
+        base = row * s.T * s.D + tb * Tbe * s.D
+        n_c = min(Tbe, s.T - tb * Tbe) * s.D
+        ref_tot, ref = O.ideal_bits(m, kv_h, mu_h, base, base + n_c, per_scalar=True)
+        got = ps[base: base + n_c].double().cpu().numpy()
+        assert np.all(np.abs(got - ref) <= 1e-3 * np.abs(ref) + 1e-6), c
+    if max_overhead is not None:
+        assert 8.0 * nb <= (1.0 + max_overhead) * tot
+    return nb, tot
+
+
+def test_qwen3_0_6b_bf16(oracle_mod):
+    w = synth.make("qwen3-0.6b-bf16", device="cuda")
+    _check(oracle_mod, w)
+
+
+def test_qwen3_32b_bf16(oracle_mod):
+    w = synth.make("qwen3-32b-bf16", device="cuda")
+    _check(oracle_mod, w)
+
+
+def test_qwen3_8b_e4m3(oracle_mod):
+    w = synth.make("qwen3-8b-e4m3", device="cuda")
+    _check(oracle_mod, w)
+
+
+@pytest.mark.parametrize("tb,G,bound", [(8, 1, None), (32, 1, 0.01), (128, 4, 0.01)])
+def test_long_32k_e4m3_chunk_sweep(oracle_mod, tb, G, bound):
+    w = synth.make("long-32k-e4m3", device="cuda")
+    nb, tot = _check(oracle_mod, w, Tb=tb, G=G, nsample=24, max_overhead=bound)
+    del w
+    torch.cuda.empty_cache()

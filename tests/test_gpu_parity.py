@@ -1,0 +1,131 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle.
+
+Bar: containers byte-identical to the oracle's, decoded caches identical to the
+input, per-scalar ideal bits within |gpu - oracle| <= 1e-3 |oracle| + 1e-6 bits,
+and coded size at most 1% over the summed ideal.  Sizes span several chunks
+and lanes with a ragged last token block; the lane count G is swept.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_helpers import container_chunk, device_views, gpu_codec, host_views, oracle_model
+
+pytestmark = pytest.mark.gpu
+
+RTOL, ATOL = 1e-3, 1e-6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _roundtrip(O, w, Tb=None, G=None, ideal=True, max_overhead=None):
+    """max_overhead: bound on coded/ideal - 1 (the configs' 1%); by default only the
+    fixed container and flush costs are allowed on top of 0.5%."""
+    codec = gpu_codec(w, Tb, G)
+    kv_d, mu_d = device_views(w)
+    buf, nb = codec.encode(kv_d, mu_d)
+    torch.cuda.synchronize()
+    got = buf[:nb].cpu().numpy()
+    m = oracle_model(O, w, Tb, G)
+    kv, mu = host_views(w)
+    rc, want = O.encode(m, kv, mu)
+    assert rc == 0
+    assert got.size == want.size and np.array_equal(got, want)
+    dec = codec.decode(buf, nb, mu_d)
+    assert torch.equal(dec, kv_d)
+    if ideal:
+        tot, ps = codec.ideal_bits(kv_d, mu_d, per_scalar=True)
+        ref_tot, ref = O.ideal_bits(m, kv, mu, per_scalar=True)
+        ps = ps.double().cpu().numpy()
+        assert np.all(np.abs(ps - ref) <= RTOL * np.abs(ref) + ATOL)
+        assert abs(tot - ps.sum()) <= 1e-9 * abs(tot)
+        assert abs(tot - ref_tot) <= RTOL * ref_tot
+        nc = m.num_chunks()
+        if max_overhead is not None:
+            assert 8.0 * nb <= (1.0 + max_overhead) * ref_tot
+        else:
+            fixed = 512 + 64 * (nc + 1) + 64 * m.s.G * nc
+            assert 8.0 * nb <= 1.005 * ref_tot + fixed
+    return nb
+
+
+def test_tiny_bf16_workload(oracle_mod):
+    _roundtrip(oracle_mod, synth.make("tiny-bf16"), max_overhead=0.01)
+
+
+@pytest.mark.parametrize("name", ["qwen3-0.6b-bf16", "qwen3-8b-e4m3"])
+def test_scaled_workload_ragged(oracle_mod, name):
+    # the full-size recipe on 2 layers x 2 heads x 600 tokens: 3 token blocks of
+    # 256, the last one ragged (88 tokens), 8 lanes
+    spec = synth.WORKLOADS[name].scaled(L=2, H=2, T=600, calib_draws=4)
+    _roundtrip(oracle_mod, synth.make(spec))
+
+
+@pytest.mark.parametrize("dtype", [synth.BF16, synth.E4M3])
+@pytest.mark.parametrize("G", [1, 2, 4, 16, 32])
+def test_lane_sweep(oracle_mod, dtype, G):
+    base = "qwen3-0.6b-bf16" if dtype == synth.BF16 else "qwen3-8b-e4m3"
+    spec = synth.WORKLOADS[base].scaled(name="lanes%d" % G, L=1, H=2, T=200, D=64, Tb=64,
+                                        calib_draws=2)
+    _roundtrip(oracle_mod, synth.make(spec), G=G)
+
+
+@pytest.mark.parametrize("T,Tb,D", [(1, 256, 8), (7, 4, 8), (33, 1000, 16), (5, 1, 128)])
+def test_odd_geometries(oracle_mod, T, Tb, D):
+    spec = synth.WORKLOADS["tiny-bf16"].scaled(name="odd", L=1, H=1, T=T, D=D, Tb=Tb, G=8)
+    _roundtrip(oracle_mod, synth.make(spec))
+    spec8 = synth.WORKLOADS["qwen3-8b-e4m3"].scaled(name="odd8", L=1, H=1, T=T, D=D, Tb=Tb, G=2)
+    _roundtrip(oracle_mod, synth.make(spec8))
+
+
+def _custom(dtype, kv_np, mu_np, sigma_np, counts=None, T=None, D=8, Tb=32, G=4):
+    n = kv_np.size
+    T = T or n // (2 * D)
+    spec = synth.Spec("custom", dtype, 1, 1, T, D, 0.03, False, 0, 0, False, Tb, G)
+    kv = torch.from_numpy(kv_np.view(np.int16) if dtype == synth.BF16 else kv_np).reshape(1, 2, 1, T, D)
+    if dtype == synth.BF16:
+        kv = kv.view(torch.bfloat16)
+    mu = torch.from_numpy(mu_np.view(np.int16)).view(torch.bfloat16).reshape(1, 2, 1, T, D)
+    sig = torch.from_numpy(sigma_np.astype(np.float32)).reshape(1, 2, 1, D)
+    cnt = None if counts is None else torch.from_numpy(counts.astype(np.int64))
+    return synth.Workload(spec, kv, mu, sig, cnt)
+
+
+def test_bf16_special_symbols(oracle_mod):
+    rng = np.random.default_rng(3)
+    specials = np.array([0xFF80, 0x7F80, 0x0000, 0x8000, 0x7F7F, 0xFF7F, 0x0001, 0x8001, 0x3F80,
+                         0x0080, 0x807F], dtype=np.uint16)
+    n = 2 * 64 * 8
+    kv = rng.choice(specials, n).astype(np.uint16)
+    mu = rng.choice(np.array([0x3F80, 0x0000, 0xC2C8, 0x0001, 0x7F7F, 0xFF7F], np.uint16), n)
+    sigma = np.array([1e-30, 1e-8, 1.0, 1e30, 1.17549435e-38, 3.0, 0.5, 1e37] * 2)
+    counts = rng.integers(0, 50, 65536).astype(np.uint64)
+    _roundtrip(oracle_mod, _custom(synth.BF16, kv, mu, sigma, counts), ideal=False)
+
+
+def test_every_e4m3_symbol(oracle_mod):
+    rng = np.random.default_rng(4)
+    codes = np.array([u for u in range(256) if u not in (0x7F, 0xFF)], dtype=np.uint8)
+    kv = np.concatenate([rng.permutation(codes) for _ in range(8)])
+    for mu_v, s in [(0.0, 1.0), (300.0, 5.0), (-0.01, 1e-3), (40.0, 200.0), (-448.0, 0.5)]:
+        mu = torch.full((kv.size,), mu_v, dtype=torch.bfloat16).view(torch.int16).numpy()
+        sigma = np.full(16, s)
+        _roundtrip(oracle_mod, _custom(synth.E4M3, kv, mu.view(np.uint16), sigma))
+
+
+def test_repeat_calls_are_deterministic(oracle_mod):
+    w = synth.make(synth.WORKLOADS["qwen3-0.6b-bf16"].scaled(L=1, H=2, T=512, calib_draws=2))
+    codec = gpu_codec(w)
+    kv_d, mu_d = device_views(w)
+    a, na = codec.encode(kv_d, mu_d)
+    a = a[:na].clone()
+    b, nb = codec.encode(kv_d, mu_d)
+    assert na == nb and torch.equal(a, b[:nb])
+    t1 = codec.ideal_bits(kv_d, mu_d)
+    t2 = codec.ideal_bits(kv_d, mu_d)
+    assert t1 == t2
