@@ -31,7 +31,8 @@
  *       half-lines to -inf / +inf; +-inf have zero-width bins.
  *   R4  Phi is evaluated from a 8193-entry table T[i] = RNE(2^26 Phi(-8+i/512))
  *       by integer linear interpolation, with the fraction taken EXACTLY:
- *       i = floor(t), fr = floor(65536 (t - floor t)), t = 512 z.
+ *       i = floor(t), fr = floor(65536 (t - floor t)) in exact arithmetic,
+ *       t = 512 z.
  *   R5  z is fp32: d = lo - mu, z1 = d * (1/sigma), z3 = d * (1/(3 sigma)),
  *       each op rounded to nearest, no fused multiply-add.
  *   R6  mixture in integers: F100 = 95 Phi_q(z1) + 3 Phi_q(z3) + 2 E_q[r],
@@ -190,8 +191,11 @@ uint32_t or_phi_q(float z) {
   if (t >= 4096.0f) return PHI_ONE;
   float f = floorf(t);
   int i = (int)f + 4096;
-  double frac = (double)t - (double)f; /* exact in binary64 */
-  uint32_t fr = (uint32_t)floor(frac * 65536.0);
+  /* fr = floor(65536 (t - f)) exactly: 65536 f is an integer, so this is
+   * floor(65536 t) - 65536 f, and 65536 t is an exact binary32 scaling.
+   * (t - f evaluated in floating point rounds to 1 for tiny negative t.) */
+  int64_t fr64 = (int64_t)floorf(t * 65536.0f) - 65536 * (int64_t)f;
+  uint32_t fr = (uint32_t)fr64;
   uint32_t a = g_phi[i], b = g_phi[i + 1];
   return a + (uint32_t)(((uint64_t)(b - a) * fr) >> 16);
 }

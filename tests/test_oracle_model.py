@@ -60,8 +60,15 @@ def test_phi_q_monotone_and_exact_fraction(oracle_mod):
     # which only an exact fraction gives (fp32 t - floor(t) would round up to 1)
     T = O.phi_table().astype(np.int64)
     want = T[4095] + (((T[4096] - T[4095]) * 65535) >> 16)
-    assert O.phi_q(np.float32(-1e-12)) == want
+    for z in (-1e-12, -3.2e-19, -1e-20, -1e-30, -1e-38, -1e-45):
+        assert O.phi_q(np.float32(z)) == want, z
     assert O.phi_q(np.float32(-0.0)) == T[4096]
+    assert O.phi_q(np.float32(1e-45)) == T[4096]
+    # just below every knot: floor(65536 (t - floor t)) = 65535 with i one knot down
+    for i in (1, 100, 4000, 4096, 8000, 8191):
+        z = np.nextafter(np.float32((-4096 + i) / 512.0), np.float32(-np.inf))
+        want_i = T[i - 1] + (((T[i] - T[i - 1]) * 65535) >> 16)
+        assert O.phi_q(z) == want_i, i
 
 
 EXTREME_SIGMA = [1.1754944e-38, 1e-30, 1e-8, 1.0, 1e30, 1e37]
