@@ -153,6 +153,28 @@ int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void 
                    const uint16_t *mu, float *per_scalar, double *total, void *workspace,
                    size_t workspace_bytes, skv_stream_t stream);
 
+/* skv_ideal_bits without a caller workspace.  The paper has no counterpart:
+ * this entry point exists for callers that cannot allocate device memory, such
+ * as serving engines that reserve all free HBM for their KV-cache pool at
+ * start-up (a later cudaMalloc fails or forces cache eviction) and plugins
+ * running inside such an engine without access to its allocator.
+ *
+ * Same arguments, results and errors as skv_ideal_bits minus the workspace.
+ * Its scratch is a fixed 2 MiB device array inside libskv.so, held by every
+ * device that loads the library until the process exits; the call allocates
+ * nothing.  Shapes whose (layers * 2 * heads * head_dim) sigma entries exceed
+ * skv_ideal_bits_noalloc_max_channels() are rejected with SKV_ERR_CAPACITY.
+ * Every call shares that one array, so calls that may overlap on the GPU (on
+ * different streams, or from different host threads) race; serialise them.
+ * The first call on a device looks up the array's device address and uploads
+ * the model constants (synchronous copies): make it before any stream capture. */
+int skv_ideal_bits_noalloc(const skv_params *params, const skv_shape *shape, const void *kv,
+                           const uint16_t *mu, float *per_scalar, double *total,
+                           skv_stream_t stream);
+
+/* Largest number of sigma entries skv_ideal_bits_noalloc accepts. */
+size_t skv_ideal_bits_noalloc_max_channels(void);
+
 /* Host helper: p-hat tables from a calibration histogram.
  *   counts   host, u64[65536], occurrences of each bf16 bit pattern (NaN
  *            patterns are ignored).

@@ -21,7 +21,8 @@ SKV_ERR_PARAM, SKV_ERR_CORRUPT, SKV_ERR_CUDA = -4, -5, -6
 NSYM = {SKV_BF16: 65282, SKV_E4M3: 254}
 
 EXPORTS = ("skv_max_encoded_bytes", "skv_workspace_bytes", "skv_encode", "skv_decode",
-           "skv_ideal_bits", "skv_build_ecdf", "skv_phi_table", "skv_strerror", "skv_version")
+           "skv_ideal_bits", "skv_ideal_bits_noalloc", "skv_ideal_bits_noalloc_max_channels",
+           "skv_build_ecdf", "skv_phi_table", "skv_strerror", "skv_version")
 
 
 class SkvParams(C.Structure):
@@ -59,6 +60,8 @@ def lib():
             "skv_encode": (C.c_int, [P, S, vp, vp, vp, sz, C.POINTER(sz), vp, sz, vp]),
             "skv_decode": (C.c_int, [P, S, vp, sz, vp, vp, vp, sz, vp]),
             "skv_ideal_bits": (C.c_int, [P, S, vp, vp, vp, C.POINTER(C.c_double), vp, sz, vp]),
+            "skv_ideal_bits_noalloc": (C.c_int, [P, S, vp, vp, vp, C.POINTER(C.c_double), vp]),
+            "skv_ideal_bits_noalloc_max_channels": (sz, []),
             "skv_build_ecdf": (C.c_int, [vp, vp, vp]),
             "skv_phi_table": (C.c_int, [vp]),
             "skv_strerror": (C.c_char_p, [C.c_int]),
@@ -100,6 +103,18 @@ def skv_ideal_bits(params, shape, kv_ptr, mu_ptr, per_scalar_ptr, ws_ptr, ws_byt
     rc = lib().skv_ideal_bits(C.byref(params), C.byref(shape), kv_ptr, mu_ptr, per_scalar_ptr,
                               C.byref(tot), ws_ptr, ws_bytes, stream)
     return rc, tot.value
+
+
+def skv_ideal_bits_noalloc(params, shape, kv_ptr, mu_ptr, per_scalar_ptr, stream):
+    """Returns (status, total bits); scratch is the library's fixed device array."""
+    tot = C.c_double(0)
+    rc = lib().skv_ideal_bits_noalloc(C.byref(params), C.byref(shape), kv_ptr, mu_ptr,
+                                      per_scalar_ptr, C.byref(tot), stream)
+    return rc, tot.value
+
+
+def skv_ideal_bits_noalloc_max_channels() -> int:
+    return int(lib().skv_ideal_bits_noalloc_max_channels())
 
 
 def skv_build_ecdf(counts):

@@ -172,6 +172,30 @@ int common_inputs(const skv_params *p, const Plan &pl, const void *kv, const uin
   return SKV_OK;
 }
 
+// ---- scratch for skv_ideal_bits_noalloc ----
+// A fixed device array instead of a caller workspace.  Every device that loads
+// the library holds it until the process exits.  Layout: the 256-byte head,
+// the per-channel reciprocal table, then the per-block fp64 partial sums.
+constexpr size_t kNoallocBytes = 2u << 20;  // 2 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[1024];
+
+// Device address of g_noalloc_scratch for the current device.  In host code the
+// symbol's name is only a host-side stand-in, so it is looked up once per device.
+int noalloc_scratch(uint8_t **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 1024) return SKV_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return SKV_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = static_cast<uint8_t *>(g_noalloc_ptr[dev]);
+  return SKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -303,6 +327,51 @@ int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void 
   if ((rc = status_from_flags(h.flags))) return rc;
   *total = h.bits;
   return SKV_OK;
+}
+
+int skv_ideal_bits_noalloc(const skv_params *params, const skv_shape *shape, const void *kv,
+                           const uint16_t *mu, float *per_scalar, double *total,
+                           skv_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  if ((rc = common_inputs(params, pl, kv, mu))) return rc;
+  if (!total) return SKV_ERR_ARG;
+  if (per_scalar && !aligned(per_scalar, 16)) return SKV_ERR_ARG;
+  if (pl.dtype == SKV_BF16 && (!params->phat || !aligned(params->phat, 4))) return SKV_ERR_ARG;
+  // the same layout as the workspace of skv_ideal_bits, inside the fixed array
+  if (ws_bytes_for(pl, SKV_OP_IDEAL_BITS) > kNoallocBytes) return SKV_ERR_CAPACITY;
+  if ((rc = ensure_device_tables())) return rc;
+  uint8_t *ws = nullptr;
+  if ((rc = noalloc_scratch(&ws))) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  WsHead *head = reinterpret_cast<WsHead *>(ws);
+  // the array keeps the previous call's contents: the flags and sums start at zero
+  if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
+  float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
+  if (launch_prep(params->sigma, pl.nsig, nullptr, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
+  IdealLaunch a;
+  a.geo = pl.geo;
+  a.dtype = pl.dtype;
+  a.kv = kv;
+  a.mu = mu;
+  a.sigma = params->sigma;
+  a.phat = params->phat;
+  a.per_scalar = per_scalar;
+  a.partials = reinterpret_cast<double *>(ws + pl.off_bits);
+  a.nblocks = pl.bits_blocks;
+  a.head = head;
+  if (launch_ideal(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  WsHead h;
+  if ((rc = read_head(head, &h, st))) return rc;
+  if ((rc = status_from_flags(h.flags))) return rc;
+  *total = h.bits;
+  return SKV_OK;
+}
+
+size_t skv_ideal_bits_noalloc_max_channels(void) {
+  // head + reciprocal table + the largest partial-sum array (4096 blocks)
+  return (kNoallocBytes - 2 * kAlign - sizeof(double) * 4096) / sizeof(float2);
 }
 
 int skv_build_ecdf(const uint64_t *counts, uint32_t *ecdf, float *phat) {
