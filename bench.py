@@ -138,6 +138,59 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+# Algorithmic work per scalar, in thread-instructions (SURVEY's per-unit
+# figures for this path): one cum evaluation is about 50 (bf16: two Phi_q, one
+# E_q load, the integer mix) or 25 (e4m3); encode = 2 evaluations + the 64/32
+# divide + renormalisation = 200 / 130; decode's minimum = the 2 evaluations
+# that verify the symbol + the state update, the stream read and the store =
+# 120 / 70; ideal bits = two Gaussian bin masses, the p-hat term and a 3-term
+# log-sum-exp = 100 (bf16), one bin mass = 50 (e4m3).
+ALG_OPS = {2: {"encode": 200, "decode": 120, "ideal_bits": 100},
+           1: {"encode": 130, "decode": 70, "ideal_bits": 50}}
+KERNEL = {"encode": "k_encode", "decode": "k_decode", "ideal_bits": "k_ideal"}
+
+
+def issue_peak_gops():
+    """Thread-instruction issue peak: SMs x 4 schedulers x 32 lanes x max SM clock."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = 2070.0
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    return sms * 128 * mhz * 1e6 / 1e9, sms, mhz
+
+
+def roofline(med_ms, n, container_bytes, bps, workload):
+    """ALU roofline of the dominant kernel (and of each kernel), plus its HBM view."""
+    peak_ops, sms, mhz = issue_peak_gops()
+    hbm_peak, peak_kind = measured_peaks()
+    cb = container_bytes / n
+    alg_bytes = {"encode": bps + 2 + cb, "decode": cb + 2 + bps, "ideal_bits": bps + 2}
+    kernels = {}
+    for op, ms in med_ms.items():
+        ops = ALG_OPS[bps][op] * n / (ms * 1e-3) / 1e9
+        gbs = alg_bytes[op] * n / (ms * 1e-3) / 1e9
+        kernels[op] = {"kernel": KERNEL[op], "ms": round(ms, 4),
+                       "alu_frac": round(ops / peak_ops, 4),
+                       "hbm_frac": round(gbs / hbm_peak, 4)}
+    top = max(med_ms, key=med_ms.get)
+    ms = med_ms[top]
+    achieved = ALG_OPS[bps][top] * n / (ms * 1e-3) / 1e9
+    gbs = alg_bytes[top] * n / (ms * 1e-3) / 1e9
+    roof = {"bound": "alu", "kernel": KERNEL[top], "achieved": round(achieved, 1),
+            "peak": round(peak_ops, 1), "unit": "Gop/s", "frac": round(achieved / peak_ops, 4),
+            "traffic": load_traffic(KERNEL[top], workload),
+            "ops_per_scalar": ALG_OPS[bps][top],
+            "peak_source": "%d SMs x 128 lanes x %.0f MHz (issue peak)" % (sms, mhz),
+            "hbm": {"achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                    "frac": round(gbs / hbm_peak, 4),
+                    "algorithmic_bytes_per_scalar": round(alg_bytes[top], 4),
+                    "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_kind}}
+    return roof, kernels
+
+
 def load_traffic(kernel: str, workload: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
     was taken on the current kernel source (else None)."""
@@ -229,7 +282,10 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     P.build()
 
-    w = synth.make(args.workload, device=dev, seed=rank_seed(rank))
+    spec = synth.WORKLOADS[args.workload]
+    if args.lanes or args.token_block:
+        spec = spec.scaled(G=args.lanes or spec.G, Tb=args.token_block or spec.Tb)
+    w = synth.make(spec, device=dev, seed=rank_seed(rank))
     s = w.spec
     bps = 2 if s.dtype == synth.BF16 else 1
     ecdf = phat = None
@@ -237,7 +293,8 @@ def run_gpu(args):
         E, ph = P.skv_build_ecdf(w.counts.cpu().numpy().astype(np.uint64))
         ecdf = torch.from_numpy(E.view(np.int32)).to(dev)
         phat = torch.from_numpy(ph).to(dev)
-    codec = P.Codec(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, w.sigma.to(dev), ecdf, phat)
+    codec = P.Codec(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, w.sigma.to(dev), ecdf, phat,
+                    flags=P.SKV_FLAG_DECODE_BISECT if args.decode_bisect else 0)
     kv = (w.kv.view(torch.int16) if s.dtype == synth.BF16 else w.kv).reshape(-1)
     mu = w.mu.view(torch.int16).reshape(-1)
     n = s.n
@@ -326,24 +383,14 @@ def run_gpu(args):
     med = {"encode": statistics.median(t_enc), "decode": statistics.median(t_dec),
            "ideal_bits": statistics.median(t_bits)}
     top = max(med, key=med.get)
-    cb = nb / n  # container bytes per scalar
-    alg = {"encode": bps + 2 + cb, "decode": cb + 2 + bps, "ideal_bits": bps + 2}
-    peak, peak_kind = measured_peaks()
-    achieved = alg[top] * n / (med[top] * 1e-3) / 1e9
-    kname = {"encode": "k_encode", "decode": "k_decode", "ideal_bits": "k_ideal"}[top]
-    roof = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
-            "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": load_traffic(kname, args.workload),
-            "algorithmic_bytes_per_scalar": round(alg[top], 4),
-            "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-            else "fallback 6.8 TB/s"}
+    roof, kernels = roofline(med, n, nb, bps, args.workload)
 
     # ---- oracle on the host cores, bounded sample ----
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         import oracle as O
         kvn, mun, sig, cnt = synth.to_numpy(w)
-        m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sig, counts=cnt)
+        m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sig, counts=cnt)  # same chunking
         nch = m.num_chunks()
         sc, dt, chunks = time_oracle(O, m, kvn.reshape(-1), mun.reshape(-1), nch,
                                      args.cpu_sample_chunks)
@@ -371,6 +418,7 @@ def run_gpu(args):
         "ideal_bits_per_scalar": round(bits / n, 5),
         "overhead_pct": round(100.0 * (8.0 * nb / bits - 1.0), 3),
         "roofline": roof,
+        "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * raw / e2e_s / 1e9, 3), "unit": "GB/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
@@ -428,13 +476,17 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["skv", "reference"], default="skv")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--cpu-sample-chunks", type=int, default=384)
     ap.add_argument("--ref-chunks-per-step", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lanes", type=int, default=0, help="override the workload's lanes per chunk")
+    ap.add_argument("--token-block", type=int, default=0, help="override the token block")
+    ap.add_argument("--decode-bisect", action="store_true",
+                    help="decode with the reference bisection search")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "skv":
         args.warmup = 3

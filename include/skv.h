@@ -81,6 +81,7 @@ typedef struct {
  *   dtype        SKV_BF16 or SKV_E4M3.
  *   token_block  tokens per chunk (Tb >= 1); chunk = Tb * head_dim scalars.
  *   lanes        rANS lanes per chunk, G in {1, 2, 4, 8, 16, 32}.
+ *   flags        SKV_FLAG_* bits; 0 for the default behaviour.
  *   sigma        device, fp32 [layers][2][heads][head_dim]; per (layer, kv,
  *                head, channel) standard deviation of the narrow component.
  *   ecdf         device, bf16 only: u32 E_q[0..65282], E_q[r] =
@@ -90,11 +91,15 @@ typedef struct {
  *                smoothed empirical probability (count + 1) / S_tot.  Read by
  *                skv_ideal_bits only; NULL is allowed for encode and decode.
  */
+/* skv_params.flags bits (all others must be 0). */
+#define SKV_FLAG_DECODE_BISECT 1 /* decode by plain bisection over ranks (reference
+                                    search; the output is identical, only slower) */
+
 typedef struct {
   int32_t dtype;
   int32_t token_block;
   int32_t lanes;
-  int32_t reserved; /* must be 0 */
+  int32_t flags;    /* SKV_FLAG_* bits */
   const float *sigma;
   const uint32_t *ecdf;
   const float *phat;

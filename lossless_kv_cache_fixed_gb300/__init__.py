@@ -16,6 +16,7 @@ from .build import LIB, build  # noqa: F401
 
 SKV_BF16, SKV_E4M3 = 0, 1
 SKV_OP_ENCODE, SKV_OP_DECODE, SKV_OP_IDEAL_BITS = 0, 1, 2
+SKV_FLAG_DECODE_BISECT = 1
 SKV_OK, SKV_ERR_ARG, SKV_ERR_CAPACITY, SKV_ERR_SYMBOL = 0, -1, -2, -3
 SKV_ERR_PARAM, SKV_ERR_CORRUPT, SKV_ERR_CUDA = -4, -5, -6
 NSYM = {SKV_BF16: 65282, SKV_E4M3: 254}
@@ -27,7 +28,7 @@ EXPORTS = ("skv_max_encoded_bytes", "skv_workspace_bytes", "skv_encode", "skv_de
 
 class SkvParams(C.Structure):
     _fields_ = [("dtype", C.c_int32), ("token_block", C.c_int32), ("lanes", C.c_int32),
-                ("reserved", C.c_int32), ("sigma", C.c_void_p), ("ecdf", C.c_void_p),
+                ("flags", C.c_int32), ("sigma", C.c_void_p), ("ecdf", C.c_void_p),
                 ("phat", C.c_void_p)]
 
 
@@ -163,11 +164,12 @@ class Codec:
     (bf16); phat: float32 [65282] (bf16, ideal bits only).
     """
 
-    def __init__(self, dtype, L, H, T, D, token_block, lanes, sigma, ecdf=None, phat=None):
+    def __init__(self, dtype, L, H, T, D, token_block, lanes, sigma, ecdf=None, phat=None,
+                 flags=0):
         import torch
         self.dtype = dtype
         self.sigma, self.ecdf, self.phat = sigma.contiguous(), ecdf, phat
-        self.params = SkvParams(dtype, token_block, lanes, 0, self.sigma.data_ptr(),
+        self.params = SkvParams(dtype, token_block, lanes, flags, self.sigma.data_ptr(),
                                 ecdf.data_ptr() if ecdf is not None else None,
                                 phat.data_ptr() if phat is not None else None)
         self.shape = SkvShape(L, 2, H, T, D)

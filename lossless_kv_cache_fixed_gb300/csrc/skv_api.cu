@@ -26,6 +26,7 @@ inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 uint32_t g_phi_host[kPhiKnots];
 float g_lo8_host[256];
+float g_hinv_host[2][kHinvN + 1];
 std::once_flag g_const_once;
 
 double e4m3_value_host(uint32_t u) {
@@ -53,6 +54,23 @@ void build_constants() {
                                    e4m3_value_host(e4m3_bits_host(r))));
   g_lo8_host[kNsymE4m3] = INFINITY;
   g_lo8_host[255] = INFINITY;
+  // Inverse of the Gaussian part of the model CDF (the decoder's first guess;
+  // any error here costs search steps, never correctness).
+  auto Phi = [](double z) { return 0.5 * std::erfc(-z / std::sqrt(2.0)); };
+  for (int t = 0; t < 2; ++t) {
+    const double umax = t == 0 ? kHinvUmaxBf16 : kHinvUmaxE4m3;
+    for (int k = 0; k <= kHinvN; ++k) {
+      const double u = umax * k / kHinvN;
+      double a = -40.0, b = 40.0;
+      for (int it = 0; it < 100; ++it) {
+        const double m = 0.5 * (a + b);
+        const double g = t == 0 ? 0.95 * Phi(m) + 0.03 * Phi(m / 3.0) : Phi(m);
+        (g < u ? a : b) = m;
+      }
+      const double z = 0.5 * (a + b);
+      g_hinv_host[t][k] = (float)(z < -14.0 ? -14.0 : (z > 14.0 ? 14.0 : z));
+    }
+  }
 }
 
 std::mutex g_dev_mu;
@@ -65,7 +83,8 @@ int ensure_device_tables() {
   if (dev < 0 || dev >= 1024) return SKV_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   if (!g_dev_ready[dev]) {
-    if (upload_tables(g_phi_host, g_lo8_host) != cudaSuccess) return SKV_ERR_CUDA;
+    if (upload_tables(g_phi_host, g_lo8_host, g_hinv_host[0], g_hinv_host[1]) != cudaSuccess)
+      return SKV_ERR_CUDA;
     g_dev_ready[dev] = true;
   }
   return SKV_OK;
@@ -76,7 +95,7 @@ struct Plan {
   int dtype;
   int64_t nsig;
   // workspace layout (byte offsets)
-  size_t off_inv, off_sizes, off_starts, off_partials, off_scratch, off_bits, total;
+  size_t off_inv, off_sizes, off_starts, off_partials, off_scratch, off_bits, off_einv, total;
   int64_t stride;  // words per chunk stack
   int bits_blocks;
 };
@@ -86,7 +105,7 @@ bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   if (!p || !s || !out) return SKV_ERR_ARG;
   if (p->dtype != SKV_BF16 && p->dtype != SKV_E4M3) return SKV_ERR_ARG;
-  if (p->reserved != 0) return SKV_ERR_ARG;
+  if (p->flags & ~SKV_FLAG_DECODE_BISECT) return SKV_ERR_ARG;
   if (s->kv != 2 || s->layers <= 0 || s->heads <= 0 || s->tokens <= 0 || s->head_dim <= 0)
     return SKV_ERR_ARG;
   if (s->head_dim % 8) return SKV_ERR_ARG;
@@ -134,13 +153,14 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   int64_t nb = (n8 + 255) / 256;
   pl.bits_blocks = (int)(nb < 4096 ? (nb > 0 ? nb : 1) : 4096);
   pl.off_bits = align_up(pl.off_inv + sizeof(float2) * (size_t)pl.nsig);
+  pl.off_einv = pl.off_bits;  // decode only: the inverse p-hat table follows the reciprocals
   *out = pl;
   return SKV_OK;
 }
 
 size_t ws_bytes_for(const Plan &pl, int op) {
   if (op == SKV_OP_ENCODE) return pl.total;
-  if (op == SKV_OP_DECODE) return pl.off_sizes;
+  if (op == SKV_OP_DECODE) return align_up(pl.off_einv + sizeof(int32_t) * (kHinvN + 1));
   return align_up(pl.off_bits + sizeof(double) * (size_t)pl.bits_blocks);
 }
 
@@ -285,6 +305,13 @@ int skv_decode(const skv_params *params, const skv_shape *shape, const void *in,
   a.kv_out = kv_out;
   a.head = head;
   a.hash_words = hash_words(pl);
+  a.bisect = (params->flags & SKV_FLAG_DECODE_BISECT) ? 1 : 0;
+  a.einv = nullptr;
+  if (pl.dtype == SKV_BF16) {
+    int32_t *einv = reinterpret_cast<int32_t *>(ws + pl.off_einv);
+    if (launch_einv(ecdf, einv, st) != cudaSuccess) return SKV_ERR_CUDA;
+    a.einv = einv;
+  }
   if (launch_decode(a, st) != cudaSuccess) return SKV_ERR_CUDA;
   WsHead h;
   if ((rc = read_head(head, &h, st))) return rc;

@@ -8,11 +8,11 @@
 // "原生 FP8 KV 缓存" the bin-integrated N(mu, sigma^2) for e4m3.
 //
 // Evaluated in fp32 in the log domain so that nothing underflows:
-//   * narrow bins (width w and centre zm in sigma units with w max(1,|zm|) <
-//     0.05): the midpoint rule with its second-order term;
+//   * bins narrow against sigma (width w and centre zm in sigma units with
+//     w max(1,|zm|) < 0.5): the midpoint rule with Hermite corrections;
 //   * otherwise the tail mass on the far side of mu via the scaled
 //     complementary error function, log Q(z) = log(erfcx(z/sqrt2)/2) - z^2/2;
-//   * the mixture by log-sum-exp.
+//   * the mixture by log-sum-exp in base 2.
 // Per-thread sums, then a fixed-order block tree and a fixed-order final sum,
 // all in fp64: the total does not depend on scheduling.
 #include <cuda_runtime.h>
@@ -29,38 +29,85 @@ __device__ __forceinline__ float log_upper_tail(float z) {
   return logf(0.5f * erfcxf(z * 0.70710678f)) - 0.5f * z * z;
 }
 
-// log of the N(mu, s^2) mass on [lo, hi); inv_s = 1/s, log_s = log s.
-__device__ float log_gauss_bin(float lo, float hi, float mu, float inv_s, float log_s) {
+constexpr float kLog2e = 1.44269504f;
+constexpr float kLog2Sqrt2Pi = 1.32574806f;  // log2 sqrt(2 pi)
+
+// The mass on the far side of mu in the natural-log domain, for wide bins and
+// outliers; kept out of line so that the common path stays small.
+__device__ __noinline__ float log2_gauss_tail(float lo, float hi, float mu, float inv_s) {
+  const float za = (lo - mu) * inv_s, zb = (hi - mu) * inv_s;
+  float ln;
+  if (za >= 0.0f) {
+    const float a = log_upper_tail(za), b = log_upper_tail(zb);
+    ln = a + logf(-expm1f(b - a));
+  } else if (zb <= 0.0f) {
+    const float a = log_upper_tail(-zb), b = log_upper_tail(-za);
+    ln = a + logf(-expm1f(b - a));
+  } else {
+    const float qa = isfinite(za) ? 0.5f * erfcf(-za * 0.70710678f) : 0.0f;
+    const float qb = isfinite(zb) ? 0.5f * erfcf(zb * 0.70710678f) : 0.0f;
+    ln = log1pf(-(qa + qb));
+  }
+  return ln * kLog2e;
+}
+
+// The common case of log2_gauss_bin alone: sets ok = false (and returns 0)
+// when the bin needs the tail evaluation.
+__device__ __forceinline__ float log2_gauss_series(float lo, float hi, float mu, float inv_s,
+                                                   float log2_s, bool &ok) {
+  ok = true;
+  if (!(hi > lo)) return -INFINITY;
+  if (isfinite(lo) && isfinite(hi)) {
+    const float width = hi - lo;
+    const float w = width * inv_s;
+    const float zm = (lo + 0.5f * width - mu) * inv_s;
+    if (w * fmaxf(1.0f, fabsf(zm)) < 0.5f) {
+      const float z2 = zm * zm, w2 = w * w;
+      const float he2 = z2 - 1.0f, he4 = fmaf(z2, z2 - 6.0f, 3.0f);
+      const float he6 = fmaf(z2, fmaf(z2, z2 - 15.0f, 45.0f), -15.0f);
+      const float y = w2 * fmaf(w2, fmaf(w2, he6 * (1.0f / 322560.0f), he4 * (1.0f / 1920.0f)),
+                                he2 * (1.0f / 24.0f));
+      const float l1p = y * fmaf(y, fmaf(y, 1.0f / 3.0f, -0.5f), 1.0f);
+      return fmaf(-0.5f * kLog2e, z2, -kLog2Sqrt2Pi) + (log2f(width) - log2_s) + l1p * kLog2e;
+    }
+  }
+  ok = false;
+  return 0.0f;
+}
+
+// log2 of the N(mu, s^2) mass on [lo, hi); inv_s = 1/s, log2_s = log2 s.
+//  * w max(1, |zm|) < 0.5 (w = width/s, zm = centre in sigma units): the
+//    mass is w phi(zm) (1 + He2 w^2/24 + He4 w^4/1920 + He6 w^6/322560),
+//    He_n the probabilists' Hermite polynomials; the next term is below
+//    4e-6 relative there.
+//  * otherwise the tail on the far side of mu, in the natural-log domain.
+__device__ float log2_gauss_bin(float lo, float hi, float mu, float inv_s, float log2_s) {
   if (!(hi > lo)) return -INFINITY;
   if (isfinite(lo) && isfinite(hi)) {
     const float width = hi - lo;  // neighbouring midpoints: exact
     const float w = width * inv_s;
     const float zm = (lo + 0.5f * width - mu) * inv_s;
-    if (w * fmaxf(1.0f, fabsf(zm)) < 0.05f) {
-      return -0.5f * zm * zm - 0.91893853f + (logf(width) - log_s) +
-             log1pf((zm * zm - 1.0f) * w * w * (1.0f / 24.0f));
+    if (w * fmaxf(1.0f, fabsf(zm)) < 0.5f) {
+      const float z2 = zm * zm, w2 = w * w;
+      const float he2 = z2 - 1.0f, he4 = fmaf(z2, z2 - 6.0f, 3.0f);
+      const float he6 = fmaf(z2, fmaf(z2, z2 - 15.0f, 45.0f), -15.0f);
+      const float y = w2 * fmaf(w2, fmaf(w2, he6 * (1.0f / 322560.0f), he4 * (1.0f / 1920.0f)),
+                                he2 * (1.0f / 24.0f));
+      const float l1p = y * fmaf(y, fmaf(y, 1.0f / 3.0f, -0.5f), 1.0f);  // log(1 + y), |y| < 0.02
+      return fmaf(-0.5f * kLog2e, z2, -kLog2Sqrt2Pi) + (log2f(width) - log2_s) + l1p * kLog2e;
     }
   }
-  const float za = (lo - mu) * inv_s, zb = (hi - mu) * inv_s;
-  if (za >= 0.0f) {
-    const float a = log_upper_tail(za), b = log_upper_tail(zb);
-    return a + logf(-expm1f(b - a));
-  }
-  if (zb <= 0.0f) {
-    const float a = log_upper_tail(-zb), b = log_upper_tail(-za);
-    return a + logf(-expm1f(b - a));
-  }
-  const float qa = isfinite(za) ? 0.5f * erfcf(-za * 0.70710678f) : 0.0f;
-  const float qb = isfinite(zb) ? 0.5f * erfcf(zb * 0.70710678f) : 0.0f;
-  return log1pf(-(qa + qb));
+  return log2_gauss_tail(lo, hi, mu, inv_s);
 }
 
 __device__ __forceinline__ float lo_e4m3_value(int32_t r);
 
-template <int DT>
+// -log2 q of one scalar.  FULL = false evaluates only the common (series)
+// case and sets `deferred` when the scalar needs the tail evaluation.
+template <int DT, bool FULL>
 __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float sigma,
-                                           const float *phat, const float *lo8,
-                                           uint32_t &flags) {
+                                           const float *phat, const float *lo8, uint32_t &flags,
+                                           bool &deferred) {
   const int32_t NS = DT == 0 ? kNsymBf16 : kNsymE4m3;
   int32_t r = DT == 0 ? rank_bf16(sym) : rank_e4m3(sym);
   if (r < 0 || r >= NS) {
@@ -75,23 +122,49 @@ __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float
   const float lo = DT == 0 ? lo_bf16(r) : lo8[r];
   const float hi = DT == 0 ? lo_bf16(r + 1) : lo8[r + 1];
   const float inv_s = 1.0f / sigma;
-  const float log_s = logf(sigma);
-  const float l1 = log_gauss_bin(lo, hi, mu, inv_s, log_s);
-  if (DT == 1) return -l1 * 1.44269504f;
-  const float a = -0.05129329f + l1;                                            // log 0.95
-  const float b = -3.5065579f + log_gauss_bin(lo, hi, mu, inv_s * (1.0f / 3.0f),
-                                              log_s + 1.0986123f);             // log 0.03
-  const float c = -3.912023f + logf(phat[r]);                                   // log 0.02
+  const float log2_s = log2f(sigma);
+  float l1, l3 = 0.0f;
+  if (FULL) {
+    l1 = log2_gauss_bin(lo, hi, mu, inv_s, log2_s);
+    if (DT == 0) l3 = log2_gauss_bin(lo, hi, mu, inv_s * (1.0f / 3.0f), log2_s + 1.5849625f);
+  } else {
+    bool ok1 = true, ok3 = true;
+    l1 = log2_gauss_series(lo, hi, mu, inv_s, log2_s, ok1);
+    if (DT == 0) l3 = log2_gauss_series(lo, hi, mu, inv_s * (1.0f / 3.0f), log2_s + 1.5849625f, ok3);
+    if (!ok1 || !ok3) {
+      deferred = true;
+      return 0.0f;
+    }
+  }
+  if (DT == 1) return -l1;
+  const float a = -0.07400058f + l1;  // log2 0.95
+  const float b = -5.0588937f + l3;   // log2 0.03 (the wide component: sigma * 3)
+  const float c = -5.6438562f + log2f(phat[r]);                               // log2 0.02
   const float m = fmaxf(a, fmaxf(b, c));
   if (m == -INFINITY) return INFINITY;
-  const float lse = m + logf(expf(a - m) + expf(b - m) + expf(c - m));
-  return -lse * 1.44269504f;
+  return -(m + log2f(exp2f(a - m) + exp2f(b - m) + exp2f(c - m)));
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t sym_at(uint4 kv4, int k) {
+  if (DT == 0) {
+    const uint32_t w = k < 2 ? kv4.x : (k < 4 ? kv4.y : (k < 6 ? kv4.z : kv4.w));
+    return (w >> (16 * (k & 1))) & 0xFFFFu;
+  }
+  const uint32_t w = k < 4 ? kv4.x : kv4.y;
+  return (w >> (8 * (k & 3))) & 0xFFu;
+}
+
+__device__ __forceinline__ uint32_t mu_at(uint4 mu4, int k) {
+  const uint32_t w = k < 2 ? mu4.x : (k < 4 ? mu4.y : (k < 6 ? mu4.z : mu4.w));
+  return (w >> (16 * (k & 1))) & 0xFFFFu;
 }
 
 template <int DT>
 __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
   __shared__ float s_lo8[256];
   __shared__ double s_part[256];
+  __shared__ float s_bits[8 * 256];
   if (DT == 1) {
     // e4m3 bin edges: midpoints of neighbouring values, +-inf at the ends
     for (int r = threadIdx.x; r < 255; r += blockDim.x) {
@@ -108,34 +181,58 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
   const int64_t n8 = a.geo.n / 8;
   uint32_t flags = 0;
   double acc = 0.0;
-  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n8;
-       g += (int64_t)gridDim.x * blockDim.x) {
-    const uint64_t i0 = (uint64_t)g * 8;
+  // The loop runs the same number of times for every lane of a warp (lanes past
+  // the end are switched off), because the deferred-lane drain below votes
+  // across the whole warp.
+  const int lane = threadIdx.x & 31;
+  for (int64_t gw = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); gw < n8;
+       gw += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t g = gw + lane;
+    const bool act = g < n8;
+    const uint64_t i0 = act ? (uint64_t)g * 8 : 0;
     const uint64_t srow = (i0 / TD) * D + (uint32_t)(i0 % D);
-    uint32_t sym[8], mub[8];
-    if (DT == 0) {
-      uint4 v = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.kv) + i0));
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sym[k] = (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
-    } else {
-      uint2 v = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint8_t *>(a.kv) + i0));
-      uint32_t w[2] = {v.x, v.y};
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sym[k] = (w[k >> 2] >> (8 * (k & 3))) & 0xFFu;
+    uint4 kv4 = make_uint4(0, 0, 0, 0), mu4 = make_uint4(0, 0, 0, 0);
+    if (act) {
+      if (DT == 0) {
+        kv4 = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.kv) + i0));
+      } else {
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint8_t *>(a.kv) + i0));
+        kv4.x = v.x;
+        kv4.y = v.y;
+      }
+      mu4 = __ldg(reinterpret_cast<const uint4 *>(a.mu + i0));
     }
-    {
-      uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.mu + i0));
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mub[k] = (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+    // pass 1: the common case for all 8 scalars; scalars that need the tail
+    // evaluation are deferred and then drained together, so that a warp pays
+    // for the tail code once per few deferred lanes instead of once per scalar
+    uint32_t pend = 0;
+#pragma unroll 1
+    for (int k = 0; k < 8 && act; ++k) {
+      bool deferred = false;
+      const float b = ideal_one<DT, false>(sym_at<DT>(kv4, k), mu_at(mu4, k),
+                                           __ldg(a.sigma + srow + k), a.phat, s_lo8, flags,
+                                           deferred);
+      if (deferred) pend |= 1u << k;
+      s_bits[k * 256 + threadIdx.x] = b;
     }
-    float bits[8];
+    while (__any_sync(0xFFFFFFFFu, pend != 0)) {
+      if (pend) {
+        const int k = __ffs(pend) - 1;
+        pend &= pend - 1;
+        bool unused = false;
+        s_bits[k * 256 + threadIdx.x] =
+            ideal_one<DT, true>(sym_at<DT>(kv4, k), mu_at(mu4, k), __ldg(a.sigma + srow + k),
+                                a.phat, s_lo8, flags, unused);
+      }
+    }
+    if (!act) continue;
+    float bits[8], part = 0.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      bits[k] = ideal_one<DT>(sym[k], mub[k], __ldg(a.sigma + srow + k), a.phat, s_lo8, flags);
-      acc += (double)bits[k];
+      bits[k] = s_bits[k * 256 + threadIdx.x];
+      part += bits[k];
     }
+    acc += (double)part;
     if (a.per_scalar) {
       float4 *o = reinterpret_cast<float4 *>(a.per_scalar + i0);
       o[0] = make_float4(bits[0], bits[1], bits[2], bits[3]);
@@ -160,11 +257,19 @@ __device__ __forceinline__ float lo_e4m3_value(int32_t r) {
   return (u & 0x80u) ? -v : v;
 }
 
-__global__ void k_ideal_final(const double *partials, int nb, WsHead *head) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  double s = 0.0;
-  for (int i = 0; i < nb; ++i) s += partials[i];
-  head->bits = s;
+// Sum of the block partials, in a fixed order: a strided pass per thread,
+// then a tree.
+__global__ void __launch_bounds__(1024) k_ideal_final(const double *partials, int nb, WsHead *head) {
+  __shared__ double s_sum[1024];
+  double v = 0.0;
+  for (int i = threadIdx.x; i < nb; i += 1024) v += partials[i];
+  s_sum[threadIdx.x] = v;
+  __syncthreads();
+  for (int off = 512; off; off >>= 1) {
+    if (threadIdx.x < off) s_sum[threadIdx.x] += s_sum[threadIdx.x + off];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) head->bits = s_sum[0];
 }
 
 cudaError_t launch_ideal(const IdealLaunch &a, cudaStream_t s) {
@@ -172,7 +277,7 @@ cudaError_t launch_ideal(const IdealLaunch &a, cudaStream_t s) {
   else k_ideal<1><<<a.nblocks, 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k_ideal_final<<<1, 32, 0, s>>>(a.partials, a.nblocks, a.head);
+  k_ideal_final<<<1, 1024, 0, s>>>(a.partials, a.nblocks, a.head);
   return cudaGetLastError();
 }
 

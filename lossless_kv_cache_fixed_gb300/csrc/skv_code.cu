@@ -11,8 +11,11 @@
 // lanes emit or consume renormalisation words inside a round comes from one
 // ballot plus a prefix popcount.  A lane's symbols are 8-scalar groups, so KV
 // and mu move as 16-byte vectors (8-byte for e4m3 KV).  Warps loop over 32-lane
-// tasks; the grid is a whole number of blocks per SM.  The Phi knot table
-// (64 KiB) and the e4m3 bin edges sit in shared memory.
+// tasks; the grid has at most one 768-thread block per SM.  The Phi knot
+// table (64 KiB), the e4m3 bin edges and the decoder's guess table sit in
+// shared memory, once per SM.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "skv_internal.h"
@@ -22,11 +25,17 @@ namespace skv {
 
 __device__ uint2 g_phi[kPhiKnots];
 __device__ float g_lo8[256];
+__device__ float2 g_hinv[2][kHinvN + 1];
 
-constexpr int kCodeThreads = 128;
+// One resident block per SM with 24 warps: a single copy of the tables per SM
+// leaves the rest of the unified L1 / shared memory to the L1 cache (the p-hat
+// prefix table, mu, the streams).
+constexpr int kCodeThreads = 768;
 constexpr size_t kCodeSmem = sizeof(uint2) * kPhiKnots + sizeof(float) * 256;
+constexpr int kDecThreads = 768;
+constexpr size_t kDecSmem = kCodeSmem + sizeof(float2) * (kHinvN + 1) + sizeof(int32_t) * (kHinvN + 1);
 
-cudaError_t upload_tables(const uint32_t *T, const float *lo8) {
+cudaError_t upload_tables(const uint32_t *T, const float *lo8, const float *hb, const float *he) {
   uint2 pairs[kPhiKnots];
   for (int i = 0; i < kPhiKnots; ++i) {
     pairs[i].x = T[i];
@@ -34,7 +43,14 @@ cudaError_t upload_tables(const uint32_t *T, const float *lo8) {
   }
   cudaError_t e = cudaMemcpyToSymbol(g_phi, pairs, sizeof(pairs));
   if (e != cudaSuccess) return e;
-  return cudaMemcpyToSymbol(g_lo8, lo8, sizeof(float) * 256);
+  if ((e = cudaMemcpyToSymbol(g_lo8, lo8, sizeof(float) * 256)) != cudaSuccess) return e;
+  float2 h[2][kHinvN + 1];
+  for (int t = 0; t < 2; ++t)
+    for (int k = 0; k <= kHinvN; ++k) {
+      const float *src = t == 0 ? hb : he;
+      h[t][k] = make_float2(src[k], k < kHinvN ? src[k + 1] - src[k] : 0.0f);
+    }
+  return cudaMemcpyToSymbol(g_hinv, h, sizeof(h));
 }
 
 int device_sm_count() {
@@ -164,12 +180,32 @@ cudaError_t launch_prep(const float *sigma, int64_t nsig, const uint32_t *ecdf, 
   return cudaGetLastError();
 }
 
+// Inverse of the p-hat prefix table for the decoder's guess in the tails that
+// only the p-hat component reaches (a guess only: any error costs search steps).
+__global__ void k_einv(const uint32_t *__restrict__ ecdf, int32_t *__restrict__ einv) {
+  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  if (k > kHinvN) return;
+  const uint32_t target = (uint32_t)(((uint64_t)k << 26) / kHinvN);
+  int32_t lo = 0, hi = kNsymBf16;  // smallest r in [0, 65282] with ecdf[r] >= target
+  while (lo < hi) {
+    const int32_t mid = (lo + hi) >> 1;
+    if (ecdf[mid] >= target) hi = mid;
+    else lo = mid + 1;
+  }
+  einv[k] = lo;
+}
+
+cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, cudaStream_t s) {
+  k_einv<<<(kHinvN + 1 + 255) / 256, 256, 0, s>>>(ecdf, einv);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------------
 // Encode: one thread per lane, rounds descending, lanes descending.
 // ------------------------------------------------------------------------
 
 template <int DT>
-__global__ void __launch_bounds__(kCodeThreads) k_encode(EncodeLaunch a) {
+__global__ void __launch_bounds__(kCodeThreads, 1) k_encode(EncodeLaunch a) {
   extern __shared__ uint2 s_phi[];
   float *s_lo8 = reinterpret_cast<float *>(s_phi + kPhiKnots);
   stage_tables(s_phi, s_lo8);
@@ -237,8 +273,9 @@ __global__ void __launch_bounds__(kCodeThreads) k_encode(EncodeLaunch a) {
         }
         sp -= n;
         if (has) {
-          const uint64_t q = x / f;
-          x = (q << M) + (x - q * f) + cst;
+          uint64_t rem;
+          const uint64_t q = divmod_u64<M>(x, f, rem);
+          x = (q << M) + rem + cst;
         }
       }
     }
@@ -382,10 +419,10 @@ __global__ void __launch_bounds__(256) k_compact(EncodeLaunch a) {
 }
 
 static int code_blocks(int64_t ntasks) {
-  // whole blocks per SM: 3 blocks of 4 warps fit next to the 66 KiB table
+  // at most one block per SM (see kCodeThreads)
   const int64_t warps_per_block = kCodeThreads / 32;
   int64_t want = (ntasks + warps_per_block - 1) / warps_per_block;
-  int64_t cap = (int64_t)device_sm_count() * 3;
+  int64_t cap = (int64_t)device_sm_count();
   return (int)(want < cap ? want : cap);
 }
 
@@ -440,15 +477,75 @@ __global__ void k_check_header(DecodeLaunch a) {
   if (!ok) atomicOr(&a.head->flags, kFlagCorrupt);
 }
 
+// One symbol's search state: the answer r satisfies lo <= r < hi, with
+// clo = cum(lo) <= slot < chi = cum(hi); done when hi = lo + 1.
+struct Bracket {
+  int32_t lo, hi;
+  uint32_t clo, chi;
+};
+
+// Narrows the bracket with cum(r) = c (never widens it).
+__device__ __forceinline__ void bracket_add(Bracket &b, int32_t r, uint32_t c, uint32_t slot) {
+  if (c <= slot) {
+    if (r > b.lo) {
+      b.lo = r;
+      b.clo = c;
+    }
+  } else if (r < b.hi) {
+    b.hi = r;
+    b.chi = c;
+  }
+}
+
+__device__ __forceinline__ float lo_value(int DT, int32_t r, const float *lo8) {
+  return DT == 0 ? lo_bf16(r) : lo8[r];
+}
+
+// Rank of the symbol an fp32 value rounds to (the decoder's guesses only).
 template <int DT>
-__global__ void __launch_bounds__(kCodeThreads) k_decode(DecodeLaunch a) {
+__device__ __forceinline__ int32_t rank_of_value(float x) {
+  if (DT == 0) {
+    const uint32_t u = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+    const int32_t r = rank_bf16(u);
+    return r < 0 ? 0 : (r >= kNsymBf16 ? kNsymBf16 - 1 : r);
+  }
+  const uint32_t u = (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+  const int32_t r = rank_e4m3(u);
+  return r < 0 ? 0 : r;
+}
+
+__device__ __forceinline__ uint32_t pick4(uint4 v, int j) {
+  return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
+}
+
+// Decode.  Per symbol: slot = x mod 2^M; find r with cum(r) <= slot < cum(r+1);
+// x = freq * (x >> M) + slot - cum(r); refill from the stream if x < 2^31.
+// Reference search (bisect): 16 (bf16) or 8 (e4m3) cum evaluations.  Default
+// search: (1) a guess from the inverted Gaussian part of the model CDF,
+// verified with cum(r), cum(r+1); (2) if it missed, one Newton step in value
+// space with that bin's exact density, verified the same way; (3) lanes still
+// unresolved are finished one at a time by the whole warp, 32 candidates per
+// step.  Every answer is checked by the exact cum bracket, so both searches
+// return the same symbol.
+template <int DT, bool BISECT>
+__global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
   extern __shared__ uint2 s_phi[];
   float *s_lo8 = reinterpret_cast<float *>(s_phi + kPhiKnots);
-  stage_tables(s_phi, s_lo8);
+  float2 *s_hinv = reinterpret_cast<float2 *>(s_lo8 + 256);
+  int32_t *s_einv = reinterpret_cast<int32_t *>(s_hinv + kHinvN + 1);
+  for (int i = threadIdx.x; i < kPhiKnots; i += blockDim.x) s_phi[i] = g_phi[i];
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) s_lo8[i] = g_lo8[i];
+  for (int i = threadIdx.x; i <= kHinvN; i += blockDim.x) {
+    s_hinv[i] = g_hinv[DT][i];
+    s_einv[i] = (DT == 0 && a.einv) ? a.einv[i] : 0;
+  }
+  __syncthreads();
 
   constexpr int M = DT == 0 ? kMBf16 : kME4m3;
   constexpr int32_t NS = DT == 0 ? kNsymBf16 : kNsymE4m3;
   constexpr uint32_t kMask = (1u << M) - 1u;
+  constexpr float kInvK = 1.0f / (float)(DT == 0 ? kKBf16 : kKE4m3);
+  constexpr float kHscale = (float)kHinvN / (DT == 0 ? kHinvUmaxBf16 : kHinvUmaxE4m3);
   const int G = a.geo.G;
   const int lane = threadIdx.x & 31;
   const int ell = lane & (G - 1);
@@ -488,42 +585,171 @@ __global__ void __launch_bounds__(kCodeThreads) k_decode(DecodeLaunch a) {
     for (uint32_t gi = 0; gi < max_groups; ++gi) {
       const bool has = gi < my_groups;
       const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * gi);
-      uint32_t mub[8], out[8];
-      ChanInv inv[8];
+      uint4 mu4 = make_uint4(0, 0, 0, 0);
+      float4 iv4[4];
       if (has) {
-        load_mu(a.mu, cg.base + p0, mub);
-        load_inv(a.inv, cg.srow + p0 % D, inv);
+        mu4 = __ldg(reinterpret_cast<const uint4 *>(a.mu + cg.base + p0));
+        const float4 *ip = reinterpret_cast<const float4 *>(a.inv + cg.srow + p0 % D);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) iv4[j] = __ldg(ip + j);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) iv4[j] = make_float4(1.f, 1.f, 1.f, 1.f);
       }
-#pragma unroll
+      uint4 out4 = make_uint4(0, 0, 0, 0);
+#pragma unroll 1
       for (int k = 0; k < 8; ++k) {
-        bool need = false;
-        out[k] = 0;
-        if (has) {
-          if (!mu_valid(mub[k])) {
-            flags |= kFlagParam;
-            mub[k] = 0;
-          }
-          const float muf = bf16_to_f32(mub[k]);
-          const uint32_t slot = (uint32_t)x & kMask;
-          // largest r with cum(r) <= slot; clo = cum(r), chi = cum(r + 1)
-          int32_t r = 0;
-          uint32_t clo = 0, chi = 1u << M;
+        uint32_t mub = (pick4(mu4, k >> 1) >> (16 * (k & 1))) & 0xFFFFu;
+        const float4 ivp = k < 2 ? iv4[0] : (k < 4 ? iv4[1] : (k < 6 ? iv4[2] : iv4[3]));
+        ChanInv inv;
+        inv.s = (k & 1) ? ivp.z : ivp.x;
+        inv.s3 = (k & 1) ? ivp.w : ivp.y;
+        if (has && !mu_valid(mub)) {
+          flags |= kFlagParam;
+          mub = 0;
+        }
+        const float muf = bf16_to_f32(mub);
+        const uint32_t slot = (uint32_t)x & kMask;
+        Bracket br;
+        br.lo = 0;
+        br.hi = NS;
+        br.clo = 0;
+        br.chi = 1u << M;
+        if (BISECT) {
+          if (has) {
+            int32_t r = 0;
 #pragma unroll
-          for (int step = DT == 0 ? (1 << 15) : (1 << 7); step >= 1; step >>= 1) {
-            const int32_t cand = r + step;
-            if (cand < NS) {
-              const uint32_t cv = cum_of<DT>(cand, muf, inv[k], s_phi, s_lo8, a.ecdf);
-              if (cv <= slot) {
-                r = cand;
-                clo = cv;
-              } else {
-                chi = cv;
+            for (int step = DT == 0 ? (1 << 15) : (1 << 7); step >= 1; step >>= 1) {
+              const int32_t cand = r + step;
+              if (cand < NS) {
+                const uint32_t cv = cum_of<DT>(cand, muf, inv, s_phi, s_lo8, a.ecdf);
+                if (cv <= slot) {
+                  r = cand;
+                  br.clo = cv;
+                } else {
+                  br.chi = cv;
+                }
               }
             }
+            br.lo = r;
+            br.hi = r + 1;
           }
-          x = (uint64_t)(chi - clo) * (x >> M) + (slot - clo);
+        } else {
+          bool done = true;
+          if (has) {
+            // (1) guess: invert the Gaussian part of the CDF
+            float u, uraw = 0.0f;
+            if (DT == 0) {
+              const int32_t rmu = rank_bf16(mub);
+              const float e = (float)__ldg(a.ecdf + rmu) * (1.0f / 67108864.0f);
+              uraw = (float)(int32_t)(slot - (uint32_t)rmu) * kInvK;
+              u = uraw - 0.02f * e;
+            } else {
+              u = (float)slot * kInvK;
+            }
+            float t = fminf(fmaxf(u * kHscale, 0.0f), (float)kHinvN - 0.001f);
+            const int kk = (int)t;
+            const float2 h = s_hinv[kk];
+            const float z = fmaf(t - (float)kk, h.y, h.x);
+            const float sig = __frcp_rn(inv.s);
+            int32_t rg = rank_of_value<DT>(fmaf(sig, z, muf));
+            if (DT == 0 && (u < 0.0f || u > kHinvUmaxBf16)) {
+              // beyond both Gaussian parts only p-hat moves the CDF: invert it
+              const float tgt = (u < 0.0f ? uraw : uraw - kHinvUmaxBf16) * (50.0f * kHinvN);
+              const float te = fminf(fmaxf(tgt, 0.0f), (float)kHinvN - 0.001f);
+              const int ke = (int)te;
+              const int32_t r0 = s_einv[ke], r1 = s_einv[ke + 1];
+              rg = min(r0 + (int32_t)((te - (float)ke) * (float)(r1 - r0)), NS - 1);
+            }
+            const uint32_t ca = cum_of<DT>(rg, muf, inv, s_phi, s_lo8, a.ecdf);
+            const uint32_t cb = cum_of<DT>(rg + 1, muf, inv, s_phi, s_lo8, a.ecdf);
+            bracket_add(br, rg, ca, slot);
+            bracket_add(br, rg + 1, cb, slot);
+            done = br.hi - br.lo == 1;
+            if (!done) {
+              // (2) Newton in value space with the density of bin rg
+              const float blo = lo_value(DT, rg, s_lo8), bhi = lo_value(DT, rg + 1, s_lo8);
+              const float dens_inv = (bhi - blo) / (float)(cb - ca);
+              const float xn = slot < ca ? blo - (float)(ca - slot) * dens_inv
+                                         : bhi + (float)(slot - cb) * dens_inv;
+              int32_t sN = isfinite(xn) ? rank_of_value<DT>(xn) : (br.lo + br.hi) >> 1;
+              sN = max(sN, br.lo);
+              sN = min(sN, br.hi - 1);
+              bool upper = true;
+              if (sN > br.lo) {
+                const uint32_t cs = cum_of<DT>(sN, muf, inv, s_phi, s_lo8, a.ecdf);
+                bracket_add(br, sN, cs, slot);
+                upper = cs <= slot;
+              }
+              if (upper && sN + 1 < br.hi) {
+                const uint32_t cs1 = cum_of<DT>(sN + 1, muf, inv, s_phi, s_lo8, a.ecdf);
+                bracket_add(br, sN + 1, cs1, slot);
+              }
+              done = br.hi - br.lo == 1;
+            }
+          }
+          // (3) the warp finishes its unresolved lanes, one lane at a time
+          uint32_t pend = __ballot_sync(0xFFFFFFFFu, !done);
+          while (pend) {
+            const int l = __ffs(pend) - 1;
+            pend &= pend - 1;
+            const uint32_t s_slot = __shfl_sync(0xFFFFFFFFu, slot, l);
+            const float s_mu = __shfl_sync(0xFFFFFFFFu, muf, l);
+            ChanInv s_inv;
+            s_inv.s = __shfl_sync(0xFFFFFFFFu, inv.s, l);
+            s_inv.s3 = __shfl_sync(0xFFFFFFFFu, inv.s3, l);
+            int32_t blo = __shfl_sync(0xFFFFFFFFu, br.lo, l);
+            int32_t bhi = __shfl_sync(0xFFFFFFFFu, br.hi, l);
+            uint32_t bclo = __shfl_sync(0xFFFFFFFFu, br.clo, l);
+            uint32_t bchi = __shfl_sync(0xFFFFFFFFu, br.chi, l);
+            for (int it = 0; it < 8 && bhi - blo > 1; ++it) {
+              const int32_t wdt = bhi - blo;
+              const int32_t nact = min(wdt - 1, 32);
+              const int32_t cand = wdt - 1 <= 32
+                                       ? blo + 1 + lane
+                                       : blo + (int32_t)(((int64_t)(lane + 1) * wdt) / 33);
+              const bool act = lane < nact;
+              const uint32_t cv = act ? cum_of<DT>(cand, s_mu, s_inv, s_phi, s_lo8, a.ecdf) : 0u;
+              const int kle = __popc(__ballot_sync(0xFFFFFFFFu, act && cv <= s_slot));
+              const int32_t c_lo = __shfl_sync(0xFFFFFFFFu, cand, kle > 0 ? kle - 1 : 0);
+              const uint32_t v_lo = __shfl_sync(0xFFFFFFFFu, cv, kle > 0 ? kle - 1 : 0);
+              const int32_t c_hi = __shfl_sync(0xFFFFFFFFu, cand, kle < nact ? kle : 0);
+              const uint32_t v_hi = __shfl_sync(0xFFFFFFFFu, cv, kle < nact ? kle : 0);
+              if (kle > 0) {
+                blo = c_lo;
+                bclo = v_lo;
+              }
+              if (kle < nact) {
+                bhi = c_hi;
+                bchi = v_hi;
+              }
+            }
+            if (lane == l) {
+              if (bhi - blo != 1) flags |= kFlagCorrupt;  // only if cum were not monotone
+              br.lo = blo;
+              br.hi = blo + 1;
+              br.clo = bclo;
+              br.chi = bchi;
+            }
+          }
+        }
+        bool need = false;
+        if (has) {
+          x = (uint64_t)(br.chi - br.clo) * (x >> M) + (slot - br.clo);
           need = x < kStateL;
-          out[k] = DT == 0 ? bits_bf16(r) : bits_e4m3(r);
+          const uint32_t sym = DT == 0 ? bits_bf16(br.lo) : bits_e4m3(br.lo);
+          if (DT == 0) {
+            const uint32_t sh = 16 * (k & 1), keep = ~(0xFFFFu << sh), v = sym << sh;
+            const int j = k >> 1;
+            if (j == 0) out4.x = (out4.x & keep) | v;
+            else if (j == 1) out4.y = (out4.y & keep) | v;
+            else if (j == 2) out4.z = (out4.z & keep) | v;
+            else out4.w = (out4.w & keep) | v;
+          } else {
+            const uint32_t sh = 8 * (k & 3), keep = ~(0xFFu << sh), v = sym << sh;
+            if (k < 4) out4.x = (out4.x & keep) | v;
+            else out4.y = (out4.y & keep) | v;
+          }
         }
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, need) & seg;
         if (need) {
@@ -539,17 +765,10 @@ __global__ void __launch_bounds__(kCodeThreads) k_decode(DecodeLaunch a) {
       }
       if (has) {
         if (DT == 0) {
-          uint4 v;
-          v.x = out[0] | (out[1] << 16);
-          v.y = out[2] | (out[3] << 16);
-          v.z = out[4] | (out[5] << 16);
-          v.w = out[6] | (out[7] << 16);
-          *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.kv_out) + cg.base + p0) = v;
+          *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.kv_out) + cg.base + p0) = out4;
         } else {
-          uint2 v;
-          v.x = out[0] | (out[1] << 8) | (out[2] << 16) | (out[3] << 24);
-          v.y = out[4] | (out[5] << 8) | (out[6] << 16) | (out[7] << 24);
-          *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.kv_out) + cg.base + p0) = v;
+          *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.kv_out) + cg.base + p0) =
+              make_uint2(out4.x, out4.y);
         }
       }
     }
@@ -561,22 +780,28 @@ __global__ void __launch_bounds__(kCodeThreads) k_decode(DecodeLaunch a) {
   }
 }
 
+template <int DT, bool BISECT>
+static cudaError_t run_decode(const DecodeLaunch &a, int blocks, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k_decode<DT, BISECT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+  if (e != cudaSuccess) return e;
+  k_decode<DT, BISECT><<<blocks, kDecThreads, kDecSmem, s>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s) {
   k_check_header<<<1, 32, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // at most one block per SM (see kCodeThreads)
   const int64_t ntasks = (a.geo.nchunks * a.geo.G + 31) / 32;
-  const int blocks = code_blocks(ntasks);
-  if (a.dtype == 0) {
-    e = cudaFuncSetAttribute(k_decode<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCodeSmem);
-    if (e != cudaSuccess) return e;
-    k_decode<0><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
-  } else {
-    e = cudaFuncSetAttribute(k_decode<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCodeSmem);
-    if (e != cudaSuccess) return e;
-    k_decode<1><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
-  }
-  return cudaGetLastError();
+  const int64_t wpb = kDecThreads / 32;
+  int64_t blocks = (ntasks + wpb - 1) / wpb;
+  const int64_t cap = (int64_t)device_sm_count();
+  if (blocks > cap) blocks = cap;
+  if (a.dtype == 0)
+    return a.bisect ? run_decode<0, true>(a, (int)blocks, s) : run_decode<0, false>(a, (int)blocks, s);
+  return a.bisect ? run_decode<1, true>(a, (int)blocks, s) : run_decode<1, false>(a, (int)blocks, s);
 }
 
 }  // namespace skv

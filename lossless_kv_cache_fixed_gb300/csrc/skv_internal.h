@@ -46,6 +46,8 @@ struct EncodeLaunch {
 struct DecodeLaunch {
   Geo geo;
   int dtype;
+  int bisect;               // 1: plain bisection search (reference path)
+  const int32_t *einv;      // bf16: inverse of the p-hat prefix table (kHinvN + 1 ranks)
   const uint8_t *in;
   uint64_t in_bytes;
   const uint16_t *mu;
@@ -69,14 +71,24 @@ struct IdealLaunch {
   WsHead *head;
 };
 
-// Device constants (Phi knot pairs, e4m3 bin edges) for the current device.
-cudaError_t upload_tables(const uint32_t *phi_knots, const float *lo8);
+// Inverse of the model CDF's Gaussian part, G0(z) = 0.95 Phi(z) + 0.03 Phi(z/3)
+// (bf16) or Phi(z) (e4m3), tabulated at kHinvN + 1 equally spaced u in
+// [0, kHinvUmax[dtype]] as (z_k, z_{k+1} - z_k): the decoder's first guess.
+constexpr int kHinvN = 1024;
+constexpr float kHinvUmaxBf16 = 0.98f, kHinvUmaxE4m3 = 1.0f;
+
+// Device constants (Phi knot pairs, e4m3 bin edges, the two inverse tables)
+// for the current device.
+cudaError_t upload_tables(const uint32_t *phi_knots, const float *lo8, const float *hinv_bf16,
+                          const float *hinv_e4m3);
 
 // Model preparation: sigma validation, per-channel reciprocals, E_q checks and
 // the model fingerprint accumulation.
 cudaError_t launch_prep(const float *sigma, int64_t nsig, const uint32_t *ecdf, float2 *inv,
                         WsHead *head, cudaStream_t s);
 cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s);
+// einv[k] = the smallest rank r with E_q[r] >= k 2^26 / kHinvN, k = 0..kHinvN.
+cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, cudaStream_t s);
 cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s);
 cudaError_t launch_ideal(const IdealLaunch &a, cudaStream_t s);
 

@@ -66,10 +66,10 @@ WORKLOADS = {
     "tiny-bf16": Spec("tiny-bf16", BF16, 2, 2, 256, 64, 0.02, False, 1, 0, False, 256, 4),
     # Qwen3-0.6B-shaped: 28 x {K,V} x 8 x 4096 x 128 = 234.9M scalars
     "qwen3-0.6b-bf16": Spec("qwen3-0.6b-bf16", BF16, 28, 8, 4096, 128, 0.03, True, 128, 512,
-                            False, 256, 8),
+                            False, 256, 16),
     # Qwen3-32B-shaped: 64 x {K,V} x 8 x 8192 x 128 = 1.07G scalars, calibrated sigma
     "qwen3-32b-bf16": Spec("qwen3-32b-bf16", BF16, 64, 8, 8192, 128, 0.015, True, 128, 512,
-                           True, 256, 8),
+                           True, 256, 16),
     # Qwen3-8B-shaped FP8: 36 x {K,V} x 8 x 16384 x 128 = 1.21G e4m3 scalars
     "qwen3-8b-e4m3": Spec("qwen3-8b-e4m3", E4M3, 36, 8, 16384, 128, 0.03, True, 0, 512, False,
                           256, 8),

@@ -12,7 +12,7 @@ def skv():
     return P
 
 
-def gpu_codec(w: synth.Workload, Tb=None, G=None):
+def gpu_codec(w: synth.Workload, Tb=None, G=None, flags=0):
     P = skv()
     s = w.spec
     dev = torch.device("cuda")
@@ -21,7 +21,8 @@ def gpu_codec(w: synth.Workload, Tb=None, G=None):
         E, ph = P.skv_build_ecdf(w.counts.cpu().numpy().astype(np.uint64))
         ecdf = torch.from_numpy(E.view(np.int32)).to(dev)
         phat = torch.from_numpy(ph).to(dev)
-    return P.Codec(s.dtype, s.L, s.H, s.T, s.D, Tb or s.Tb, G or s.G, w.sigma.to(dev), ecdf, phat)
+    return P.Codec(s.dtype, s.L, s.H, s.T, s.D, Tb or s.Tb, G or s.G, w.sigma.to(dev), ecdf, phat,
+                   flags=flags)
 
 
 def oracle_model(O, w: synth.Workload, Tb=None, G=None):

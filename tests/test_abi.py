@@ -82,7 +82,7 @@ def test_argument_errors_without_gpu(skv):
                 P.SkvParams(P.SKV_BF16, 256, 64, 0, 1, 1, None),
                 P.SkvParams(P.SKV_BF16, 0, 8, 0, 1, 1, None),
                 P.SkvParams(5, 256, 8, 0, 1, 1, None),
-                P.SkvParams(P.SKV_BF16, 256, 8, 1, 1, 1, None)]:
+                P.SkvParams(P.SKV_BF16, 256, 8, 2, 1, 1, None)]:
         assert P.skv_max_encoded_bytes(bad, shape) == 0
         rc, _ = P.skv_encode(bad, shape, 1 << 20, 1 << 20, 1 << 20, 1 << 30, 1 << 20, 1 << 30, None)
         assert rc == P.SKV_ERR_ARG

@@ -37,8 +37,12 @@ def _check(O, w, Tb=None, G=None, nsample=32, max_overhead=0.01):
     dec = codec.decode(buf, nb, mu_d)
     assert torch.equal(dec, kv_d)
     del dec
+    if s.n <= 300_000_000:   # the bisection reference search on the smaller caches
+        ref = gpu_codec(w, Tb, G, flags=1).decode(buf, nb, mu_d)
+        assert torch.equal(ref, kv_d)
+        del ref
     tot, ps = codec.ideal_bits(kv_d, mu_d, per_scalar=True)
-    assert abs(tot - ps.double().sum().item()) <= 1e-9 * tot
+    assert abs(tot - ps.double().sum().item()) <= 1e-6 * tot  # fp32 sums of 8 inside fp64
     m = oracle_model(O, w, Tb, G)
     nc = m.num_chunks()
     host = buf[:nb].cpu().numpy()

@@ -38,12 +38,15 @@ def _roundtrip(O, w, Tb=None, G=None, ideal=True, max_overhead=None):
     assert got.size == want.size and np.array_equal(got, want)
     dec = codec.decode(buf, nb, mu_d)
     assert torch.equal(dec, kv_d)
+    # the reference bisection search returns the same symbols
+    ref = gpu_codec(w, Tb, G, flags=1).decode(buf, nb, mu_d)
+    assert torch.equal(ref, kv_d)
     if ideal:
         tot, ps = codec.ideal_bits(kv_d, mu_d, per_scalar=True)
         ref_tot, ref = O.ideal_bits(m, kv, mu, per_scalar=True)
         ps = ps.double().cpu().numpy()
         assert np.all(np.abs(ps - ref) <= RTOL * np.abs(ref) + ATOL)
-        assert abs(tot - ps.sum()) <= 1e-9 * abs(tot)
+        assert abs(tot - ps.sum()) <= 1e-6 * abs(tot)  # fp32 sums of 8 inside fp64
         assert abs(tot - ref_tot) <= RTOL * ref_tot
         nc = m.num_chunks()
         if max_overhead is not None:
