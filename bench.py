@@ -343,6 +343,9 @@ def run_gpu(args):
     value = world * raw / (ms_step * 1e-3) / 1e9
 
     # ---- end to end through the C ABI with host buffers ----
+    if args.no_e2e:
+        return finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value,
+                           t_enc, t_dec, t_bits, clk, None, w)
     kv_h = kv.cpu().pin_memory()
     mu_h = mu.cpu().pin_memory()
     box_h = torch.empty(codec.max_bytes, dtype=torch.uint8).pin_memory()
@@ -376,8 +379,18 @@ def run_gpu(args):
     h2d = raw + 2 * n + nb2
     d2h = nb2 + raw + 8 + 3 * 32  # container, cache, total, three status reads
 
+    e2e = {"value": round(world * raw / e2e_s / 1e9, 3), "unit": "GB/s",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+    return finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value,
+                       t_enc, t_dec, t_bits, clk, e2e, w)
+
+
+def finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value, t_enc, t_dec, t_bits,
+                clk, e2e, w):
     if rank != 0:
         return None
+    import synth
+    raw = n * bps
 
     # ---- roofline of the dominant kernel ----
     med = {"encode": statistics.median(t_enc), "decode": statistics.median(t_dec),
@@ -420,8 +433,7 @@ def run_gpu(args):
         "roofline": roof,
         "kernels": kernels,
         "cpu_baseline": cpu,
-        "e2e": {"value": round(world * raw / e2e_s / 1e9, 3), "unit": "GB/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "e2e": e2e,
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clk.summary(),
     }
@@ -483,6 +495,7 @@ def main(argv=None):
     ap.add_argument("--cpu-sample-chunks", type=int, default=384)
     ap.add_argument("--ref-chunks-per-step", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host round trip")
     ap.add_argument("--lanes", type=int, default=0, help="override the workload's lanes per chunk")
     ap.add_argument("--token-block", type=int, default=0, help="override the token block")
     ap.add_argument("--decode-bisect", action="store_true",

@@ -1,0 +1,148 @@
+"""Fault injection on the GPU path, made on the host (no GPU fault is ever
+provoked): corrupted, truncated or mismatched containers and invalid inputs
+must come back as an error status -- or, for a payload bit flip that still
+decodes cleanly, as different data -- and the library must stay usable.
+
+Every read of the decoder is bounded by its chunk's extent and every wait is
+absent by construction, so none of these cases can fault or hang.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_helpers import device_views, gpu_codec
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@pytest.fixture(scope="module")
+def enc():
+    import lossless_kv_cache_fixed_gb300 as P
+    spec = synth.WORKLOADS["qwen3-0.6b-bf16"].scaled(name="faults", L=1, H=2, T=512,
+                                                     calib_draws=2)
+    w = synth.make(spec)
+    codec = gpu_codec(w)
+    kv, mu = device_views(w)
+    buf, nb = codec.encode(kv, mu)
+    return P, w, codec, kv, mu, buf[:nb].clone(), nb
+
+
+def _decode_rc(P, codec, buf, nb, mu, stream=None):
+    out = torch.empty(codec.n, dtype=torch.int16, device="cuda")
+    ws = codec.workspace(P.SKV_OP_DECODE)
+    rc = P.skv_decode(codec.params, codec.shape, buf.data_ptr(), nb, mu.data_ptr(),
+                      out.data_ptr(), ws.data_ptr(), ws.numel(), P._stream_handle(stream))
+    return rc, out
+
+
+def test_clean_roundtrip_then_library_still_usable(enc):
+    P, w, codec, kv, mu, buf, nb = enc
+    rc, out = _decode_rc(P, codec, buf, nb, mu)
+    assert rc == P.SKV_OK and torch.equal(out, kv)
+
+
+def test_payload_bit_flips(enc):
+    P, w, codec, kv, mu, buf, nb = enc
+    nc = codec.n // (codec.shape.head_dim * codec.params.token_block)
+    head = 64 + 8 * (nc + 1)
+    rng = np.random.default_rng(0)
+    for _ in range(40):
+        t = buf.clone()
+        pos = int(rng.integers(head, nb))
+        t[pos] ^= 1 << int(rng.integers(0, 8))
+        rc, out = _decode_rc(P, codec, t, nb, mu)
+        # a clean finish on a changed stream would be a different cache
+        assert rc == P.SKV_ERR_CORRUPT or (rc == P.SKV_OK and not torch.equal(out, kv))
+    test_clean_roundtrip_then_library_still_usable(enc)
+
+
+def test_truncated_and_padded(enc):
+    P, w, codec, kv, mu, buf, nb = enc
+    for cut in (4, 64, 1000, nb // 2):
+        rc, _ = _decode_rc(P, codec, buf, nb - cut, mu)
+        assert rc == P.SKV_ERR_CORRUPT, cut
+    longer = torch.cat([buf, torch.zeros(16, dtype=torch.uint8, device="cuda")])
+    rc, _ = _decode_rc(P, codec, longer, nb + 16, mu)
+    assert rc == P.SKV_ERR_CORRUPT
+    rc, _ = _decode_rc(P, codec, buf, 10, mu)
+    assert rc == P.SKV_ERR_CORRUPT
+
+
+def test_header_and_offset_tampering(enc):
+    P, w, codec, kv, mu, buf, nb = enc
+    for off in (0, 4, 6, 7, 8, 16, 20, 24, 28, 32, 40, 48, 56, 63):
+        t = buf.clone()
+        t[off] ^= 0x10
+        assert _decode_rc(P, codec, t, nb, mu)[0] == P.SKV_ERR_CORRUPT, off
+    # offsets: point a chunk past the payload, make one decrease, misalign one
+    for j, val in ((3, 1 << 40), (5, 4), (7, None)):
+        t = buf.clone()
+        o = t[64:64 + 8 * 16].view(torch.int64)
+        o[j] = val if val is not None else o[j] + 2
+        assert _decode_rc(P, codec, t, nb, mu)[0] == P.SKV_ERR_CORRUPT, j
+
+
+def test_model_mismatch(enc):
+    P, w, codec, kv, mu, buf, nb = enc
+    # one sigma one ulp off: the fingerprint in the header no longer matches
+    sig = w.sigma.clone()
+    sig.view(-1)[3] = torch.nextafter(sig.view(-1)[3], torch.tensor(10.0))
+    w2 = synth.Workload(w.spec, w.kv, w.mu, sig, w.counts)
+    rc, _ = _decode_rc(P, gpu_codec(w2), buf, nb, mu)
+    assert rc == P.SKV_ERR_CORRUPT
+    # a different p-hat table
+    cnt = w.counts.clone()
+    cnt[0x3F80] += 1000
+    w3 = synth.Workload(w.spec, w.kv, w.mu, w.sigma, cnt)
+    rc, _ = _decode_rc(P, gpu_codec(w3), buf, nb, mu)
+    assert rc == P.SKV_ERR_CORRUPT
+    # mu off by one ulp somewhere: an error or a different cache, never a fault
+    mu2 = mu.clone()
+    mu2[1234] ^= 1
+    rc, out = _decode_rc(P, codec, buf, nb, mu2)
+    assert rc in (P.SKV_OK, P.SKV_ERR_CORRUPT)
+    test_clean_roundtrip_then_library_still_usable(enc)
+
+
+def test_invalid_inputs(enc):
+    P, w, codec, kv, mu, buf, nb = enc
+    bad = kv.clone()
+    bad[77] = 0x7FC1                          # a NaN pattern
+    with pytest.raises(P.SkvError) as e:
+        codec.encode(bad, mu)
+    assert e.value.status == P.SKV_ERR_SYMBOL
+    badmu = mu.clone()
+    badmu[5] = 0x7F80                         # mu = +inf
+    with pytest.raises(P.SkvError) as e:
+        codec.encode(kv, badmu)
+    assert e.value.status == P.SKV_ERR_PARAM
+    for v in (0.0, float("nan"), float("inf"), -1.0, 1e-39):
+        sig = w.sigma.clone()
+        sig.view(-1)[0] = v
+        c2 = gpu_codec(synth.Workload(w.spec, w.kv, w.mu, sig, w.counts))
+        with pytest.raises(P.SkvError) as e:
+            c2.encode(kv, mu)
+        assert e.value.status == P.SKV_ERR_PARAM, v
+    # too small an output buffer
+    small = torch.empty(nb - 100, dtype=torch.uint8, device="cuda")
+    with pytest.raises(P.SkvError) as e:
+        codec.encode(kv, mu, out=small)
+    assert e.value.status == P.SKV_ERR_CAPACITY
+    # a p-hat prefix table that is not non-decreasing
+    import lossless_kv_cache_fixed_gb300 as PP
+    E, ph = PP.skv_build_ecdf(w.counts.cpu().numpy().astype(np.uint64))
+    E[1000], E[1001] = E[1001] + 5, E[1000]
+    c3 = PP.Codec(w.spec.dtype, w.spec.L, w.spec.H, w.spec.T, w.spec.D, w.spec.Tb, w.spec.G,
+                  w.sigma.cuda(), torch.from_numpy(E.view(np.int32)).cuda(),
+                  torch.from_numpy(ph).cuda())
+    with pytest.raises(P.SkvError) as e:
+        c3.encode(kv, mu)
+    assert e.value.status == P.SKV_ERR_PARAM
+    test_clean_roundtrip_then_library_still_usable(enc)
