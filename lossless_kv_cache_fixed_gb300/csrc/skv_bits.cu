@@ -68,7 +68,7 @@ __device__ __forceinline__ float log2_gauss_series(float lo, float hi, float mu,
       const float y = w2 * fmaf(w2, fmaf(w2, he6 * (1.0f / 322560.0f), he4 * (1.0f / 1920.0f)),
                                 he2 * (1.0f / 24.0f));
       const float l1p = y * fmaf(y, fmaf(y, 1.0f / 3.0f, -0.5f), 1.0f);
-      return fmaf(-0.5f * kLog2e, z2, -kLog2Sqrt2Pi) + (log2f(width) - log2_s) + l1p * kLog2e;
+      return fmaf(-0.5f * kLog2e, z2, -kLog2Sqrt2Pi) + (__log2f(width) - log2_s) + l1p * kLog2e;
     }
   }
   ok = false;
@@ -121,8 +121,9 @@ __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float
   const float mu = bf16_to_f32(mu_bits);
   const float lo = DT == 0 ? lo_bf16(r) : lo8[r];
   const float hi = DT == 0 ? lo_bf16(r + 1) : lo8[r + 1];
-  const float inv_s = 1.0f / sigma;
-  const float log2_s = log2f(sigma);
+  // fp32 to about 1e-7 relative is far inside the 1e-3 tolerance of the ideal
+  const float inv_s = __fdividef(1.0f, sigma);
+  const float log2_s = __log2f(sigma);
   float l1, l3 = 0.0f;
   if (FULL) {
     l1 = log2_gauss_bin(lo, hi, mu, inv_s, log2_s);
@@ -137,12 +138,17 @@ __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float
     }
   }
   if (DT == 1) return -l1;
+  const float ph = phat[r];
+  if (l1 > -100.0f && l3 > -100.0f) {
+    // no component can underflow: sum the mixture directly
+    return -__log2f(fmaf(0.95f, exp2f(l1), fmaf(0.03f, exp2f(l3), 0.02f * ph)));
+  }
   const float a = -0.07400058f + l1;  // log2 0.95
   const float b = -5.0588937f + l3;   // log2 0.03 (the wide component: sigma * 3)
-  const float c = -5.6438562f + log2f(phat[r]);                               // log2 0.02
+  const float c = -5.6438562f + __log2f(ph);  // log2 0.02
   const float m = fmaxf(a, fmaxf(b, c));
   if (m == -INFINITY) return INFINITY;
-  return -(m + log2f(exp2f(a - m) + exp2f(b - m) + exp2f(c - m)));
+  return -(m + __log2f(exp2f(a - m) + exp2f(b - m) + exp2f(c - m)));
 }
 
 template <int DT>

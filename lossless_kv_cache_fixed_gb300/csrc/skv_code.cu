@@ -651,7 +651,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
             const int kk = (int)t;
             const float2 h = s_hinv[kk];
             const float z = fmaf(t - (float)kk, h.y, h.x);
-            const float sig = __frcp_rn(inv.s);
+            const float sig = __fdividef(1.0f, inv.s);  // a guess: approximate is enough
             int32_t rg = rank_of_value<DT>(fmaf(sig, z, muf));
             if (DT == 0 && (u < 0.0f || u > kHinvUmaxBf16)) {
               // beyond both Gaussian parts only p-hat moves the CDF: invert it
@@ -669,7 +669,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
             if (!done) {
               // (2) Newton in value space with the density of bin rg
               const float blo = lo_value(DT, rg, s_lo8), bhi = lo_value(DT, rg + 1, s_lo8);
-              const float dens_inv = (bhi - blo) / (float)(cb - ca);
+              const float dens_inv = __fdividef(bhi - blo, (float)(cb - ca));
               const float xn = slot < ca ? blo - (float)(ca - slot) * dens_inv
                                          : bhi + (float)(slot - cb) * dens_inv;
               int32_t sN = isfinite(xn) ? rank_of_value<DT>(xn) : (br.lo + br.hi) >> 1;
