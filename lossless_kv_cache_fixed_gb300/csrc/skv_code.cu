@@ -38,8 +38,10 @@ constexpr size_t kDecSmem = kCodeSmem + sizeof(float2) * (kHinvN + 1) + sizeof(i
 cudaError_t upload_tables(const uint32_t *T, const float *lo8, const float *hb, const float *he) {
   uint2 pairs[kPhiKnots];
   for (int i = 0; i < kPhiKnots; ++i) {
+    const uint32_t step = i + 1 < kPhiKnots ? T[i + 1] - T[i] : 0u;
+    if (step >= 65536u) return cudaErrorInvalidValue;  // 2^26 phi(0) / 512 < 52,300
     pairs[i].x = T[i];
-    pairs[i].y = i + 1 < kPhiKnots ? T[i + 1] - T[i] : 0u;
+    pairs[i].y = step << 16;
   }
   cudaError_t e = cudaMemcpyToSymbol(g_phi, pairs, sizeof(pairs));
   if (e != cudaSuccess) return e;
@@ -514,10 +516,6 @@ __device__ __forceinline__ int32_t rank_of_value(float x) {
   return r < 0 ? 0 : r;
 }
 
-__device__ __forceinline__ uint32_t pick4(uint4 v, int j) {
-  return j == 0 ? v.x : (j == 1 ? v.y : (j == 2 ? v.z : v.w));
-}
-
 // Decode.  Per symbol: slot = x mod 2^M; find r with cum(r) <= slot < cum(r+1);
 // x = freq * (x >> M) + slot - cum(r); refill from the stream if x < 2^31.
 // Reference search (bisect): 16 (bf16) or 8 (e4m3) cum evaluations.  Default
@@ -585,25 +583,20 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
     for (uint32_t gi = 0; gi < max_groups; ++gi) {
       const bool has = gi < my_groups;
       const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * gi);
-      uint4 mu4 = make_uint4(0, 0, 0, 0);
-      float4 iv4[4];
-      if (has) {
-        mu4 = __ldg(reinterpret_cast<const uint4 *>(a.mu + cg.base + p0));
-        const float4 *ip = reinterpret_cast<const float4 *>(a.inv + cg.srow + p0 % D);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) iv4[j] = __ldg(ip + j);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) iv4[j] = make_float4(1.f, 1.f, 1.f, 1.f);
-      }
-      uint4 out4 = make_uint4(0, 0, 0, 0);
+      const uint16_t *mup = a.mu + cg.base + p0;
+      const float2 *ivp2 = a.inv + cg.srow + p0 % D;
 #pragma unroll 1
       for (int k = 0; k < 8; ++k) {
-        uint32_t mub = (pick4(mu4, k >> 1) >> (16 * (k & 1))) & 0xFFFFu;
-        const float4 ivp = k < 2 ? iv4[0] : (k < 4 ? iv4[1] : (k < 6 ? iv4[2] : iv4[3]));
+        uint32_t mub = has ? (uint32_t)__ldg(mup + k) : 0u;
         ChanInv inv;
-        inv.s = (k & 1) ? ivp.z : ivp.x;
-        inv.s3 = (k & 1) ? ivp.w : ivp.y;
+        if (has) {
+          const float2 v = __ldg(ivp2 + k);
+          inv.s = v.x;
+          inv.s3 = v.y;
+        } else {
+          inv.s = 1.0f;
+          inv.s3 = 1.0f;
+        }
         if (has && !mu_valid(mub)) {
           flags |= kFlagParam;
           mub = 0;
@@ -637,30 +630,38 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
         } else {
           bool done = true;
           if (has) {
-            // (1) guess: invert the Gaussian part of the CDF
-            float u, uraw = 0.0f;
-            if (DT == 0) {
-              const int32_t rmu = rank_bf16(mub);
-              const float e = (float)__ldg(a.ecdf + rmu) * (1.0f / 67108864.0f);
-              uraw = (float)(int32_t)(slot - (uint32_t)rmu) * kInvK;
-              u = uraw - 0.02f * e;
-            } else {
-              u = (float)slot * kInvK;
-            }
-            float t = fminf(fmaxf(u * kHscale, 0.0f), (float)kHinvN - 0.001f);
-            const int kk = (int)t;
-            const float2 h = s_hinv[kk];
-            const float z = fmaf(t - (float)kk, h.y, h.x);
+            // (1) guess: invert the CDF's Gaussian part around a reference
+            // symbol: slot ~ K F(x) + rank(x) with F = 0.95 Phi(z) + 0.03 Phi(z/3)
+            // + 0.02 E(x), with rank and E taken at mu.  For e4m3 a second pass
+            // takes the rank term at the first guess (for bf16 that pass mainly
+            // helps through E at the guess, whose dependent load costs as much
+            // as the Newton steps it saves).
             const float sig = __fdividef(1.0f, inv.s);  // a guess: approximate is enough
-            int32_t rg = rank_of_value<DT>(fmaf(sig, z, muf));
-            if (DT == 0 && (u < 0.0f || u > kHinvUmaxBf16)) {
-              // beyond both Gaussian parts only p-hat moves the CDF: invert it
-              const float tgt = (u < 0.0f ? uraw : uraw - kHinvUmaxBf16) * (50.0f * kHinvN);
-              const float te = fminf(fmaxf(tgt, 0.0f), (float)kHinvN - 0.001f);
-              const int ke = (int)te;
-              const int32_t r0 = s_einv[ke], r1 = s_einv[ke + 1];
-              rg = min(r0 + (int32_t)((te - (float)ke) * (float)(r1 - r0)), NS - 1);
-            }
+            auto guess = [&](int32_t rref) -> int32_t {
+              float u, uraw;
+              uraw = (float)(int32_t)(slot - (uint32_t)rref) * kInvK;
+              if (DT == 0) {
+                const float e = (float)__ldg(a.ecdf + rref) * (1.0f / 67108864.0f);
+                u = uraw - 0.02f * e;
+              } else {
+                u = uraw;
+              }
+              const float t = fminf(fmaxf(u * kHscale, 0.0f), (float)kHinvN - 0.001f);
+              const int kk = (int)t;
+              const float2 h = s_hinv[kk];
+              int32_t r = rank_of_value<DT>(fmaf(sig, fmaf(t - (float)kk, h.y, h.x), muf));
+              if (DT == 0 && (u < 0.0f || u > kHinvUmaxBf16)) {
+                // beyond both Gaussian parts only p-hat moves the CDF: invert it
+                const float tgt = (u < 0.0f ? uraw : uraw - kHinvUmaxBf16) * (50.0f * kHinvN);
+                const float te = fminf(fmaxf(tgt, 0.0f), (float)kHinvN - 0.001f);
+                const int ke = (int)te;
+                const int32_t r0 = s_einv[ke], r1 = s_einv[ke + 1];
+                r = min(r0 + (int32_t)((te - (float)ke) * (float)(r1 - r0)), NS - 1);
+              }
+              return r;
+            };
+            int32_t rg = guess(DT == 0 ? rank_bf16(mub) : rank_of_value<DT>(muf));
+            if (DT == 1) rg = guess(rg);  // e4m3: the rank term is up to 0.4% of the CDF
             const uint32_t ca = cum_of<DT>(rg, muf, inv, s_phi, s_lo8, a.ecdf);
             const uint32_t cb = cum_of<DT>(rg + 1, muf, inv, s_phi, s_lo8, a.ecdf);
             bracket_add(br, rg, ca, slot);
@@ -738,18 +739,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
           x = (uint64_t)(br.chi - br.clo) * (x >> M) + (slot - br.clo);
           need = x < kStateL;
           const uint32_t sym = DT == 0 ? bits_bf16(br.lo) : bits_e4m3(br.lo);
-          if (DT == 0) {
-            const uint32_t sh = 16 * (k & 1), keep = ~(0xFFFFu << sh), v = sym << sh;
-            const int j = k >> 1;
-            if (j == 0) out4.x = (out4.x & keep) | v;
-            else if (j == 1) out4.y = (out4.y & keep) | v;
-            else if (j == 2) out4.z = (out4.z & keep) | v;
-            else out4.w = (out4.w & keep) | v;
-          } else {
-            const uint32_t sh = 8 * (k & 3), keep = ~(0xFFu << sh), v = sym << sh;
-            if (k < 4) out4.x = (out4.x & keep) | v;
-            else out4.y = (out4.y & keep) | v;
-          }
+          if (DT == 0) static_cast<uint16_t *>(a.kv_out)[cg.base + p0 + k] = (uint16_t)sym;
+          else static_cast<uint8_t *>(a.kv_out)[cg.base + p0 + k] = (uint8_t)sym;
         }
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, need) & seg;
         if (need) {
@@ -762,14 +753,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
           }
         }
         cur += __popc(m);
-      }
-      if (has) {
-        if (DT == 0) {
-          *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.kv_out) + cg.base + p0) = out4;
-        } else {
-          *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.kv_out) + cg.base + p0) =
-              make_uint2(out4.x, out4.y);
-        }
       }
     }
     if (ok) {

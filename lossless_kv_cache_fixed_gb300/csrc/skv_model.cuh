@@ -53,16 +53,15 @@ __device__ __forceinline__ uint32_t bits_e4m3(int32_t r) {
 
 // Lower edge of bf16 symbol r's round-to-nearest bin, as fp32 bits.  The edge
 // between two neighbours is their midpoint: the smaller magnitude's pattern
-// followed by a half-ulp bit.  Ranks 0, 1 (-inf, -max) start at -inf, ranks
-// 65281, 65282 (+inf, end) at +inf, and -0 | +0 split at 0.
+// followed by a half-ulp bit.  With k = r - rank(+0) and a = |k|, the edge's
+// magnitude bits are (a << 16) - 0x8000 (0 for a = 0: -0 | +0 split at 0) and
+// its sign is k's; a >= 32640 gives infinity, so ranks 0, 1 (-inf, -max) start
+// at -inf and ranks 65281, 65282 (+inf, end) at +inf.
 __device__ __forceinline__ float lo_bf16(int32_t r) {
-  uint32_t pos = ((uint32_t)(r + 126 - 32768) << 16) | 0x8000u;           // r >= 32642
-  uint32_t neg = 0x80000000u | ((uint32_t)(32640 - r) << 16) | 0x8000u;   // r <= 32640
-  uint32_t b = r >= 32642 ? pos : neg;
-  b = r == 32641 ? 0u : b;
-  b = r <= 1 ? 0xFF800000u : b;
-  b = r >= 65281 ? 0x7F800000u : b;
-  return __uint_as_float(b);
+  const int32_t k = r - 32641;
+  const int32_t a = abs(k);
+  const uint32_t mag = a >= 32640 ? 0x7F800000u : (uint32_t)max(a * 65536 - 0x8000, 0);
+  return __uint_as_float(mag | ((uint32_t)k & 0x80000000u));
 }
 
 // ---- Phi_q: 2^26 Phi(z) by integer interpolation of the knot table ----
@@ -71,13 +70,15 @@ __device__ __forceinline__ float lo_bf16(int32_t r) {
 // fr = floor(65536 (t - floor t)).  Both come out of one integer,
 // q = floor(2^25 z) = 65536 floor(t) + fr: i = (q >> 16) + 4096, fr = q & 0xFFFF.
 // 2^25 z is an exact scaling (or +-inf, which the clamps map to the ends).
-// `phi` holds (T[i], T[i+1] - T[i]) pairs; the last pair is (2^26, 0).
+// `phi` holds (T[i], (T[i+1] - T[i]) << 16) pairs (the step is below 2^16);
+// the last pair is (2^26, 0).  ((T[i+1] - T[i]) fr) >> 16 is then the high
+// word of ((T[i+1] - T[i]) << 16) * fr.
 __device__ __forceinline__ uint32_t phi_q(float z, const uint2 *phi) {
   int32_t q = __float2int_rd(__fmul_rn(z, 33554432.0f));
   q = max(q, -(1 << 28));
   q = min(q, 1 << 28);
-  uint2 e = phi[(q >> 16) + 4096];
-  return e.x + ((e.y * ((uint32_t)q & 0xFFFFu)) >> 16);
+  const uint2 e = phi[(q >> 16) + 4096];
+  return e.x + __umulhi(e.y, (uint32_t)q & 0xFFFFu);
 }
 
 // Per-channel reciprocals: IEEE round-to-nearest 1/sigma and 1/(3 sigma).
