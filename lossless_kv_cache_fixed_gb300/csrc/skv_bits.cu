@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
   __shared__ float s_lo8[256];
   __shared__ double s_part[256];
   __shared__ float s_bits[8 * 256];
+  __shared__ uint16_t s_queue[8 * 256];  // per warp: up to 8 deferred scalars per lane
   if (DT == 1) {
     // e4m3 bin edges: midpoints of neighbouring values, +-inf at the ends
     for (int r = threadIdx.x; r < 255; r += blockDim.x) {
@@ -188,8 +189,8 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
   uint32_t flags = 0;
   double acc = 0.0;
   // The loop runs the same number of times for every lane of a warp (lanes past
-  // the end are switched off), because the deferred-lane drain below votes
-  // across the whole warp.
+  // the end are switched off), because the deferred-scalar queue below is
+  // filled and worked off by the whole warp.
   const int lane = threadIdx.x & 31;
   for (int64_t gw = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); gw < n8;
        gw += (int64_t)gridDim.x * blockDim.x) {
@@ -208,29 +209,41 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
       }
       mu4 = __ldg(reinterpret_cast<const uint4 *>(a.mu + i0));
     }
-    // pass 1: the common case for all 8 scalars; scalars that need the tail
-    // evaluation are deferred and then drained together, so that a warp pays
-    // for the tail code once per few deferred lanes instead of once per scalar
-    uint32_t pend = 0;
+    // pass 1: the common case for all 8 scalars.  Scalars that need the tail
+    // evaluation go to a per-warp queue, which the whole warp then works off
+    // 32 at a time, so that no lane idles through the (long) tail code.
+    uint16_t *q = s_queue + (threadIdx.x >> 5) * 256;
+    int qn = 0;
 #pragma unroll 1
-    for (int k = 0; k < 8 && act; ++k) {
+    for (int k = 0; k < 8; ++k) {
       bool deferred = false;
-      const float b = ideal_one<DT, false>(sym_at<DT>(kv4, k), mu_at(mu4, k),
-                                           __ldg(a.sigma + srow + k), a.phat, s_lo8, flags,
-                                           deferred);
-      if (deferred) pend |= 1u << k;
+      float b = 0.0f;
+      // e4m3 bins are wide against sigma, so the tail case is the common one
+      // there: evaluate it in place instead of queueing nearly every scalar
+      if (act)
+        b = ideal_one<DT, DT == 1>(sym_at<DT>(kv4, k), mu_at(mu4, k), __ldg(a.sigma + srow + k),
+                                   a.phat, s_lo8, flags, deferred);
       s_bits[k * 256 + threadIdx.x] = b;
+      const uint32_t dm = __ballot_sync(0xFFFFFFFFu, deferred);
+      if (deferred) q[qn + __popc(dm & ((1u << lane) - 1u))] = (uint16_t)((k << 5) | lane);
+      qn += __popc(dm);
     }
-    while (__any_sync(0xFFFFFFFFu, pend != 0)) {
-      if (pend) {
-        const int k = __ffs(pend) - 1;
-        pend &= pend - 1;
+    __syncwarp();
+    for (int base = 0; base < qn; base += 32) {
+      if (base + lane < qn) {
+        const uint32_t e = q[base + lane];
+        const int k = (int)(e >> 5), owner = (int)(e & 31u);
+        const uint64_t j = (uint64_t)(gw + owner) * 8 + k;  // the owner's scalar
+        const uint32_t sym = DT == 0 ? (uint32_t)static_cast<const uint16_t *>(a.kv)[j]
+                                     : (uint32_t)static_cast<const uint8_t *>(a.kv)[j];
+        const uint64_t srow_j = (j / TD) * D + (uint32_t)(j % D);
         bool unused = false;
-        s_bits[k * 256 + threadIdx.x] =
-            ideal_one<DT, true>(sym_at<DT>(kv4, k), mu_at(mu4, k), __ldg(a.sigma + srow + k),
-                                a.phat, s_lo8, flags, unused);
+        s_bits[k * 256 + (threadIdx.x & ~31) + owner] =
+            ideal_one<DT, true>(sym, (uint32_t)a.mu[j], __ldg(a.sigma + srow_j), a.phat, s_lo8,
+                                flags, unused);
       }
     }
+    __syncwarp();
     if (!act) continue;
     float bits[8], part = 0.0f;
 #pragma unroll
