@@ -50,7 +50,8 @@ def build(force: bool = False) -> str:
 class _Model(C.Structure):
     _fields_ = [("dtype", C.c_int32), ("L", C.c_int32), ("H", C.c_int32), ("T", C.c_int32),
                 ("D", C.c_int32), ("Tb", C.c_int32), ("G", C.c_int32), ("w1", C.c_int32),
-                ("w3", C.c_int32), ("we", C.c_int32), ("sigma", C.c_void_p), ("E", C.c_void_p),
+                ("w3", C.c_int32), ("we", C.c_int32), ("block_scale", C.c_int32),
+                ("sigma", C.c_void_p), ("E", C.c_void_p),
                 ("counts", C.c_void_p)]
 
 
@@ -85,6 +86,8 @@ def lib():
             "or_encode": (C.c_int, [P, vp, vp, vp, u64, C.POINTER(u64)]),
             "or_check_header": (C.c_int, [P, vp, u64]),
             "or_decode": (C.c_int, [P, vp, u64, vp, vp]),
+            "or_scale_mult": (C.c_float, [i32]),
+            "or_chunk_scales": (C.c_int, [P, vp, vp, u64, vp]),
             "or_log_q": (dbl, [dbl]),
             "or_log_mass": (dbl, [dbl, dbl]),
             "or_ideal_bits_one": (dbl, [P, u32, C.c_uint16, C.c_float]),
@@ -106,7 +109,7 @@ class Model:
     """Coding model: shape, chunking and the (sigma, p-hat) tables."""
 
     def __init__(self, dtype, L, H, T, D, Tb, G, sigma, E=None, counts=None,
-                 weights=(95, 3, 2)):
+                 weights=(95, 3, 2), block_scale=False):
         self.dtype = dtype
         self.sigma = np.ascontiguousarray(sigma, dtype=np.float32)
         assert self.sigma.size == L * 2 * H * D
@@ -118,7 +121,8 @@ class Model:
             assert self.E is not None and self.E.size == NSYM[BF16] + 1
         self.shape = (L, 2, H, T, D)
         self.s = _Model(dtype, L, H, T, D, Tb, G, weights[0], weights[1], weights[2],
-                        _ptr(self.sigma), _ptr(self.E), _ptr(self.counts))
+                        1 if block_scale else 0, _ptr(self.sigma), _ptr(self.E),
+                        _ptr(self.counts))
 
     @property
     def ref(self):
@@ -224,7 +228,7 @@ def encode_chunk(model, kv, mu, c):
 
 def _encode_chunk_raw(model, kv, mu, c):
     L, _, H, T, D = model.shape
-    cap = model.s.Tb * D + 2 * model.s.G
+    cap = model.s.Tb * D + 2 * model.s.G + (D // 8 + 3) // 4
     out = np.zeros(cap, dtype=np.uint32)
     nw = C.c_uint64(0)
     rc = lib().or_encode_chunk(model.ref, _ptr(kv), _ptr(mu), int(c), _ptr(out), cap,
@@ -273,6 +277,17 @@ def model_bits_chunk(model, kv, mu, c):
     if rc:
         raise RuntimeError("oracle model_bits rc=%d" % rc)
     return b.value
+
+
+def scale_mult(s):
+    return float(lib().or_scale_mult(int(s)))
+
+
+def chunk_scales(model, kv, mu, c):
+    kv, mu = _as_sym(model, kv), _as_mu(model, mu)
+    out = np.zeros(256, dtype=np.uint8)
+    lib().or_chunk_scales(model.ref, _ptr(kv), _ptr(mu), int(c), _ptr(out))
+    return out[: model.shape[4] // 8].copy()
 
 
 def log_q(z):

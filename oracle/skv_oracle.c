@@ -44,6 +44,18 @@
  *   R9  sigma is given per (layer, kv, head, channel); valid iff finite,
  *       >= FLT_MIN and 3 sigma finite.  mu must be finite.
  *   R10 ideal bits = -log2 q(x), q the exact bin mass of the continuous model.
+ *   R11 optional per-block sigma scales (section "下一步计划": sigma varies
+ *       with prompt and position, so a static per-channel sigma costs bits):
+ *       one byte s per (chunk, 8-channel group), sigma_eff = fp32(sigma m(s)),
+ *       m(s) = fp32(2^((s - 128) / 32)).  s = b + C, b the median of the
+ *       group's bins of |x - mu| / sigma, a bin being 32 (exponent + mantissa
+ *       fraction) read from the fp32 bits (floor of 32 log2 with the mantissa
+ *       taken as linear: 2.33 bins low on average).  C puts s at 128 when the
+ *       residuals follow the model with the static sigma: the median of |r|
+ *       is 0.706 sigma under 0.95 N(0, s^2) + 0.03 N(0, 9 s^2) (bf16: C = 18)
+ *       and 0.6745 sigma under N(0, s^2) (e4m3: C = 21).  A group whose
+ *       sigma_eff would leave the valid range takes s = 128.  The bytes open
+ *       the chunk's payload.
  */
 #include <float.h>
 #include <math.h>
@@ -317,12 +329,78 @@ static uint32_t sym_at(const or_model *m, const void *kv, uint64_t idx) {
   return m->dtype == OR_BF16 ? ((const uint16_t *)kv)[idx] : ((const uint8_t *)kv)[idx];
 }
 
+float or_scale_mult(int32_t s) { return (float)exp2((double)(s - 128) / 32.0); }
+
+static double sym_value(const or_model *m, uint32_t sym) {
+  return m->dtype == OR_BF16 ? or_bf16_value((uint16_t)sym) : or_e4m3_value((uint8_t)sym);
+}
+
+/* R11: one scale byte per 8-channel group of chunk c (the chunk's tokens) */
+int or_chunk_scales(const or_model *m, const void *kv, const uint16_t *mu, uint64_t c,
+                    uint8_t *scales) {
+  init_tables();
+  geom_t g = chunk_geom(m, c);
+  const uint64_t ntok = 8 * g.ngroup / (uint64_t)m->D;
+  for (int32_t grp = 0; grp < m->D / 8; ++grp) {
+    uint64_t hist[256];
+    memset(hist, 0, sizeof(hist));
+    uint64_t n = 0;
+    for (uint64_t t = 0; t < ntok; ++t) {
+      for (int32_t k = 0; k < 8; ++k) {
+        const int32_t d = 8 * grp + k;
+        const uint64_t idx = g.base + t * (uint64_t)m->D + (uint64_t)d;
+        const float x = (float)sym_value(m, sym_at(m, kv, idx));
+        const float muv = mu_value(mu[idx]);
+        const float inv = 1.0f / m->sigma[g.srow + (uint64_t)d];
+        const float a = fabsf(x - muv) * inv;
+        int32_t bin;
+        if (!(a > 0.0f)) bin = 0;
+        else if (!isfinite(a)) bin = 255;
+        else {
+          uint32_t b;
+          memcpy(&b, &a, 4);
+          bin = (int32_t)(b >> 18) - 127 * 32 + 128; /* 32 * log2 with a linear mantissa */
+          bin = bin < 0 ? 0 : (bin > 255 ? 255 : bin);
+        }
+        hist[bin]++;
+        n++;
+      }
+    }
+    int32_t med = 0;
+    uint64_t acc = 0;
+    for (int32_t b = 0; b < 256; ++b) {
+      acc += hist[b];
+      if (acc >= (n + 1) / 2) {
+        med = b;
+        break;
+      }
+    }
+    int32_t sc = med + (m->dtype == OR_BF16 ? 18 : 21);
+    sc = sc < 0 ? 0 : (sc > 255 ? 255 : sc);
+    for (int32_t k = 0; k < 8; ++k)
+      if (!or_sigma_valid(m->sigma[g.srow + (uint64_t)(8 * grp + k)] * or_scale_mult(sc))) sc = 128;
+    scales[grp] = (uint8_t)sc;
+  }
+  return OR_OK;
+}
+
+static float sigma_eff(const or_model *m, const geom_t *g, const uint8_t *scales, uint64_t p) {
+  const uint64_t d = p % (uint64_t)m->D;
+  const float s = m->sigma[g->srow + d];
+  return m->block_scale ? s * or_scale_mult(scales[d / 8]) : s;
+}
+
+static uint64_t scale_words(const or_model *m) {
+  return m->block_scale ? (uint64_t)(m->D / 8 + 3) / 4 : 0;
+}
+
 int or_model_check(const or_model *m) {
   if (m->dtype != OR_BF16 && m->dtype != OR_E4M3) return OR_ERR_ARG;
   if (m->L <= 0 || m->H <= 0 || m->T <= 0 || m->D <= 0 || m->Tb <= 0) return OR_ERR_ARG;
   if (m->D % 8) return OR_ERR_ARG;
   if (m->G < 1 || m->G > 32 || (m->G & (m->G - 1))) return OR_ERR_ARG;
   if (m->w1 + m->w3 + m->we != 100) return OR_ERR_ARG;
+  if (m->block_scale != 0 && m->block_scale != 1) return OR_ERR_ARG;
   return OR_OK;
 }
 
@@ -346,7 +424,10 @@ int or_encode_chunk(const or_model *m, const void *kv, const uint16_t *mu, uint6
   const int G = m->G;
   geom_t g = chunk_geom(m, c);
   uint64_t n0 = lane_nsym(&g, G, 0);
-  uint64_t cap = 8 * g.ngroup + 2 * (uint64_t)G;
+  uint8_t scales[256];
+  if (m->block_scale) or_chunk_scales(m, kv, mu, c, scales);
+  const uint64_t nsw = scale_words(m);
+  uint64_t cap = 8 * g.ngroup + 2 * (uint64_t)G + nsw;
   uint32_t *stack = (uint32_t *)malloc(sizeof(uint32_t) * cap);
   if (!stack) return OR_ERR_ARG;
   uint64_t sp = 0;
@@ -361,6 +442,7 @@ int or_encode_chunk(const or_model *m, const void *kv, const uint16_t *mu, uint6
       float sigma = m->sigma[g.srow + p % (uint64_t)m->D];
       float muv = mu_value(mu[idx]);
       if (!or_sigma_valid(sigma) || !isfinite(muv)) { free(stack); return OR_ERR_PARAM; }
+      sigma = sigma_eff(m, &g, scales, p);
       int32_t r = or_rank(m->dtype, sym_at(m, kv, idx));
       if (r < 0) { free(stack); return OR_ERR_SYMBOL; }
       uint32_t cr = or_cum(m, r, muv, sigma);
@@ -376,6 +458,15 @@ int or_encode_chunk(const or_model *m, const void *kv, const uint16_t *mu, uint6
   for (int l = G - 1; l >= 0; --l) {
     stack[sp++] = (uint32_t)(x[l] >> 32);
     stack[sp++] = (uint32_t)x[l];
+  }
+  /* the scale bytes open the chunk: word w holds groups 4w..4w+3, low byte first */
+  for (uint64_t wi = nsw; wi-- > 0;) {
+    uint32_t word = 0;
+    for (int b = 3; b >= 0; --b) {
+      const uint64_t grp = 4 * wi + (uint64_t)b;
+      word = (word << 8) | (grp < (uint64_t)(m->D / 8) ? scales[grp] : 0u);
+    }
+    stack[sp++] = word;
   }
   *nwords = sp;
   if (sp > cap_words) { free(stack); return OR_ERR_CAPACITY; }
@@ -405,10 +496,23 @@ int or_decode_chunk(const or_model *m, const uint32_t *w, uint64_t nwords, const
   const int G = m->G;
   geom_t g = chunk_geom(m, c);
   uint64_t n0 = lane_nsym(&g, G, 0);
-  if (nwords < 2 * (uint64_t)G) return OR_ERR_CORRUPT;
+  const uint64_t nsw = scale_words(m);
+  if (nwords < 2 * (uint64_t)G + nsw) return OR_ERR_CORRUPT;
+  uint8_t scales[256];
+  for (int32_t grp = 0; grp < m->D / 8; ++grp) {
+    scales[grp] = (uint8_t)(w[grp / 4] >> (8 * (grp % 4)));
+    /* a scale the encoder cannot have chosen (an invalid static sigma is the
+       caller's error, reported per symbol below) */
+    for (int32_t k = 0; m->block_scale && k < 8; ++k) {
+      const float sg = m->sigma[g.srow + (uint64_t)(8 * grp + k)];
+      if (or_sigma_valid(sg) && !or_sigma_valid(sg * or_scale_mult(scales[grp])))
+        return OR_ERR_CORRUPT;
+    }
+  }
+  const uint32_t *ws = w + nsw;
   uint64_t x[32];
-  for (int l = 0; l < G; ++l) x[l] = (uint64_t)w[2 * l] | ((uint64_t)w[2 * l + 1] << 32);
-  uint64_t cur = 2 * (uint64_t)G;
+  for (int l = 0; l < G; ++l) x[l] = (uint64_t)ws[2 * l] | ((uint64_t)ws[2 * l + 1] << 32);
+  uint64_t cur = 2 * (uint64_t)G + nsw;
 
   for (uint64_t j = 0; j < n0; ++j) {
     for (int l = 0; l < G; ++l) {
@@ -418,6 +522,7 @@ int or_decode_chunk(const or_model *m, const uint32_t *w, uint64_t nwords, const
       float sigma = m->sigma[g.srow + p % (uint64_t)m->D];
       float muv = mu_value(mu[idx]);
       if (!or_sigma_valid(sigma) || !isfinite(muv)) return OR_ERR_PARAM;
+      sigma = sigma_eff(m, &g, scales, p);
       uint32_t slot = (uint32_t)(x[l] & mask);
       int32_t r = find_rank(m, slot, muv, sigma);
       uint32_t cr = or_cum(m, r, muv, sigma);
@@ -480,6 +585,7 @@ static void write_header(const or_model *m, uint8_t *h, uint64_t nchunks, uint64
   h[34] = 8;
   h[35] = 9;
   put16(h + 36, 8);
+  put16(h + 38, (uint16_t)(m->block_scale ? 1 : 0)); /* feature bits */
   put64(h + 40, nchunks);
   put64(h + 48, payload);
   put64(h + 56, or_model_hash(m));
@@ -488,7 +594,7 @@ static void write_header(const or_model *m, uint8_t *h, uint64_t nchunks, uint64
 uint64_t or_max_encoded_bytes(const or_model *m) {
   uint64_t n = (uint64_t)m->L * 2 * m->H * m->T * m->D;
   uint64_t nc = or_num_chunks(m);
-  return 64 + 8 * (nc + 1) + 4 * (n + 2 * (uint64_t)m->G * nc);
+  return 64 + 8 * (nc + 1) + 4 * (n + (2 * (uint64_t)m->G + scale_words(m)) * nc);
 }
 
 int or_encode(const or_model *m, const void *kv, const uint16_t *mu, uint8_t *out, uint64_t cap,
@@ -504,7 +610,7 @@ int or_encode(const or_model *m, const void *kv, const uint16_t *mu, uint8_t *ou
     uint64_t room = (cap - head - pos) / 4, nw = 0;
     /* words are assembled in a scratch buffer to keep the output byte order explicit */
     geom_t g = chunk_geom(m, c);
-    uint64_t need = 8 * g.ngroup + 2 * (uint64_t)m->G;
+    uint64_t need = 8 * g.ngroup + 2 * (uint64_t)m->G + scale_words(m);
     uint32_t *tmp = (uint32_t *)malloc(sizeof(uint32_t) * need);
     if (!tmp) return OR_ERR_ARG;
     rc = or_encode_chunk(m, kv, mu, c, tmp, need, &nw);
@@ -641,28 +747,36 @@ int or_ideal_bits(const or_model *m, const void *kv, const uint16_t *mu, uint64_
   double stot = 0;
   if (m->dtype == OR_BF16)
     for (int32_t k = 0; k < NSYM_BF16; ++k) stot += (double)m->counts[g_bits_bf16[k]] + 1.0;
-  uint64_t TD = (uint64_t)m->T * m->D;
   double acc = 0;
-  for (uint64_t i = begin; i < end; ++i) {
-    uint32_t sym = sym_at(m, kv, i);
-    int32_t r = or_rank(m->dtype, sym);
-    if (r < 0) return OR_ERR_SYMBOL;
-    float sigma = m->sigma[(i / TD) * m->D + i % m->D];
-    double muv = or_bf16_value(mu[i]);
-    if (!or_sigma_valid(sigma) || !isfinite(muv)) return OR_ERR_PARAM;
-    double s = (double)sigma;
-    double lo = (double)or_lo(m->dtype, r), hi = (double)or_lo(m->dtype, r + 1);
-    double bits;
-    if (m->dtype == OR_E4M3) {
-      bits = -log_gauss_bin(lo, hi, muv, s) / M_LN2;
-    } else {
-      double lp1 = log(m->w1 / 100.0) + log_gauss_bin(lo, hi, muv, s);
-      double lp3 = log(m->w3 / 100.0) + log_gauss_bin(lo, hi, muv, 3.0 * s);
-      double lpe = log(m->we / 100.0) + log(((double)m->counts[sym] + 1.0) / stot);
-      bits = -lse3(lp1, lp3, lpe) / M_LN2;
+  const uint64_t nc = or_num_chunks(m);
+  for (uint64_t c = 0; c < nc; ++c) {
+    geom_t g = chunk_geom(m, c);
+    const uint64_t c0 = g.base, c1 = g.base + 8 * g.ngroup;
+    if (c1 <= begin || c0 >= end) continue;
+    uint8_t scales[256];
+    if (m->block_scale) or_chunk_scales(m, kv, mu, c, scales);
+    for (uint64_t i = c0 > begin ? c0 : begin; i < (c1 < end ? c1 : end); ++i) {
+      uint32_t sym = sym_at(m, kv, i);
+      int32_t r = or_rank(m->dtype, sym);
+      if (r < 0) return OR_ERR_SYMBOL;
+      float sigma = m->sigma[g.srow + (i - g.base) % (uint64_t)m->D];
+      double muv = or_bf16_value(mu[i]);
+      if (!or_sigma_valid(sigma) || !isfinite(muv)) return OR_ERR_PARAM;
+      sigma = sigma_eff(m, &g, scales, i - g.base);
+      double s = (double)sigma;
+      double lo = (double)or_lo(m->dtype, r), hi = (double)or_lo(m->dtype, r + 1);
+      double bits;
+      if (m->dtype == OR_E4M3) {
+        bits = -log_gauss_bin(lo, hi, muv, s) / M_LN2;
+      } else {
+        double lp1 = log(m->w1 / 100.0) + log_gauss_bin(lo, hi, muv, s);
+        double lp3 = log(m->w3 / 100.0) + log_gauss_bin(lo, hi, muv, 3.0 * s);
+        double lpe = log(m->we / 100.0) + log(((double)m->counts[sym] + 1.0) / stot);
+        bits = -lse3(lp1, lp3, lpe) / M_LN2;
+      }
+      if (per_scalar) per_scalar[i - begin] = bits;
+      acc += bits;
     }
-    if (per_scalar) per_scalar[i - begin] = bits;
-    acc += bits;
   }
   *total = acc;
   return OR_OK;
@@ -674,10 +788,12 @@ int or_model_bits_chunk(const or_model *m, const void *kv, const uint16_t *mu, u
   init_tables();
   const int M = m->dtype == OR_BF16 ? 28 : 16;
   geom_t g = chunk_geom(m, c);
+  uint8_t scales[256];
+  if (m->block_scale) or_chunk_scales(m, kv, mu, c, scales);
   double acc = 0;
   for (uint64_t p = 0; p < 8 * g.ngroup; ++p) {
     uint64_t idx = g.base + p;
-    float sigma = m->sigma[g.srow + p % (uint64_t)m->D];
+    float sigma = sigma_eff(m, &g, scales, p);
     float muv = mu_value(mu[idx]);
     int32_t r = or_rank(m->dtype, sym_at(m, kv, idx));
     if (r < 0) return OR_ERR_SYMBOL;

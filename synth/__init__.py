@@ -22,7 +22,12 @@ shapes stand in for them:
 * p-hat counts: a histogram of the calibration draws' x by bf16 bit pattern
   (seed 1 for the tiny workload, seeds 1..128 of 512 tokens otherwise);
 * e4m3 workloads: s = absmax|x| / 448 per (layer, head), x8 = e4m3(x / s)
-  saturated to +-448, mu = bf16(fp32(mu) / s), sigma = sc / s.
+  saturated to +-448, mu = bf16(fp32(mu) / s), sigma = sc / s;
+* position-varying error scale (``drift`` > 0; the pages, section "下一步计划",
+  note that sigma varies with prompt and position): sc is multiplied by
+  exp(drift * W(t)) per (layer, kv, head), W a Brownian path over the tokens
+  with Var W(T) = 1 (cumulative sums of N(0, 1/T)), drawn per seed, so the
+  static sigma table sees only its average.
 
 Torch is used as the random-number and array library on whatever device the
 caller names; the bytes it produces are what both sides consume.
@@ -52,6 +57,7 @@ class Spec:
     calibrated_sigma: bool
     Tb: int
     G: int
+    drift: float = 0.0         # std of the log error scale's walk over the sequence
 
     @property
     def n(self) -> int:
@@ -76,6 +82,9 @@ WORKLOADS = {
     # long-context FP8 stress: 64 x {K,V} x 8 x 32768 x 128 = 2^32 e4m3 scalars
     "long-32k-e4m3": Spec("long-32k-e4m3", E4M3, 64, 8, 32768, 128, 0.03, True, 0, 512, False,
                           128, 4),
+    # the Qwen3-0.6B shape with an error scale that drifts along the sequence
+    "qwen3-0.6b-bf16-drift": Spec("qwen3-0.6b-bf16-drift", BF16, 28, 8, 4096, 128, 0.03, True,
+                                  128, 512, False, 256, 16, 1.0),
 }
 
 
@@ -111,6 +120,10 @@ def _draw_layer(spec: Spec, scale_l: torch.Tensor, seed: int, layer: int, T: int
     s = scale_l[:, :, None, :]
     x = (s * torch.randn(shp, generator=g, device=device)).to(torch.bfloat16)
     sc = spec.sigma_c * s
+    if spec.drift > 0:
+        gd = _gen(device, spec.name, "drift", seed, layer)
+        walk = torch.cumsum(torch.randn(2, spec.H, T, generator=gd, device=device), dim=2)
+        sc = sc * torch.exp(spec.drift * walk / T ** 0.5)[..., None]
     u = torch.rand(shp, generator=g, device=device)
     n = torch.randn(shp, generator=g, device=device)
     e = torch.empty(shp, device=device).exponential_(1.0, generator=g)
