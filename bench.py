@@ -30,8 +30,10 @@ if ROOT not in sys.path:
 METRIC = "raw-KV encode & decode GB/s on 1 GB300 (% of roofline); bits/scalar vs ideal"
 DEFAULT_WORKLOAD = "qwen3-0.6b-bf16"
 # launches of our kernels per step: encode (prep, encode, 2 scans, compact),
-# decode (prep, header check, decode), ideal bits (prep, bits, final sum)
+# decode (prep, header check, decode), ideal bits (prep, bits, final sum); with
+# per-block scales one more in each (scale estimate, scale load, scale estimate)
 LAUNCHES_PER_STEP = 11
+LAUNCHES_BLOCK_SCALE = 3
 
 
 def _dist():
@@ -244,14 +246,15 @@ def _scratch_for(kv):
     return _SCRATCH[key]
 
 
-def oracle_setup(workload_name, seed, device):
+def oracle_setup(workload_name, seed, device, block_scale=False):
     import oracle as O
     import synth
     O.build()
     w = synth.make(workload_name, device=device, seed=seed)
     kv, mu, sigma, counts = synth.to_numpy(w)
     s = w.spec
-    m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sigma, counts=counts)
+    m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sigma, counts=counts,
+                block_scale=block_scale)
     return O, w, m, kv.reshape(-1), mu.reshape(-1)
 
 
@@ -293,8 +296,10 @@ def run_gpu(args):
         E, ph = P.skv_build_ecdf(w.counts.cpu().numpy().astype(np.uint64))
         ecdf = torch.from_numpy(E.view(np.int32)).to(dev)
         phat = torch.from_numpy(ph).to(dev)
+    flags = (P.SKV_FLAG_DECODE_BISECT if args.decode_bisect else 0) | (
+        P.SKV_FLAG_BLOCK_SCALE if args.block_scale else 0)
     codec = P.Codec(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, w.sigma.to(dev), ecdf, phat,
-                    flags=P.SKV_FLAG_DECODE_BISECT if args.decode_bisect else 0)
+                    flags=flags)
     kv = (w.kv.view(torch.int16) if s.dtype == synth.BF16 else w.kv).reshape(-1)
     mu = w.mu.view(torch.int16).reshape(-1)
     n = s.n
@@ -428,7 +433,8 @@ def finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value, t_enc, t
     if world == 1 and not args.no_cpu_baseline:
         import oracle as O
         kvn, mun, sig, cnt = synth.to_numpy(w)
-        m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sig, counts=cnt)  # same chunking
+        m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sig, counts=cnt,  # same chunking
+                    block_scale=args.block_scale)
         nch = m.num_chunks()
         sc, dt, chunks = time_oracle(O, m, kvn.reshape(-1), mun.reshape(-1), nch,
                                      args.cpu_sample_chunks)
@@ -446,6 +452,7 @@ def finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value, t_enc, t
         "config": {"workload": args.workload, "symbols": "bf16" if bps == 2 else "e4m3",
                    "layers": s.L, "heads": s.H, "tokens": s.T, "head_dim": s.D,
                    "scalars_per_gpu": n, "token_block": s.Tb, "lanes": s.G,
+                   "block_scale": bool(args.block_scale),
                    "parallelism": "dp%d (independent caches)" % world,
                    "l2": "inputs larger than L2: %.0f MB KV + %.0f MB mu per step" % (
                        raw / 1e6, 2 * n / 1e6)},
@@ -459,7 +466,8 @@ def finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value, t_enc, t
         "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": (LAUNCHES_PER_STEP + (LAUNCHES_BLOCK_SCALE if args.block_scale else 0))
+                        * args.steps,
         "clocks": clk.summary(),
     }
     return line
@@ -472,7 +480,7 @@ def run_reference(args):
         return None
     import torch
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    O, w, m, kv, mu = oracle_setup(args.workload, 0, device)
+    O, w, m, kv, mu = oracle_setup(args.workload, 0, device, block_scale=args.block_scale)
     s = w.spec
     bps = 2 if s.dtype == 0 else 1
     nch = m.num_chunks()
@@ -501,7 +509,7 @@ def run_reference(args):
         "ms_per_step": round(1e3 * dt / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
         "config": {"workload": args.workload, "scalars_per_gpu": s.n, "token_block": s.Tb,
-                   "lanes": s.G},
+                   "lanes": s.G, "block_scale": bool(args.block_scale)},
         "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": "%d chunks per step of %d scalars each (every %d-th chunk), "
                                    "encode + decode + ideal bits" % (per_step, s.Tb * s.D, stride)},
@@ -525,6 +533,8 @@ def main(argv=None):
     ap.add_argument("--token-block", type=int, default=0, help="override the token block")
     ap.add_argument("--decode-bisect", action="store_true",
                     help="decode with the reference bisection search")
+    ap.add_argument("--block-scale", action="store_true",
+                    help="per-(chunk, 8-channel group) sigma scales in the container")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "skv":
         args.warmup = 3

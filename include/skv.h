@@ -94,6 +94,18 @@ typedef struct {
 /* skv_params.flags bits (all others must be 0). */
 #define SKV_FLAG_DECODE_BISECT 1 /* decode by plain bisection over ranks (reference
                                     search; the output is identical, only slower) */
+/* Per-block sigma scales (the pages' section "下一步计划": the error scale moves
+ * with prompt and position).  Every (chunk, 8-channel group) codes with
+ * sigma_eff = fp32(sigma * m(s)), m(s) = fp32(2^((s - 128) / 32)), s one byte
+ * chosen by the encoder: b + C, b the median over the group's residuals of
+ * the bin (bits(|x - mu| / sigma) >> 18) - 127*32 + 128 clamped to [0, 255]
+ * (0 for a zero or NaN residual, 255 for infinity), C = 18 (bf16) or 21
+ * (e4m3); 128 if sigma_eff would be invalid for a channel of the group.  The
+ * bytes travel in the container (header feature bit 0, ceil(head_dim / 32)
+ * words at the start of each chunk).  Requires head_dim <= 2048.  Encode,
+ * decode and ideal bits must all be given the flag; skv_ideal_bits_noalloc
+ * rejects it (SKV_ERR_ARG). */
+#define SKV_FLAG_BLOCK_SCALE 2
 
 typedef struct {
   int32_t dtype;
@@ -123,11 +135,14 @@ size_t skv_workspace_bytes(const skv_params *params, const skv_shape *shape, int
  *   out_bytes     host; receives the container size.
  * Container v1 (little-endian): a 64-byte header {u32 magic "SKV1", u16 version
  * 1, u8 dtype, u8 M, u32 layers, u32 2, u32 heads, u32 tokens, u32 head_dim,
- * u32 token_block, u16 lanes, u8 8, u8 9, u16 8, u16 0, u64 num_chunks, u64
- * payload_bytes, u64 model fingerprint of sigma (and E_q for bf16)}, then u64
- * offsets[num_chunks + 1] (byte offsets from the payload start), then the
- * payload: chunk c (index ((l*2 + kv)*heads + h)*ceil(tokens/Tb) + tb) is u32
- * words in decoder order -- lane states (lo, hi) for lanes 0..G-1, then the
+ * u32 token_block, u16 lanes, u8 8, u8 9, u16 8, u16 features (bit 0:
+ * SKV_FLAG_BLOCK_SCALE), u64 num_chunks, u64 payload_bytes, u64 model
+ * fingerprint of sigma (and E_q for bf16)}, then u64 offsets[num_chunks + 1]
+ * (byte offsets from the payload start, multiples of 4), then the payload:
+ * chunk c (index ((l*2 + kv)*heads + h)*ceil(tokens/Tb) + tb) is u32 words in
+ * decoder order -- with per-block scales first ceil(head_dim / 32) words
+ * holding the scale bytes (group g in word g / 4, byte g % 4, low byte first;
+ * unused bytes 0), then the lane states (lo, hi) for lanes 0..G-1, then the
  * renormalisation words.  Errors: SKV_ERR_ARG, SKV_ERR_CAPACITY (out or
  * workspace too small; nothing useful is written), SKV_ERR_SYMBOL,
  * SKV_ERR_PARAM, SKV_ERR_CUDA.  Synchronizes `stream`. */
@@ -169,6 +184,8 @@ int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void 
  * device that loads the library until the process exits; the call allocates
  * nothing.  Shapes whose (layers * 2 * heads * head_dim) sigma entries exceed
  * skv_ideal_bits_noalloc_max_channels() are rejected with SKV_ERR_CAPACITY.
+ * SKV_FLAG_BLOCK_SCALE is rejected with SKV_ERR_ARG: its per-(chunk, channel)
+ * table grows with the cache and has no fixed bound.
  * Every call shares that one array, so calls that may overlap on the GPU (on
  * different streams, or from different host threads) race; serialise them.
  * The first call on a device looks up the array's device address and uploads

@@ -27,6 +27,7 @@ inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 uint32_t g_phi_host[kPhiKnots];
 float g_lo8_host[256];
 float g_hinv_host[2][kHinvN + 1];
+float g_scale_mult_host[256];
 std::once_flag g_const_once;
 
 double e4m3_value_host(uint32_t u) {
@@ -71,6 +72,9 @@ void build_constants() {
       g_hinv_host[t][k] = (float)(z < -14.0 ? -14.0 : (z > 14.0 ? 14.0 : z));
     }
   }
+  // per-block scale multipliers m(s) = fp32(2^((s - 128) / 32)); binary64 exp2
+  // is within an ulp of 2^(k/32), whose fp32 rounding is never that close to a tie
+  for (int k = 0; k < 256; ++k) g_scale_mult_host[k] = (float)std::exp2((k - 128) / 32.0);
 }
 
 std::mutex g_dev_mu;
@@ -85,6 +89,7 @@ int ensure_device_tables() {
   if (!g_dev_ready[dev]) {
     if (upload_tables(g_phi_host, g_lo8_host, g_hinv_host[0], g_hinv_host[1]) != cudaSuccess)
       return SKV_ERR_CUDA;
+    if (upload_scale_mult(g_scale_mult_host) != cudaSuccess) return SKV_ERR_CUDA;
     g_dev_ready[dev] = true;
   }
   return SKV_OK;
@@ -94,8 +99,12 @@ struct Plan {
   Geo geo;
   int dtype;
   int64_t nsig;
+  int32_t nsw;     // per-block scale words per chunk (0: static sigma)
   // workspace layout (byte offsets)
   size_t off_inv, off_sizes, off_starts, off_partials, off_scratch, off_bits, off_einv, total;
+  size_t off_enc_cinv, off_enc_words, enc_total;  // encode: per-chunk tables after the stacks
+  size_t off_dec_cinv, dec_total;                 // decode: after the inverse p-hat table
+  size_t off_bits_csig, bits_total;               // ideal bits: after the partial sums
   int64_t stride;  // words per chunk stack
   int bits_blocks;
 };
@@ -105,10 +114,12 @@ bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   if (!p || !s || !out) return SKV_ERR_ARG;
   if (p->dtype != SKV_BF16 && p->dtype != SKV_E4M3) return SKV_ERR_ARG;
-  if (p->flags & ~SKV_FLAG_DECODE_BISECT) return SKV_ERR_ARG;
+  if (p->flags & ~(SKV_FLAG_DECODE_BISECT | SKV_FLAG_BLOCK_SCALE)) return SKV_ERR_ARG;
   if (s->kv != 2 || s->layers <= 0 || s->heads <= 0 || s->tokens <= 0 || s->head_dim <= 0)
     return SKV_ERR_ARG;
   if (s->head_dim % 8) return SKV_ERR_ARG;
+  const bool scaled = (p->flags & SKV_FLAG_BLOCK_SCALE) != 0;
+  if (scaled && s->head_dim > kMaxScaledD) return SKV_ERR_ARG;
   const int G = p->lanes;
   if (G < 1 || G > 32 || (G & (G - 1))) return SKV_ERR_ARG;
   if (p->token_block <= 0) return SKV_ERR_ARG;
@@ -136,7 +147,8 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   const int64_t nlane = 8 * ((ngroup + G - 1) / G);
   int64_t wl = (nlane * (M + 1) + 31) / 32;
   if (wl > nlane) wl = nlane;
-  pl.stride = ((G * (wl + 2)) + 3) / 4 * 4;
+  pl.nsw = scaled ? scale_words(s->head_dim) : 0;
+  pl.stride = ((G * (wl + 2)) + pl.nsw + 3) / 4 * 4;
   size_t off = align_up(sizeof(WsHead));
   pl.off_inv = off;
   off = align_up(off + sizeof(float2) * (size_t)pl.nsig);
@@ -154,14 +166,23 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   pl.bits_blocks = (int)(nb < 4096 ? (nb > 0 ? nb : 1) : 4096);
   pl.off_bits = align_up(pl.off_inv + sizeof(float2) * (size_t)pl.nsig);
   pl.off_einv = pl.off_bits;  // decode only: the inverse p-hat table follows the reciprocals
+  // per-block scales: (chunk, channel) tables appended to each operation's layout
+  const size_t ccells = scaled ? (size_t)pl.geo.nchunks * (size_t)s->head_dim : 0;
+  pl.off_enc_cinv = pl.total;
+  pl.off_enc_words = align_up(pl.off_enc_cinv + sizeof(float2) * ccells);
+  pl.enc_total = align_up(pl.off_enc_words + sizeof(uint32_t) * (size_t)pl.nsw * (size_t)pl.geo.nchunks);
+  pl.off_dec_cinv = align_up(pl.off_einv + sizeof(int32_t) * (kHinvN + 1));
+  pl.dec_total = align_up(pl.off_dec_cinv + sizeof(float2) * ccells);
+  pl.off_bits_csig = align_up(pl.off_bits + sizeof(double) * (size_t)pl.bits_blocks);
+  pl.bits_total = align_up(pl.off_bits_csig + sizeof(float) * ccells);
   *out = pl;
   return SKV_OK;
 }
 
 size_t ws_bytes_for(const Plan &pl, int op) {
-  if (op == SKV_OP_ENCODE) return pl.total;
-  if (op == SKV_OP_DECODE) return align_up(pl.off_einv + sizeof(int32_t) * (kHinvN + 1));
-  return align_up(pl.off_bits + sizeof(double) * (size_t)pl.bits_blocks);
+  if (op == SKV_OP_ENCODE) return pl.enc_total;
+  if (op == SKV_OP_DECODE) return pl.dec_total;
+  return pl.bits_total;
 }
 
 uint64_t hash_words(const Plan &pl) {
@@ -190,6 +211,16 @@ int common_inputs(const skv_params *p, const Plan &pl, const void *kv, const uin
   if (!aligned(kv, 16) || !aligned(mu, 16) || !aligned(p->sigma, 4)) return SKV_ERR_ARG;
   if (pl.dtype == SKV_BF16 && (!p->ecdf || !aligned(p->ecdf, 4))) return SKV_ERR_ARG;
   return SKV_OK;
+}
+
+ScaleLaunch scale_launch(const Plan &pl, const skv_params *p, WsHead *head) {
+  ScaleLaunch sl;
+  std::memset(&sl, 0, sizeof(sl));
+  sl.geo = pl.geo;
+  sl.dtype = pl.dtype;
+  sl.sigma = p->sigma;
+  sl.head = head;
+  return sl;
 }
 
 // ---- scratch for skv_ideal_bits_noalloc ----
@@ -224,7 +255,7 @@ size_t skv_max_encoded_bytes(const skv_params *params, const skv_shape *shape) {
   Plan pl;
   if (make_plan(params, shape, &pl) != SKV_OK) return 0;
   return 64 + 8 * (size_t)(pl.geo.nchunks + 1) +
-         4 * ((size_t)pl.geo.n + 2 * (size_t)pl.geo.G * (size_t)pl.geo.nchunks);
+         4 * ((size_t)pl.geo.n + (2 * (size_t)pl.geo.G + (size_t)pl.nsw) * (size_t)pl.geo.nchunks);
 }
 
 size_t skv_workspace_bytes(const skv_params *params, const skv_shape *shape, int op) {
@@ -258,6 +289,19 @@ int skv_encode(const skv_params *params, const skv_shape *shape, const void *kv,
   a.kv = kv;
   a.mu = mu;
   a.inv = inv;
+  a.inv_chunk = nullptr;
+  a.scale_words = nullptr;
+  a.nsw = pl.nsw;
+  if (pl.nsw) {
+    ScaleLaunch sl = scale_launch(pl, params, head);
+    sl.kv = kv;
+    sl.mu = mu;
+    sl.inv = reinterpret_cast<float2 *>(ws + pl.off_enc_cinv);
+    sl.words = reinterpret_cast<uint32_t *>(ws + pl.off_enc_words);
+    if (launch_scales(sl, st) != cudaSuccess) return SKV_ERR_CUDA;
+    a.inv_chunk = sl.inv;
+    a.scale_words = sl.words;
+  }
   a.ecdf = ecdf;
   a.scratch = reinterpret_cast<uint32_t *>(ws + pl.off_scratch);
   a.stride = pl.stride;
@@ -301,6 +345,16 @@ int skv_decode(const skv_params *params, const skv_shape *shape, const void *in,
   a.in_bytes = in_bytes;
   a.mu = mu;
   a.inv = inv;
+  a.inv_chunk = nullptr;
+  a.nsw = pl.nsw;
+  if (pl.nsw) {
+    ScaleLaunch sl = scale_launch(pl, params, head);
+    sl.in = static_cast<const uint8_t *>(in);
+    sl.in_bytes = in_bytes;
+    sl.inv = reinterpret_cast<float2 *>(ws + pl.off_dec_cinv);
+    if (launch_scales(sl, st) != cudaSuccess) return SKV_ERR_CUDA;
+    a.inv_chunk = sl.inv;
+  }
   a.ecdf = ecdf;
   a.kv_out = kv_out;
   a.head = head;
@@ -343,6 +397,15 @@ int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void 
   a.kv = kv;
   a.mu = mu;
   a.sigma = params->sigma;
+  a.sigma_chunk = nullptr;
+  if (pl.nsw) {
+    ScaleLaunch sl = scale_launch(pl, params, head);
+    sl.kv = kv;
+    sl.mu = mu;
+    sl.sig = reinterpret_cast<float *>(ws + pl.off_bits_csig);
+    if (launch_scales(sl, st) != cudaSuccess) return SKV_ERR_CUDA;
+    a.sigma_chunk = sl.sig;
+  }
   a.phat = params->phat;
   a.per_scalar = per_scalar;
   a.partials = reinterpret_cast<double *>(ws + pl.off_bits);
@@ -364,6 +427,8 @@ int skv_ideal_bits_noalloc(const skv_params *params, const skv_shape *shape, con
   if (rc) return rc;
   if ((rc = common_inputs(params, pl, kv, mu))) return rc;
   if (!total) return SKV_ERR_ARG;
+  // the per-(chunk, channel) table of per-block scales grows with the cache
+  if (pl.nsw) return SKV_ERR_ARG;
   if (per_scalar && !aligned(per_scalar, 16)) return SKV_ERR_ARG;
   if (pl.dtype == SKV_BF16 && (!params->phat || !aligned(params->phat, 4))) return SKV_ERR_ARG;
   // the same layout as the workspace of skv_ideal_bits, inside the fixed array
@@ -383,6 +448,7 @@ int skv_ideal_bits_noalloc(const skv_params *params, const skv_shape *shape, con
   a.kv = kv;
   a.mu = mu;
   a.sigma = params->sigma;
+  a.sigma_chunk = nullptr;
   a.phat = params->phat;
   a.per_scalar = per_scalar;
   a.partials = reinterpret_cast<double *>(ws + pl.off_bits);

@@ -166,6 +166,18 @@ __device__ __forceinline__ uint32_t mu_at(uint4 mu4, int k) {
   return (w >> (16 * (k & 1))) & 0xFFFFu;
 }
 
+// Index of scalar i's sigma: (row, channel) in the static table, or (chunk,
+// channel) in the per-block table.
+__device__ __forceinline__ uint64_t sigma_index(const IdealLaunch &a, uint64_t i, uint64_t TD) {
+  const uint64_t D = (uint64_t)a.geo.D;
+  const uint64_t row = i / TD, in_row = i - row * TD;
+  if (!a.sigma_chunk) return row * D + in_row % D;
+  const uint64_t cw = D * (uint64_t)a.geo.Tb;  // scalars of a full chunk
+  const uint64_t tb = (TD >> 32) == 0 && (cw >> 32) == 0 ? (uint32_t)in_row / (uint32_t)cw
+                                                         : in_row / cw;
+  return (row * (uint64_t)a.geo.ntb + tb) * D + in_row % D;
+}
+
 template <int DT>
 __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
   __shared__ float s_lo8[256];
@@ -184,8 +196,8 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
     __syncthreads();
   }
   const uint64_t TD = (uint64_t)a.geo.T * (uint64_t)a.geo.D;
-  const uint32_t D = (uint32_t)a.geo.D;
   const int64_t n8 = a.geo.n / 8;
+  const float *sig = a.sigma_chunk ? a.sigma_chunk : a.sigma;
   uint32_t flags = 0;
   double acc = 0.0;
   // The loop runs the same number of times for every lane of a warp (lanes past
@@ -197,7 +209,7 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
     const int64_t g = gw + lane;
     const bool act = g < n8;
     const uint64_t i0 = act ? (uint64_t)g * 8 : 0;
-    const uint64_t srow = (i0 / TD) * D + (uint32_t)(i0 % D);
+    const uint64_t srow = sigma_index(a, i0, TD);
     uint4 kv4 = make_uint4(0, 0, 0, 0), mu4 = make_uint4(0, 0, 0, 0);
     if (act) {
       if (DT == 0) {
@@ -221,7 +233,7 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
       // e4m3 bins are wide against sigma, so the tail case is the common one
       // there: evaluate it in place instead of queueing nearly every scalar
       if (act)
-        b = ideal_one<DT, DT == 1>(sym_at<DT>(kv4, k), mu_at(mu4, k), __ldg(a.sigma + srow + k),
+        b = ideal_one<DT, DT == 1>(sym_at<DT>(kv4, k), mu_at(mu4, k), __ldg(sig + srow + k),
                                    a.phat, s_lo8, flags, deferred);
       s_bits[k * 256 + threadIdx.x] = b;
       const uint32_t dm = __ballot_sync(0xFFFFFFFFu, deferred);
@@ -236,10 +248,10 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
         const uint64_t j = (uint64_t)(gw + owner) * 8 + k;  // the owner's scalar
         const uint32_t sym = DT == 0 ? (uint32_t)static_cast<const uint16_t *>(a.kv)[j]
                                      : (uint32_t)static_cast<const uint8_t *>(a.kv)[j];
-        const uint64_t srow_j = (j / TD) * D + (uint32_t)(j % D);
+        const uint64_t srow_j = sigma_index(a, j, TD);
         bool unused = false;
         s_bits[k * 256 + (threadIdx.x & ~31) + owner] =
-            ideal_one<DT, true>(sym, (uint32_t)a.mu[j], __ldg(a.sigma + srow_j), a.phat, s_lo8,
+            ideal_one<DT, true>(sym, (uint32_t)a.mu[j], __ldg(sig + srow_j), a.phat, s_lo8,
                                 flags, unused);
       }
     }

@@ -77,24 +77,6 @@ __device__ __forceinline__ void stage_tables(uint2 *s_phi, float *s_lo8) {
   __syncthreads();
 }
 
-struct ChunkGeo {
-  uint64_t base;    // first scalar
-  uint64_t srow;    // first sigma entry of the (l, kv, h) row
-  uint32_t ngroup;  // 8-scalar groups in the chunk
-};
-
-__device__ __forceinline__ ChunkGeo chunk_geo(const Geo &g, int64_t c) {
-  int64_t row = c / g.ntb, tb = c - row * g.ntb;
-  int64_t t0 = tb * g.Tb;
-  int64_t tn = (int64_t)g.T - t0;
-  if (tn > g.Tb) tn = g.Tb;
-  ChunkGeo r;
-  r.base = (uint64_t)row * (uint64_t)g.T * (uint64_t)g.D + (uint64_t)t0 * (uint64_t)g.D;
-  r.srow = (uint64_t)row * (uint64_t)g.D;
-  r.ngroup = (uint32_t)(tn * g.D / 8);
-  return r;
-}
-
 // 8 consecutive symbols of a group (bf16 patterns or e4m3 codes)
 template <int DT>
 __device__ __forceinline__ void load_syms(const void *kv, uint64_t at, uint32_t (&s)[8]) {
@@ -232,6 +214,8 @@ __global__ void __launch_bounds__(kCodeThreads, 1) k_encode(EncodeLaunch a) {
         (live && (uint32_t)ell < cg.ngroup) ? (cg.ngroup - ell + G - 1) / G : 0u;
     const uint32_t max_groups = __reduce_max_sync(0xFFFFFFFFu, my_groups);
     uint32_t *region = a.scratch + (live ? c : 0) * a.stride;
+    const float2 *invrow = a.inv_chunk ? a.inv_chunk + (uint64_t)(live ? c : 0) * D
+                                       : a.inv + cg.srow;
     int64_t sp = a.stride;
     uint64_t x = kStateL;
     uint32_t flags = 0;
@@ -244,7 +228,7 @@ __global__ void __launch_bounds__(kCodeThreads, 1) k_encode(EncodeLaunch a) {
       if (has) {
         load_syms<DT>(a.kv, cg.base + p0, sym);
         load_mu(a.mu, cg.base + p0, mub);
-        load_inv(a.inv, cg.srow + p0 % D, inv);
+        load_inv(invrow, p0 % D, inv);
       }
 #pragma unroll
       for (int k = 7; k >= 0; --k) {
@@ -289,8 +273,14 @@ __global__ void __launch_bounds__(kCodeThreads, 1) k_encode(EncodeLaunch a) {
       } else {
         flags |= kFlagOverflow;
       }
+      // the scale words open the chunk, ahead of the lane states
+      const int64_t s0 = sp - 2 * G - a.nsw;
+      for (int j = ell; j < a.nsw; j += G) {
+        if (s0 + j >= 0) region[s0 + j] = a.scale_words[(uint64_t)c * a.nsw + j];
+        else flags |= kFlagOverflow;
+      }
       if (ell == 0) {
-        const int64_t start = sp - 2 * G < 0 ? 0 : sp - 2 * G;
+        const int64_t start = s0 < 0 ? 0 : s0;
         a.starts[c] = (uint32_t)start;
         a.sizes[c] = 4ull * (uint64_t)(a.stride - start);
       }
@@ -369,7 +359,7 @@ __device__ __forceinline__ void put_u64(uint8_t *p, uint64_t v) {
 
 // The 64-byte container header for this geometry (see skv.h).
 __device__ void make_header(uint8_t *h, const Geo &g, int dtype, uint64_t payload,
-                            uint64_t hash) {
+                            uint64_t hash, bool block_scale) {
   for (int i = 0; i < 64; ++i) h[i] = 0;
   put_u32(h + 0, 0x31564B53u);
   put_u16(h + 4, 1);
@@ -385,6 +375,7 @@ __device__ void make_header(uint8_t *h, const Geo &g, int dtype, uint64_t payloa
   h[34] = 8;
   h[35] = 9;
   put_u16(h + 36, 8);
+  put_u16(h + 38, block_scale ? 1u : 0u);  // feature bits
   put_u64(h + 40, (uint64_t)g.nchunks);
   put_u64(h + 48, payload);
   put_u64(h + 56, hash);
@@ -415,7 +406,7 @@ __global__ void __launch_bounds__(256) k_compact(EncodeLaunch a) {
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     offs[nc] = total;
     uint8_t h[64];
-    make_header(h, a.geo, a.dtype, total, mix64(a.head->hash_acc ^ a.hash_words));
+    make_header(h, a.geo, a.dtype, total, mix64(a.head->hash_acc ^ a.hash_words), a.nsw > 0);
     for (int i = 0; i < 64; ++i) a.out[i] = h[i];
   }
 }
@@ -471,7 +462,7 @@ __global__ void k_check_header(DecodeLaunch a) {
   const uint64_t hbytes = 64 + 8 * (uint64_t)(nc + 1);
   const uint64_t payload = a.in_bytes - hbytes;
   uint8_t want[64];
-  make_header(want, a.geo, a.dtype, payload, mix64(a.head->hash_acc ^ a.hash_words));
+  make_header(want, a.geo, a.dtype, payload, mix64(a.head->hash_acc ^ a.hash_words), a.nsw > 0);
   bool ok = true;
   for (int i = 0; i < 64; ++i) ok &= a.in[i] == want[i];
   ok &= get_u64(a.in + 64) == 0;
@@ -568,8 +559,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
       off_a = offs[c];
       off_b = offs[c + 1];
     }
-    const bool ok = live && off_a <= off_b && off_b <= payload_bytes && ((off_b - off_a) & 3) == 0 &&
-                    (off_b - off_a) / 4 >= 2ull * G;
+    // both ends word-aligned (a misaligned word read would fault), inside the payload
+    const bool ok = live && off_a <= off_b && off_b <= payload_bytes && ((off_a | off_b) & 3) == 0 &&
+                    (off_b - off_a) / 4 >= 2ull * G + (uint64_t)a.nsw;
     if (live && !ok) flags |= kFlagCorrupt;
     const uint32_t *w = reinterpret_cast<const uint32_t *>(payload + (ok ? off_a : 0));
     const uint64_t nw = ok ? (off_b - off_a) / 4 : 0;
@@ -577,14 +569,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
     const uint32_t my_groups =
         (ok && (uint32_t)ell < cg.ngroup) ? (cg.ngroup - ell + G - 1) / G : 0u;
     const uint32_t max_groups = __reduce_max_sync(0xFFFFFFFFu, my_groups);
-    uint64_t x = ok ? ((uint64_t)w[2 * ell] | ((uint64_t)w[2 * ell + 1] << 32)) : kStateL;
-    uint64_t cur = 2ull * G;
+    const uint32_t *ws0 = w + a.nsw;  // the lane states follow the scale words
+    uint64_t x = ok ? ((uint64_t)ws0[2 * ell] | ((uint64_t)ws0[2 * ell + 1] << 32)) : kStateL;
+    uint64_t cur = 2ull * G + (uint64_t)a.nsw;
+    const float2 *invrow = a.inv_chunk ? a.inv_chunk + (uint64_t)(live ? c : 0) * D
+                                       : a.inv + cg.srow;
 
     for (uint32_t gi = 0; gi < max_groups; ++gi) {
       const bool has = gi < my_groups;
       const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * gi);
       const uint16_t *mup = a.mu + cg.base + p0;
-      const float2 *ivp2 = a.inv + cg.srow + p0 % D;
+      const float2 *ivp2 = invrow + p0 % D;
 #pragma unroll 1
       for (int k = 0; k < 8; ++k) {
         uint32_t mub = has ? (uint32_t)__ldg(mup + k) : 0u;

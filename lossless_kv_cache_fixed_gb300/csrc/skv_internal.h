@@ -14,6 +14,31 @@ struct Geo {
   int64_t n;  // scalars
 };
 
+// One chunk's extent: its first scalar, the first sigma entry of its
+// (l, kv, h) row and its number of 8-scalar groups.
+struct ChunkGeo {
+  uint64_t base;
+  uint64_t srow;
+  uint32_t ngroup;
+};
+
+__device__ __forceinline__ ChunkGeo chunk_geo(const Geo &g, int64_t c) {
+  int64_t row = c / g.ntb, tb = c - row * g.ntb;
+  int64_t t0 = tb * g.Tb;
+  int64_t tn = (int64_t)g.T - t0;
+  if (tn > g.Tb) tn = g.Tb;
+  ChunkGeo r;
+  r.base = (uint64_t)row * (uint64_t)g.T * (uint64_t)g.D + (uint64_t)t0 * (uint64_t)g.D;
+  r.srow = (uint64_t)row * (uint64_t)g.D;
+  r.ngroup = (uint32_t)(tn * g.D / 8);
+  return r;
+}
+
+// Per-block sigma scales: one byte per (chunk, 8-channel group), packed four
+// to a word, low byte first; the words open the chunk's payload.
+__host__ __device__ constexpr int32_t scale_words(int32_t D) { return (D / 8 + 3) / 4; }
+constexpr int kMaxScaledD = 2048;  // 256 groups
+
 // Workspace head, at offset 0 of every workspace (256 bytes reserved).
 struct WsHead {
   uint32_t flags;                 // skv::kFlag* bits
@@ -31,6 +56,9 @@ struct EncodeLaunch {
   const void *kv;
   const uint16_t *mu;
   const float2 *inv;        // per-channel (1/sigma, 1/(3 sigma)) table in the workspace
+  const float2 *inv_chunk;  // per-block scales: the same per (chunk, channel), else null
+  const uint32_t *scale_words;  // per-block scales: nsw words per chunk
+  int32_t nsw;              // scale words per chunk (0 without per-block scales)
   const uint32_t *ecdf;
   uint32_t *scratch;        // nchunks * stride words
   int64_t stride;           // words per chunk stack
@@ -52,6 +80,8 @@ struct DecodeLaunch {
   uint64_t in_bytes;
   const uint16_t *mu;
   const float2 *inv;
+  const float2 *inv_chunk;  // per-block scales: per (chunk, channel) reciprocals, else null
+  int32_t nsw;
   const uint32_t *ecdf;
   void *kv_out;
   WsHead *head;
@@ -64,6 +94,7 @@ struct IdealLaunch {
   const void *kv;
   const uint16_t *mu;
   const float *sigma;
+  const float *sigma_chunk;  // per-block scales: sigma_eff per (chunk, channel), else null
   const float *phat;
   float *per_scalar;
   double *partials;
@@ -77,10 +108,31 @@ struct IdealLaunch {
 constexpr int kHinvN = 1024;
 constexpr float kHinvUmaxBf16 = 0.98f, kHinvUmaxE4m3 = 1.0f;
 
-// Device constants (Phi knot pairs, e4m3 bin edges, the two inverse tables)
-// for the current device.
+// Per-block sigma scales.  Estimate mode (kv, mu set): choose each group's
+// scale byte from the residuals; load mode (in set): read them from the
+// container's chunks.  Either way, write sigma_eff = sigma m(s) per (chunk,
+// channel) as reciprocal pairs (inv) and/or plain values (sig), and in
+// estimate mode the packed scale words.
+struct ScaleLaunch {
+  Geo geo;
+  int dtype;
+  const void *kv;
+  const uint16_t *mu;
+  const uint8_t *in;
+  uint64_t in_bytes;
+  const float *sigma;
+  uint32_t *words;
+  float2 *inv;
+  float *sig;
+  WsHead *head;
+};
+
+// Device constants (Phi knot pairs, e4m3 bin edges, the two inverse tables,
+// the scale multipliers m(s)) for the current device.
 cudaError_t upload_tables(const uint32_t *phi_knots, const float *lo8, const float *hinv_bf16,
                           const float *hinv_e4m3);
+cudaError_t upload_scale_mult(const float *mult);
+cudaError_t launch_scales(const ScaleLaunch &a, cudaStream_t s);
 
 // Model preparation: sigma validation, per-channel reciprocals, E_q checks and
 // the model fingerprint accumulation.

@@ -1,0 +1,230 @@
+// skv_scale.cu -- per-block sigma scales (an extension of the static model).
+//
+// Page "推测式 KV 编码无损压缩 KV 缓存最高可达约 4 倍" (Speculative KV coding),
+// section "下一步计划": the prediction error's scale moves with the prompt and
+// the position, so one static sigma per (layer, kv, head, channel) pays for the
+// mismatch in bits.  Here every (chunk, 8-channel group) carries one byte s and
+// codes with sigma_eff = RN(sigma m(s)), m(s) = RN(2^((s - 128) / 32)): scales
+// from 1/16 to 16 in 1/32-octave steps, 16 bytes per 32K-scalar chunk at
+// head_dim 128.
+//
+// The encoder's choice is an exact integer rule, so any implementation of it
+// gives the same container: bin every residual a = |x - mu| / sigma (fp32,
+// round to nearest) by b = (bits(a) >> 18) - 127*32 + 128, i.e. 32 (exponent +
+// mantissa fraction) clamped to [0, 255] (0 for a = 0 or NaN, 255 for +inf);
+// take the group's median bin (the smallest b with at least ceil(n/2) of its n
+// residuals at or below it) and add C: 18 for bf16, 21 for e4m3.  C is
+// -32 log2(median |r| / sigma) under the model with the static sigma (0.706
+// for 0.95 N(0, 1) + 0.03 N(0, 9), 0.6745 for N(0, 1)) plus 2.33, the mean
+// amount by which the linear-mantissa floor reads low.  A group whose sigma_eff
+// would be out of range for any of its channels takes s = 128.
+//
+// Estimate kernel: one 256-thread block per chunk (grid-stride), 128 channels
+// at a time with a 256-bin shared histogram per group.  A thread owns one
+// group and reads its 8 channels as one vector per token row (a warp: two
+// whole rows of 128 channels), so at most two lanes of a warp add into the
+// same histogram.  Load kernel: one thread per (chunk, channel).
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "skv_internal.h"
+#include "skv_model.cuh"
+
+namespace skv {
+
+__device__ float g_scale_mult[256];
+
+cudaError_t upload_scale_mult(const float *mult) {
+  return cudaMemcpyToSymbol(g_scale_mult, mult, sizeof(float) * 256);
+}
+
+constexpr int kScaleThreads = 256;
+constexpr int kScaleCols = 128;  // channels per histogram pass: 16 groups
+
+__device__ __forceinline__ float sym_value(int DT, uint32_t u) {
+  if (DT == 0) return __uint_as_float(u << 16);
+  const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)u, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+__device__ __forceinline__ int scale_bin(float a) {
+  if (!(a > 0.0f)) return 0;
+  if (a == INFINITY) return 255;
+  const int b = (int)(__float_as_uint(a) >> 18) - 127 * 32 + 128;
+  return min(max(b, 0), 255);
+}
+
+// sigma_eff valid for all 8 channels of the group at scale s
+__device__ __forceinline__ bool group_ok(const float *sig8, int s) {
+  const float m = g_scale_mult[s];
+  bool ok = true;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) ok &= sigma_valid(__fmul_rn(__ldg(sig8 + k), m));
+  return ok;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kScaleThreads) k_scale_est(ScaleLaunch a) {
+  __shared__ uint32_t s_hist[kScaleCols / 8][256];
+  __shared__ uint8_t s_sc[kMaxScaledD / 8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int D = a.geo.D, NG = D / 8, nsw = scale_words(D);
+  const int C = DT == 0 ? 18 : 21;
+  for (int64_t c = blockIdx.x; c < a.geo.nchunks; c += gridDim.x) {
+    const ChunkGeo cg = chunk_geo(a.geo, c);
+    const uint32_t tn = cg.ngroup * 8u / (uint32_t)D;  // tokens in the chunk
+    const uint32_t need = (tn * 8u + 1u) / 2u;
+    for (int c0 = 0; c0 < D; c0 += kScaleCols) {
+      for (int i = tid; i < (kScaleCols / 8) * 256; i += kScaleThreads) (&s_hist[0][0])[i] = 0u;
+      __syncthreads();
+      // thread t: group t % 16 of the pass, token rows t / 16, t / 16 + 16, ...
+      // (a warp covers two token rows: two lanes per histogram at most)
+      const int gl = tid & (kScaleCols / 8 - 1);
+      const int col = c0 + 8 * gl;
+      if (col < D) {
+        float inv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) inv[k] = __frcp_rn(__ldg(a.sigma + cg.srow + col + k));
+        uint32_t *h = s_hist[gl];
+        for (uint32_t t = (uint32_t)(tid >> 4); t < tn; t += kScaleThreads / (kScaleCols / 8)) {
+          const uint64_t i = cg.base + (uint64_t)t * (uint64_t)D + (uint64_t)col;
+          uint32_t kw[4];
+          if (DT == 0) {
+            const uint4 v =
+                __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.kv) + i));
+            kw[0] = v.x, kw[1] = v.y, kw[2] = v.z, kw[3] = v.w;
+          } else {
+            const uint2 v =
+                __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint8_t *>(a.kv) + i));
+            kw[0] = v.x, kw[1] = v.y, kw[2] = 0u, kw[3] = 0u;
+          }
+          const uint4 mv = __ldg(reinterpret_cast<const uint4 *>(a.mu + i));
+          const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t u = DT == 0 ? (kw[k >> 1] >> (16 * (k & 1))) & 0xFFFFu
+                                       : (kw[k >> 2] >> (8 * (k & 3))) & 0xFFu;
+            const float x = sym_value(DT, u);
+            const float mu = bf16_to_f32((mw[k >> 1] >> (16 * (k & 1))) & 0xFFFFu);
+            const float r = fabsf(__fsub_rn(x, mu));
+            atomicAdd(&h[scale_bin(__fmul_rn(r, inv[k]))], 1u);
+          }
+        }
+      }
+      __syncthreads();
+      // the median bin of each group: lane k holds bins 8k .. 8k+7
+      const int ng = min(kScaleCols / 8, NG - c0 / 8);
+      for (int gm = warp; gm < ng; gm += kScaleThreads / 32) {
+        uint32_t v[8], sum = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[j] = s_hist[gm][8 * lane + j];
+          sum += v[j];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl >= need);
+        const int first = hit ? __ffs(hit) - 1 : 31;
+        int med = 255;
+        if (lane == first) {
+          uint32_t run = incl - sum;
+          med = 8 * lane + 7;
+          for (int j = 0; j < 8; ++j) {
+            run += v[j];
+            if (run >= need) {
+              med = 8 * lane + j;
+              break;
+            }
+          }
+        }
+        med = __shfl_sync(0xFFFFFFFFu, med, first);
+        if (lane == 0) {
+          int s = min(max(med + C, 0), 255);
+          const int g = c0 / 8 + gm;
+          if (!group_ok(a.sigma + cg.srow + 8 * g, s)) s = 128;
+          s_sc[g] = (uint8_t)s;
+        }
+      }
+      __syncthreads();
+    }
+    // sigma_eff per channel, and the packed words
+    for (int d = tid; d < D; d += kScaleThreads) {
+      const float se = __fmul_rn(__ldg(a.sigma + cg.srow + d), g_scale_mult[s_sc[d >> 3]]);
+      const uint64_t at = (uint64_t)c * (uint64_t)D + (uint64_t)d;
+      if (a.inv) {
+        const ChanInv ci = chan_inv(se);
+        a.inv[at] = make_float2(ci.s, ci.s3);
+      }
+      if (a.sig) a.sig[at] = se;
+    }
+    if (a.words) {
+      for (int j = tid; j < nsw; j += kScaleThreads) {
+        uint32_t w = 0;
+        for (int b = 3; b >= 0; --b) {
+          const int g = 4 * j + b;
+          w = (w << 8) | (g < NG ? (uint32_t)s_sc[g] : 0u);
+        }
+        a.words[(uint64_t)c * (uint64_t)nsw + j] = w;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Load mode: the scale bytes from the chunk's first words.  Chunks whose offsets
+// are invalid are left alone (the decoder reports them); a scale that puts
+// sigma_eff out of range marks the container corrupt.
+__global__ void __launch_bounds__(256) k_scale_load(ScaleLaunch a) {
+  const int D = a.geo.D, nsw = scale_words(D);
+  const int64_t nc = a.geo.nchunks;
+  const uint64_t hbytes = 64 + 8 * (uint64_t)(nc + 1);
+  const uint64_t payload_bytes = a.in_bytes - hbytes;
+  const uint64_t *offs = reinterpret_cast<const uint64_t *>(a.in + 64);
+  const int64_t total = nc * (int64_t)D;
+  uint32_t flags = 0;
+  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total;
+       k += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t c = k / D;
+    const int d = (int)(k - c * D);
+    const uint64_t oa = offs[c], ob = offs[c + 1];
+    if (!(oa <= ob && ob <= payload_bytes && ((oa | ob) & 3) == 0 &&
+          (ob - oa) / 4 >= (uint64_t)nsw + 2ull * a.geo.G))
+      continue;
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(a.in + hbytes + oa);
+    const int g = d >> 3;
+    const int s = (int)((w[g >> 2] >> (8 * (g & 3))) & 0xFFu);
+    const ChunkGeo cg = chunk_geo(a.geo, c);
+    const float sig = __ldg(a.sigma + cg.srow + d);
+    float se = __fmul_rn(sig, g_scale_mult[s]);
+    if (!sigma_valid(se)) {
+      if (sigma_valid(sig)) flags |= kFlagCorrupt;
+      se = 1.0f;
+    }
+    const ChanInv ci = chan_inv(se);
+    a.inv[k] = make_float2(ci.s, ci.s3);
+  }
+  if (flags) atomicOr(&a.head->flags, flags);
+}
+
+cudaError_t launch_scales(const ScaleLaunch &a, cudaStream_t s) {
+  const int64_t cap = (int64_t)device_sm_count() * 8;
+  if (a.in) {
+    const int64_t total = a.geo.nchunks * (int64_t)a.geo.D;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > cap) blocks = cap;
+    k_scale_load<<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, s>>>(a);
+    return cudaGetLastError();
+  }
+  int64_t blocks = a.geo.nchunks;
+  if (blocks > cap) blocks = cap;
+  if (a.dtype == 0) k_scale_est<0><<<(unsigned)blocks, kScaleThreads, 0, s>>>(a);
+  else k_scale_est<1><<<(unsigned)blocks, kScaleThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace skv

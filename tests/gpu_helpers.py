@@ -25,11 +25,12 @@ def gpu_codec(w: synth.Workload, Tb=None, G=None, flags=0):
                    flags=flags)
 
 
-def oracle_model(O, w: synth.Workload, Tb=None, G=None):
+def oracle_model(O, w: synth.Workload, Tb=None, G=None, block_scale=False):
     s = w.spec
     sigma = w.sigma.cpu().numpy().astype(np.float32)
     counts = None if w.counts is None else w.counts.cpu().numpy().astype(np.uint64)
-    return O.Model(s.dtype, s.L, s.H, s.T, s.D, Tb or s.Tb, G or s.G, sigma, counts=counts)
+    return O.Model(s.dtype, s.L, s.H, s.T, s.D, Tb or s.Tb, G or s.G, sigma, counts=counts,
+                   block_scale=block_scale)
 
 
 def host_views(w: synth.Workload):

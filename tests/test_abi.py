@@ -82,10 +82,20 @@ def test_argument_errors_without_gpu(skv):
                 P.SkvParams(P.SKV_BF16, 256, 64, 0, 1, 1, None),
                 P.SkvParams(P.SKV_BF16, 0, 8, 0, 1, 1, None),
                 P.SkvParams(5, 256, 8, 0, 1, 1, None),
-                P.SkvParams(P.SKV_BF16, 256, 8, 2, 1, 1, None)]:
+                P.SkvParams(P.SKV_BF16, 256, 8, 4, 1, 1, None)]:
         assert P.skv_max_encoded_bytes(bad, shape) == 0
         rc, _ = P.skv_encode(bad, shape, 1 << 20, 1 << 20, 1 << 20, 1 << 30, 1 << 20, 1 << 30, None)
         assert rc == P.SKV_ERR_ARG
+    # per-block scales: ceil(head_dim / 32) more words per chunk, head_dim <= 2048,
+    # and no fixed-scratch ideal bits
+    scaled = P.SkvParams(P.SKV_BF16, 256, 8, P.SKV_FLAG_BLOCK_SCALE, 1 << 20, 1 << 21, 1 << 22)
+    assert P.skv_max_encoded_bytes(scaled, shape) == 64 + 8 * 9 + 4 * (131072 + (2 * 8 + 2) * 8)
+    assert (P.skv_workspace_bytes(scaled, shape, P.SKV_OP_ENCODE)
+            > P.skv_workspace_bytes(good, shape, P.SKV_OP_ENCODE))
+    assert P.skv_max_encoded_bytes(scaled, P.SkvShape(1, 2, 1, 4, 2048)) > 0
+    assert P.skv_max_encoded_bytes(scaled, P.SkvShape(1, 2, 1, 4, 2056)) == 0
+    rc, _ = P.skv_ideal_bits_noalloc(scaled, shape, 1 << 20, 1 << 20, None, None)
+    assert rc == P.SKV_ERR_ARG
     # NULL and misaligned pointers
     rc, _ = P.skv_encode(good, shape, None, 1 << 20, 1 << 20, 1 << 30, 1 << 20, 1 << 30, None)
     assert rc == P.SKV_ERR_ARG

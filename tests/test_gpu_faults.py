@@ -87,6 +87,13 @@ def test_header_and_offset_tampering(enc):
         o = t[64:64 + 8 * 16].view(torch.int64)
         o[j] = val if val is not None else o[j] + 2
         assert _decode_rc(P, codec, t, nb, mu)[0] == P.SKV_ERR_CORRUPT, j
+    # every offset shifted by 2: all differences stay multiples of 4, but no
+    # chunk starts on a word boundary (the decoder must not read misaligned)
+    nc = codec.n // (codec.shape.head_dim * codec.params.token_block)
+    t = buf.clone()
+    o = t[64:64 + 8 * (nc + 1)].view(torch.int64)
+    o[:nc] += 2
+    assert _decode_rc(P, codec, t, nb, mu)[0] == P.SKV_ERR_CORRUPT
 
 
 def test_model_mismatch(enc):
