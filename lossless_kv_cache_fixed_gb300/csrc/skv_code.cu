@@ -516,6 +516,16 @@ __device__ __forceinline__ int32_t rank_of_value(float x) {
 // unresolved are finished one at a time by the whole warp, 32 candidates per
 // step.  Every answer is checked by the exact cum bracket, so both searches
 // return the same symbol.
+// The warp's next task: after a first round in grid order, tasks go to whichever
+// warp is free first, so a few slow chunks (their search work depends on how
+// well the model fits) do not leave the rest of the GPU idle.  Called by all
+// lanes of the warp.
+__device__ __forceinline__ int64_t next_task(WsHead *h, int64_t nwarps) {
+  unsigned long long t = 0;
+  if ((threadIdx.x & 31) == 0) t = atomicAdd(&h->next_task, 1ull);
+  return nwarps + (int64_t)__shfl_sync(0xFFFFFFFFu, t, 0);
+}
+
 template <int DT, bool BISECT>
 __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
   extern __shared__ uint2 s_phi[];
@@ -549,7 +559,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
   const uint8_t *payload = a.in + hbytes;
 
   for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks;
-       task += nwarps) {
+       task = next_task(a.head, nwarps)) {
     const int64_t c = (task * 32 + lane) / G;
     const bool live = c < nc;
     uint32_t flags = 0;

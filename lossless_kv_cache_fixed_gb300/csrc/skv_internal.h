@@ -46,6 +46,7 @@ struct WsHead {
   unsigned long long hash_acc;    // sum of mix64 terms of the model tables
   unsigned long long total;       // encode: payload bytes
   double bits;                    // ideal bits total
+  unsigned long long next_task;   // decode: tasks handed out after the first round
 };
 
 constexpr int kScanBlock = 2048;  // chunks per scan block
