@@ -111,8 +111,9 @@ class Model:
     def __init__(self, dtype, L, H, T, D, Tb, G, sigma, E=None, counts=None,
                  weights=(95, 3, 2), block_scale=False):
         self.dtype = dtype
-        self.sigma = np.ascontiguousarray(sigma, dtype=np.float32)
-        assert self.sigma.size == L * 2 * H * D
+        # the order-0 baseline (weights (0, 0, 100)) reads no sigma: None is allowed
+        self.sigma = None if sigma is None else np.ascontiguousarray(sigma, dtype=np.float32)
+        assert self.sigma is None or self.sigma.size == L * 2 * H * D
         self.E = None if E is None else np.ascontiguousarray(E, dtype=np.uint32)
         self.counts = None if counts is None else np.ascontiguousarray(counts, dtype=np.uint64)
         if dtype == BF16:
@@ -193,6 +194,8 @@ def _as_sym(model, kv):
 
 
 def _as_mu(model, mu):
+    if mu is None:          # the order-0 baseline reads no mu
+        return None
     mu = np.ascontiguousarray(mu).view(np.uint16).reshape(-1)
     assert mu.size == model.n
     return mu

@@ -56,6 +56,11 @@
  *       and 0.6745 sigma under N(0, s^2) (e4m3: C = 21).  A group whose
  *       sigma_eff would leave the valid range takes s = 128.  The bytes open
  *       the chunk's payload.
+ *   R12 order-0 baseline (the pages' introduction: an entropy coder over the
+ *       bf16 symbols alone reaches about 11 bits per value): the same coder
+ *       with weights (0, 0, 100), i.e. q = p-hat, one static histogram with no
+ *       mu and no sigma.  bf16 only; mu and sigma are never read (they may be
+ *       NULL), sigma is left out of the fingerprint, header feature bit 1.
  */
 #include <float.h>
 #include <math.h>
@@ -218,6 +223,8 @@ int or_sigma_valid(float s) {
 
 static float mu_value(uint16_t mu_bits) { return (float)or_bf16_value(mu_bits); }
 
+static int order0(const or_model *m);
+
 uint32_t or_cum(const or_model *m, int32_t r, float mu, float sigma) {
   init_tables();
   float inv_s = 1.0f / sigma;
@@ -226,8 +233,8 @@ uint32_t or_cum(const or_model *m, int32_t r, float mu, float sigma) {
     float d = g_lo_bf16[r] - mu;
     float z1 = d * inv_s;
     float z3 = d * inv_3s;
-    uint64_t F = (uint64_t)m->w1 * or_phi_q(z1) + (uint64_t)m->w3 * or_phi_q(z3) +
-                 (uint64_t)m->we * m->E[r];
+    uint64_t F = (uint64_t)m->we * m->E[r];
+    if (!order0(m)) F += (uint64_t)m->w1 * or_phi_q(z1) + (uint64_t)m->w3 * or_phi_q(z3);
     unsigned __int128 num = (unsigned __int128)((1ull << 28) - NSYM_BF16) * F;
     unsigned __int128 one = (unsigned __int128)100 << 26;
     return (uint32_t)(num / one) + (uint32_t)r;
@@ -269,8 +276,11 @@ static uint64_t mix64(uint64_t z) {
   return z ^ (z >> 31);
 }
 
+/* R12: the order-0 baseline model (p-hat alone) */
+static int order0(const or_model *m) { return m->dtype == OR_BF16 && m->w1 == 0 && m->w3 == 0; }
+
 uint64_t or_model_hash(const or_model *m) {
-  uint64_t nsig = (uint64_t)m->L * 2 * m->H * m->D;
+  uint64_t nsig = order0(m) ? 0 : (uint64_t)m->L * 2 * m->H * m->D;
   uint64_t h = 0, k = 0;
   for (uint64_t i = 0; i < nsig; ++i, ++k) {
     uint32_t w;
@@ -401,6 +411,8 @@ int or_model_check(const or_model *m) {
   if (m->G < 1 || m->G > 32 || (m->G & (m->G - 1))) return OR_ERR_ARG;
   if (m->w1 + m->w3 + m->we != 100) return OR_ERR_ARG;
   if (m->block_scale != 0 && m->block_scale != 1) return OR_ERR_ARG;
+  if (m->dtype == OR_E4M3 && m->w1 == 0 && m->w3 == 0) return OR_ERR_ARG; /* bf16 only */
+  if (order0(m) && m->block_scale) return OR_ERR_ARG;
   return OR_OK;
 }
 
@@ -439,10 +451,13 @@ int or_encode_chunk(const or_model *m, const void *kv, const uint16_t *mu, uint6
       if (jj >= lane_nsym(&g, G, l)) continue;
       uint64_t p = lane_pos(G, l, jj);
       uint64_t idx = g.base + p;
-      float sigma = m->sigma[g.srow + p % (uint64_t)m->D];
-      float muv = mu_value(mu[idx]);
-      if (!or_sigma_valid(sigma) || !isfinite(muv)) { free(stack); return OR_ERR_PARAM; }
-      sigma = sigma_eff(m, &g, scales, p);
+      float sigma = 1.0f, muv = 0.0f;
+      if (!order0(m)) {
+        sigma = m->sigma[g.srow + p % (uint64_t)m->D];
+        muv = mu_value(mu[idx]);
+        if (!or_sigma_valid(sigma) || !isfinite(muv)) { free(stack); return OR_ERR_PARAM; }
+        sigma = sigma_eff(m, &g, scales, p);
+      }
       int32_t r = or_rank(m->dtype, sym_at(m, kv, idx));
       if (r < 0) { free(stack); return OR_ERR_SYMBOL; }
       uint32_t cr = or_cum(m, r, muv, sigma);
@@ -519,10 +534,13 @@ int or_decode_chunk(const or_model *m, const uint32_t *w, uint64_t nwords, const
       if (j >= lane_nsym(&g, G, l)) continue;
       uint64_t p = lane_pos(G, l, j);
       uint64_t idx = g.base + p;
-      float sigma = m->sigma[g.srow + p % (uint64_t)m->D];
-      float muv = mu_value(mu[idx]);
-      if (!or_sigma_valid(sigma) || !isfinite(muv)) return OR_ERR_PARAM;
-      sigma = sigma_eff(m, &g, scales, p);
+      float sigma = 1.0f, muv = 0.0f;
+      if (!order0(m)) {
+        sigma = m->sigma[g.srow + p % (uint64_t)m->D];
+        muv = mu_value(mu[idx]);
+        if (!or_sigma_valid(sigma) || !isfinite(muv)) return OR_ERR_PARAM;
+        sigma = sigma_eff(m, &g, scales, p);
+      }
       uint32_t slot = (uint32_t)(x[l] & mask);
       int32_t r = find_rank(m, slot, muv, sigma);
       uint32_t cr = or_cum(m, r, muv, sigma);
@@ -585,7 +603,7 @@ static void write_header(const or_model *m, uint8_t *h, uint64_t nchunks, uint64
   h[34] = 8;
   h[35] = 9;
   put16(h + 36, 8);
-  put16(h + 38, (uint16_t)(m->block_scale ? 1 : 0)); /* feature bits */
+  put16(h + 38, (uint16_t)((m->block_scale ? 1 : 0) | (order0(m) ? 2 : 0))); /* feature bits */
   put64(h + 40, nchunks);
   put64(h + 48, payload);
   put64(h + 56, or_model_hash(m));
@@ -759,6 +777,12 @@ int or_ideal_bits(const or_model *m, const void *kv, const uint16_t *mu, uint64_
       uint32_t sym = sym_at(m, kv, i);
       int32_t r = or_rank(m->dtype, sym);
       if (r < 0) return OR_ERR_SYMBOL;
+      if (order0(m)) { /* R12: q = p-hat */
+        const double bits = -log(((double)m->counts[sym] + 1.0) / stot) / M_LN2;
+        if (per_scalar) per_scalar[i - begin] = bits;
+        acc += bits;
+        continue;
+      }
       float sigma = m->sigma[g.srow + (i - g.base) % (uint64_t)m->D];
       double muv = or_bf16_value(mu[i]);
       if (!or_sigma_valid(sigma) || !isfinite(muv)) return OR_ERR_PARAM;
@@ -793,8 +817,8 @@ int or_model_bits_chunk(const or_model *m, const void *kv, const uint16_t *mu, u
   double acc = 0;
   for (uint64_t p = 0; p < 8 * g.ngroup; ++p) {
     uint64_t idx = g.base + p;
-    float sigma = sigma_eff(m, &g, scales, p);
-    float muv = mu_value(mu[idx]);
+    float sigma = order0(m) ? 1.0f : sigma_eff(m, &g, scales, p);
+    float muv = order0(m) ? 0.0f : mu_value(mu[idx]);
     int32_t r = or_rank(m->dtype, sym_at(m, kv, idx));
     if (r < 0) return OR_ERR_SYMBOL;
     uint32_t freq = or_cum(m, r + 1, muv, sigma) - or_cum(m, r, muv, sigma);
