@@ -30,10 +30,11 @@ if ROOT not in sys.path:
 METRIC = "raw-KV encode & decode GB/s on 1 GB300 (% of roofline); bits/scalar vs ideal"
 DEFAULT_WORKLOAD = "qwen3-0.6b-bf16"
 # launches of our kernels per step: encode (prep, encode, 2 scans, compact),
-# decode (prep, header check, decode), ideal bits (prep, bits, final sum); with
-# per-block scales one more in each (scale estimate, scale load, scale estimate)
-LAUNCHES_PER_STEP = 11
-LAUNCHES_BLOCK_SCALE = 3
+# decode (prep, header check, decode; bf16 adds the inverse p-hat table),
+# ideal bits (prep, bits, final sum); with per-block scales one more in each
+# (scale estimate, scale load, scale estimate)
+def launches_per_step(bf16: bool, block_scale: bool) -> int:
+    return 5 + (4 if bf16 else 3) + 3 + (3 if block_scale else 0)
 
 
 def _dist():
@@ -148,8 +149,14 @@ def measured_peaks():
 # 120 / 70; ideal bits = two Gaussian bin masses, the p-hat term and a 3-term
 # log-sum-exp = 100 (bf16), one bin mass = 50 (e4m3).
 ALG_OPS = {2: {"encode": 200, "decode": 120, "ideal_bits": 100},
-           1: {"encode": 130, "decode": 70, "ideal_bits": 50}}
+           1: {"encode": 130, "decode": 70, "ideal_bits": 50},
+           # order-0 baseline: one cum evaluation is an E_q load, a multiply and
+           # a shift (about 8); encode = 2 of them + the divide + renorm = 100;
+           # decode = the table bracket + ~6 bisection steps + 2 evaluations +
+           # the state update = 90; ideal bits = one log2 = 20
+           "o0": {"encode": 100, "decode": 90, "ideal_bits": 20}}
 KERNEL = {"encode": "k_encode", "decode": "k_decode", "ideal_bits": "k_ideal"}
+KERNEL_O0 = {"encode": "k_encode", "decode": "k_decode_o0", "ideal_bits": "k_ideal"}
 
 
 def issue_peak_gops():
@@ -164,27 +171,30 @@ def issue_peak_gops():
     return sms * 128 * mhz * 1e6 / 1e9, sms, mhz
 
 
-def roofline(med_ms, n, container_bytes, bps, workload):
+def roofline(med_ms, n, container_bytes, bps, workload, order0=False):
     """ALU roofline of the dominant kernel (and of each kernel), plus its HBM view."""
     peak_ops, sms, mhz = issue_peak_gops()
     hbm_peak, peak_kind = measured_peaks()
     cb = container_bytes / n
-    alg_bytes = {"encode": bps + 2 + cb, "decode": cb + 2 + bps, "ideal_bits": bps + 2}
+    mub = 0 if order0 else 2          # the order-0 baseline reads no mu
+    alg_bytes = {"encode": bps + mub + cb, "decode": cb + mub + bps, "ideal_bits": bps + mub}
+    ops_tab = ALG_OPS["o0"] if order0 else ALG_OPS[bps]
+    kname = KERNEL_O0 if order0 else KERNEL
     kernels = {}
     for op, ms in med_ms.items():
-        ops = ALG_OPS[bps][op] * n / (ms * 1e-3) / 1e9
+        ops = ops_tab[op] * n / (ms * 1e-3) / 1e9
         gbs = alg_bytes[op] * n / (ms * 1e-3) / 1e9
-        kernels[op] = {"kernel": KERNEL[op], "ms": round(ms, 4),
+        kernels[op] = {"kernel": kname[op], "ms": round(ms, 4),
                        "alu_frac": round(ops / peak_ops, 4),
                        "hbm_frac": round(gbs / hbm_peak, 4)}
     top = max(med_ms, key=med_ms.get)
     ms = med_ms[top]
-    achieved = ALG_OPS[bps][top] * n / (ms * 1e-3) / 1e9
+    achieved = ops_tab[top] * n / (ms * 1e-3) / 1e9
     gbs = alg_bytes[top] * n / (ms * 1e-3) / 1e9
-    roof = {"bound": "alu", "kernel": KERNEL[top], "achieved": round(achieved, 1),
+    roof = {"bound": "alu", "kernel": kname[top], "achieved": round(achieved, 1),
             "peak": round(peak_ops, 1), "unit": "Gop/s", "frac": round(achieved / peak_ops, 4),
-            "traffic": load_traffic(KERNEL[top], workload),
-            "ops_per_scalar": ALG_OPS[bps][top],
+            "traffic": load_traffic(kname[top], workload),
+            "ops_per_scalar": ops_tab[top],
             "peak_source": "%d SMs x 128 lanes x %.0f MHz (issue peak)" % (sms, mhz),
             "hbm": {"achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                     "frac": round(gbs / hbm_peak, 4),
@@ -246,13 +256,17 @@ def _scratch_for(kv):
     return _SCRATCH[key]
 
 
-def oracle_setup(workload_name, seed, device, block_scale=False):
+def oracle_setup(workload_name, seed, device, block_scale=False, order0=False):
     import oracle as O
     import synth
     O.build()
     w = synth.make(workload_name, device=device, seed=seed)
     kv, mu, sigma, counts = synth.to_numpy(w)
     s = w.spec
+    if order0:
+        m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, None, counts=counts,
+                    weights=(0, 0, 100))
+        return O, w, m, kv.reshape(-1), None
     m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sigma, counts=counts,
                 block_scale=block_scale)
     return O, w, m, kv.reshape(-1), mu.reshape(-1)
@@ -297,11 +311,13 @@ def run_gpu(args):
         ecdf = torch.from_numpy(E.view(np.int32)).to(dev)
         phat = torch.from_numpy(ph).to(dev)
     flags = (P.SKV_FLAG_DECODE_BISECT if args.decode_bisect else 0) | (
-        P.SKV_FLAG_BLOCK_SCALE if args.block_scale else 0)
-    codec = P.Codec(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, w.sigma.to(dev), ecdf, phat,
-                    flags=flags)
+        P.SKV_FLAG_BLOCK_SCALE if args.block_scale else 0) | (
+        P.SKV_FLAG_ORDER0 if args.order0 else 0)
+    codec = P.Codec(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G,
+                    None if args.order0 else w.sigma.to(dev), ecdf, phat, flags=flags)
     kv = (w.kv.view(torch.int16) if s.dtype == synth.BF16 else w.kv).reshape(-1)
-    mu = w.mu.view(torch.int16).reshape(-1)
+    # the order-0 baseline codes the cache alone: no prediction is read
+    mu = None if args.order0 else w.mu.view(torch.int16).reshape(-1)
     n = s.n
     raw = n * bps
     out = torch.empty(codec.max_bytes, dtype=torch.uint8, device=dev)
@@ -352,16 +368,18 @@ def run_gpu(args):
         return finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value,
                            t_enc, t_dec, t_bits, clk, None, w)
     kv_h = kv.cpu().pin_memory()
-    mu_h = mu.cpu().pin_memory()
+    mu_h = None if mu is None else mu.cpu().pin_memory()
     box_h = torch.empty(codec.max_bytes, dtype=torch.uint8).pin_memory()
     kv_back = torch.empty_like(kv_h).pin_memory()
     kv_d = torch.empty_like(kv)
-    mu_d = torch.empty_like(mu)
+    mu_d = None if mu is None else torch.empty_like(mu)
     box_d = torch.empty_like(out)
+    mub = 0 if mu is None else 2      # mu bytes per scalar moved
 
     def e2e_step():
         kv_d.copy_(kv_h, non_blocking=True)
-        mu_d.copy_(mu_h, non_blocking=True)
+        if mu_d is not None:
+            mu_d.copy_(mu_h, non_blocking=True)
         _, nb2 = codec.encode(kv_d, mu_d, out=box_d)
         box_h[:nb2].copy_(box_d[:nb2], non_blocking=True)
         box_d[:nb2].copy_(box_h[:nb2], non_blocking=True)
@@ -381,7 +399,7 @@ def run_gpu(args):
     e2e_s = max_over_ranks((time.perf_counter() - t0) / args.steps, world, dev)
     if not torch.equal(kv_back, kv_h):
         raise RuntimeError("end-to-end round trip mismatch")
-    h2d = raw + 2 * n + nb2
+    h2d = raw + mub * n + nb2
     d2h = nb2 + raw + 8 + 3 * 32  # container, cache, total, three status reads
 
     # the same step with the kernels reading and writing the pinned host buffers
@@ -404,7 +422,7 @@ def run_gpu(args):
     if not torch.equal(kv_back, kv_h):
         raise RuntimeError("zero-copy round trip mismatch")
     zc = {"value": round(world * raw / zc_s / 1e9, 3), "unit": "GB/s",
-          "h2d_bytes_per_step": int(2 * raw + 2 * n + nb3 + 2 * n + raw + 2 * n),
+          "h2d_bytes_per_step": int(2 * raw + mub * n + nb3 + mub * n + raw + mub * n),
           "d2h_bytes_per_step": int(nb3 + raw + 8 + 3 * 32),
           "mode": "kernels read and write pinned host memory over the link"}
 
@@ -426,18 +444,23 @@ def finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value, t_enc, t
     med = {"encode": statistics.median(t_enc), "decode": statistics.median(t_dec),
            "ideal_bits": statistics.median(t_bits)}
     top = max(med, key=med.get)
-    roof, kernels = roofline(med, n, nb, bps, args.workload)
+    roof, kernels = roofline(med, n, nb, bps, args.workload, order0=args.order0)
 
     # ---- oracle on the host cores, bounded sample ----
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         import oracle as O
         kvn, mun, sig, cnt = synth.to_numpy(w)
-        m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sig, counts=cnt,  # same chunking
-                    block_scale=args.block_scale)
+        if args.order0:
+            m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, None, counts=cnt,
+                        weights=(0, 0, 100))
+            mun = None
+        else:
+            m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sig, counts=cnt,  # same chunking
+                        block_scale=args.block_scale)
+            mun = mun.reshape(-1)
         nch = m.num_chunks()
-        sc, dt, chunks = time_oracle(O, m, kvn.reshape(-1), mun.reshape(-1), nch,
-                                     args.cpu_sample_chunks)
+        sc, dt, chunks = time_oracle(O, m, kvn.reshape(-1), mun, nch, args.cpu_sample_chunks)
         cpu = {"value": round(sc * bps / dt / 1e9, 6), "unit": "GB/s", "cores": 1,
                "kind": "oracle",
                "sample": "%d of %d chunks (%d scalars, every %d-th chunk): encode + decode + "
@@ -453,6 +476,8 @@ def finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value, t_enc, t
                    "layers": s.L, "heads": s.H, "tokens": s.T, "head_dim": s.D,
                    "scalars_per_gpu": n, "token_block": s.Tb, "lanes": s.G,
                    "block_scale": bool(args.block_scale),
+                   "coder": "order-0 baseline (p-hat alone)" if args.order0
+                            else "speculative (mu, sigma mixture)",
                    "parallelism": "dp%d (independent caches)" % world,
                    "l2": "inputs larger than L2: %.0f MB KV + %.0f MB mu per step" % (
                        raw / 1e6, 2 * n / 1e6)},
@@ -466,8 +491,7 @@ def finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value, t_enc, t
         "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (LAUNCHES_PER_STEP + (LAUNCHES_BLOCK_SCALE if args.block_scale else 0))
-                        * args.steps,
+        "gpu_launches": launches_per_step(bps == 2, args.block_scale) * args.steps,
         "clocks": clk.summary(),
     }
     return line
@@ -480,7 +504,8 @@ def run_reference(args):
         return None
     import torch
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    O, w, m, kv, mu = oracle_setup(args.workload, 0, device, block_scale=args.block_scale)
+    O, w, m, kv, mu = oracle_setup(args.workload, 0, device, block_scale=args.block_scale,
+                                   order0=args.order0)
     s = w.spec
     bps = 2 if s.dtype == 0 else 1
     nch = m.num_chunks()
@@ -509,7 +534,9 @@ def run_reference(args):
         "ms_per_step": round(1e3 * dt / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
         "config": {"workload": args.workload, "scalars_per_gpu": s.n, "token_block": s.Tb,
-                   "lanes": s.G, "block_scale": bool(args.block_scale)},
+                   "lanes": s.G, "block_scale": bool(args.block_scale),
+                   "coder": "order-0 baseline (p-hat alone)" if args.order0
+                            else "speculative (mu, sigma mixture)"},
         "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": "%d chunks per step of %d scalars each (every %d-th chunk), "
                                    "encode + decode + ideal bits" % (per_step, s.Tb * s.D, stride)},
@@ -535,6 +562,8 @@ def main(argv=None):
                     help="decode with the reference bisection search")
     ap.add_argument("--block-scale", action="store_true",
                     help="per-(chunk, 8-channel group) sigma scales in the container")
+    ap.add_argument("--order0", action="store_true",
+                    help="the order-0 baseline coder (p-hat alone, no mu/sigma; bf16)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "skv":
         args.warmup = 3

@@ -106,6 +106,13 @@ typedef struct {
  * decode and ideal bits must all be given the flag; skv_ideal_bits_noalloc
  * rejects it (SKV_ERR_ARG). */
 #define SKV_FLAG_BLOCK_SCALE 2
+/* Order-0 baseline (the pages' introduction: an entropy coder over the bf16
+ * symbols alone reaches about 11 bits per value): the same coder with q =
+ * p-hat, i.e. cum(r) = floor(K * E_q[r] / 2^26) + r, without prediction.
+ * bf16 only, not with SKV_FLAG_BLOCK_SCALE.  mu and sigma are not read and
+ * may be NULL; sigma is not part of the model fingerprint; header feature
+ * bit 1.  Ideal bits are -log2 p-hat.  skv_ideal_bits_noalloc rejects it. */
+#define SKV_FLAG_ORDER0 4
 
 typedef struct {
   int32_t dtype;
@@ -136,7 +143,7 @@ size_t skv_workspace_bytes(const skv_params *params, const skv_shape *shape, int
  * Container v1 (little-endian): a 64-byte header {u32 magic "SKV1", u16 version
  * 1, u8 dtype, u8 M, u32 layers, u32 2, u32 heads, u32 tokens, u32 head_dim,
  * u32 token_block, u16 lanes, u8 8, u8 9, u16 8, u16 features (bit 0:
- * SKV_FLAG_BLOCK_SCALE), u64 num_chunks, u64 payload_bytes, u64 model
+ * SKV_FLAG_BLOCK_SCALE, bit 1: SKV_FLAG_ORDER0), u64 num_chunks, u64 payload_bytes, u64 model
  * fingerprint of sigma (and E_q for bf16)}, then u64 offsets[num_chunks + 1]
  * (byte offsets from the payload start, multiples of 4), then the payload:
  * chunk c (index ((l*2 + kv)*heads + h)*ceil(tokens/Tb) + tb) is u32 words in
@@ -185,7 +192,7 @@ int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void 
  * nothing.  Shapes whose (layers * 2 * heads * head_dim) sigma entries exceed
  * skv_ideal_bits_noalloc_max_channels() are rejected with SKV_ERR_CAPACITY.
  * SKV_FLAG_BLOCK_SCALE is rejected with SKV_ERR_ARG: its per-(chunk, channel)
- * table grows with the cache and has no fixed bound.
+ * table grows with the cache and has no fixed bound.  So is SKV_FLAG_ORDER0.
  * Every call shares that one array, so calls that may overlap on the GPU (on
  * different streams, or from different host threads) race; serialise them.
  * The first call on a device looks up the array's device address and uploads

@@ -18,6 +18,7 @@ SKV_BF16, SKV_E4M3 = 0, 1
 SKV_OP_ENCODE, SKV_OP_DECODE, SKV_OP_IDEAL_BITS = 0, 1, 2
 SKV_FLAG_DECODE_BISECT = 1
 SKV_FLAG_BLOCK_SCALE = 2
+SKV_FLAG_ORDER0 = 4
 SKV_OK, SKV_ERR_ARG, SKV_ERR_CAPACITY, SKV_ERR_SYMBOL = 0, -1, -2, -3
 SKV_ERR_PARAM, SKV_ERR_CORRUPT, SKV_ERR_CUDA = -4, -5, -6
 NSYM = {SKV_BF16: 65282, SKV_E4M3: 254}
@@ -158,24 +159,30 @@ def _stream_handle(stream=None):
     return C.c_void_p(s.cuda_stream)
 
 
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
 class Codec:
     """Owns device buffers for one (model, shape) and calls the C ABI.
 
     sigma: float32 [L, 2, H, D] on the device; ecdf: int32/uint32 [65283]
-    (bf16); phat: float32 [65282] (bf16, ideal bits only).
+    (bf16); phat: float32 [65282] (bf16, ideal bits only).  With
+    SKV_FLAG_ORDER0 sigma and mu may be None (the baseline reads neither).
     """
 
     def __init__(self, dtype, L, H, T, D, token_block, lanes, sigma, ecdf=None, phat=None,
                  flags=0):
         import torch
         self.dtype = dtype
-        self.sigma, self.ecdf, self.phat = sigma.contiguous(), ecdf, phat
-        self.params = SkvParams(dtype, token_block, lanes, flags, self.sigma.data_ptr(),
+        self.sigma = None if sigma is None else sigma.contiguous()
+        self.ecdf, self.phat = ecdf, phat
+        self.params = SkvParams(dtype, token_block, lanes, flags, _ptr(self.sigma),
                                 ecdf.data_ptr() if ecdf is not None else None,
                                 phat.data_ptr() if phat is not None else None)
         self.shape = SkvShape(L, 2, H, T, D)
         self.n = L * 2 * H * T * D
-        self.device = sigma.device
+        self.device = (sigma if sigma is not None else ecdf).device
         self._ws = {}
         self.max_bytes = skv_max_encoded_bytes(self.params, self.shape)
         if self.max_bytes == 0:
@@ -197,7 +204,7 @@ class Codec:
         if out is None:
             out = self.torch.empty(self.max_bytes, dtype=self.torch.uint8, device=self.device)
         ws = self.workspace(SKV_OP_ENCODE)
-        rc, nb = skv_encode(self.params, self.shape, kv.data_ptr(), mu.data_ptr(), out.data_ptr(),
+        rc, nb = skv_encode(self.params, self.shape, kv.data_ptr(), _ptr(mu), out.data_ptr(),
                             out.numel(), ws.data_ptr(), ws.numel(), _stream_handle(stream))
         if rc:
             raise SkvError(rc, "skv_encode")
@@ -207,7 +214,7 @@ class Codec:
         if out is None:
             out = self.torch.empty(self.n, dtype=self.kv_dtype(), device=self.device)
         ws = self.workspace(SKV_OP_DECODE)
-        rc = skv_decode(self.params, self.shape, buf.data_ptr(), nbytes, mu.data_ptr(),
+        rc = skv_decode(self.params, self.shape, buf.data_ptr(), nbytes, _ptr(mu),
                         out.data_ptr(), ws.data_ptr(), ws.numel(), _stream_handle(stream))
         if rc:
             raise SkvError(rc, "skv_decode")
@@ -218,7 +225,7 @@ class Codec:
         ps = None
         if per_scalar:
             ps = self.torch.empty(self.n, dtype=self.torch.float32, device=self.device)
-        rc, tot = skv_ideal_bits(self.params, self.shape, kv.data_ptr(), mu.data_ptr(),
+        rc, tot = skv_ideal_bits(self.params, self.shape, kv.data_ptr(), _ptr(mu),
                                  ps.data_ptr() if ps is not None else None, ws.data_ptr(),
                                  ws.numel(), _stream_handle(stream))
         if rc:

@@ -100,6 +100,8 @@ struct Plan {
   int dtype;
   int64_t nsig;
   int32_t nsw;     // per-block scale words per chunk (0: static sigma)
+  int order0;      // order-0 baseline: p-hat alone, no mu and no sigma
+  int64_t nsig_model;  // sigma entries the model reads (0 for the order-0 baseline)
   // workspace layout (byte offsets)
   size_t off_inv, off_sizes, off_starts, off_partials, off_scratch, off_bits, off_einv, total;
   size_t off_enc_cinv, off_enc_words, enc_total;  // encode: per-chunk tables after the stacks
@@ -114,7 +116,10 @@ bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   if (!p || !s || !out) return SKV_ERR_ARG;
   if (p->dtype != SKV_BF16 && p->dtype != SKV_E4M3) return SKV_ERR_ARG;
-  if (p->flags & ~(SKV_FLAG_DECODE_BISECT | SKV_FLAG_BLOCK_SCALE)) return SKV_ERR_ARG;
+  if (p->flags & ~(SKV_FLAG_DECODE_BISECT | SKV_FLAG_BLOCK_SCALE | SKV_FLAG_ORDER0))
+    return SKV_ERR_ARG;
+  const bool order0 = (p->flags & SKV_FLAG_ORDER0) != 0;
+  if (order0 && (p->dtype != SKV_BF16 || (p->flags & SKV_FLAG_BLOCK_SCALE))) return SKV_ERR_ARG;
   if (s->kv != 2 || s->layers <= 0 || s->heads <= 0 || s->tokens <= 0 || s->head_dim <= 0)
     return SKV_ERR_ARG;
   if (s->head_dim % 8) return SKV_ERR_ARG;
@@ -139,6 +144,8 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   // a chunk's scalar offsets are 32-bit inside the kernels
   if (tb_eff * s->head_dim >= (1ll << 31)) return SKV_ERR_ARG;
   pl.nsig = rows * s->head_dim;
+  pl.order0 = order0 ? 1 : 0;
+  pl.nsig_model = order0 ? 0 : pl.nsig;
   // worst case words of one full chunk: every lane emits at most one word per
   // symbol and, since a symbol adds at most M + log2(1 + 2^(M-31)) < M + 1
   // bits of state, at most ceil(n (M + 1) / 32) words; plus 2 flush words.
@@ -171,7 +178,8 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   pl.off_enc_cinv = pl.total;
   pl.off_enc_words = align_up(pl.off_enc_cinv + sizeof(float2) * ccells);
   pl.enc_total = align_up(pl.off_enc_words + sizeof(uint32_t) * (size_t)pl.nsw * (size_t)pl.geo.nchunks);
-  pl.off_dec_cinv = align_up(pl.off_einv + sizeof(int32_t) * (kHinvN + 1));
+  // the decoder's inverse p-hat table: kHinvN + 1 entries, kO0InvN + 1 for order 0
+  pl.off_dec_cinv = align_up(pl.off_einv + sizeof(int32_t) * ((order0 ? kO0InvN : kHinvN) + 1));
   pl.dec_total = align_up(pl.off_dec_cinv + sizeof(float2) * ccells);
   pl.off_bits_csig = align_up(pl.off_bits + sizeof(double) * (size_t)pl.bits_blocks);
   pl.bits_total = align_up(pl.off_bits_csig + sizeof(float) * ccells);
@@ -186,7 +194,7 @@ size_t ws_bytes_for(const Plan &pl, int op) {
 }
 
 uint64_t hash_words(const Plan &pl) {
-  return (uint64_t)pl.nsig + (pl.dtype == SKV_BF16 ? (uint64_t)kNsymBf16 + 1 : 0);
+  return (uint64_t)pl.nsig_model + (pl.dtype == SKV_BF16 ? (uint64_t)kNsymBf16 + 1 : 0);
 }
 
 int status_from_flags(uint32_t f) {
@@ -207,8 +215,11 @@ int read_head(WsHead *dev, WsHead *host, cudaStream_t st) {
 }
 
 int common_inputs(const skv_params *p, const Plan &pl, const void *kv, const uint16_t *mu) {
-  if (!kv || !mu || !p->sigma) return SKV_ERR_ARG;
-  if (!aligned(kv, 16) || !aligned(mu, 16) || !aligned(p->sigma, 4)) return SKV_ERR_ARG;
+  if (!kv || !aligned(kv, 16)) return SKV_ERR_ARG;
+  // the order-0 baseline reads neither mu nor sigma (both may be NULL)
+  if (!pl.order0) {
+    if (!mu || !p->sigma || !aligned(mu, 16) || !aligned(p->sigma, 4)) return SKV_ERR_ARG;
+  }
   if (pl.dtype == SKV_BF16 && (!p->ecdf || !aligned(p->ecdf, 4))) return SKV_ERR_ARG;
   return SKV_OK;
 }
@@ -282,7 +293,7 @@ int skv_encode(const skv_params *params, const skv_shape *shape, const void *kv,
   if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
   float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
   const uint32_t *ecdf = pl.dtype == SKV_BF16 ? params->ecdf : nullptr;
-  if (launch_prep(params->sigma, pl.nsig, ecdf, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
+  if (launch_prep(params->sigma, pl.nsig_model, ecdf, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
   EncodeLaunch a;
   a.geo = pl.geo;
   a.dtype = pl.dtype;
@@ -292,6 +303,7 @@ int skv_encode(const skv_params *params, const skv_shape *shape, const void *kv,
   a.inv_chunk = nullptr;
   a.scale_words = nullptr;
   a.nsw = pl.nsw;
+  a.order0 = pl.order0;
   if (pl.nsw) {
     ScaleLaunch sl = scale_launch(pl, params, head);
     sl.kv = kv;
@@ -337,7 +349,7 @@ int skv_decode(const skv_params *params, const skv_shape *shape, const void *in,
   if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
   float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
   const uint32_t *ecdf = pl.dtype == SKV_BF16 ? params->ecdf : nullptr;
-  if (launch_prep(params->sigma, pl.nsig, ecdf, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
+  if (launch_prep(params->sigma, pl.nsig_model, ecdf, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
   DecodeLaunch a;
   a.geo = pl.geo;
   a.dtype = pl.dtype;
@@ -347,6 +359,7 @@ int skv_decode(const skv_params *params, const skv_shape *shape, const void *in,
   a.inv = inv;
   a.inv_chunk = nullptr;
   a.nsw = pl.nsw;
+  a.order0 = pl.order0;
   if (pl.nsw) {
     ScaleLaunch sl = scale_launch(pl, params, head);
     sl.in = static_cast<const uint8_t *>(in);
@@ -363,7 +376,7 @@ int skv_decode(const skv_params *params, const skv_shape *shape, const void *in,
   a.einv = nullptr;
   if (pl.dtype == SKV_BF16) {
     int32_t *einv = reinterpret_cast<int32_t *>(ws + pl.off_einv);
-    if (launch_einv(ecdf, einv, st) != cudaSuccess) return SKV_ERR_CUDA;
+    if (launch_einv(ecdf, einv, pl.order0 ? kO0InvN : kHinvN, st) != cudaSuccess) return SKV_ERR_CUDA;
     a.einv = einv;
   }
   if (launch_decode(a, st) != cudaSuccess) return SKV_ERR_CUDA;
@@ -390,7 +403,7 @@ int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void 
   if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
   float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
   // sigma validity only: the p-hat table enters through `phat`
-  if (launch_prep(params->sigma, pl.nsig, nullptr, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
+  if (launch_prep(params->sigma, pl.nsig_model, nullptr, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
   IdealLaunch a;
   a.geo = pl.geo;
   a.dtype = pl.dtype;
@@ -398,6 +411,7 @@ int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void 
   a.mu = mu;
   a.sigma = params->sigma;
   a.sigma_chunk = nullptr;
+  a.order0 = pl.order0;
   if (pl.nsw) {
     ScaleLaunch sl = scale_launch(pl, params, head);
     sl.kv = kv;
@@ -427,8 +441,9 @@ int skv_ideal_bits_noalloc(const skv_params *params, const skv_shape *shape, con
   if (rc) return rc;
   if ((rc = common_inputs(params, pl, kv, mu))) return rc;
   if (!total) return SKV_ERR_ARG;
-  // the per-(chunk, channel) table of per-block scales grows with the cache
-  if (pl.nsw) return SKV_ERR_ARG;
+  // the per-(chunk, channel) table of per-block scales grows with the cache;
+  // the order-0 baseline has its own entry points' workspace only
+  if (pl.nsw || pl.order0) return SKV_ERR_ARG;
   if (per_scalar && !aligned(per_scalar, 16)) return SKV_ERR_ARG;
   if (pl.dtype == SKV_BF16 && (!params->phat || !aligned(params->phat, 4))) return SKV_ERR_ARG;
   // the same layout as the workspace of skv_ideal_bits, inside the fixed array
@@ -441,7 +456,7 @@ int skv_ideal_bits_noalloc(const skv_params *params, const skv_shape *shape, con
   // the array keeps the previous call's contents: the flags and sums start at zero
   if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
   float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
-  if (launch_prep(params->sigma, pl.nsig, nullptr, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
+  if (launch_prep(params->sigma, pl.nsig_model, nullptr, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
   IdealLaunch a;
   a.geo = pl.geo;
   a.dtype = pl.dtype;
@@ -449,6 +464,7 @@ int skv_ideal_bits_noalloc(const skv_params *params, const skv_shape *shape, con
   a.mu = mu;
   a.sigma = params->sigma;
   a.sigma_chunk = nullptr;
+  a.order0 = 0;
   a.phat = params->phat;
   a.per_scalar = per_scalar;
   a.partials = reinterpret_cast<double *>(ws + pl.off_bits);

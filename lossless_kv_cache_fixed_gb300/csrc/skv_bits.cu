@@ -178,7 +178,7 @@ __device__ __forceinline__ uint64_t sigma_index(const IdealLaunch &a, uint64_t i
   return (row * (uint64_t)a.geo.ntb + tb) * D + in_row % D;
 }
 
-template <int DT>
+template <int DT, bool O0>
 __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
   __shared__ float s_lo8[256];
   __shared__ double s_part[256];
@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
         kv4.x = v.x;
         kv4.y = v.y;
       }
-      mu4 = __ldg(reinterpret_cast<const uint4 *>(a.mu + i0));
+      if (!O0) mu4 = __ldg(reinterpret_cast<const uint4 *>(a.mu + i0));
     }
     // pass 1: the common case for all 8 scalars.  Scalars that need the tail
     // evaluation go to a per-warp queue, which the whole warp then works off
@@ -232,9 +232,15 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
       float b = 0.0f;
       // e4m3 bins are wide against sigma, so the tail case is the common one
       // there: evaluate it in place instead of queueing nearly every scalar
-      if (act)
+      if (act && O0) {
+        // order-0 baseline: q = p-hat
+        const int32_t r = rank_bf16(sym_at<DT>(kv4, k));
+        if (r < 0 || r >= kNsymBf16) flags |= kFlagSymbol;
+        else b = -log2f(__ldg(a.phat + r));
+      } else if (act) {
         b = ideal_one<DT, DT == 1>(sym_at<DT>(kv4, k), mu_at(mu4, k), __ldg(sig + srow + k),
                                    a.phat, s_lo8, flags, deferred);
+      }
       s_bits[k * 256 + threadIdx.x] = b;
       const uint32_t dm = __ballot_sync(0xFFFFFFFFu, deferred);
       if (deferred) q[qn + __popc(dm & ((1u << lane) - 1u))] = (uint16_t)((k << 5) | lane);
@@ -304,8 +310,9 @@ __global__ void __launch_bounds__(1024) k_ideal_final(const double *partials, in
 }
 
 cudaError_t launch_ideal(const IdealLaunch &a, cudaStream_t s) {
-  if (a.dtype == 0) k_ideal<0><<<a.nblocks, 256, 0, s>>>(a);
-  else k_ideal<1><<<a.nblocks, 256, 0, s>>>(a);
+  if (a.dtype == 0 && a.order0) k_ideal<0, true><<<a.nblocks, 256, 0, s>>>(a);
+  else if (a.dtype == 0) k_ideal<0, false><<<a.nblocks, 256, 0, s>>>(a);
+  else k_ideal<1, false><<<a.nblocks, 256, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   k_ideal_final<<<1, 1024, 0, s>>>(a.partials, a.nblocks, a.head);

@@ -112,6 +112,12 @@ __device__ __forceinline__ void load_inv(const float2 *inv, uint64_t at, ChanInv
   }
 }
 
+// Order-0 baseline: cum(r) = floor(K E_q[r] / 2^26) + r (the mixture with
+// weights (0, 0, 100): the factor 100 cancels exactly).
+__device__ __forceinline__ uint32_t cum_order0(int32_t r, const uint32_t *__restrict__ ecdf) {
+  return (uint32_t)(((uint64_t)kKBf16 * __ldg(ecdf + r)) >> 26) + (uint32_t)r;
+}
+
 template <int DT>
 __device__ __forceinline__ uint32_t cum_of(int32_t r, float mu, ChanInv inv, const uint2 *phi,
                                            const float *lo8, const uint32_t *ecdf) {
@@ -158,6 +164,7 @@ __global__ void k_prep(const float *__restrict__ sigma, int64_t nsig,
 cudaError_t launch_prep(const float *sigma, int64_t nsig, const uint32_t *ecdf, float2 *inv,
                         WsHead *head, cudaStream_t s) {
   int64_t n = nsig + (ecdf ? kNsymBf16 + 1 : 0);
+  if (n == 0) return cudaSuccess;  // nothing to check or hash (order-0 ideal bits)
   int blocks = (int)((n + 255) / 256);
   if (blocks > 1024) blocks = 1024;
   k_prep<<<blocks, 256, 0, s>>>(sigma, nsig, ecdf, inv, head);
@@ -166,10 +173,10 @@ cudaError_t launch_prep(const float *sigma, int64_t nsig, const uint32_t *ecdf, 
 
 // Inverse of the p-hat prefix table for the decoder's guess in the tails that
 // only the p-hat component reaches (a guess only: any error costs search steps).
-__global__ void k_einv(const uint32_t *__restrict__ ecdf, int32_t *__restrict__ einv) {
+__global__ void k_einv(const uint32_t *__restrict__ ecdf, int32_t *__restrict__ einv, int n) {
   const int k = blockIdx.x * blockDim.x + threadIdx.x;
-  if (k > kHinvN) return;
-  const uint32_t target = (uint32_t)(((uint64_t)k << 26) / kHinvN);
+  if (k > n) return;
+  const uint32_t target = (uint32_t)(((uint64_t)k << 26) / (uint64_t)n);
   int32_t lo = 0, hi = kNsymBf16;  // smallest r in [0, 65282] with ecdf[r] >= target
   while (lo < hi) {
     const int32_t mid = (lo + hi) >> 1;
@@ -179,8 +186,8 @@ __global__ void k_einv(const uint32_t *__restrict__ ecdf, int32_t *__restrict__ 
   einv[k] = lo;
 }
 
-cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, cudaStream_t s) {
-  k_einv<<<(kHinvN + 1 + 255) / 256, 256, 0, s>>>(ecdf, einv);
+cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, int n, cudaStream_t s) {
+  k_einv<<<(n + 1 + 255) / 256, 256, 0, s>>>(ecdf, einv, n);
   return cudaGetLastError();
 }
 
@@ -188,7 +195,7 @@ cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, cudaStream_t s) {
 // Encode: one thread per lane, rounds descending, lanes descending.
 // ------------------------------------------------------------------------
 
-template <int DT>
+template <int DT, bool O0>
 __global__ void __launch_bounds__(kCodeThreads, 1) k_encode(EncodeLaunch a) {
   extern __shared__ uint2 s_phi[];
   float *s_lo8 = reinterpret_cast<float *>(s_phi + kPhiKnots);
@@ -227,8 +234,10 @@ __global__ void __launch_bounds__(kCodeThreads, 1) k_encode(EncodeLaunch a) {
       ChanInv inv[8];
       if (has) {
         load_syms<DT>(a.kv, cg.base + p0, sym);
-        load_mu(a.mu, cg.base + p0, mub);
-        load_inv(invrow, p0 % D, inv);
+        if (!O0) {
+          load_mu(a.mu, cg.base + p0, mub);
+          load_inv(invrow, p0 % D, inv);
+        }
       }
 #pragma unroll
       for (int k = 7; k >= 0; --k) {
@@ -240,13 +249,18 @@ __global__ void __launch_bounds__(kCodeThreads, 1) k_encode(EncodeLaunch a) {
             flags |= kFlagSymbol;
             r = 0;
           }
-          if (!mu_valid(mub[k])) {
-            flags |= kFlagParam;
-            mub[k] = 0;
+          if (O0) {
+            cst = cum_order0(r, a.ecdf);
+            f = cum_order0(r + 1, a.ecdf) - cst;
+          } else {
+            if (!mu_valid(mub[k])) {
+              flags |= kFlagParam;
+              mub[k] = 0;
+            }
+            const float muf = bf16_to_f32(mub[k]);
+            cst = cum_of<DT>(r, muf, inv[k], s_phi, s_lo8, a.ecdf);
+            f = cum_of<DT>(r + 1, muf, inv[k], s_phi, s_lo8, a.ecdf) - cst;
           }
-          const float muf = bf16_to_f32(mub[k]);
-          cst = cum_of<DT>(r, muf, inv[k], s_phi, s_lo8, a.ecdf);
-          f = cum_of<DT>(r + 1, muf, inv[k], s_phi, s_lo8, a.ecdf) - cst;
           emit = x >= ((uint64_t)f << (63 - M));
         }
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, emit) & seg;
@@ -359,7 +373,7 @@ __device__ __forceinline__ void put_u64(uint8_t *p, uint64_t v) {
 
 // The 64-byte container header for this geometry (see skv.h).
 __device__ void make_header(uint8_t *h, const Geo &g, int dtype, uint64_t payload,
-                            uint64_t hash, bool block_scale) {
+                            uint64_t hash, uint32_t features) {
   for (int i = 0; i < 64; ++i) h[i] = 0;
   put_u32(h + 0, 0x31564B53u);
   put_u16(h + 4, 1);
@@ -375,7 +389,7 @@ __device__ void make_header(uint8_t *h, const Geo &g, int dtype, uint64_t payloa
   h[34] = 8;
   h[35] = 9;
   put_u16(h + 36, 8);
-  put_u16(h + 38, block_scale ? 1u : 0u);  // feature bits
+  put_u16(h + 38, features);  // bit 0: per-block scales, bit 1: order-0 baseline
   put_u64(h + 40, (uint64_t)g.nchunks);
   put_u64(h + 48, payload);
   put_u64(h + 56, hash);
@@ -406,7 +420,8 @@ __global__ void __launch_bounds__(256) k_compact(EncodeLaunch a) {
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     offs[nc] = total;
     uint8_t h[64];
-    make_header(h, a.geo, a.dtype, total, mix64(a.head->hash_acc ^ a.hash_words), a.nsw > 0);
+    make_header(h, a.geo, a.dtype, total, mix64(a.head->hash_acc ^ a.hash_words),
+                (a.nsw > 0 ? 1u : 0u) | (a.order0 ? 2u : 0u));
     for (int i = 0; i < 64; ++i) a.out[i] = h[i];
   }
 }
@@ -423,14 +438,21 @@ cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s) {
   const int64_t ntasks = (a.geo.nchunks * a.geo.G + 31) / 32;
   const int blocks = code_blocks(ntasks);
   cudaError_t e;
-  if (a.dtype == 0) {
-    e = cudaFuncSetAttribute(k_encode<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCodeSmem);
+  if (a.dtype == 0 && a.order0) {
+    e = cudaFuncSetAttribute(k_encode<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kCodeSmem);
     if (e != cudaSuccess) return e;
-    k_encode<0><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
+    k_encode<0, true><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
+  } else if (a.dtype == 0) {
+    e = cudaFuncSetAttribute(k_encode<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kCodeSmem);
+    if (e != cudaSuccess) return e;
+    k_encode<0, false><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
   } else {
-    e = cudaFuncSetAttribute(k_encode<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCodeSmem);
+    e = cudaFuncSetAttribute(k_encode<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kCodeSmem);
     if (e != cudaSuccess) return e;
-    k_encode<1><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
+    k_encode<1, false><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int64_t nb = (a.geo.nchunks + kScanBlock - 1) / kScanBlock;
@@ -462,7 +484,8 @@ __global__ void k_check_header(DecodeLaunch a) {
   const uint64_t hbytes = 64 + 8 * (uint64_t)(nc + 1);
   const uint64_t payload = a.in_bytes - hbytes;
   uint8_t want[64];
-  make_header(want, a.geo, a.dtype, payload, mix64(a.head->hash_acc ^ a.hash_words), a.nsw > 0);
+  make_header(want, a.geo, a.dtype, payload, mix64(a.head->hash_acc ^ a.hash_words),
+              (a.nsw > 0 ? 1u : 0u) | (a.order0 ? 2u : 0u));
   bool ok = true;
   for (int i = 0; i < 64; ++i) ok &= a.in[i] == want[i];
   ok &= get_u64(a.in + 64) == 0;
@@ -768,6 +791,107 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
   }
 }
 
+
+// Order-0 baseline decode: cum(r) = floor(K E_q[r] / 2^26) + r needs no mu and
+// no sigma.  einv[k] is the smallest r with E_q[r] >= k 2^26 / n (n = kO0InvN).
+// Because K E_q[r] / 2^26 - 1 + r < cum(r) <= K E_q[r] / 2^26 + r and r < |S|,
+// the answer r* (cum(r*) <= slot < cum(r* + 1)) satisfies
+//   E_q[r*] < (slot + 1) 2^26 / K       ->  r* < einv[floor((slot + 1) n / K) + 1]
+//   E_q[r* + 1] > (slot - |S|) 2^26 / K ->  r* >= einv[floor((slot - |S|) n / K)] - 1,
+// a bracket of one or two table steps, which bisection finishes.
+__global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
+  extern __shared__ int32_t s_einv0[];
+  for (int i = threadIdx.x; i <= kO0InvN; i += blockDim.x) s_einv0[i] = a.einv[i];
+  __syncthreads();
+  constexpr int M = kMBf16;
+  constexpr uint32_t kMask = (1u << M) - 1u;
+  const int G = a.geo.G;
+  const int lane = threadIdx.x & 31;
+  const int ell = lane & (G - 1);
+  const uint32_t seg = G == 32 ? 0xFFFFFFFFu : (((1u << G) - 1u) << (lane & ~(G - 1)));
+  const uint32_t lt = seg & ((1u << lane) - 1u);
+  const int64_t ntasks = (a.geo.nchunks * G + 31) / 32;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t nc = a.geo.nchunks;
+  const uint64_t hbytes = 64 + 8 * (uint64_t)(nc + 1);
+  const uint64_t payload_bytes = a.in_bytes - hbytes;
+  const uint8_t *payload = a.in + hbytes;
+  uint16_t *out = static_cast<uint16_t *>(a.kv_out);
+
+  for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks;
+       task = next_task(a.head, nwarps)) {
+    const int64_t c = (task * 32 + lane) / G;
+    const bool live = c < nc;
+    uint32_t flags = 0;
+    uint64_t off_a = 0, off_b = 0;
+    if (live) {
+      const uint64_t *offs = reinterpret_cast<const uint64_t *>(a.in + 64);
+      off_a = offs[c];
+      off_b = offs[c + 1];
+    }
+    const bool ok = live && off_a <= off_b && off_b <= payload_bytes && ((off_a | off_b) & 3) == 0 &&
+                    (off_b - off_a) / 4 >= 2ull * G;
+    if (live && !ok) flags |= kFlagCorrupt;
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(payload + (ok ? off_a : 0));
+    const uint64_t nw = ok ? (off_b - off_a) / 4 : 0;
+    ChunkGeo cg = chunk_geo(a.geo, live ? c : 0);
+    const uint32_t my_groups =
+        (ok && (uint32_t)ell < cg.ngroup) ? (cg.ngroup - ell + G - 1) / G : 0u;
+    const uint32_t max_groups = __reduce_max_sync(0xFFFFFFFFu, my_groups);
+    uint64_t x = ok ? ((uint64_t)w[2 * ell] | ((uint64_t)w[2 * ell + 1] << 32)) : kStateL;
+    uint64_t cur = 2ull * G;
+
+    for (uint32_t gi = 0; gi < max_groups; ++gi) {
+      const bool has = gi < my_groups;
+      const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * gi);
+      uint32_t sym8[4] = {0u, 0u, 0u, 0u};
+#pragma unroll 1
+      for (int k = 0; k < 8; ++k) {
+        bool need = false;
+        if (has) {
+          const uint32_t slot = (uint32_t)x & kMask;
+          const uint32_t kh = (uint32_t)(((uint64_t)(slot + 1u) * kO0InvN) / kKBf16) + 1u;
+          int32_t hi = kh <= (uint32_t)kO0InvN ? s_einv0[kh] : kNsymBf16;
+          int32_t lo = 0;
+          if (slot >= (uint32_t)kNsymBf16) {
+            const uint32_t kl = (uint32_t)(((uint64_t)(slot - kNsymBf16) * kO0InvN) / kKBf16);
+            lo = max(s_einv0[kl] - 1, 0);
+          }
+          hi = max(hi, lo + 1);
+          while (hi - lo > 1) {  // cum(lo) <= slot < cum(hi)
+            const int32_t mid = (lo + hi) >> 1;
+            if (cum_order0(mid, a.ecdf) <= slot) lo = mid;
+            else hi = mid;
+          }
+          const uint32_t clo = cum_order0(lo, a.ecdf), chi = cum_order0(lo + 1, a.ecdf);
+          if (clo > slot || chi <= slot) flags |= kFlagCorrupt;  // only if E_q were not monotone
+          x = (uint64_t)(chi - clo) * (x >> M) + (slot - clo);
+          need = x < kStateL;
+          sym8[k >> 1] |= bits_bf16(lo) << (16 * (k & 1));
+        }
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, need) & seg;
+        if (need) {
+          const uint64_t pos = cur + __popc(m & lt);
+          if (pos < nw) {
+            x = (x << 32) | w[pos];
+          } else {
+            flags |= kFlagCorrupt;
+            x = kStateL;
+          }
+        }
+        cur += __popc(m);
+      }
+      if (has)
+        *reinterpret_cast<uint4 *>(out + cg.base + p0) = make_uint4(sym8[0], sym8[1], sym8[2], sym8[3]);
+    }
+    if (ok) {
+      if (x != kStateL) flags |= kFlagCorrupt;
+      if (ell == 0 && cur != nw) flags |= kFlagCorrupt;
+    }
+    if (flags) atomicOr(&a.head->flags, flags);
+  }
+}
+
 template <int DT, bool BISECT>
 static cudaError_t run_decode(const DecodeLaunch &a, int blocks, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k_decode<DT, BISECT>,
@@ -787,6 +911,13 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s) {
   int64_t blocks = (ntasks + wpb - 1) / wpb;
   const int64_t cap = (int64_t)device_sm_count();
   if (blocks > cap) blocks = cap;
+  if (a.order0) {
+    constexpr size_t smem = sizeof(int32_t) * (kO0InvN + 1);
+    e = cudaFuncSetAttribute(k_decode_o0, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k_decode_o0<<<(int)blocks, kDecThreads, smem, s>>>(a);
+    return cudaGetLastError();
+  }
   if (a.dtype == 0)
     return a.bisect ? run_decode<0, true>(a, (int)blocks, s) : run_decode<0, false>(a, (int)blocks, s);
   return a.bisect ? run_decode<1, true>(a, (int)blocks, s) : run_decode<1, false>(a, (int)blocks, s);

@@ -60,6 +60,7 @@ struct EncodeLaunch {
   const float2 *inv_chunk;  // per-block scales: the same per (chunk, channel), else null
   const uint32_t *scale_words;  // per-block scales: nsw words per chunk
   int32_t nsw;              // scale words per chunk (0 without per-block scales)
+  int32_t order0;           // 1: order-0 baseline (p-hat alone; kv only)
   const uint32_t *ecdf;
   uint32_t *scratch;        // nchunks * stride words
   int64_t stride;           // words per chunk stack
@@ -83,6 +84,7 @@ struct DecodeLaunch {
   const float2 *inv;
   const float2 *inv_chunk;  // per-block scales: per (chunk, channel) reciprocals, else null
   int32_t nsw;
+  int32_t order0;           // 1: order-0 baseline; einv then has kO0InvN + 1 entries
   const uint32_t *ecdf;
   void *kv_out;
   WsHead *head;
@@ -96,6 +98,7 @@ struct IdealLaunch {
   const uint16_t *mu;
   const float *sigma;
   const float *sigma_chunk;  // per-block scales: sigma_eff per (chunk, channel), else null
+  int32_t order0;            // 1: order-0 baseline, -log2 p-hat (kv only)
   const float *phat;
   float *per_scalar;
   double *partials;
@@ -107,6 +110,8 @@ struct IdealLaunch {
 // (bf16) or Phi(z) (e4m3), tabulated at kHinvN + 1 equally spaced u in
 // [0, kHinvUmax[dtype]] as (z_k, z_{k+1} - z_k): the decoder's first guess.
 constexpr int kHinvN = 1024;
+// Order-0 decode: inverse of the p-hat prefix table at kO0InvN + 1 points.
+constexpr int kO0InvN = 8192;
 constexpr float kHinvUmaxBf16 = 0.98f, kHinvUmaxE4m3 = 1.0f;
 
 // Per-block sigma scales.  Estimate mode (kv, mu set): choose each group's
@@ -140,8 +145,8 @@ cudaError_t launch_scales(const ScaleLaunch &a, cudaStream_t s);
 cudaError_t launch_prep(const float *sigma, int64_t nsig, const uint32_t *ecdf, float2 *inv,
                         WsHead *head, cudaStream_t s);
 cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s);
-// einv[k] = the smallest rank r with E_q[r] >= k 2^26 / kHinvN, k = 0..kHinvN.
-cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, cudaStream_t s);
+// einv[k] = the smallest rank r with E_q[r] >= k 2^26 / n, k = 0..n (n divides 2^26).
+cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, int n, cudaStream_t s);
 cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s);
 cudaError_t launch_ideal(const IdealLaunch &a, cudaStream_t s);
 

@@ -82,7 +82,7 @@ def test_argument_errors_without_gpu(skv):
                 P.SkvParams(P.SKV_BF16, 256, 64, 0, 1, 1, None),
                 P.SkvParams(P.SKV_BF16, 0, 8, 0, 1, 1, None),
                 P.SkvParams(5, 256, 8, 0, 1, 1, None),
-                P.SkvParams(P.SKV_BF16, 256, 8, 4, 1, 1, None)]:
+                P.SkvParams(P.SKV_BF16, 256, 8, 8, 1, 1, None)]:
         assert P.skv_max_encoded_bytes(bad, shape) == 0
         rc, _ = P.skv_encode(bad, shape, 1 << 20, 1 << 20, 1 << 20, 1 << 30, 1 << 20, 1 << 30, None)
         assert rc == P.SKV_ERR_ARG
@@ -96,6 +96,16 @@ def test_argument_errors_without_gpu(skv):
     assert P.skv_max_encoded_bytes(scaled, P.SkvShape(1, 2, 1, 4, 2056)) == 0
     rc, _ = P.skv_ideal_bits_noalloc(scaled, shape, 1 << 20, 1 << 20, None, None)
     assert rc == P.SKV_ERR_ARG
+    # the order-0 baseline: bf16 only, not with block scales, no fixed-scratch ideal bits
+    o0 = P.SkvParams(P.SKV_BF16, 256, 8, P.SKV_FLAG_ORDER0, None, 1 << 21, 1 << 22)
+    assert P.skv_max_encoded_bytes(o0, shape) == P.skv_max_encoded_bytes(good, shape)
+    for f, dt in ((P.SKV_FLAG_ORDER0, P.SKV_E4M3),
+                  (P.SKV_FLAG_ORDER0 | P.SKV_FLAG_BLOCK_SCALE, P.SKV_BF16), (8, P.SKV_BF16)):
+        assert P.skv_max_encoded_bytes(P.SkvParams(dt, 256, 8, f, 1, 1, 1), shape) == 0
+    rc, _ = P.skv_ideal_bits_noalloc(o0, shape, 1 << 20, None, None, None)
+    assert rc == P.SKV_ERR_ARG
+    rc, _ = P.skv_encode(o0, shape, None, None, 1 << 20, 1 << 30, 1 << 20, 1 << 30, None)
+    assert rc == P.SKV_ERR_ARG                       # kv is still required
     # NULL and misaligned pointers
     rc, _ = P.skv_encode(good, shape, None, 1 << 20, 1 << 20, 1 << 30, 1 << 20, 1 << 30, None)
     assert rc == P.SKV_ERR_ARG
