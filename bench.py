@@ -214,7 +214,8 @@ def load_traffic(kernel: str, workload: str):
     ent = d.get(kernel, {}).get(workload)
     if not ent:
         return None
-    import lossless_kv_cache_fixed_gb300.build as B
+    import importlib
+    B = importlib.import_module("lossless_kv_cache_fixed_gb300.build")  # the module, not P.build()
     if ent.get("source_digest") != B.source_digest():
         return None
     return ent.get("bytes_per_launch")

@@ -613,6 +613,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
       const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * gi);
       const uint16_t *mup = a.mu + cg.base + p0;
       const float2 *ivp2 = invrow + p0 % D;
+      uint64_t out_lo = 0, out_hi = 0;  // the group's 8 symbols, shifted in from the top
 #pragma unroll 1
       for (int k = 0; k < 8; ++k) {
         uint32_t mub = has ? (uint32_t)__ldg(mup + k) : 0u;
@@ -767,8 +768,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
           x = (uint64_t)(br.chi - br.clo) * (x >> M) + (slot - br.clo);
           need = x < kStateL;
           const uint32_t sym = DT == 0 ? bits_bf16(br.lo) : bits_e4m3(br.lo);
-          if (DT == 0) static_cast<uint16_t *>(a.kv_out)[cg.base + p0 + k] = (uint16_t)sym;
-          else static_cast<uint8_t *>(a.kv_out)[cg.base + p0 + k] = (uint8_t)sym;
+          if (DT == 0) {
+            out_lo = (out_lo >> 16) | (out_hi << 48);
+            out_hi = (out_hi >> 16) | ((uint64_t)sym << 48);
+          } else {
+            out_lo = (out_lo >> 8) | ((uint64_t)sym << 56);
+          }
         }
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, need) & seg;
         if (need) {
@@ -781,6 +786,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
           }
         }
         cur += __popc(m);
+      }
+      // one vector store per group (one lane per chunk would otherwise write
+      // 32 scattered sectors per symbol)
+      if (has) {
+        if (DT == 0)
+          *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.kv_out) + cg.base + p0) =
+              make_uint4((uint32_t)out_lo, (uint32_t)(out_lo >> 32), (uint32_t)out_hi,
+                         (uint32_t)(out_hi >> 32));
+        else
+          *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.kv_out) + cg.base + p0) =
+              make_uint2((uint32_t)out_lo, (uint32_t)(out_lo >> 32));
       }
     }
     if (ok) {
@@ -844,7 +860,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
     for (uint32_t gi = 0; gi < max_groups; ++gi) {
       const bool has = gi < my_groups;
       const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * gi);
-      uint32_t sym8[4] = {0u, 0u, 0u, 0u};
+      uint64_t out_lo = 0, out_hi = 0;  // the group's 8 symbols, shifted in from the top
 #pragma unroll 1
       for (int k = 0; k < 8; ++k) {
         bool need = false;
@@ -867,7 +883,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
           if (clo > slot || chi <= slot) flags |= kFlagCorrupt;  // only if E_q were not monotone
           x = (uint64_t)(chi - clo) * (x >> M) + (slot - clo);
           need = x < kStateL;
-          sym8[k >> 1] |= bits_bf16(lo) << (16 * (k & 1));
+          out_lo = (out_lo >> 16) | (out_hi << 48);
+          out_hi = (out_hi >> 16) | ((uint64_t)bits_bf16(lo) << 48);
         }
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, need) & seg;
         if (need) {
@@ -882,7 +899,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
         cur += __popc(m);
       }
       if (has)
-        *reinterpret_cast<uint4 *>(out + cg.base + p0) = make_uint4(sym8[0], sym8[1], sym8[2], sym8[3]);
+        *reinterpret_cast<uint4 *>(out + cg.base + p0) =
+            make_uint4((uint32_t)out_lo, (uint32_t)(out_lo >> 32), (uint32_t)out_hi,
+                       (uint32_t)(out_hi >> 32));
     }
     if (ok) {
       if (x != kStateL) flags |= kFlagCorrupt;
