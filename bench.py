@@ -427,15 +427,95 @@ def run_gpu(args):
           "d2h_bytes_per_step": int(nb3 + raw + 8 + 3 * 32),
           "mode": "kernels read and write pinned host memory over the link"}
 
-    e2e = {"value": round(world * raw / e2e_s / 1e9, 3), "unit": "GB/s",
-           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-           "mode": "staging copies to and from device buffers", "zero_copy": zc}
+    staged_e2e = {"value": round(world * raw / e2e_s / 1e9, 3), "unit": "GB/s",
+                  "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                  "mode": "staging copies to and from device buffers"}
+    # the headline is the faster of the two end-to-end modes; both are reported
+    best, other = (zc, staged_e2e) if zc["value"] > staged_e2e["value"] else (staged_e2e, zc)
+    e2e = dict(best)
+    e2e["other_mode"] = other
+    off = offload(codec, out, nb, kv, kv_h, mu, s, raw, world, dev, args)
     return finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value,
-                       t_enc, t_dec, t_bits, clk, e2e, w)
+                       t_enc, t_dec, t_bits, clk, e2e, w, off)
+
+
+def offload(codec, out, nb, kv, kv_h, mu, s, raw, world, dev, args, pieces=2):
+    """The cache held compressed in pinned host memory and brought back to the
+    device where mu is (the pages' section "该方法的用途"): raw KV bytes delivered
+    per second by (a) a plain copy of the raw cache over the link, (b) decoding
+    the container in place from host memory, (c) copying the container's chunk
+    ranges in on a second stream while the previous range decodes."""
+    import torch
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    nc = (s.L * 2 * s.H) * ((s.T + s.Tb - 1) // s.Tb)
+    head = 64 + 8 * (nc + 1)
+    box_h = torch.empty(nb, dtype=torch.uint8).pin_memory()
+    box_h.copy_(out[:nb])
+    box_d = torch.empty(nb, dtype=torch.uint8, device=dev)
+    dst = torch.empty_like(kv)
+    offs = box_h[64:head].view(torch.int64)
+    cuts = [nc * i // pieces for i in range(pieces + 1)]
+    reps = max(3, min(args.steps, 10))
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(main)
+        for _ in range(reps):
+            fn()
+        b.record(main)
+        torch.cuda.synchronize()
+        return max_over_ranks(a.elapsed_time(b) / reps, world, dev)
+
+    def raw_copy():
+        dst.copy_(kv_h, non_blocking=True)
+
+    def box_copy():
+        box_d.copy_(box_h, non_blocking=True)
+
+    def direct():
+        codec.decode_range(box_h, nb, 0, nc, mu, dst, first=True)
+
+    def staged():
+        side.wait_stream(main)
+        box_d[:head].copy_(box_h[:head], non_blocking=True)
+        codec.decode_range(box_d, nb, 0, 0, mu, dst, first=True)
+        evs = []
+        with torch.cuda.stream(side):
+            for i in range(pieces):
+                a, b = head + int(offs[cuts[i]]), head + (int(offs[cuts[i + 1]]) if cuts[i + 1] < nc
+                                                         else nb - head)
+                box_d[a:b].copy_(box_h[a:b], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(side)
+                evs.append(e)
+        for i in range(pieces):
+            main.wait_event(evs[i])
+            codec.decode_range(box_d, nb, cuts[i], cuts[i + 1], mu, dst)
+
+    # the link's own rate: best of two timings of each plain copy
+    t_raw = min(timed(raw_copy), timed(raw_copy))
+    t_box = min(timed(box_copy), timed(box_copy))
+    t_dir, t_stg = timed(direct), timed(staged)
+    codec.decode_status()
+    if not torch.equal(dst, kv):
+        raise RuntimeError("offload decode mismatch")
+    g = lambda nbytes, ms: round(world * nbytes / (ms * 1e-3) / 1e9, 2)
+    return {"unit": "GB/s of raw KV delivered to the device (mu already there)",
+            "raw_h2d": g(raw, t_raw), "container_h2d_link": g(nb, t_box),
+            "direct_decode_from_host": g(raw, t_dir),
+            "staged_pipelined_decode": g(raw, t_stg), "pieces": pieces,
+            "staged_note": "each range decode costs about one chunk's decode latency, so "
+                           "the pipeline only pays with few, large ranges",
+            "raw_over_container": round(raw / nb, 3),
+            "best_vs_raw_copy": round(max(t_raw / t_dir, t_raw / t_stg), 3)}
 
 
 def finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value, t_enc, t_dec, t_bits,
-                clk, e2e, w):
+                clk, e2e, w, off=None):
     if rank != 0:
         return None
     import synth
@@ -492,6 +572,7 @@ def finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value, t_enc, t
         "kernels": kernels,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "offload": off,
         "gpu_launches": launches_per_step(bps == 2, args.block_scale) * args.steps,
         "clocks": clk.summary(),
     }

@@ -169,6 +169,46 @@ int skv_decode(const skv_params *params, const skv_shape *shape, const void *in,
                size_t in_bytes, const uint16_t *mu, void *kv_out, void *workspace,
                size_t workspace_bytes, skv_stream_t stream);
 
+/* Decode part of a container, asynchronously, into a contiguous or a paged
+ * layout: the decoder fused with its consumer (the pages' section "该方法的用途":
+ * caches offloaded to host memory over a slow link are streamed back and
+ * decoded where they are needed; section "下一步计划": the decoder must keep up
+ * with the fast side).
+ *   in, in_bytes    the whole container as skv_encode wrote it.  It may sit in
+ *                   pinned host memory (the kernels then stream the payload
+ *                   over the CPU-GPU link) or in device memory; only the
+ *                   header, the offset table and the payload of the chunks
+ *                   being decoded are read, so a caller may copy a device
+ *                   buffer's chunk ranges in just before decoding them.
+ *   chunk_begin, chunk_end   chunks [chunk_begin, chunk_end) in container order.
+ *   mu, kv_out      device.  Without a page table: the [L][2][H][T][D] tensors
+ *                   of skv_decode.  With page_of_chunk (device, u32 per chunk
+ *                   of the container, num_pages > 0): page pools of num_pages
+ *                   pages of token_block * head_dim scalars each, chunk c's
+ *                   scalars in page page_of_chunk[c] in their contiguous order
+ *                   (a short last token block fills the start of its page).
+ *                   A page index >= num_pages is reported as SKV_ERR_ARG by
+ *                   skv_decode_status and that chunk is not written.
+ *   range_flags     SKV_RANGE_FIRST on the first call for a container: clears
+ *                   the status, prepares the model tables in the workspace and
+ *                   checks the header and the model fingerprint.  Later calls
+ *                   for the same container reuse them and must be ordered
+ *                   after it (same stream, or caller-made ordering).
+ * Argument errors (SKV_ERR_ARG, SKV_ERR_CAPACITY, a container shorter than its
+ * offset table: SKV_ERR_CORRUPT) return at once; data errors accumulate in the
+ * workspace until skv_decode_status.  Does not synchronize. */
+#define SKV_RANGE_FIRST 1
+int skv_decode_range(const skv_params *params, const skv_shape *shape, const void *in,
+                     size_t in_bytes, uint64_t chunk_begin, uint64_t chunk_end,
+                     const uint16_t *mu, void *kv_out, const uint32_t *page_of_chunk,
+                     uint64_t num_pages, int range_flags, void *workspace,
+                     size_t workspace_bytes, skv_stream_t stream);
+
+/* Status accumulated by skv_decode_range calls on this decode workspace since
+ * the last SKV_RANGE_FIRST: SKV_OK, SKV_ERR_ARG (a page index), SKV_ERR_PARAM,
+ * SKV_ERR_CORRUPT.  Synchronizes `stream`. */
+int skv_decode_status(const void *workspace, skv_stream_t stream);
+
 /* Ideal code length: the cross-entropy -log2 q(x) of every scalar under the
  * continuous model (bin mass of the mixture, or of N(mu, sigma^2) for e4m3),
  * evaluated in tail-safe fp32 and summed in fp64 in a fixed order.

@@ -19,12 +19,13 @@ SKV_OP_ENCODE, SKV_OP_DECODE, SKV_OP_IDEAL_BITS = 0, 1, 2
 SKV_FLAG_DECODE_BISECT = 1
 SKV_FLAG_BLOCK_SCALE = 2
 SKV_FLAG_ORDER0 = 4
+SKV_RANGE_FIRST = 1
 SKV_OK, SKV_ERR_ARG, SKV_ERR_CAPACITY, SKV_ERR_SYMBOL = 0, -1, -2, -3
 SKV_ERR_PARAM, SKV_ERR_CORRUPT, SKV_ERR_CUDA = -4, -5, -6
 NSYM = {SKV_BF16: 65282, SKV_E4M3: 254}
 
 EXPORTS = ("skv_max_encoded_bytes", "skv_workspace_bytes", "skv_encode", "skv_decode",
-           "skv_ideal_bits", "skv_ideal_bits_noalloc", "skv_ideal_bits_noalloc_max_channels",
+           "skv_decode_range", "skv_decode_status", "skv_ideal_bits", "skv_ideal_bits_noalloc", "skv_ideal_bits_noalloc_max_channels",
            "skv_build_ecdf", "skv_phi_table", "skv_strerror", "skv_version")
 
 
@@ -62,6 +63,9 @@ def lib():
             "skv_workspace_bytes": (sz, [P, S, C.c_int]),
             "skv_encode": (C.c_int, [P, S, vp, vp, vp, sz, C.POINTER(sz), vp, sz, vp]),
             "skv_decode": (C.c_int, [P, S, vp, sz, vp, vp, vp, sz, vp]),
+            "skv_decode_range": (C.c_int, [P, S, vp, sz, C.c_uint64, C.c_uint64, vp, vp, vp,
+                                           C.c_uint64, C.c_int, vp, sz, vp]),
+            "skv_decode_status": (C.c_int, [vp, vp]),
             "skv_ideal_bits": (C.c_int, [P, S, vp, vp, vp, C.POINTER(C.c_double), vp, sz, vp]),
             "skv_ideal_bits_noalloc": (C.c_int, [P, S, vp, vp, vp, C.POINTER(C.c_double), vp]),
             "skv_ideal_bits_noalloc_max_channels": (sz, []),
@@ -98,6 +102,18 @@ def skv_encode(params, shape, kv_ptr, mu_ptr, out_ptr, out_capacity, ws_ptr, ws_
 def skv_decode(params, shape, in_ptr, in_bytes, mu_ptr, kv_out_ptr, ws_ptr, ws_bytes, stream):
     return lib().skv_decode(C.byref(params), C.byref(shape), in_ptr, in_bytes, mu_ptr, kv_out_ptr,
                             ws_ptr, ws_bytes, stream)
+
+
+def skv_decode_range(params, shape, in_ptr, in_bytes, chunk_begin, chunk_end, mu_ptr,
+                     kv_out_ptr, pages_ptr, num_pages, range_flags, ws_ptr, ws_bytes, stream):
+    """Enqueues the decode of chunks [chunk_begin, chunk_end); returns the argument status."""
+    return lib().skv_decode_range(C.byref(params), C.byref(shape), in_ptr, in_bytes, chunk_begin,
+                                  chunk_end, mu_ptr, kv_out_ptr, pages_ptr, num_pages,
+                                  range_flags, ws_ptr, ws_bytes, stream)
+
+
+def skv_decode_status(ws_ptr, stream):
+    return lib().skv_decode_status(ws_ptr, stream)
 
 
 def skv_ideal_bits(params, shape, kv_ptr, mu_ptr, per_scalar_ptr, ws_ptr, ws_bytes, stream):
@@ -219,6 +235,24 @@ class Codec:
         if rc:
             raise SkvError(rc, "skv_decode")
         return out
+
+    def decode_range(self, buf, nbytes, chunk_begin, chunk_end, mu, out, pages=None,
+                     num_pages=0, first=False, stream=None):
+        """Enqueue the decode of chunks [chunk_begin, chunk_end) into `out` (the
+        [L,2,H,T,D] tensor, or a page pool when `pages` maps chunks to pages).
+        No synchronisation; call decode_status() for the accumulated status."""
+        ws = self.workspace(SKV_OP_DECODE)
+        rc = skv_decode_range(self.params, self.shape, buf.data_ptr(), nbytes, chunk_begin,
+                              chunk_end, _ptr(mu), out.data_ptr(), _ptr(pages), num_pages,
+                              SKV_RANGE_FIRST if first else 0, ws.data_ptr(), ws.numel(),
+                              _stream_handle(stream))
+        if rc:
+            raise SkvError(rc, "skv_decode_range")
+
+    def decode_status(self, stream=None):
+        rc = skv_decode_status(self.workspace(SKV_OP_DECODE).data_ptr(), _stream_handle(stream))
+        if rc:
+            raise SkvError(rc, "skv_decode_status")
 
     def ideal_bits(self, kv, mu, per_scalar=False, stream=None):
         ws = self.workspace(SKV_OP_IDEAL_BITS)

@@ -198,6 +198,7 @@ uint64_t hash_words(const Plan &pl) {
 }
 
 int status_from_flags(uint32_t f) {
+  if (f & kFlagArg) return SKV_ERR_ARG;
   if (f & kFlagSymbol) return SKV_ERR_SYMBOL;
   if (f & kFlagParam) return SKV_ERR_PARAM;
   if (f & kFlagCorrupt) return SKV_ERR_CORRUPT;
@@ -232,6 +233,71 @@ ScaleLaunch scale_launch(const Plan &pl, const skv_params *p, WsHead *head) {
   sl.sigma = p->sigma;
   sl.head = head;
   return sl;
+}
+
+// Decode of chunks [c0, c1) of a container, enqueued on `stream` without a
+// host synchronisation.  `first` zeroes the status, prepares the model tables
+// (reciprocals, fingerprint, inverse p-hat table) and checks the header; later
+// calls for the same container reuse them.  With a page table, mu and kv_out
+// are page pools of num_pages pages of token_block * head_dim scalars.
+int decode_enqueue(const skv_params *params, const Plan &pl, const void *in, size_t in_bytes,
+                   uint64_t c0, uint64_t c1, const uint16_t *mu, void *kv_out,
+                   const uint32_t *pages, uint64_t num_pages, bool first, void *workspace,
+                   size_t workspace_bytes, skv_stream_t stream) {
+  int rc = common_inputs(params, pl, kv_out, mu);
+  if (rc) return rc;
+  if (!in || !aligned(in, 8) || !workspace || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
+  if (workspace_bytes < ws_bytes_for(pl, SKV_OP_DECODE)) return SKV_ERR_CAPACITY;
+  if (in_bytes < 64 + 8 * (size_t)(pl.geo.nchunks + 1)) return SKV_ERR_CORRUPT;
+  if ((rc = ensure_device_tables())) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  WsHead *head = reinterpret_cast<WsHead *>(ws);
+  float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
+  const uint32_t *ecdf = pl.dtype == SKV_BF16 ? params->ecdf : nullptr;
+  int32_t *einv = pl.dtype == SKV_BF16 ? reinterpret_cast<int32_t *>(ws + pl.off_einv) : nullptr;
+  if (first) {
+    if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
+    if (launch_prep(params->sigma, pl.nsig_model, ecdf, inv, head, st) != cudaSuccess)
+      return SKV_ERR_CUDA;
+    if (einv && launch_einv(ecdf, einv, pl.order0 ? kO0InvN : kHinvN, st) != cudaSuccess)
+      return SKV_ERR_CUDA;
+  }
+  DecodeLaunch a;
+  std::memset(&a, 0, sizeof(a));
+  a.geo = pl.geo;
+  a.dtype = pl.dtype;
+  a.in = static_cast<const uint8_t *>(in);
+  a.in_bytes = in_bytes;
+  a.mu = mu;
+  a.inv = inv;
+  a.inv_chunk = nullptr;
+  a.nsw = pl.nsw;
+  a.order0 = pl.order0;
+  a.c_begin = (int64_t)c0;
+  a.c_end = (int64_t)c1;
+  a.check_header = first ? 1 : 0;
+  a.page_of_chunk = pages;
+  a.num_pages = num_pages;
+  a.page_scalars = (uint64_t)pl.geo.Tb * (uint64_t)pl.geo.D;
+  if (pl.nsw) {
+    ScaleLaunch sl = scale_launch(pl, params, head);
+    sl.in = static_cast<const uint8_t *>(in);
+    sl.in_bytes = in_bytes;
+    sl.inv = reinterpret_cast<float2 *>(ws + pl.off_dec_cinv);
+    sl.c_begin = (int64_t)c0;
+    sl.c_end = (int64_t)c1;
+    if (launch_scales(sl, st) != cudaSuccess) return SKV_ERR_CUDA;
+    a.inv_chunk = sl.inv;
+  }
+  a.ecdf = ecdf;
+  a.kv_out = kv_out;
+  a.head = head;
+  a.hash_words = hash_words(pl);
+  a.bisect = (params->flags & SKV_FLAG_DECODE_BISECT) ? 1 : 0;
+  a.einv = einv;
+  if (launch_decode(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  return SKV_OK;
 }
 
 // ---- scratch for skv_ideal_bits_noalloc ----
@@ -338,50 +404,38 @@ int skv_decode(const skv_params *params, const skv_shape *shape, const void *in,
   Plan pl;
   int rc = make_plan(params, shape, &pl);
   if (rc) return rc;
-  if ((rc = common_inputs(params, pl, kv_out, mu))) return rc;
-  if (!in || !aligned(in, 8) || !workspace || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
-  if (workspace_bytes < ws_bytes_for(pl, SKV_OP_DECODE)) return SKV_ERR_CAPACITY;
-  if (in_bytes < 64 + 8 * (size_t)(pl.geo.nchunks + 1)) return SKV_ERR_CORRUPT;
-  if ((rc = ensure_device_tables())) return rc;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t *ws = static_cast<uint8_t *>(workspace);
-  WsHead *head = reinterpret_cast<WsHead *>(ws);
-  if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
-  float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
-  const uint32_t *ecdf = pl.dtype == SKV_BF16 ? params->ecdf : nullptr;
-  if (launch_prep(params->sigma, pl.nsig_model, ecdf, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
-  DecodeLaunch a;
-  a.geo = pl.geo;
-  a.dtype = pl.dtype;
-  a.in = static_cast<const uint8_t *>(in);
-  a.in_bytes = in_bytes;
-  a.mu = mu;
-  a.inv = inv;
-  a.inv_chunk = nullptr;
-  a.nsw = pl.nsw;
-  a.order0 = pl.order0;
-  if (pl.nsw) {
-    ScaleLaunch sl = scale_launch(pl, params, head);
-    sl.in = static_cast<const uint8_t *>(in);
-    sl.in_bytes = in_bytes;
-    sl.inv = reinterpret_cast<float2 *>(ws + pl.off_dec_cinv);
-    if (launch_scales(sl, st) != cudaSuccess) return SKV_ERR_CUDA;
-    a.inv_chunk = sl.inv;
-  }
-  a.ecdf = ecdf;
-  a.kv_out = kv_out;
-  a.head = head;
-  a.hash_words = hash_words(pl);
-  a.bisect = (params->flags & SKV_FLAG_DECODE_BISECT) ? 1 : 0;
-  a.einv = nullptr;
-  if (pl.dtype == SKV_BF16) {
-    int32_t *einv = reinterpret_cast<int32_t *>(ws + pl.off_einv);
-    if (launch_einv(ecdf, einv, pl.order0 ? kO0InvN : kHinvN, st) != cudaSuccess) return SKV_ERR_CUDA;
-    a.einv = einv;
-  }
-  if (launch_decode(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  if ((rc = decode_enqueue(params, pl, in, in_bytes, 0, (uint64_t)pl.geo.nchunks, mu, kv_out,
+                           nullptr, 0, true, workspace, workspace_bytes, stream)))
+    return rc;
   WsHead h;
-  if ((rc = read_head(head, &h, st))) return rc;
+  if ((rc = read_head(static_cast<WsHead *>(workspace), &h,
+                      reinterpret_cast<cudaStream_t>(stream))))
+    return rc;
+  return status_from_flags(h.flags);
+}
+
+int skv_decode_range(const skv_params *params, const skv_shape *shape, const void *in,
+                     size_t in_bytes, uint64_t chunk_begin, uint64_t chunk_end,
+                     const uint16_t *mu, void *kv_out, const uint32_t *page_of_chunk,
+                     uint64_t num_pages, int range_flags, void *workspace,
+                     size_t workspace_bytes, skv_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  if (range_flags & ~SKV_RANGE_FIRST) return SKV_ERR_ARG;
+  if (chunk_begin > chunk_end || chunk_end > (uint64_t)pl.geo.nchunks) return SKV_ERR_ARG;
+  if (page_of_chunk && (!aligned(page_of_chunk, 4) || num_pages == 0)) return SKV_ERR_ARG;
+  return decode_enqueue(params, pl, in, in_bytes, chunk_begin, chunk_end, mu, kv_out,
+                        page_of_chunk, num_pages, (range_flags & SKV_RANGE_FIRST) != 0, workspace,
+                        workspace_bytes, stream);
+}
+
+int skv_decode_status(const void *workspace, skv_stream_t stream) {
+  if (!workspace || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
+  WsHead h;
+  int rc = read_head(static_cast<WsHead *>(const_cast<void *>(workspace)), &h,
+                     reinterpret_cast<cudaStream_t>(stream));
+  if (rc) return rc;
   return status_from_flags(h.flags);
 }
 

@@ -539,6 +539,22 @@ __device__ __forceinline__ int32_t rank_of_value(float x) {
 // unresolved are finished one at a time by the whole warp, 32 candidates per
 // step.  Every answer is checked by the exact cum bracket, so both searches
 // return the same symbol.
+// First scalar of chunk c in mu and in the output: its place in the
+// [L][2][H][T][D] tensor, or its page in a page pool (then an out-of-range
+// page index is an argument error and the chunk is skipped).
+__device__ __forceinline__ uint64_t chunk_out_base(const DecodeLaunch &a, int64_t c, bool &ok,
+                                                   uint32_t &flags) {
+  if (!a.page_of_chunk) return chunk_geo(a.geo, c < a.c_end ? c : 0).base;
+  if (!ok) return 0;
+  const uint32_t pg = a.page_of_chunk[c];
+  if ((uint64_t)pg >= a.num_pages) {
+    flags |= kFlagArg;
+    ok = false;
+    return 0;
+  }
+  return (uint64_t)pg * a.page_scalars;
+}
+
 // The warp's next task: after a first round in grid order, tasks go to whichever
 // warp is free first, so a few slow chunks (their search work depends on how
 // well the model fits) do not leave the rest of the GPU idle.  Called by all
@@ -573,7 +589,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
   const int ell = lane & (G - 1);
   const uint32_t seg = G == 32 ? 0xFFFFFFFFu : (((1u << G) - 1u) << (lane & ~(G - 1)));
   const uint32_t lt = seg & ((1u << lane) - 1u);
-  const int64_t ntasks = (a.geo.nchunks * G + 31) / 32;
+  const int64_t ntasks = ((a.c_end - a.c_begin) * G + 31) / 32;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const uint32_t D = (uint32_t)a.geo.D;
   const int64_t nc = a.geo.nchunks;
@@ -583,8 +599,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
 
   for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks;
        task = next_task(a.head, nwarps)) {
-    const int64_t c = (task * 32 + lane) / G;
-    const bool live = c < nc;
+    const int64_t c = a.c_begin + (task * 32 + lane) / G;
+    const bool live = c < a.c_end;
     uint32_t flags = 0;
     uint64_t off_a = 0, off_b = 0;
     if (live) {
@@ -593,9 +609,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
       off_b = offs[c + 1];
     }
     // both ends word-aligned (a misaligned word read would fault), inside the payload
-    const bool ok = live && off_a <= off_b && off_b <= payload_bytes && ((off_a | off_b) & 3) == 0 &&
-                    (off_b - off_a) / 4 >= 2ull * G + (uint64_t)a.nsw;
+    bool ok = live && off_a <= off_b && off_b <= payload_bytes && ((off_a | off_b) & 3) == 0 &&
+              (off_b - off_a) / 4 >= 2ull * G + (uint64_t)a.nsw;
     if (live && !ok) flags |= kFlagCorrupt;
+    const uint64_t obase = chunk_out_base(a, c, ok, flags);  // mu and output
     const uint32_t *w = reinterpret_cast<const uint32_t *>(payload + (ok ? off_a : 0));
     const uint64_t nw = ok ? (off_b - off_a) / 4 : 0;
     ChunkGeo cg = chunk_geo(a.geo, live ? c : 0);
@@ -611,7 +628,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
     for (uint32_t gi = 0; gi < max_groups; ++gi) {
       const bool has = gi < my_groups;
       const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * gi);
-      const uint16_t *mup = a.mu + cg.base + p0;
+      const uint16_t *mup = a.mu + obase + p0;
       const float2 *ivp2 = invrow + p0 % D;
       uint64_t out_lo = 0, out_hi = 0;  // the group's 8 symbols, shifted in from the top
 #pragma unroll 1
@@ -791,11 +808,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
       // 32 scattered sectors per symbol)
       if (has) {
         if (DT == 0)
-          *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.kv_out) + cg.base + p0) =
+          *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.kv_out) + obase + p0) =
               make_uint4((uint32_t)out_lo, (uint32_t)(out_lo >> 32), (uint32_t)out_hi,
                          (uint32_t)(out_hi >> 32));
         else
-          *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.kv_out) + cg.base + p0) =
+          *reinterpret_cast<uint2 *>(static_cast<uint8_t *>(a.kv_out) + obase + p0) =
               make_uint2((uint32_t)out_lo, (uint32_t)(out_lo >> 32));
       }
     }
@@ -826,7 +843,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
   const int ell = lane & (G - 1);
   const uint32_t seg = G == 32 ? 0xFFFFFFFFu : (((1u << G) - 1u) << (lane & ~(G - 1)));
   const uint32_t lt = seg & ((1u << lane) - 1u);
-  const int64_t ntasks = (a.geo.nchunks * G + 31) / 32;
+  const int64_t ntasks = ((a.c_end - a.c_begin) * G + 31) / 32;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t nc = a.geo.nchunks;
   const uint64_t hbytes = 64 + 8 * (uint64_t)(nc + 1);
@@ -836,8 +853,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
 
   for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks;
        task = next_task(a.head, nwarps)) {
-    const int64_t c = (task * 32 + lane) / G;
-    const bool live = c < nc;
+    const int64_t c = a.c_begin + (task * 32 + lane) / G;
+    const bool live = c < a.c_end;
     uint32_t flags = 0;
     uint64_t off_a = 0, off_b = 0;
     if (live) {
@@ -845,9 +862,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
       off_a = offs[c];
       off_b = offs[c + 1];
     }
-    const bool ok = live && off_a <= off_b && off_b <= payload_bytes && ((off_a | off_b) & 3) == 0 &&
-                    (off_b - off_a) / 4 >= 2ull * G;
+    bool ok = live && off_a <= off_b && off_b <= payload_bytes && ((off_a | off_b) & 3) == 0 &&
+              (off_b - off_a) / 4 >= 2ull * G;
     if (live && !ok) flags |= kFlagCorrupt;
+    const uint64_t obase = chunk_out_base(a, c, ok, flags);
     const uint32_t *w = reinterpret_cast<const uint32_t *>(payload + (ok ? off_a : 0));
     const uint64_t nw = ok ? (off_b - off_a) / 4 : 0;
     ChunkGeo cg = chunk_geo(a.geo, live ? c : 0);
@@ -899,7 +917,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
         cur += __popc(m);
       }
       if (has)
-        *reinterpret_cast<uint4 *>(out + cg.base + p0) =
+        *reinterpret_cast<uint4 *>(out + obase + p0) =
             make_uint4((uint32_t)out_lo, (uint32_t)(out_lo >> 32), (uint32_t)out_hi,
                        (uint32_t)(out_hi >> 32));
     }
@@ -921,11 +939,17 @@ static cudaError_t run_decode(const DecodeLaunch &a, int blocks, cudaStream_t s)
 }
 
 cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s) {
-  k_check_header<<<1, 32, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (a.check_header) {
+    k_check_header<<<1, 32, 0, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (a.c_end <= a.c_begin) return cudaSuccess;
+  // the task counter of this launch starts at zero
+  e = cudaMemsetAsync(&a.head->next_task, 0, sizeof(unsigned long long), s);
   if (e != cudaSuccess) return e;
   // at most one block per SM (see kCodeThreads)
-  const int64_t ntasks = (a.geo.nchunks * a.geo.G + 31) / 32;
+  const int64_t ntasks = ((a.c_end - a.c_begin) * a.geo.G + 31) / 32;
   const int64_t wpb = kDecThreads / 32;
   int64_t blocks = (ntasks + wpb - 1) / wpb;
   const int64_t cap = (int64_t)device_sm_count();

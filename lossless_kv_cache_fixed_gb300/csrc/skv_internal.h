@@ -89,6 +89,11 @@ struct DecodeLaunch {
   void *kv_out;
   WsHead *head;
   uint64_t hash_words;
+  int64_t c_begin, c_end;   // chunks to decode
+  int32_t check_header;     // 1: check the header and offset-table ends first
+  const uint32_t *page_of_chunk;  // paged layout (mu and kv_out are page pools), else null
+  uint64_t num_pages;
+  uint64_t page_scalars;    // token_block * head_dim
 };
 
 struct IdealLaunch {
@@ -131,6 +136,7 @@ struct ScaleLaunch {
   float2 *inv;
   float *sig;
   WsHead *head;
+  int64_t c_begin, c_end;   // load mode: chunks to read
 };
 
 // Device constants (Phi knot pairs, e4m3 bin edges, the two inverse tables,

@@ -179,6 +179,7 @@ enum : uint32_t {
   kFlagCorrupt = 4u,
   kFlagOverflow = 8u,
   kFlagCapacity = 16u,
+  kFlagArg = 32u,  // an argument only the device can check (a page index)
 };
 
 }  // namespace skv

@@ -185,12 +185,13 @@ __global__ void __launch_bounds__(256) k_scale_load(ScaleLaunch a) {
   const uint64_t hbytes = 64 + 8 * (uint64_t)(nc + 1);
   const uint64_t payload_bytes = a.in_bytes - hbytes;
   const uint64_t *offs = reinterpret_cast<const uint64_t *>(a.in + 64);
-  const int64_t total = nc * (int64_t)D;
+  const int64_t total = (a.c_end - a.c_begin) * (int64_t)D;
   uint32_t flags = 0;
-  for (int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; k < total;
-       k += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t c = k / D;
-    const int d = (int)(k - c * D);
+  for (int64_t kk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; kk < total;
+       kk += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t c = a.c_begin + kk / D;
+    const int d = (int)(kk % D);
+    const int64_t k = c * D + d;
     const uint64_t oa = offs[c], ob = offs[c + 1];
     if (!(oa <= ob && ob <= payload_bytes && ((oa | ob) & 3) == 0 &&
           (ob - oa) / 4 >= (uint64_t)nsw + 2ull * a.geo.G))
@@ -214,7 +215,8 @@ __global__ void __launch_bounds__(256) k_scale_load(ScaleLaunch a) {
 cudaError_t launch_scales(const ScaleLaunch &a, cudaStream_t s) {
   const int64_t cap = (int64_t)device_sm_count() * 8;
   if (a.in) {
-    const int64_t total = a.geo.nchunks * (int64_t)a.geo.D;
+    const int64_t total = (a.c_end - a.c_begin) * (int64_t)a.geo.D;
+    if (total <= 0) return cudaSuccess;
     int64_t blocks = (total + 255) / 256;
     if (blocks > cap) blocks = cap;
     k_scale_load<<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, s>>>(a);

@@ -106,6 +106,13 @@ def test_argument_errors_without_gpu(skv):
     assert rc == P.SKV_ERR_ARG
     rc, _ = P.skv_encode(o0, shape, None, None, 1 << 20, 1 << 30, 1 << 20, 1 << 30, None)
     assert rc == P.SKV_ERR_ARG                       # kv is still required
+    # range decode: range, flags and page-table arguments are checked on the host
+    for c0, c1, fl, pages, npg in ((5, 4, 1, None, 0), (0, 9, 1, None, 0), (0, 8, 2, None, 0),
+                                   (0, 8, 1, 1 << 20, 0), (0, 8, 1, (1 << 20) + 2, 8)):
+        rc = P.skv_decode_range(good, shape, 1 << 20, 1 << 20, c0, c1, 1 << 20, 1 << 20, pages,
+                                npg, fl, 1 << 20, 1 << 30, None)
+        assert rc == P.SKV_ERR_ARG, (c0, c1, fl, pages, npg)
+    assert P.skv_decode_status(None, None) == P.SKV_ERR_ARG
     # NULL and misaligned pointers
     rc, _ = P.skv_encode(good, shape, None, 1 << 20, 1 << 20, 1 << 30, 1 << 20, 1 << 30, None)
     assert rc == P.SKV_ERR_ARG
