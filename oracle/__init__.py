@@ -51,6 +51,7 @@ class _Model(C.Structure):
     _fields_ = [("dtype", C.c_int32), ("L", C.c_int32), ("H", C.c_int32), ("T", C.c_int32),
                 ("D", C.c_int32), ("Tb", C.c_int32), ("G", C.c_int32), ("w1", C.c_int32),
                 ("w3", C.c_int32), ("we", C.c_int32), ("block_scale", C.c_int32),
+                ("adaptive", C.c_int32),
                 ("sigma", C.c_void_p), ("E", C.c_void_p),
                 ("counts", C.c_void_p)]
 
@@ -87,6 +88,7 @@ def lib():
             "or_check_header": (C.c_int, [P, vp, u64]),
             "or_decode": (C.c_int, [P, vp, u64, vp, vp]),
             "or_scale_mult": (C.c_float, [i32]),
+            "or_adaptive_table": (C.c_int, [P, vp, u64, vp, vp]),
             "or_chunk_scales": (C.c_int, [P, vp, vp, u64, vp]),
             "or_log_q": (dbl, [dbl]),
             "or_log_mass": (dbl, [dbl, dbl]),
@@ -109,7 +111,7 @@ class Model:
     """Coding model: shape, chunking and the (sigma, p-hat) tables."""
 
     def __init__(self, dtype, L, H, T, D, Tb, G, sigma, E=None, counts=None,
-                 weights=(95, 3, 2), block_scale=False):
+                 weights=(95, 3, 2), block_scale=False, adaptive=False):
         self.dtype = dtype
         # the order-0 baseline (weights (0, 0, 100)) reads no sigma: None is allowed
         self.sigma = None if sigma is None else np.ascontiguousarray(sigma, dtype=np.float32)
@@ -122,7 +124,8 @@ class Model:
             assert self.E is not None and self.E.size == NSYM[BF16] + 1
         self.shape = (L, 2, H, T, D)
         self.s = _Model(dtype, L, H, T, D, Tb, G, weights[0], weights[1], weights[2],
-                        1 if block_scale else 0, _ptr(self.sigma), _ptr(self.E),
+                        1 if block_scale else 0, 1 if adaptive else 0, _ptr(self.sigma),
+                        _ptr(self.E),
                         _ptr(self.counts))
 
     @property
@@ -280,6 +283,17 @@ def model_bits_chunk(model, kv, mu, c):
     if rc:
         raise RuntimeError("oracle model_bits rc=%d" % rc)
     return b.value
+
+
+def adaptive_table(model, kv, c):
+    """(E table uint32[65283], P uint64[65282]) of chunk c of an adaptive model."""
+    kv = _as_sym(model, kv)
+    E = np.zeros(NSYM[BF16] + 1, dtype=np.uint32)
+    P = np.zeros(NSYM[BF16], dtype=np.uint64)
+    rc = lib().or_adaptive_table(model.ref, _ptr(kv), int(c), _ptr(E), _ptr(P))
+    if rc:
+        raise RuntimeError("oracle adaptive_table rc=%d" % rc)
+    return E, P
 
 
 def scale_mult(s):

@@ -61,6 +61,20 @@
  *       with weights (0, 0, 100), i.e. q = p-hat, one static histogram with no
  *       mu and no sigma.  bf16 only; mu and sigma are never read (they may be
  *       NULL), sigma is left out of the fingerprint, header feature bit 1.
+ *   R13 adaptive counts (the virtual-sliding-window estimator of the page
+ *       "KV 缓存压缩的熵估计与动态适应", sections "虚拟滑动窗口的设计原理",
+ *       "平滑更新算法", "参数配置建议"): the order-0 coder with one model per
+ *       (layer, kv, head) row, updated after every chunk, so the token block
+ *       is the update period N_update.  Integers only: A = round(0.97 2^16) =
+ *       63570, B = round(0.9 2^16) = 58982; token weights W[Tb-1] = 2^16,
+ *       W[t-1] = floor(W[t] A / 2^16) (alpha^(Tb-1-t)), block decay
+ *       Dk = floor(W[0] A / 2^16); counts C_0 = 0,
+ *       C_{b+1}[r] = floor(C_b[r] Dk / 2^16) + sum over the block's scalars of
+ *       rank r of W[token in block]; P_0[r] = (E_q[r+1] - E_q[r]) 2^6 (the
+ *       calibration prior, the page's cold-start remedy),
+ *       P_{b+1}[r] = floor((B P_b[r] + (2^16 - B) floor(2^32 C[r] / sum C)) / 2^16);
+ *       block b codes with E[r] = floor(2^26 S[r] / S_tot), S over P_b + 1.
+ *       bf16 only, weights (0, 0, 100), no block scales; header feature bit 2.
  */
 #include <float.h>
 #include <math.h>
@@ -413,7 +427,62 @@ int or_model_check(const or_model *m) {
   if (m->block_scale != 0 && m->block_scale != 1) return OR_ERR_ARG;
   if (m->dtype == OR_E4M3 && m->w1 == 0 && m->w3 == 0) return OR_ERR_ARG; /* bf16 only */
   if (order0(m) && m->block_scale) return OR_ERR_ARG;
+  if (m->adaptive != 0 && m->adaptive != 1) return OR_ERR_ARG;
+  if (m->adaptive && !order0(m)) return OR_ERR_ARG;
   return OR_OK;
+}
+
+/* R13: the coding table of chunk c from the row's earlier blocks of kv (for a
+   decoder: the cache decoded so far).  P, if given, receives P_b (NSYM_BF16). */
+int or_adaptive_table(const or_model *m, const void *kv, uint64_t c, uint32_t *E, uint64_t *P) {
+  init_tables();
+  const uint64_t ntb = ((uint64_t)m->T + m->Tb - 1) / m->Tb;
+  const uint64_t row = c / ntb, b = c % ntb;
+  const uint64_t A = 63570, B = 58982;
+  uint64_t *Pb = (uint64_t *)malloc(sizeof(uint64_t) * NSYM_BF16);
+  uint64_t *C = (uint64_t *)calloc(NSYM_BF16, sizeof(uint64_t));
+  uint64_t *W = (uint64_t *)malloc(sizeof(uint64_t) * (uint64_t)m->Tb);
+  if (!Pb || !C || !W) { free(Pb); free(C); free(W); return OR_ERR_ARG; }
+  for (int32_t r = 0; r < NSYM_BF16; ++r) Pb[r] = (uint64_t)(m->E[r + 1] - m->E[r]) << 6;
+  W[m->Tb - 1] = 65536;
+  for (int32_t t = m->Tb - 1; t > 0; --t) W[t - 1] = (W[t] * A) >> 16;
+  const uint64_t Dk = (W[0] * A) >> 16;
+  for (uint64_t blk = 0; blk < b; ++blk) {
+    for (int32_t r = 0; r < NSYM_BF16; ++r) C[r] = (C[r] * Dk) >> 16;
+    for (uint64_t t = 0; t < (uint64_t)m->Tb; ++t)   /* earlier blocks are whole */
+      for (uint64_t d = 0; d < (uint64_t)m->D; ++d) {
+        const uint64_t idx = (row * (uint64_t)m->T + blk * m->Tb + t) * m->D + d;
+        C[or_rank(OR_BF16, ((const uint16_t *)kv)[idx])] += W[t];
+      }
+    uint64_t sum = 0;
+    for (int32_t r = 0; r < NSYM_BF16; ++r) sum += C[r];
+    for (int32_t r = 0; r < NSYM_BF16; ++r) {
+      const uint64_t est = (uint64_t)(((unsigned __int128)C[r] << 32) / sum);
+      Pb[r] = (B * Pb[r] + (65536 - B) * est) >> 16;
+    }
+  }
+  uint64_t stot = 0;
+  for (int32_t r = 0; r < NSYM_BF16; ++r) stot += Pb[r] + 1;
+  uint64_t acc = 0;
+  for (int32_t r = 0; r <= NSYM_BF16; ++r) {
+    E[r] = (uint32_t)(((unsigned __int128)acc << 26) / stot);
+    if (r < NSYM_BF16) acc += Pb[r] + 1;
+  }
+  if (P) memcpy(P, Pb, sizeof(uint64_t) * NSYM_BF16);
+  free(Pb); free(C); free(W);
+  return OR_OK;
+}
+
+/* R13: a copy of m whose E is chunk c's table (E points at the caller's
+   NSYM_BF16 + 1 buffer); m itself if the model is not adaptive. */
+static const or_model *chunk_model(const or_model *m, const void *hist, uint64_t c,
+                                   or_model *copy, uint32_t *E, uint64_t *P, int *rc) {
+  *rc = OR_OK;
+  if (!m->adaptive) return m;
+  *rc = or_adaptive_table(m, hist, c, E, P);
+  *copy = *m;
+  copy->E = E;
+  return copy;
 }
 
 /* ------------------------------------------------------------------ */
@@ -432,6 +501,12 @@ int or_encode_chunk(const or_model *m, const void *kv, const uint16_t *mu, uint6
   init_tables();
   int rc = or_model_check(m);
   if (rc) return rc;
+  /* R13: the chunk's own table from the row's earlier blocks, then order 0 */
+  uint32_t *Ea = m->adaptive ? (uint32_t *)malloc(sizeof(uint32_t) * (NSYM_BF16 + 1)) : NULL;
+  or_model ma;
+  if (m->adaptive && !Ea) return OR_ERR_ARG;
+  m = chunk_model(m, kv, c, &ma, Ea, NULL, &rc);
+  if (rc) { free(Ea); return rc; }
   const int M = m->dtype == OR_BF16 ? 28 : 16;
   const int G = m->G;
   geom_t g = chunk_geom(m, c);
@@ -441,7 +516,7 @@ int or_encode_chunk(const or_model *m, const void *kv, const uint16_t *mu, uint6
   const uint64_t nsw = scale_words(m);
   uint64_t cap = 8 * g.ngroup + 2 * (uint64_t)G + nsw;
   uint32_t *stack = (uint32_t *)malloc(sizeof(uint32_t) * cap);
-  if (!stack) return OR_ERR_ARG;
+  if (!stack) { free(Ea); return OR_ERR_ARG; }
   uint64_t sp = 0;
   uint64_t x[32];
   for (int l = 0; l < G; ++l) x[l] = STATE_L;
@@ -455,11 +530,11 @@ int or_encode_chunk(const or_model *m, const void *kv, const uint16_t *mu, uint6
       if (!order0(m)) {
         sigma = m->sigma[g.srow + p % (uint64_t)m->D];
         muv = mu_value(mu[idx]);
-        if (!or_sigma_valid(sigma) || !isfinite(muv)) { free(stack); return OR_ERR_PARAM; }
+        if (!or_sigma_valid(sigma) || !isfinite(muv)) { free(stack); free(Ea); return OR_ERR_PARAM; }
         sigma = sigma_eff(m, &g, scales, p);
       }
       int32_t r = or_rank(m->dtype, sym_at(m, kv, idx));
-      if (r < 0) { free(stack); return OR_ERR_SYMBOL; }
+      if (r < 0) { free(stack); free(Ea); return OR_ERR_SYMBOL; }
       uint32_t cr = or_cum(m, r, muv, sigma);
       uint32_t freq = or_cum(m, r + 1, muv, sigma) - cr;
       uint64_t xmax = ((STATE_L >> M) << 32) * freq;
@@ -484,9 +559,10 @@ int or_encode_chunk(const or_model *m, const void *kv, const uint16_t *mu, uint6
     stack[sp++] = word;
   }
   *nwords = sp;
-  if (sp > cap_words) { free(stack); return OR_ERR_CAPACITY; }
+  if (sp > cap_words) { free(stack); free(Ea); return OR_ERR_CAPACITY; }
   for (uint64_t i = 0; i < sp; ++i) out[i] = stack[sp - 1 - i];
   free(stack);
+  free(Ea);
   return OR_OK;
 }
 
@@ -501,11 +577,26 @@ static int32_t find_rank(const or_model *m, uint32_t slot, float muv, float sigm
   return lo;
 }
 
+static int decode_chunk_with(const or_model *m, const uint32_t *w, uint64_t nwords,
+                             const uint16_t *mu, uint64_t c, void *kv_out);
+
 int or_decode_chunk(const or_model *m, const uint32_t *w, uint64_t nwords, const uint16_t *mu,
                     uint64_t c, void *kv_out) {
   init_tables();
   int rc = or_model_check(m);
   if (rc) return rc;
+  /* R13: the table is built from the blocks already decoded into kv_out */
+  uint32_t *Ea = m->adaptive ? (uint32_t *)malloc(sizeof(uint32_t) * (NSYM_BF16 + 1)) : NULL;
+  or_model ma;
+  if (m->adaptive && !Ea) return OR_ERR_ARG;
+  m = chunk_model(m, kv_out, c, &ma, Ea, NULL, &rc);
+  if (!rc) rc = decode_chunk_with(m, w, nwords, mu, c, kv_out);
+  free(Ea);
+  return rc;
+}
+
+static int decode_chunk_with(const or_model *m, const uint32_t *w, uint64_t nwords,
+                             const uint16_t *mu, uint64_t c, void *kv_out) {
   const int M = m->dtype == OR_BF16 ? 28 : 16;
   const uint64_t mask = (1ull << M) - 1;
   const int G = m->G;
@@ -603,7 +694,8 @@ static void write_header(const or_model *m, uint8_t *h, uint64_t nchunks, uint64
   h[34] = 8;
   h[35] = 9;
   put16(h + 36, 8);
-  put16(h + 38, (uint16_t)((m->block_scale ? 1 : 0) | (order0(m) ? 2 : 0))); /* feature bits */
+  put16(h + 38, (uint16_t)((m->block_scale ? 1 : 0) | (order0(m) ? 2 : 0) |
+                           (m->adaptive ? 4 : 0))); /* feature bits */
   put64(h + 40, nchunks);
   put64(h + 48, payload);
   put64(h + 56, or_model_hash(m));
@@ -763,8 +855,16 @@ int or_ideal_bits(const or_model *m, const void *kv, const uint16_t *mu, uint64_
   int rc = or_model_check(m);
   if (rc) return rc;
   double stot = 0;
-  if (m->dtype == OR_BF16)
+  if (m->dtype == OR_BF16 && m->counts)
     for (int32_t k = 0; k < NSYM_BF16; ++k) stot += (double)m->counts[g_bits_bf16[k]] + 1.0;
+  uint64_t *Pa = NULL;
+  uint32_t *Ea2 = NULL;
+  double pa_stot = 0;
+  if (m->adaptive) {
+    Pa = (uint64_t *)malloc(sizeof(uint64_t) * NSYM_BF16);
+    Ea2 = (uint32_t *)malloc(sizeof(uint32_t) * (NSYM_BF16 + 1));
+    if (!Pa || !Ea2) { free(Pa); free(Ea2); return OR_ERR_ARG; }
+  }
   double acc = 0;
   const uint64_t nc = or_num_chunks(m);
   for (uint64_t c = 0; c < nc; ++c) {
@@ -773,10 +873,21 @@ int or_ideal_bits(const or_model *m, const void *kv, const uint16_t *mu, uint64_
     if (c1 <= begin || c0 >= end) continue;
     uint8_t scales[256];
     if (m->block_scale) or_chunk_scales(m, kv, mu, c, scales);
+    if (m->adaptive) {
+      if ((rc = or_adaptive_table(m, kv, c, Ea2, Pa))) { free(Pa); free(Ea2); return rc; }
+      pa_stot = 0;
+      for (int32_t k = 0; k < NSYM_BF16; ++k) pa_stot += (double)Pa[k] + 1.0;
+    }
     for (uint64_t i = c0 > begin ? c0 : begin; i < (c1 < end ? c1 : end); ++i) {
       uint32_t sym = sym_at(m, kv, i);
       int32_t r = or_rank(m->dtype, sym);
-      if (r < 0) return OR_ERR_SYMBOL;
+      if (r < 0) { free(Pa); free(Ea2); return OR_ERR_SYMBOL; }
+      if (m->adaptive) { /* R13: q = (P_b + 1) / S_tot of the chunk's model */
+        const double bits = -log(((double)Pa[r] + 1.0) / pa_stot) / M_LN2;
+        if (per_scalar) per_scalar[i - begin] = bits;
+        acc += bits;
+        continue;
+      }
       if (order0(m)) { /* R12: q = p-hat */
         const double bits = -log(((double)m->counts[sym] + 1.0) / stot) / M_LN2;
         if (per_scalar) per_scalar[i - begin] = bits;
@@ -785,7 +896,7 @@ int or_ideal_bits(const or_model *m, const void *kv, const uint16_t *mu, uint64_
       }
       float sigma = m->sigma[g.srow + (i - g.base) % (uint64_t)m->D];
       double muv = or_bf16_value(mu[i]);
-      if (!or_sigma_valid(sigma) || !isfinite(muv)) return OR_ERR_PARAM;
+      if (!or_sigma_valid(sigma) || !isfinite(muv)) { free(Pa); free(Ea2); return OR_ERR_PARAM; }
       sigma = sigma_eff(m, &g, scales, i - g.base);
       double s = (double)sigma;
       double lo = (double)or_lo(m->dtype, r), hi = (double)or_lo(m->dtype, r + 1);
@@ -802,6 +913,8 @@ int or_ideal_bits(const or_model *m, const void *kv, const uint16_t *mu, uint64_
       acc += bits;
     }
   }
+  free(Pa);
+  free(Ea2);
   *total = acc;
   return OR_OK;
 }
@@ -810,6 +923,12 @@ int or_ideal_bits(const or_model *m, const void *kv, const uint16_t *mu, uint64_
 int or_model_bits_chunk(const or_model *m, const void *kv, const uint16_t *mu, uint64_t c,
                         double *bits) {
   init_tables();
+  int rc;
+  uint32_t *Ea = m->adaptive ? (uint32_t *)malloc(sizeof(uint32_t) * (NSYM_BF16 + 1)) : NULL;
+  or_model ma;
+  if (m->adaptive && !Ea) return OR_ERR_ARG;
+  m = chunk_model(m, kv, c, &ma, Ea, NULL, &rc);
+  if (rc) { free(Ea); return rc; }
   const int M = m->dtype == OR_BF16 ? 28 : 16;
   geom_t g = chunk_geom(m, c);
   uint8_t scales[256];
@@ -820,10 +939,11 @@ int or_model_bits_chunk(const or_model *m, const void *kv, const uint16_t *mu, u
     float sigma = order0(m) ? 1.0f : sigma_eff(m, &g, scales, p);
     float muv = order0(m) ? 0.0f : mu_value(mu[idx]);
     int32_t r = or_rank(m->dtype, sym_at(m, kv, idx));
-    if (r < 0) return OR_ERR_SYMBOL;
+    if (r < 0) { free(Ea); return OR_ERR_SYMBOL; }
     uint32_t freq = or_cum(m, r + 1, muv, sigma) - or_cum(m, r, muv, sigma);
     acc += (double)M - log2((double)freq);
   }
+  free(Ea);
   *bits = acc;
   return OR_OK;
 }

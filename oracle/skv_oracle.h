@@ -16,6 +16,7 @@ typedef struct {
   int32_t Tb, G;                /* token block, lanes per chunk */
   int32_t w1, w3, we;           /* mixture weights in percent (95, 3, 2) */
   int32_t block_scale;          /* 1: per-(chunk, 8-channel group) sigma scales */
+  int32_t adaptive;             /* 1: adaptive order-0 counts per (layer, kv, head) row */
   const float *sigma;           /* [L][2][H][D] */
   const uint32_t *E;            /* bf16: empirical prefix table, 65283 entries */
   const uint64_t *counts;       /* bf16: calibration counts by bit pattern, 65536 */
@@ -49,6 +50,7 @@ int or_decode(const or_model *m, const uint8_t *in, uint64_t in_bytes, const uin
 float or_scale_mult(int32_t s);
 int or_chunk_scales(const or_model *m, const void *kv, const uint16_t *mu, uint64_t c,
                     uint8_t *scales);
+int or_adaptive_table(const or_model *m, const void *kv, uint64_t c, uint32_t *E, uint64_t *P);
 double or_log_q(double z);
 double or_log_mass(double za, double zb);
 double or_ideal_bits_one(const or_model *m, uint32_t sym, uint16_t mu_bits, float sigma);
