@@ -33,7 +33,10 @@ DEFAULT_WORKLOAD = "qwen3-0.6b-bf16"
 # decode (prep, header check, decode; bf16 adds the inverse p-hat table),
 # ideal bits (prep, bits, final sum); with per-block scales one more in each
 # (scale estimate, scale load, scale estimate)
-def launches_per_step(bf16: bool, block_scale: bool) -> int:
+def launches_per_step(bf16: bool, block_scale: bool, adaptive_blocks: int = 0) -> int:
+    if adaptive_blocks:   # one phase per token block (tables, chunks, update)
+        nb = adaptive_blocks
+        return (5 + 3 * nb - 1) + (4 + 2 * nb + nb - 1) + (2 + nb + nb - 1)
     return 5 + (4 if bf16 else 3) + 3 + (3 if block_scale else 0)
 
 
@@ -231,6 +234,8 @@ def oracle_sample_step(O, m, kv, mu, chunks):
     D, T, Tb = s.D, s.T, s.Tb
     ntb = (T + Tb - 1) // Tb
     dec = _scratch_for(kv)
+    if getattr(m.s, "adaptive", 0):
+        dec[:] = kv        # adaptive tables read the row's earlier blocks from here
     scalars = 0
     for c in chunks:
         words = O._encode_chunk_raw(m, kv, mu, c)
@@ -257,16 +262,20 @@ def _scratch_for(kv):
     return _SCRATCH[key]
 
 
-def oracle_setup(workload_name, seed, device, block_scale=False, order0=False):
+def oracle_setup(workload_name, seed, device, block_scale=False, order0=False, adaptive=False,
+                 token_block=0):
     import oracle as O
     import synth
     O.build()
-    w = synth.make(workload_name, device=device, seed=seed)
+    spec = synth.WORKLOADS[workload_name]
+    if token_block:
+        spec = spec.scaled(Tb=token_block)
+    w = synth.make(spec, device=device, seed=seed)
     kv, mu, sigma, counts = synth.to_numpy(w)
     s = w.spec
     if order0:
         m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, None, counts=counts,
-                    weights=(0, 0, 100))
+                    weights=(0, 0, 100), adaptive=adaptive)
         return O, w, m, kv.reshape(-1), None
     m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sigma, counts=counts,
                 block_scale=block_scale)
@@ -301,6 +310,8 @@ def run_gpu(args):
     P.build()
 
     spec = synth.WORKLOADS[args.workload]
+    if args.adaptive and not args.token_block:
+        args.token_block = 128   # the entropy-estimation page's N_update
     if args.lanes or args.token_block:
         spec = spec.scaled(G=args.lanes or spec.G, Tb=args.token_block or spec.Tb)
     w = synth.make(spec, device=dev, seed=rank_seed(rank))
@@ -313,7 +324,7 @@ def run_gpu(args):
         phat = torch.from_numpy(ph).to(dev)
     flags = (P.SKV_FLAG_DECODE_BISECT if args.decode_bisect else 0) | (
         P.SKV_FLAG_BLOCK_SCALE if args.block_scale else 0) | (
-        P.SKV_FLAG_ORDER0 if args.order0 else 0)
+        P.SKV_FLAG_ORDER0 if args.order0 else 0) | (P.SKV_FLAG_ADAPTIVE if args.adaptive else 0)
     codec = P.Codec(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G,
                     None if args.order0 else w.sigma.to(dev), ecdf, phat, flags=flags)
     kv = (w.kv.view(torch.int16) if s.dtype == synth.BF16 else w.kv).reshape(-1)
@@ -434,7 +445,8 @@ def run_gpu(args):
     best, other = (zc, staged_e2e) if zc["value"] > staged_e2e["value"] else (staged_e2e, zc)
     e2e = dict(best)
     e2e["other_mode"] = other
-    off = offload(codec, out, nb, kv, kv_h, mu, s, raw, world, dev, args)
+    # range decode (the offload paths) takes whole containers only for adaptive counts
+    off = None if args.adaptive else offload(codec, out, nb, kv, kv_h, mu, s, raw, world, dev, args)
     return finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value,
                        t_enc, t_dec, t_bits, clk, e2e, w, off)
 
@@ -534,7 +546,7 @@ def finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value, t_enc, t
         kvn, mun, sig, cnt = synth.to_numpy(w)
         if args.order0:
             m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, None, counts=cnt,
-                        weights=(0, 0, 100))
+                        weights=(0, 0, 100), adaptive=args.adaptive)
             mun = None
         else:
             m = O.Model(s.dtype, s.L, s.H, s.T, s.D, s.Tb, s.G, sig, counts=cnt,  # same chunking
@@ -557,8 +569,7 @@ def finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value, t_enc, t
                    "layers": s.L, "heads": s.H, "tokens": s.T, "head_dim": s.D,
                    "scalars_per_gpu": n, "token_block": s.Tb, "lanes": s.G,
                    "block_scale": bool(args.block_scale),
-                   "coder": "order-0 baseline (p-hat alone)" if args.order0
-                            else "speculative (mu, sigma mixture)",
+                   "coder": coder_name(args),
                    "parallelism": "dp%d (independent caches)" % world,
                    "l2": "inputs larger than L2: %.0f MB KV + %.0f MB mu per step" % (
                        raw / 1e6, 2 * n / 1e6)},
@@ -573,10 +584,18 @@ def finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value, t_enc, t
         "cpu_baseline": cpu,
         "e2e": e2e,
         "offload": off,
-        "gpu_launches": launches_per_step(bps == 2, args.block_scale) * args.steps,
+        "gpu_launches": launches_per_step(bps == 2, args.block_scale,
+                                          s.T // s.Tb + (s.T % s.Tb > 0) if args.adaptive else 0)
+                        * args.steps,
         "clocks": clk.summary(),
     }
     return line
+
+
+def coder_name(args) -> str:
+    if args.adaptive:
+        return "order-0 with adaptive per-row counts"
+    return "order-0 baseline (p-hat alone)" if args.order0 else "speculative (mu, sigma mixture)"
 
 
 def run_reference(args):
@@ -586,8 +605,11 @@ def run_reference(args):
         return None
     import torch
     device = "cuda" if torch.cuda.is_available() else "cpu"
+    if args.adaptive and not args.token_block:
+        args.token_block = 128
     O, w, m, kv, mu = oracle_setup(args.workload, 0, device, block_scale=args.block_scale,
-                                   order0=args.order0)
+                                   order0=args.order0, adaptive=args.adaptive,
+                                   token_block=args.token_block)
     s = w.spec
     bps = 2 if s.dtype == 0 else 1
     nch = m.num_chunks()
@@ -617,8 +639,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
         "config": {"workload": args.workload, "scalars_per_gpu": s.n, "token_block": s.Tb,
                    "lanes": s.G, "block_scale": bool(args.block_scale),
-                   "coder": "order-0 baseline (p-hat alone)" if args.order0
-                            else "speculative (mu, sigma mixture)"},
+                   "coder": coder_name(args)},
         "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": "%d chunks per step of %d scalars each (every %d-th chunk), "
                                    "encode + decode + ideal bits" % (per_step, s.Tb * s.D, stride)},
@@ -646,7 +667,11 @@ def main(argv=None):
                     help="per-(chunk, 8-channel group) sigma scales in the container")
     ap.add_argument("--order0", action="store_true",
                     help="the order-0 baseline coder (p-hat alone, no mu/sigma; bf16)")
+    ap.add_argument("--adaptive", action="store_true",
+                    help="adaptive counts per row on the order-0 coder (token block 128)")
     args = ap.parse_args(argv)
+    if args.adaptive:
+        args.order0 = True
     if args.warmup < 3 and args.impl == "skv":
         args.warmup = 3
     line = run_reference(args) if args.impl == "reference" else run_gpu(args)

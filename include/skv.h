@@ -113,6 +113,16 @@ typedef struct {
  * may be NULL; sigma is not part of the model fingerprint; header feature
  * bit 1.  Ideal bits are -log2 p-hat.  skv_ideal_bits_noalloc rejects it. */
 #define SKV_FLAG_ORDER0 4
+/* Adaptive counts (the entropy-estimation page's virtual sliding window:
+ * decayed counts C = 0.97 C + delta per token, smoothed updates P = 0.9 P +
+ * 0.1 C / sum C): with SKV_FLAG_ORDER0, one model per (layer, kv, head) row,
+ * updated after every chunk from the row's earlier token blocks, so the token
+ * block is the update period.  Integer arithmetic throughout, the prior is
+ * E_q.  The coder then runs one phase per token block (rows in parallel,
+ * blocks of a row in order).  Requires head_dim <= 512 and token_block <=
+ * 65536; header feature bit 2;
+ * skv_decode_range and skv_ideal_bits_noalloc reject it (SKV_ERR_ARG). */
+#define SKV_FLAG_ADAPTIVE 8
 
 typedef struct {
   int32_t dtype;
@@ -143,7 +153,7 @@ size_t skv_workspace_bytes(const skv_params *params, const skv_shape *shape, int
  * Container v1 (little-endian): a 64-byte header {u32 magic "SKV1", u16 version
  * 1, u8 dtype, u8 M, u32 layers, u32 2, u32 heads, u32 tokens, u32 head_dim,
  * u32 token_block, u16 lanes, u8 8, u8 9, u16 8, u16 features (bit 0:
- * SKV_FLAG_BLOCK_SCALE, bit 1: SKV_FLAG_ORDER0), u64 num_chunks, u64 payload_bytes, u64 model
+ * SKV_FLAG_BLOCK_SCALE, bit 1: SKV_FLAG_ORDER0, bit 2: SKV_FLAG_ADAPTIVE), u64 num_chunks, u64 payload_bytes, u64 model
  * fingerprint of sigma (and E_q for bf16)}, then u64 offsets[num_chunks + 1]
  * (byte offsets from the payload start, multiples of 4), then the payload:
  * chunk c (index ((l*2 + kv)*heads + h)*ceil(tokens/Tb) + tb) is u32 words in

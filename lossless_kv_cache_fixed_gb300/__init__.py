@@ -19,6 +19,7 @@ SKV_OP_ENCODE, SKV_OP_DECODE, SKV_OP_IDEAL_BITS = 0, 1, 2
 SKV_FLAG_DECODE_BISECT = 1
 SKV_FLAG_BLOCK_SCALE = 2
 SKV_FLAG_ORDER0 = 4
+SKV_FLAG_ADAPTIVE = 8
 SKV_RANGE_FIRST = 1
 SKV_OK, SKV_ERR_ARG, SKV_ERR_CAPACITY, SKV_ERR_SYMBOL = 0, -1, -2, -3
 SKV_ERR_PARAM, SKV_ERR_CORRUPT, SKV_ERR_CUDA = -4, -5, -6

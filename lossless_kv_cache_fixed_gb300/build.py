@@ -11,7 +11,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libskv.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["skv_code.cu", "skv_bits.cu", "skv_scale.cu", "skv_api.cu"]
+SOURCES = ["skv_code.cu", "skv_bits.cu", "skv_scale.cu", "skv_adapt.cu", "skv_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

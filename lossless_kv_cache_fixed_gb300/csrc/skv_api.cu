@@ -7,6 +7,7 @@
 // the empirical bf16 distribution that skv_build_ecdf tabulates.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -101,6 +102,12 @@ struct Plan {
   int64_t nsig;
   int32_t nsw;     // per-block scale words per chunk (0: static sigma)
   int order0;      // order-0 baseline: p-hat alone, no mu and no sigma
+  int adaptive;    // adaptive counts per row (order 0), one phase per token block
+  int64_t nrows;   // layers * 2 * heads
+  size_t ad_P, ad_C, ad_E, ad_W, ad_inv, ad_part;  // adaptive regions, relative offsets
+  size_t ad_bytes_enc, ad_bytes_dec, ad_bytes_bits;
+  size_t ad_base_enc, ad_base_dec, ad_base_bits;  // where each operation's region starts
+  int ad_bx;       // ideal-bits blocks per (row, token block)
   int64_t nsig_model;  // sigma entries the model reads (0 for the order-0 baseline)
   // workspace layout (byte offsets)
   size_t off_inv, off_sizes, off_starts, off_partials, off_scratch, off_bits, off_einv, total;
@@ -116,10 +123,14 @@ bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   if (!p || !s || !out) return SKV_ERR_ARG;
   if (p->dtype != SKV_BF16 && p->dtype != SKV_E4M3) return SKV_ERR_ARG;
-  if (p->flags & ~(SKV_FLAG_DECODE_BISECT | SKV_FLAG_BLOCK_SCALE | SKV_FLAG_ORDER0))
+  if (p->flags & ~(SKV_FLAG_DECODE_BISECT | SKV_FLAG_BLOCK_SCALE | SKV_FLAG_ORDER0 |
+                   SKV_FLAG_ADAPTIVE))
     return SKV_ERR_ARG;
   const bool order0 = (p->flags & SKV_FLAG_ORDER0) != 0;
   if (order0 && (p->dtype != SKV_BF16 || (p->flags & SKV_FLAG_BLOCK_SCALE))) return SKV_ERR_ARG;
+  const bool adaptive = (p->flags & SKV_FLAG_ADAPTIVE) != 0;
+  // the counts' fixed point (a row's decayed total below 2^31) needs head_dim <= 512
+  if (adaptive && (!order0 || s->head_dim > 512 || p->token_block > 65536)) return SKV_ERR_ARG;
   if (s->kv != 2 || s->layers <= 0 || s->heads <= 0 || s->tokens <= 0 || s->head_dim <= 0)
     return SKV_ERR_ARG;
   if (s->head_dim % 8) return SKV_ERR_ARG;
@@ -146,6 +157,8 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   pl.nsig = rows * s->head_dim;
   pl.order0 = order0 ? 1 : 0;
   pl.nsig_model = order0 ? 0 : pl.nsig;
+  pl.adaptive = adaptive ? 1 : 0;
+  pl.nrows = rows;
   // worst case words of one full chunk: every lane emits at most one word per
   // symbol and, since a symbol adds at most M + log2(1 + 2^(M-31)) < M + 1
   // bits of state, at most ceil(n (M + 1) / 32) words; plus 2 flush words.
@@ -183,6 +196,27 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   pl.dec_total = align_up(pl.off_dec_cinv + sizeof(float2) * ccells);
   pl.off_bits_csig = align_up(pl.off_bits + sizeof(double) * (size_t)pl.bits_blocks);
   pl.bits_total = align_up(pl.off_bits_csig + sizeof(float) * ccells);
+  // adaptive counts: per-row P, C, E (and decode's inverse tables), the token
+  // weights and the ideal-bits partial sums, appended to each operation's layout
+  pl.ad_bx = (int)std::min<int64_t>(16, (tb_eff * s->head_dim + 2047) / 2048);
+  if (adaptive) {
+    const size_t nr = (size_t)rows;
+    pl.ad_P = 0;
+    pl.ad_C = align_up(pl.ad_P + sizeof(uint64_t) * nr * kNsymBf16);
+    pl.ad_E = align_up(pl.ad_C + sizeof(uint64_t) * nr * kNsymBf16);
+    pl.ad_W = align_up(pl.ad_E + sizeof(uint32_t) * nr * (kNsymBf16 + 1));
+    pl.ad_inv = align_up(pl.ad_W + sizeof(uint64_t) * (size_t)(p->token_block + 1));
+    pl.ad_part = pl.ad_inv;  // ideal bits use this region for its partial sums instead
+    pl.ad_bytes_enc = pl.ad_inv;
+    pl.ad_bytes_dec = align_up(pl.ad_inv + sizeof(int32_t) * nr * (kO0InvN + 1));
+    pl.ad_bytes_bits = align_up(pl.ad_part + sizeof(double) * (size_t)pl.geo.ntb * nr * pl.ad_bx);
+    pl.ad_base_enc = pl.enc_total;
+    pl.ad_base_dec = pl.dec_total;
+    pl.ad_base_bits = pl.bits_total;
+    pl.enc_total += pl.ad_bytes_enc;
+    pl.dec_total += pl.ad_bytes_dec;
+    pl.bits_total += pl.ad_bytes_bits;
+  }
   *out = pl;
   return SKV_OK;
 }
@@ -276,6 +310,10 @@ int decode_enqueue(const skv_params *params, const Plan &pl, const void *in, siz
   a.order0 = pl.order0;
   a.c_begin = (int64_t)c0;
   a.c_end = (int64_t)c1;
+  a.c_step = 1;
+  a.ecdf_row_stride = 0;
+  a.einv_row_stride = 0;
+  a.adaptive = pl.adaptive;
   a.check_header = first ? 1 : 0;
   a.page_of_chunk = pages;
   a.num_pages = num_pages;
@@ -296,6 +334,34 @@ int decode_enqueue(const skv_params *params, const Plan &pl, const void *in, siz
   a.hash_words = hash_words(pl);
   a.bisect = (params->flags & SKV_FLAG_DECODE_BISECT) ? 1 : 0;
   a.einv = einv;
+  if (pl.adaptive) {
+    // the whole container, one phase per token block: each block's tables come
+    // from the blocks decoded before it
+    uint8_t *ad = ws + pl.ad_base_dec;
+    uint64_t *P = reinterpret_cast<uint64_t *>(ad + pl.ad_P);
+    uint64_t *Cn = reinterpret_cast<uint64_t *>(ad + pl.ad_C);
+    uint32_t *Et = reinterpret_cast<uint32_t *>(ad + pl.ad_E);
+    uint64_t *W = reinterpret_cast<uint64_t *>(ad + pl.ad_W);
+    int32_t *Ei = reinterpret_cast<int32_t *>(ad + pl.ad_inv);
+    if (launch_ad_init(ecdf, P, Cn, pl.nrows, W, pl.geo.Tb, st) != cudaSuccess) return SKV_ERR_CUDA;
+    a.ecdf = Et;
+    a.ecdf_row_stride = kNsymBf16 + 1;
+    a.einv = Ei;
+    a.einv_row_stride = kO0InvN + 1;
+    a.c_step = pl.geo.ntb;
+    a.c_end = pl.geo.nchunks;
+    for (int64_t b = 0; b < pl.geo.ntb; ++b) {
+      if (launch_ad_table(P, Et, Ei, kO0InvN, pl.nrows, st) != cudaSuccess) return SKV_ERR_CUDA;
+      a.c_begin = b;
+      a.check_header = b == 0 ? 1 : 0;
+      if (launch_decode(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+      if (b + 1 < pl.geo.ntb &&
+          launch_ad_update(pl.geo, static_cast<const uint16_t *>(kv_out), b, P, Cn, W, head,
+                           pl.nrows, st) != cudaSuccess)
+        return SKV_ERR_CUDA;
+    }
+    return SKV_OK;
+  }
   if (launch_decode(a, st) != cudaSuccess) return SKV_ERR_CUDA;
   return SKV_OK;
 }
@@ -390,7 +456,36 @@ int skv_encode(const skv_params *params, const skv_shape *shape, const void *kv,
   a.out = static_cast<uint8_t *>(out);
   a.capacity = out_capacity;
   a.hash_words = hash_words(pl);
-  if (launch_encode(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  a.adaptive = pl.adaptive;
+  a.c_first = 0;
+  a.c_step = 1;
+  a.c_count = pl.geo.nchunks;
+  a.ecdf_row_stride = 0;
+  if (pl.adaptive) {
+    // one phase per token block: the rows' tables, block b of every row, the update
+    uint8_t *ad = ws + pl.ad_base_enc;
+    uint64_t *P = reinterpret_cast<uint64_t *>(ad + pl.ad_P);
+    uint64_t *Cn = reinterpret_cast<uint64_t *>(ad + pl.ad_C);
+    uint32_t *Et = reinterpret_cast<uint32_t *>(ad + pl.ad_E);
+    uint64_t *W = reinterpret_cast<uint64_t *>(ad + pl.ad_W);
+    if (launch_ad_init(ecdf, P, Cn, pl.nrows, W, pl.geo.Tb, st) != cudaSuccess) return SKV_ERR_CUDA;
+    a.ecdf = Et;
+    a.ecdf_row_stride = kNsymBf16 + 1;
+    a.c_step = pl.geo.ntb;
+    a.c_count = pl.nrows;
+    for (int64_t b = 0; b < pl.geo.ntb; ++b) {
+      if (launch_ad_table(P, Et, nullptr, 0, pl.nrows, st) != cudaSuccess) return SKV_ERR_CUDA;
+      a.c_first = b;
+      if (launch_encode_chunks(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+      if (b + 1 < pl.geo.ntb &&
+          launch_ad_update(pl.geo, static_cast<const uint16_t *>(kv), b, P, Cn, W, head, pl.nrows,
+                           st) != cudaSuccess)
+        return SKV_ERR_CUDA;
+    }
+    if (launch_encode_finish(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  } else if (launch_encode(a, st) != cudaSuccess) {
+    return SKV_ERR_CUDA;
+  }
   WsHead h;
   if ((rc = read_head(head, &h, st))) return rc;
   if ((rc = status_from_flags(h.flags))) return rc;
@@ -423,6 +518,8 @@ int skv_decode_range(const skv_params *params, const skv_shape *shape, const voi
   int rc = make_plan(params, shape, &pl);
   if (rc) return rc;
   if (range_flags & ~SKV_RANGE_FIRST) return SKV_ERR_ARG;
+  // adaptive tables depend on every earlier block of a row: whole containers only
+  if (pl.adaptive) return SKV_ERR_ARG;
   if (chunk_begin > chunk_end || chunk_end > (uint64_t)pl.geo.nchunks) return SKV_ERR_ARG;
   if (page_of_chunk && (!aligned(page_of_chunk, 4) || num_pages == 0)) return SKV_ERR_ARG;
   return decode_enqueue(params, pl, in, in_bytes, chunk_begin, chunk_end, mu, kv_out,
@@ -479,7 +576,29 @@ int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void 
   a.partials = reinterpret_cast<double *>(ws + pl.off_bits);
   a.nblocks = pl.bits_blocks;
   a.head = head;
-  if (launch_ideal(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  if (pl.adaptive) {
+    // per-row models, one phase per token block, partial sums in a fixed order
+    uint8_t *ad = ws + pl.ad_base_bits;
+    uint64_t *P = reinterpret_cast<uint64_t *>(ad + pl.ad_P);
+    uint64_t *Cn = reinterpret_cast<uint64_t *>(ad + pl.ad_C);
+    uint64_t *W = reinterpret_cast<uint64_t *>(ad + pl.ad_W);
+    double *part = reinterpret_cast<double *>(ad + pl.ad_part);
+    const uint32_t *ecdf = params->ecdf;
+    const uint16_t *kv16 = static_cast<const uint16_t *>(kv);
+    if (launch_ad_init(ecdf, P, Cn, pl.nrows, W, pl.geo.Tb, st) != cudaSuccess) return SKV_ERR_CUDA;
+    for (int64_t b = 0; b < pl.geo.ntb; ++b) {
+      if (launch_ad_ideal(pl.geo, kv16, b, P, per_scalar, part + b * pl.nrows * pl.ad_bx, pl.ad_bx,
+                          head, pl.nrows, st) != cudaSuccess)
+        return SKV_ERR_CUDA;
+      if (b + 1 < pl.geo.ntb &&
+          launch_ad_update(pl.geo, kv16, b, P, Cn, W, head, pl.nrows, st) != cudaSuccess)
+        return SKV_ERR_CUDA;
+    }
+    if (launch_ideal_final(part, (int)(pl.geo.ntb * pl.nrows * pl.ad_bx), head, st) != cudaSuccess)
+      return SKV_ERR_CUDA;
+  } else if (launch_ideal(a, st) != cudaSuccess) {
+    return SKV_ERR_CUDA;
+  }
   WsHead h;
   if ((rc = read_head(head, &h, st))) return rc;
   if ((rc = status_from_flags(h.flags))) return rc;

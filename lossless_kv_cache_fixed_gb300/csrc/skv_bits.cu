@@ -309,6 +309,11 @@ __global__ void __launch_bounds__(1024) k_ideal_final(const double *partials, in
   if (threadIdx.x == 0) head->bits = s_sum[0];
 }
 
+cudaError_t launch_ideal_final(const double *partials, int n, WsHead *head, cudaStream_t s) {
+  k_ideal_final<<<1, 1024, 0, s>>>(partials, n, head);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_ideal(const IdealLaunch &a, cudaStream_t s) {
   if (a.dtype == 0 && a.order0) k_ideal<0, true><<<a.nblocks, 256, 0, s>>>(a);
   else if (a.dtype == 0) k_ideal<0, false><<<a.nblocks, 256, 0, s>>>(a);

@@ -208,21 +208,22 @@ __global__ void __launch_bounds__(kCodeThreads, 1) k_encode(EncodeLaunch a) {
   const int ell = lane & (G - 1);
   const uint32_t seg = G == 32 ? 0xFFFFFFFFu : (((1u << G) - 1u) << (lane & ~(G - 1)));
   const uint32_t lt = seg & ((1u << lane) - 1u);
-  const int64_t ntasks = (a.geo.nchunks * G + 31) / 32;
+  const int64_t ntasks = (a.c_count * G + 31) / 32;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const uint32_t D = (uint32_t)a.geo.D;
 
   for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks;
        task += nwarps) {
-    const int64_t c = (task * 32 + lane) / G;
-    const bool live = c < a.geo.nchunks;
-    ChunkGeo cg = chunk_geo(a.geo, live ? c : 0);
+    const int64_t ci = (task * 32 + lane) / G;
+    const bool live = ci < a.c_count;
+    const int64_t c = live ? a.c_first + a.c_step * ci : 0;
+    ChunkGeo cg = chunk_geo(a.geo, c);
+    const uint32_t *ecdf = a.ecdf + (a.ecdf_row_stride ? (uint64_t)(c / a.geo.ntb) * a.ecdf_row_stride : 0);
     const uint32_t my_groups =
         (live && (uint32_t)ell < cg.ngroup) ? (cg.ngroup - ell + G - 1) / G : 0u;
     const uint32_t max_groups = __reduce_max_sync(0xFFFFFFFFu, my_groups);
-    uint32_t *region = a.scratch + (live ? c : 0) * a.stride;
-    const float2 *invrow = a.inv_chunk ? a.inv_chunk + (uint64_t)(live ? c : 0) * D
-                                       : a.inv + cg.srow;
+    uint32_t *region = a.scratch + c * a.stride;
+    const float2 *invrow = a.inv_chunk ? a.inv_chunk + (uint64_t)c * D : a.inv + cg.srow;
     int64_t sp = a.stride;
     uint64_t x = kStateL;
     uint32_t flags = 0;
@@ -250,8 +251,8 @@ __global__ void __launch_bounds__(kCodeThreads, 1) k_encode(EncodeLaunch a) {
             r = 0;
           }
           if (O0) {
-            cst = cum_order0(r, a.ecdf);
-            f = cum_order0(r + 1, a.ecdf) - cst;
+            cst = cum_order0(r, ecdf);
+            f = cum_order0(r + 1, ecdf) - cst;
           } else {
             if (!mu_valid(mub[k])) {
               flags |= kFlagParam;
@@ -389,7 +390,7 @@ __device__ void make_header(uint8_t *h, const Geo &g, int dtype, uint64_t payloa
   h[34] = 8;
   h[35] = 9;
   put_u16(h + 36, 8);
-  put_u16(h + 38, features);  // bit 0: per-block scales, bit 1: order-0 baseline
+  put_u16(h + 38, features);  // bit 0: per-block scales, bit 1: order-0, bit 2: adaptive
   put_u64(h + 40, (uint64_t)g.nchunks);
   put_u64(h + 48, payload);
   put_u64(h + 56, hash);
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(256) k_compact(EncodeLaunch a) {
     offs[nc] = total;
     uint8_t h[64];
     make_header(h, a.geo, a.dtype, total, mix64(a.head->hash_acc ^ a.hash_words),
-                (a.nsw > 0 ? 1u : 0u) | (a.order0 ? 2u : 0u));
+                (a.nsw > 0 ? 1u : 0u) | (a.order0 ? 2u : 0u) | (a.adaptive ? 4u : 0u));
     for (int i = 0; i < 64; ++i) a.out[i] = h[i];
   }
 }
@@ -435,7 +436,14 @@ static int code_blocks(int64_t ntasks) {
 }
 
 cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s) {
-  const int64_t ntasks = (a.geo.nchunks * a.geo.G + 31) / 32;
+  cudaError_t e = launch_encode_chunks(a, s);
+  if (e != cudaSuccess) return e;
+  return launch_encode_finish(a, s);
+}
+
+cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s) {
+  const int64_t ntasks = (a.c_count * a.geo.G + 31) / 32;
+  if (ntasks == 0) return cudaSuccess;
   const int blocks = code_blocks(ntasks);
   cudaError_t e;
   if (a.dtype == 0 && a.order0) {
@@ -454,7 +462,11 @@ cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     k_encode<1, false><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
   }
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_encode_finish(const EncodeLaunch &a, cudaStream_t s) {
+  cudaError_t e;
   const int64_t nb = (a.geo.nchunks + kScanBlock - 1) / kScanBlock;
   k_scan_local<<<(unsigned)nb, 256, 0, s>>>(a.sizes, a.geo.nchunks, a.partials);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -485,7 +497,7 @@ __global__ void k_check_header(DecodeLaunch a) {
   const uint64_t payload = a.in_bytes - hbytes;
   uint8_t want[64];
   make_header(want, a.geo, a.dtype, payload, mix64(a.head->hash_acc ^ a.hash_words),
-              (a.nsw > 0 ? 1u : 0u) | (a.order0 ? 2u : 0u));
+              (a.nsw > 0 ? 1u : 0u) | (a.order0 ? 2u : 0u) | (a.adaptive ? 4u : 0u));
   bool ok = true;
   for (int i = 0; i < 64; ++i) ok &= a.in[i] == want[i];
   ok &= get_u64(a.in + 64) == 0;
@@ -589,7 +601,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
   const int ell = lane & (G - 1);
   const uint32_t seg = G == 32 ? 0xFFFFFFFFu : (((1u << G) - 1u) << (lane & ~(G - 1)));
   const uint32_t lt = seg & ((1u << lane) - 1u);
-  const int64_t ntasks = ((a.c_end - a.c_begin) * G + 31) / 32;
+  const int64_t ntasks = (((a.c_end - a.c_begin + a.c_step - 1) / a.c_step) * G + 31) / 32;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const uint32_t D = (uint32_t)a.geo.D;
   const int64_t nc = a.geo.nchunks;
@@ -599,7 +611,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
 
   for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks;
        task = next_task(a.head, nwarps)) {
-    const int64_t c = a.c_begin + (task * 32 + lane) / G;
+    const int64_t c = a.c_begin + a.c_step * ((task * 32 + lane) / G);
     const bool live = c < a.c_end;
     uint32_t flags = 0;
     uint64_t off_a = 0, off_b = 0;
@@ -834,7 +846,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
 // a bracket of one or two table steps, which bisection finishes.
 __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
   extern __shared__ int32_t s_einv0[];
-  for (int i = threadIdx.x; i <= kO0InvN; i += blockDim.x) s_einv0[i] = a.einv[i];
+  if (!a.einv_row_stride)  // one table for all chunks: stage it once per SM
+    for (int i = threadIdx.x; i <= kO0InvN; i += blockDim.x) s_einv0[i] = a.einv[i];
   __syncthreads();
   constexpr int M = kMBf16;
   constexpr uint32_t kMask = (1u << M) - 1u;
@@ -843,7 +856,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
   const int ell = lane & (G - 1);
   const uint32_t seg = G == 32 ? 0xFFFFFFFFu : (((1u << G) - 1u) << (lane & ~(G - 1)));
   const uint32_t lt = seg & ((1u << lane) - 1u);
-  const int64_t ntasks = ((a.c_end - a.c_begin) * G + 31) / 32;
+  const int64_t ntasks = (((a.c_end - a.c_begin + a.c_step - 1) / a.c_step) * G + 31) / 32;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t nc = a.geo.nchunks;
   const uint64_t hbytes = 64 + 8 * (uint64_t)(nc + 1);
@@ -853,7 +866,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
 
   for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < ntasks;
        task = next_task(a.head, nwarps)) {
-    const int64_t c = a.c_begin + (task * 32 + lane) / G;
+    const int64_t c = a.c_begin + a.c_step * ((task * 32 + lane) / G);
     const bool live = c < a.c_end;
     uint32_t flags = 0;
     uint64_t off_a = 0, off_b = 0;
@@ -874,6 +887,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
     const uint32_t max_groups = __reduce_max_sync(0xFFFFFFFFu, my_groups);
     uint64_t x = ok ? ((uint64_t)w[2 * ell] | ((uint64_t)w[2 * ell + 1] << 32)) : kStateL;
     uint64_t cur = 2ull * G;
+    // adaptive counts: the chunk's row has its own tables
+    const uint64_t arow = live && a.ecdf_row_stride ? (uint64_t)(c / a.geo.ntb) : 0;
+    const uint32_t *ecdf = a.ecdf + arow * a.ecdf_row_stride;
+    const int32_t *einv = a.einv_row_stride ? a.einv + arow * a.einv_row_stride : s_einv0;
 
     for (uint32_t gi = 0; gi < max_groups; ++gi) {
       const bool has = gi < my_groups;
@@ -885,19 +902,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
         if (has) {
           const uint32_t slot = (uint32_t)x & kMask;
           const uint32_t kh = (uint32_t)(((uint64_t)(slot + 1u) * kO0InvN) / kKBf16) + 1u;
-          int32_t hi = kh <= (uint32_t)kO0InvN ? s_einv0[kh] : kNsymBf16;
+          int32_t hi = kh <= (uint32_t)kO0InvN ? einv[kh] : kNsymBf16;
           int32_t lo = 0;
           if (slot >= (uint32_t)kNsymBf16) {
             const uint32_t kl = (uint32_t)(((uint64_t)(slot - kNsymBf16) * kO0InvN) / kKBf16);
-            lo = max(s_einv0[kl] - 1, 0);
+            lo = max(einv[kl] - 1, 0);
           }
           hi = max(hi, lo + 1);
           while (hi - lo > 1) {  // cum(lo) <= slot < cum(hi)
             const int32_t mid = (lo + hi) >> 1;
-            if (cum_order0(mid, a.ecdf) <= slot) lo = mid;
+            if (cum_order0(mid, ecdf) <= slot) lo = mid;
             else hi = mid;
           }
-          const uint32_t clo = cum_order0(lo, a.ecdf), chi = cum_order0(lo + 1, a.ecdf);
+          const uint32_t clo = cum_order0(lo, ecdf), chi = cum_order0(lo + 1, ecdf);
           if (clo > slot || chi <= slot) flags |= kFlagCorrupt;  // only if E_q were not monotone
           x = (uint64_t)(chi - clo) * (x >> M) + (slot - clo);
           need = x < kStateL;
@@ -949,7 +966,7 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s) {
   e = cudaMemsetAsync(&a.head->next_task, 0, sizeof(unsigned long long), s);
   if (e != cudaSuccess) return e;
   // at most one block per SM (see kCodeThreads)
-  const int64_t ntasks = ((a.c_end - a.c_begin) * a.geo.G + 31) / 32;
+  const int64_t ntasks = (((a.c_end - a.c_begin + a.c_step - 1) / a.c_step) * a.geo.G + 31) / 32;
   const int64_t wpb = kDecThreads / 32;
   int64_t blocks = (ntasks + wpb - 1) / wpb;
   const int64_t cap = (int64_t)device_sm_count();

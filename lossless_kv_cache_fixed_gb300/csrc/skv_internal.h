@@ -61,6 +61,9 @@ struct EncodeLaunch {
   const uint32_t *scale_words;  // per-block scales: nsw words per chunk
   int32_t nsw;              // scale words per chunk (0 without per-block scales)
   int32_t order0;           // 1: order-0 baseline (p-hat alone; kv only)
+  int32_t adaptive;         // 1: adaptive counts (header feature bit 2)
+  int64_t c_first, c_step, c_count;  // chunks c_first + c_step * i, i < c_count
+  uint64_t ecdf_row_stride; // adaptive counts: one E table per row, else 0
   const uint32_t *ecdf;
   uint32_t *scratch;        // nchunks * stride words
   int64_t stride;           // words per chunk stack
@@ -85,11 +88,14 @@ struct DecodeLaunch {
   const float2 *inv_chunk;  // per-block scales: per (chunk, channel) reciprocals, else null
   int32_t nsw;
   int32_t order0;           // 1: order-0 baseline; einv then has kO0InvN + 1 entries
+  int32_t adaptive;         // 1: adaptive counts (header feature bit 2)
   const uint32_t *ecdf;
   void *kv_out;
   WsHead *head;
   uint64_t hash_words;
-  int64_t c_begin, c_end;   // chunks to decode
+  int64_t c_begin, c_end;   // chunks to decode: c_begin + c_step * i < c_end
+  int64_t c_step;
+  uint64_t ecdf_row_stride, einv_row_stride;  // adaptive counts: per-row tables, else 0
   int32_t check_header;     // 1: check the header and offset-table ends first
   const uint32_t *page_of_chunk;  // paged layout (mu and kv_out are page pools), else null
   uint64_t num_pages;
@@ -151,6 +157,24 @@ cudaError_t launch_scales(const ScaleLaunch &a, cudaStream_t s);
 cudaError_t launch_prep(const float *sigma, int64_t nsig, const uint32_t *ecdf, float2 *inv,
                         WsHead *head, cudaStream_t s);
 cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s);
+// The encode kernel alone over a.c_first + a.c_step * i, and the size scan and
+// compaction that follow it (launch_encode = both).
+cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s);
+cudaError_t launch_encode_finish(const EncodeLaunch &a, cudaStream_t s);
+
+// Adaptive counts (skv_adapt.cu): per-row probabilities P and counts C (u64,
+// kNsymBf16 per row), per-row tables E (kNsymBf16 + 1) and, for decode, their
+// inverses; W holds the Tb token weights and the block decay.
+cudaError_t launch_ad_init(const uint32_t *ecdf, uint64_t *P, uint64_t *C, int64_t nrows, uint64_t *W,
+                           int Tb, cudaStream_t s);
+cudaError_t launch_ad_table(const uint64_t *P, uint32_t *E, int32_t *einv, int n_inv, int64_t nrows,
+                            cudaStream_t s);
+cudaError_t launch_ad_update(const Geo &g, const uint16_t *kv, int64_t b, uint64_t *P, uint64_t *C,
+                             const uint64_t *W, WsHead *head, int64_t nrows, cudaStream_t s);
+cudaError_t launch_ad_ideal(const Geo &g, const uint16_t *kv, int64_t b, const uint64_t *P,
+                            float *per_scalar, double *partials, int bx, WsHead *head,
+                            int64_t nrows, cudaStream_t s);
+cudaError_t launch_ideal_final(const double *partials, int n, WsHead *head, cudaStream_t s);
 // einv[k] = the smallest rank r with E_q[r] >= k 2^26 / n, k = 0..n (n divides 2^26).
 cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, int n, cudaStream_t s);
 cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s);

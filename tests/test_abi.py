@@ -106,6 +106,18 @@ def test_argument_errors_without_gpu(skv):
     assert rc == P.SKV_ERR_ARG
     rc, _ = P.skv_encode(o0, shape, None, None, 1 << 20, 1 << 30, 1 << 20, 1 << 30, None)
     assert rc == P.SKV_ERR_ARG                       # kv is still required
+    # adaptive counts: only with the order-0 coder, head_dim <= 512, whole containers
+    ad = P.SkvParams(P.SKV_BF16, 256, 8, P.SKV_FLAG_ORDER0 | P.SKV_FLAG_ADAPTIVE, None, 1 << 21,
+                     1 << 22)
+    assert P.skv_max_encoded_bytes(ad, shape) > 0
+    assert (P.skv_workspace_bytes(ad, shape, P.SKV_OP_DECODE)
+            > P.skv_workspace_bytes(o0, shape, P.SKV_OP_DECODE))
+    assert P.skv_max_encoded_bytes(P.SkvParams(P.SKV_BF16, 256, 8, P.SKV_FLAG_ADAPTIVE, 1, 1, 1),
+                                   shape) == 0
+    assert P.skv_max_encoded_bytes(ad, P.SkvShape(1, 2, 1, 4, 520)) == 0
+    rc = P.skv_decode_range(ad, shape, 1 << 20, 1 << 20, 0, 8, None, 1 << 20, None, 0, 1,
+                            1 << 20, 1 << 30, None)
+    assert rc == P.SKV_ERR_ARG
     # range decode: range, flags and page-table arguments are checked on the host
     for c0, c1, fl, pages, npg in ((5, 4, 1, None, 0), (0, 9, 1, None, 0), (0, 8, 2, None, 0),
                                    (0, 8, 1, 1 << 20, 0), (0, 8, 1, (1 << 20) + 2, 8)):
