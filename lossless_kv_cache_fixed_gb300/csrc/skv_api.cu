@@ -575,6 +575,7 @@ int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void 
   a.per_scalar = per_scalar;
   a.partials = reinterpret_cast<double *>(ws + pl.off_bits);
   a.nblocks = pl.bits_blocks;
+  a.td_rcp = ~0ull / ((uint64_t)pl.geo.T * (uint64_t)pl.geo.D);
   a.head = head;
   if (pl.adaptive) {
     // per-row models, one phase per token block, partial sums in a fixed order
@@ -642,6 +643,7 @@ int skv_ideal_bits_noalloc(const skv_params *params, const skv_shape *shape, con
   a.per_scalar = per_scalar;
   a.partials = reinterpret_cast<double *>(ws + pl.off_bits);
   a.nblocks = pl.bits_blocks;
+  a.td_rcp = ~0ull / ((uint64_t)pl.geo.T * (uint64_t)pl.geo.D);
   a.head = head;
   if (launch_ideal(a, st) != cudaSuccess) return SKV_ERR_CUDA;
   WsHead h;

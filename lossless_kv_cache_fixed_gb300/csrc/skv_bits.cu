@@ -104,6 +104,32 @@ __device__ __forceinline__ float lo_e4m3_value(int32_t r);
 
 // -log2 q of one scalar.  FULL = false evaluates only the common (series)
 // case and sets `deferred` when the scalar needs the tail evaluation.
+// bf16, both Gaussian bins narrow against their sigma (the series case): the
+// mixture in the linear domain, each component w phi(z_m) (1 + y) with the
+// Hermite correction y of log2_gauss_series, then one logarithm.  A Gaussian
+// term too small for fp32 only drops below the p-hat term's 0.02 p-hat floor.
+// Returns false (and nothing) when the bin needs the tail evaluation.
+__device__ __forceinline__ bool ideal_series_bf16(float lo, float hi, float mu, float inv_s,
+                                                  float ph, float &bits) {
+  if (!(hi > lo) || !isfinite(lo) || !isfinite(hi)) return false;
+  const float width = hi - lo;
+  const float w = width * inv_s;
+  const float zm = (lo + 0.5f * width - mu) * inv_s;
+  if (!(w * fmaxf(1.0f, fabsf(zm)) < 0.5f)) return false;  // then also for 3 sigma
+  auto comp = [](float w, float zm) {
+    const float z2 = zm * zm, w2 = w * w;
+    const float he2 = z2 - 1.0f, he4 = fmaf(z2, z2 - 6.0f, 3.0f);
+    const float he6 = fmaf(z2, fmaf(z2, z2 - 15.0f, 45.0f), -15.0f);
+    const float y = w2 * fmaf(w2, fmaf(w2, he6 * (1.0f / 322560.0f), he4 * (1.0f / 1920.0f)),
+                              he2 * (1.0f / 24.0f));
+    return w * 0.39894228f * __expf(-0.5f * z2) * (1.0f + y);  // w phi(zm) (1 + y)
+  };
+  const float q = fmaf(0.95f, comp(w, zm),
+                       fmaf(0.03f, comp(w * (1.0f / 3.0f), zm * (1.0f / 3.0f)), 0.02f * ph));
+  bits = -__log2f(q);
+  return true;
+}
+
 template <int DT, bool FULL>
 __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float sigma,
                                            const float *phat, const float *lo8, uint32_t &flags,
@@ -123,6 +149,12 @@ __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float
   const float hi = DT == 0 ? lo_bf16(r + 1) : lo8[r + 1];
   // fp32 to about 1e-7 relative is far inside the 1e-3 tolerance of the ideal
   const float inv_s = __fdividef(1.0f, sigma);
+  if (DT == 0 && !FULL) {
+    float bits;
+    if (ideal_series_bf16(lo, hi, mu, inv_s, phat[r], bits)) return bits;
+    deferred = true;
+    return 0.0f;
+  }
   const float log2_s = __log2f(sigma);
   float l1, l3 = 0.0f;
   if (FULL) {
@@ -170,12 +202,16 @@ __device__ __forceinline__ uint32_t mu_at(uint4 mu4, int k) {
 // channel) in the per-block table.
 __device__ __forceinline__ uint64_t sigma_index(const IdealLaunch &a, uint64_t i, uint64_t TD) {
   const uint64_t D = (uint64_t)a.geo.D;
-  const uint64_t row = i / TD, in_row = i - row * TD;
-  if (!a.sigma_chunk) return row * D + in_row % D;
+  // i / TD by multiply-high with the host's reciprocal (at most one below), then exact
+  uint64_t row = __umul64hi(i, a.td_rcp);
+  if ((row + 1) * TD <= i) ++row;
+  const uint64_t in_row = i - row * TD;
+  const uint64_t ch = (in_row >> 32) == 0 ? (uint32_t)in_row % (uint32_t)D : in_row % D;
+  if (!a.sigma_chunk) return row * D + ch;
   const uint64_t cw = D * (uint64_t)a.geo.Tb;  // scalars of a full chunk
   const uint64_t tb = (TD >> 32) == 0 && (cw >> 32) == 0 ? (uint32_t)in_row / (uint32_t)cw
                                                          : in_row / cw;
-  return (row * (uint64_t)a.geo.ntb + tb) * D + in_row % D;
+  return (row * (uint64_t)a.geo.ntb + tb) * D + ch;
 }
 
 template <int DT, bool O0>

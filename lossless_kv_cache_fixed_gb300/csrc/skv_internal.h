@@ -115,6 +115,7 @@ struct IdealLaunch {
   double *partials;
   int nblocks;
   WsHead *head;
+  uint64_t td_rcp;           // floor((2^64 - 1) / (T * D)): row of a scalar by multiply-high
 };
 
 // Inverse of the model CDF's Gaussian part, G0(z) = 0.95 Phi(z) + 0.03 Phi(z/3)
