@@ -104,6 +104,20 @@ __device__ __forceinline__ float lo_e4m3_value(int32_t r);
 
 // -log2 q of one scalar.  FULL = false evaluates only the common (series)
 // case and sets `deferred` when the scalar needs the tail evaluation.
+// N(mu, s^2) mass on [lo, hi) as Q(a) - Q(b), Q(z) = erfc(z / sqrt 2) / 2 the
+// upper tail, with the bin mirrored when it lies below mu so that a < b and a
+// is the edge on the far side of mu (both of a straddling bin's edges: Q(a)
+// near 1 then carries absolute error only).  Outside the series case
+// w max(1, |z_m|) >= 0.5 gives Q(a) / Q(b) >= e^0.5, so the difference keeps
+// the relative accuracy of erfcf.  `far` receives a (deep tails: a >= 9).
+__device__ __forceinline__ float gauss_mass(float lo, float hi, float mu, float inv_s, float &far) {
+  const float za = (lo - mu) * inv_s, zb = (hi - mu) * inv_s;
+  const bool below = zb <= 0.0f;
+  const float a = below ? -zb : za, b = below ? -za : zb;
+  far = a;
+  return 0.5f * (erfcf(a * 0.70710678f) - erfcf(b * 0.70710678f));
+}
+
 // bf16, both Gaussian bins narrow against their sigma (the series case): the
 // mixture in the linear domain, each component w phi(z_m) (1 + y) with the
 // Hermite correction y of log2_gauss_series, then one logarithm.  A Gaussian
@@ -157,9 +171,24 @@ __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float
   }
   const float log2_s = __log2f(sigma);
   float l1, l3 = 0.0f;
+  if (FULL && DT == 0) {
+    // the mixture in the linear domain: p-hat's 0.02 floor keeps q normal, so a
+    // Gaussian mass below fp32's range does not matter
+    float far;
+    const float m1 = hi > lo ? gauss_mass(lo, hi, mu, inv_s, far) : 0.0f;
+    const float m3 = hi > lo ? gauss_mass(lo, hi, mu, inv_s * (1.0f / 3.0f), far) : 0.0f;
+    return -log2f(fmaf(0.95f, fmaxf(m1, 0.0f), fmaf(0.03f, fmaxf(m3, 0.0f), 0.02f * phat[r])));
+  }
   if (FULL) {
-    l1 = log2_gauss_bin(lo, hi, mu, inv_s, log2_s);
-    if (DT == 0) l3 = log2_gauss_bin(lo, hi, mu, inv_s * (1.0f / 3.0f), log2_s + 1.5849625f);
+    // e4m3: one branch-free difference of tails for every bin short of the deep
+    // tails, which keep the log-domain evaluation
+    bool ok = true;
+    l1 = log2_gauss_series(lo, hi, mu, inv_s, log2_s, ok);
+    if (!ok) {
+      float far;
+      const float m = hi > lo ? gauss_mass(lo, hi, mu, inv_s, far) : 0.0f;
+      l1 = (far < 9.0f && m > 0.0f) ? log2f(m) : log2_gauss_tail(lo, hi, mu, inv_s);
+    }
   } else {
     bool ok1 = true, ok3 = true;
     l1 = log2_gauss_series(lo, hi, mu, inv_s, log2_s, ok1);
