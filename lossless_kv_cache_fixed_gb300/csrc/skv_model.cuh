@@ -119,19 +119,28 @@ __device__ __forceinline__ uint32_t cum_e4m3(int32_t r, float mu, float inv_s, c
   return (uint32_t)(((uint64_t)kKE4m3 * p) >> 26) + (uint32_t)r;
 }
 
-// Estimate of y / f = y * rf for a signed 64-bit y, |y| < 2^63, using only
-// 32-bit conversions (64-bit integer <-> float conversions run on the slow
-// FP64 unit of this part).  |y| is split into three exact 24-bit limbs, so the
-// float value carries only relative error; the quotient (< 2^48 here) comes
-// back as floor(qf / 2^24) plus an exactly representable 24-bit rest.  With
-// the roundings of the two FMAs, of 1/f (and of f itself above 2^24), of the
-// product and of the rest, the estimate is within 5 * 2^-24 |y/f| + 1.
-__device__ __forceinline__ int64_t est_div(int64_t y, float rf) {
-  const bool neg = y < 0;
-  const uint64_t a = neg ? (uint64_t)(-y) : (uint64_t)y;
+// Estimate of y / f = y * rf using only 32-bit conversions (64-bit integer
+// <-> float conversions run on the slow FP64 unit of this part).  |y| is split
+// into exact 24-bit limbs, so the float value carries only relative error; the
+// quotient (< 2^48 here) comes back as floor(qf / 2^24) plus an exactly
+// representable 24-bit rest.  With the roundings of the FMAs, of 1/f (and of f
+// itself above 2^24), of the product and of the rest, the estimate is within
+// 5 * 2^-24 |y/f| + 1.  est_div_pos takes x >= 0 (three limbs, no sign);
+// est_div48 a signed |y| < 2^48 (two limbs: y >> 24 < 2^24 is exact in fp32).
+__device__ __forceinline__ int64_t est_div_pos(uint64_t a, float rf) {
   const float af = fmaf((float)(uint32_t)(a >> 48), 281474976710656.0f,
                         fmaf((float)(uint32_t)((a >> 24) & 0xFFFFFFu), 16777216.0f,
                              (float)(uint32_t)(a & 0xFFFFFFu)));
+  const float qf = af * rf;
+  const uint32_t qh = __float2uint_rd(qf * (1.0f / 16777216.0f));
+  const uint32_t ql = __float2uint_rn(fmaf(-(float)qh, 16777216.0f, qf));
+  return (int64_t)qh * 16777216 + ql;
+}
+
+__device__ __forceinline__ int64_t est_div48(int64_t y, float rf) {
+  const bool neg = y < 0;
+  const uint64_t a = neg ? (uint64_t)(-y) : (uint64_t)y;
+  const float af = fmaf((float)(uint32_t)(a >> 24), 16777216.0f, (float)(uint32_t)(a & 0xFFFFFFu));
   const float qf = af * rf;
   const uint32_t qh = __float2uint_rd(qf * (1.0f / 16777216.0f));
   const uint32_t ql = __float2uint_rn(fmaf(-(float)qh, 16777216.0f, qf));
@@ -141,18 +150,20 @@ __device__ __forceinline__ int64_t est_div(int64_t y, float rf) {
 
 // floor(x / f) and x mod f for x < 2^63 and 1 <= f <= 2^28, without the FP64
 // division routine.  Starting from y = x with |x/f| < 2^(63 - M), the error
-// bound of est_div gives:
+// bound of the estimates gives:
 //   M = 28: <= 5 * 2^11 + 1, then <= 1.003 after one refinement;
 //   M = 16: <= 5 * 2^23 + 1, then <= 13.3, then <= 1.001 after two.
-// The remainder is then within 3f of [0, f), and the loops below fix it.
+// The remainder after the first estimate is below (5 * 2^23 + 1) 2^16 and
+// (5 * 2^11 + 1) 2^28, both < 2^42, so the refinements take two limbs.  The
+// remainder is then within 3f of [0, f), and the loops below fix it.
 template <int M>
 __device__ __forceinline__ uint64_t divmod_u64(uint64_t x, uint32_t f, uint64_t &rem) {
   const float rf = __frcp_rn((float)f);
-  int64_t q = est_div((int64_t)x, rf);
+  int64_t q = est_div_pos(x, rf);
   int64_t r = (int64_t)x - q * (int64_t)f;
 #pragma unroll
   for (int i = 0; i < (M >= 24 ? 1 : 2); ++i) {
-    const int64_t d = est_div(r, rf);
+    const int64_t d = est_div48(r, rf);
     q += d;
     r -= d * (int64_t)f;
   }
