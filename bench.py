@@ -441,14 +441,79 @@ def run_gpu(args):
     staged_e2e = {"value": round(world * raw / e2e_s / 1e9, 3), "unit": "GB/s",
                   "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                   "mode": "staging copies to and from device buffers"}
-    # the headline is the faster of the two end-to-end modes; both are reported
-    best, other = (zc, staged_e2e) if zc["value"] > staged_e2e["value"] else (staged_e2e, zc)
-    e2e = dict(best)
-    e2e["other_mode"] = other
+    pipe = e2e_pipelined(P, s, w, ecdf, phat, flags, kv_h, mu_h, raw, world, dev, args)
+    # the headline is the fastest end-to-end mode; all are reported
+    modes = sorted([m for m in (zc, staged_e2e, pipe) if m], key=lambda m: -m["value"])
+    e2e = dict(modes[0])
+    e2e["other_modes"] = modes[1:]
     # range decode (the offload paths) takes whole containers only for adaptive counts
     off = None if args.adaptive else offload(codec, out, nb, kv, kv_h, mu, s, raw, world, dev, args)
     return finish_line(args, rank, world, s, n, nb, bits, bps, ms_step, value,
                        t_enc, t_dec, t_bits, clk, e2e, w, off)
+
+
+def e2e_pipelined(P, s, w, ecdf, phat, flags, kv_h, mu_h, raw, world, dev, args, parts=4):
+    """The end-to-end step with the cache split into layer groups, each coded as
+    its own container on its own stream from its own host thread: one group's
+    host-device copies run on the copy engines while other groups compute."""
+    import threading
+    import torch
+    if s.L % parts or mu_h is None:
+        return None
+    lp = s.L // parts
+    per = kv_h.numel() // parts
+    groups = []
+    for g in range(parts):
+        sig = w.sigma[g * lp:(g + 1) * lp].to(dev).contiguous()
+        codec = P.Codec(s.dtype, lp, s.H, s.T, s.D, s.Tb, s.G, sig, ecdf, phat, flags=flags)
+        st = torch.cuda.Stream()
+        groups.append(dict(
+            codec=codec, stream=st,
+            kv_h=kv_h[g * per:(g + 1) * per], mu_h=mu_h[g * per:(g + 1) * per],
+            kv_d=torch.empty(per, dtype=kv_h.dtype, device=dev),
+            mu_d=torch.empty(per, dtype=mu_h.dtype, device=dev),
+            box_d=torch.empty(codec.max_bytes, dtype=torch.uint8, device=dev),
+            box_h=torch.empty(codec.max_bytes, dtype=torch.uint8).pin_memory(),
+            back_d=torch.empty(per, dtype=kv_h.dtype, device=dev),
+            back_h=torch.empty(per, dtype=kv_h.dtype).pin_memory(), nb=0))
+
+    def run(gr):
+        with torch.cuda.stream(gr["stream"]):
+            gr["kv_d"].copy_(gr["kv_h"], non_blocking=True)
+            gr["mu_d"].copy_(gr["mu_h"], non_blocking=True)
+            _, nb = gr["codec"].encode(gr["kv_d"], gr["mu_d"], out=gr["box_d"], stream=gr["stream"])
+            gr["box_h"][:nb].copy_(gr["box_d"][:nb], non_blocking=True)
+            gr["codec"].decode(gr["box_d"], nb, gr["mu_d"], out=gr["back_d"], stream=gr["stream"])
+            gr["back_h"].copy_(gr["back_d"], non_blocking=True)
+            gr["codec"].ideal_bits(gr["kv_d"], gr["mu_d"], stream=gr["stream"])
+            gr["stream"].synchronize()
+            gr["nb"] = nb
+
+    def step():
+        ts = [threading.Thread(target=run, args=(gr,)) for gr in groups]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = max_over_ranks((time.perf_counter() - t0) / args.steps, world, dev)
+    for gr in groups:
+        if not torch.equal(gr["back_h"], gr["kv_h"]):
+            raise RuntimeError("pipelined end-to-end round trip mismatch")
+    nbs = sum(gr["nb"] for gr in groups)
+    return {"value": round(world * raw / dt / 1e9, 3), "unit": "GB/s",
+            "h2d_bytes_per_step": int(raw + 2 * s.n),
+            "d2h_bytes_per_step": int(nbs + raw + parts * (8 + 3 * 32)),
+            "mode": "%d layer groups, each its own container on its own stream and host "
+                    "thread: copies overlap other groups' kernels" % parts,
+            "container_bytes": int(nbs)}
 
 
 def offload(codec, out, nb, kv, kv_h, mu, s, raw, world, dev, args, pieces=2):
