@@ -149,15 +149,40 @@ __device__ __forceinline__ int64_t est_div48(int64_t y, float rf) {
 }
 
 // floor(x / f) and x mod f for x < 2^63 and 1 <= f <= 2^28, without the FP64
-// division routine.  Starting from y = x with |x/f| < 2^(63 - M), the error
-// bound of the estimates gives:
+// division routine.  For M <= 16 exact integer steps (above); otherwise, starting
+// from y = x with |x/f| < 2^(63 - M), the error bound of the estimates gives:
 //   M = 28: <= 5 * 2^11 + 1, then <= 1.003 after one refinement;
 //   M = 16: <= 5 * 2^23 + 1, then <= 13.3, then <= 1.001 after two.
 // The remainder after the first estimate is below (5 * 2^23 + 1) 2^16 and
 // (5 * 2^11 + 1) 2^28, both < 2^42, so the refinements take two limbs.  The
 // remainder is then within 3f of [0, f), and the loops below fix it.
+// floor(n / f), n mod f for n < 2^32 from m = floor((2^32 - 1) / f): the
+// multiply-high estimate is at most one below the quotient.
+__device__ __forceinline__ uint32_t div32_recip(uint32_t n, uint32_t f, uint32_t m, uint32_t &r) {
+  uint32_t q = __umulhi(n, m);
+  r = n - q * f;
+  if (r >= f) {
+    ++q;
+    r -= f;
+  }
+  return q;
+}
+
 template <int M>
 __device__ __forceinline__ uint64_t divmod_u64(uint64_t x, uint32_t f, uint64_t &rem) {
+  if (M <= 16) {
+    // f < 2^16 and x < f 2^47: three exact 32-bit divisions by one reciprocal,
+    // over the high word and then 16 bits at a time (each partial remainder is
+    // below f, so every dividend stays below f 2^16 <= 2^32)
+    const uint32_t m = 0xFFFFFFFFu / f;
+    const uint32_t xh = (uint32_t)(x >> 32), xl = (uint32_t)x;
+    uint32_t r1, r2, r3;
+    const uint32_t q1 = div32_recip(xh, f, m, r1);
+    const uint32_t q2 = div32_recip((r1 << 16) | (xl >> 16), f, m, r2);
+    const uint32_t q3 = div32_recip((r2 << 16) | (xl & 0xFFFFu), f, m, r3);
+    rem = r3;
+    return ((uint64_t)q1 << 32) + ((uint64_t)q2 << 16) + q3;
+  }
   const float rf = __frcp_rn((float)f);
   int64_t q = est_div_pos(x, rf);
   int64_t r = (int64_t)x - q * (int64_t)f;
