@@ -704,6 +704,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
               } else {
                 u = uraw;
               }
+              if (DT == 1) {
+                // beyond both ends of Phi_q's range cum(r) = r (below mu) or
+                // K + r (above): the rank follows from the slot directly
+                if (u <= 0.0f) return min((int32_t)slot, NS - 1);
+                if (u >= 1.0f) return max(min((int32_t)slot - (int32_t)kKE4m3, NS - 1), 0);
+              }
               const float t = fminf(fmaxf(u * kHscale, 0.0f), (float)kHinvN - 0.001f);
               const int kk = (int)t;
               const float2 h = s_hinv[kk];
