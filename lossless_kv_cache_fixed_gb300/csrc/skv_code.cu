@@ -9,11 +9,13 @@
 // GPU mapping.  One thread is one rANS lane; the G lanes of a chunk sit in
 // consecutive threads of one warp (32/G chunks per warp), so the order in which
 // lanes emit or consume renormalisation words inside a round comes from one
-// ballot plus a prefix popcount.  A lane's symbols are 8-scalar groups, so KV
-// and mu move as 16-byte vectors (8-byte for e4m3 KV).  Warps loop over 32-lane
-// tasks; the grid has at most one 768-thread block per SM.  The Phi knot
-// table (64 KiB), the e4m3 bin edges and the decoder's guess table sit in
-// shared memory, once per SM.
+// ballot plus a prefix popcount.  A lane's symbols are 8-scalar groups: the
+// encoder reads KV and mu as 16-byte vectors (8-byte for e4m3 KV); the decoder
+// reads mu a symbol at a time (fewer live registers) and writes each group's
+// 8 decoded symbols as one vector.  Warps loop over 32-lane tasks (the decoder
+// hands out tasks after the first round from an atomic counter); the grid has
+// at most one 768-thread block per SM.  The Phi knot table (64 KiB), the e4m3
+// bin edges and the decoder's guess tables sit in shared memory, once per SM.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
