@@ -7,12 +7,17 @@
 // "早期结果" gives q for bf16 (0.95 / 0.03 / 0.02 mixture), section
 // "原生 FP8 KV 缓存" the bin-integrated N(mu, sigma^2) for e4m3.
 //
-// Evaluated in fp32 in the log domain so that nothing underflows:
-//   * bins narrow against sigma (width w and centre zm in sigma units with
-//     w max(1,|zm|) < 0.5): the midpoint rule with Hermite corrections;
-//   * otherwise the tail mass on the far side of mu via the scaled
-//     complementary error function, log Q(z) = log(erfcx(z/sqrt2)/2) - z^2/2;
-//   * the mixture by log-sum-exp in base 2.
+// Evaluated in fp32 (w = bin width and zm = bin centre, both in sigma units):
+//   * bf16, w < 1 and w |zm| < 2 (about 99% of scalars): each Gaussian
+//     component's bin mass by the midpoint rule with Hermite corrections up to
+//     He6 (the first dropped term is below 3e-6 relative there), the mixture in
+//     the linear domain, one logarithm;
+//   * bf16 otherwise (queued per warp): each component's mass as a difference
+//     of complementary error functions on the far side of mu, the mixture in
+//     the linear domain (p-hat's 0.02 floor keeps it a normal float);
+//   * e4m3: the same difference of tails for bins at least 1e-3 sigma wide, the
+//     log-domain tail log Q(z) = log(erfcx(z/sqrt2)/2) - z^2/2 for deep tails,
+//     the series (in log2) for narrower bins.
 // Per-thread sums, then a fixed-order block tree and a fixed-order final sum,
 // all in fp64: the total does not depend on scheduling.
 #include <cuda_runtime.h>
@@ -51,8 +56,10 @@ __device__ __noinline__ float log2_gauss_tail(float lo, float hi, float mu, floa
   return ln * kLog2e;
 }
 
-// The common case of log2_gauss_bin alone: sets ok = false (and returns 0)
-// when the bin needs the tail evaluation.
+// log2 of the N(mu, s^2) mass on [lo, hi) by the midpoint rule, for bins with
+// w max(1, |zm|) < 0.5 (else ok = false and 0): w phi(zm) (1 + y),
+// y = He2 w^2/24 + He4 w^4/1920 + He6 w^6/322560 (He_n the probabilists'
+// Hermite polynomials), the logarithm of 1 + y by its series (|y| < 0.02).
 __device__ __forceinline__ float log2_gauss_series(float lo, float hi, float mu, float inv_s,
                                                    float log2_s, bool &ok) {
   ok = true;
@@ -75,41 +82,14 @@ __device__ __forceinline__ float log2_gauss_series(float lo, float hi, float mu,
   return 0.0f;
 }
 
-// log2 of the N(mu, s^2) mass on [lo, hi); inv_s = 1/s, log2_s = log2 s.
-//  * w max(1, |zm|) < 0.5 (w = width/s, zm = centre in sigma units): the
-//    mass is w phi(zm) (1 + He2 w^2/24 + He4 w^4/1920 + He6 w^6/322560),
-//    He_n the probabilists' Hermite polynomials; the next term is below
-//    4e-6 relative there.
-//  * otherwise the tail on the far side of mu, in the natural-log domain.
-__device__ float log2_gauss_bin(float lo, float hi, float mu, float inv_s, float log2_s) {
-  if (!(hi > lo)) return -INFINITY;
-  if (isfinite(lo) && isfinite(hi)) {
-    const float width = hi - lo;  // neighbouring midpoints: exact
-    const float w = width * inv_s;
-    const float zm = (lo + 0.5f * width - mu) * inv_s;
-    if (w * fmaxf(1.0f, fabsf(zm)) < 0.5f) {
-      const float z2 = zm * zm, w2 = w * w;
-      const float he2 = z2 - 1.0f, he4 = fmaf(z2, z2 - 6.0f, 3.0f);
-      const float he6 = fmaf(z2, fmaf(z2, z2 - 15.0f, 45.0f), -15.0f);
-      const float y = w2 * fmaf(w2, fmaf(w2, he6 * (1.0f / 322560.0f), he4 * (1.0f / 1920.0f)),
-                                he2 * (1.0f / 24.0f));
-      const float l1p = y * fmaf(y, fmaf(y, 1.0f / 3.0f, -0.5f), 1.0f);  // log(1 + y), |y| < 0.02
-      return fmaf(-0.5f * kLog2e, z2, -kLog2Sqrt2Pi) + (log2f(width) - log2_s) + l1p * kLog2e;
-    }
-  }
-  return log2_gauss_tail(lo, hi, mu, inv_s);
-}
-
 __device__ __forceinline__ float lo_e4m3_value(int32_t r);
 
-// -log2 q of one scalar.  FULL = false evaluates only the common (series)
-// case and sets `deferred` when the scalar needs the tail evaluation.
 // N(mu, s^2) mass on [lo, hi) as Q(a) - Q(b), Q(z) = erfc(z / sqrt 2) / 2 the
 // upper tail, with the bin mirrored when it lies below mu so that a < b and a
 // is the edge on the far side of mu (both of a straddling bin's edges: Q(a)
-// near 1 then carries absolute error only).  Outside the series case
-// w max(1, |z_m|) >= 0.5 gives Q(a) / Q(b) >= e^0.5, so the difference keeps
-// the relative accuracy of erfcf.  `far` receives a (deep tails: a >= 9).
+// near 1 then carries absolute error only).  On the bf16 bins outside the
+// series case (w >= 1 or w |zm| >= 2) Q(a) / Q(b) >= e^0.5, so the difference
+// keeps the relative accuracy of erfcf.  `far` receives a (deep tails: a >= 9).
 __device__ __forceinline__ float gauss_mass(float lo, float hi, float mu, float inv_s, float &far) {
   const float za = (lo - mu) * inv_s, zb = (hi - mu) * inv_s;
   const bool below = zb <= 0.0f;
@@ -118,18 +98,21 @@ __device__ __forceinline__ float gauss_mass(float lo, float hi, float mu, float 
   return 0.5f * (erfcf(a * 0.70710678f) - erfcf(b * 0.70710678f));
 }
 
-// bf16, both Gaussian bins narrow against their sigma (the series case): the
-// mixture in the linear domain, each component w phi(z_m) (1 + y) with the
-// Hermite correction y of log2_gauss_series, then one logarithm.  A Gaussian
-// term too small for fp32 only drops below the p-hat term's 0.02 p-hat floor.
-// Returns false (and nothing) when the bin needs the tail evaluation.
+// bf16, the series case w < 1 and w |zm| < 2 (then w/3 and zm/3 qualify for
+// the 3 sigma component too): the mixture in the linear domain, each component
+// w phi(zm) (1 + y) with the Hermite correction y of log2_gauss_series, then
+// one logarithm.  The first dropped term, He8 w^8 / 92897280, is at most
+// 132 / 92897280 (|zm| <= 1, w < 1) or about 2^8 / 92897280 (w |zm| < 2), both
+// below 3e-6 relative.  A Gaussian term too small for fp32 only drops below the
+// p-hat term's 0.02 p-hat floor.  Returns false (and nothing) when the bin
+// needs the tail evaluation.
 __device__ __forceinline__ bool ideal_series_bf16(float lo, float hi, float mu, float inv_s,
                                                   float ph, float &bits) {
   if (!(hi > lo) || !isfinite(lo) || !isfinite(hi)) return false;
   const float width = hi - lo;
   const float w = width * inv_s;
   const float zm = (lo + 0.5f * width - mu) * inv_s;
-  if (!(w * fmaxf(1.0f, fabsf(zm)) < 0.5f)) return false;  // then also for 3 sigma
+  if (!(w < 1.0f && w * fabsf(zm) < 2.0f)) return false;
   auto comp = [](float w, float zm) {
     const float z2 = zm * zm, w2 = w * w;
     const float he2 = z2 - 1.0f, he4 = fmaf(z2, z2 - 6.0f, 3.0f);
@@ -144,6 +127,8 @@ __device__ __forceinline__ bool ideal_series_bf16(float lo, float hi, float mu, 
   return true;
 }
 
+// -log2 q of one scalar.  FULL = false (bf16) evaluates only the series case
+// and sets `deferred` when the scalar needs the tail evaluation.
 template <int DT, bool FULL>
 __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float sigma,
                                            const float *phat, const float *lo8, uint32_t &flags,
@@ -163,15 +148,13 @@ __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float
   const float hi = DT == 0 ? lo_bf16(r + 1) : lo8[r + 1];
   // fp32 to about 1e-7 relative is far inside the 1e-3 tolerance of the ideal
   const float inv_s = __fdividef(1.0f, sigma);
-  if (DT == 0 && !FULL) {
-    float bits;
-    if (ideal_series_bf16(lo, hi, mu, inv_s, phat[r], bits)) return bits;
-    deferred = true;
-    return 0.0f;
-  }
-  const float log2_s = __log2f(sigma);
-  float l1, l3 = 0.0f;
-  if (FULL && DT == 0) {
+  if (DT == 0) {
+    if (!FULL) {
+      float bits;
+      if (ideal_series_bf16(lo, hi, mu, inv_s, phat[r], bits)) return bits;
+      deferred = true;
+      return 0.0f;
+    }
     // the mixture in the linear domain: p-hat's 0.02 floor keeps q normal, so a
     // Gaussian mass below fp32's range does not matter
     float far;
@@ -179,40 +162,20 @@ __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float
     const float m3 = hi > lo ? gauss_mass(lo, hi, mu, inv_s * (1.0f / 3.0f), far) : 0.0f;
     return -log2f(fmaf(0.95f, fmaxf(m1, 0.0f), fmaf(0.03f, fmaxf(m3, 0.0f), 0.02f * phat[r])));
   }
-  if (FULL) {
-    // e4m3: one branch-free difference of tails for every bin but the deep
-    // tails (log domain) and bins under 1e-3 sigma wide (the series, where the
-    // difference would cancel); the difference's relative error, about
-    // 6e-8 / (a w), is below 1e-4 of the mass from w = 1e-3 on
-    const float wz = (hi - lo) * inv_s;
-    bool ok = false;
-    if (wz < 1e-3f) l1 = log2_gauss_series(lo, hi, mu, inv_s, log2_s, ok);
-    if (!ok) {
-      float far;
-      const float m = hi > lo ? gauss_mass(lo, hi, mu, inv_s, far) : 0.0f;
-      l1 = (far < 9.0f && m > 0.0f) ? log2f(m) : log2_gauss_tail(lo, hi, mu, inv_s);
-    }
-  } else {
-    bool ok1 = true, ok3 = true;
-    l1 = log2_gauss_series(lo, hi, mu, inv_s, log2_s, ok1);
-    if (DT == 0) l3 = log2_gauss_series(lo, hi, mu, inv_s * (1.0f / 3.0f), log2_s + 1.5849625f, ok3);
-    if (!ok1 || !ok3) {
-      deferred = true;
-      return 0.0f;
-    }
+  // e4m3 (always the full evaluation): one branch-free difference of tails for
+  // every bin but the deep tails (log domain) and bins under 1e-3 sigma wide
+  // (the series, where the difference would cancel); the difference's relative
+  // error, about 6e-8 / (a w), is below 1e-4 of the mass from w = 1e-3 on
+  const float wz = (hi - lo) * inv_s;
+  bool ok = false;
+  float l1 = 0.0f;
+  if (wz < 1e-3f) l1 = log2_gauss_series(lo, hi, mu, inv_s, __log2f(sigma), ok);
+  if (!ok) {
+    float far;
+    const float m = hi > lo ? gauss_mass(lo, hi, mu, inv_s, far) : 0.0f;
+    l1 = (far < 9.0f && m > 0.0f) ? log2f(m) : log2_gauss_tail(lo, hi, mu, inv_s);
   }
-  if (DT == 1) return -l1;
-  const float ph = phat[r];
-  if (l1 > -100.0f && l3 > -100.0f) {
-    // no component can underflow: sum the mixture directly
-    return -__log2f(fmaf(0.95f, exp2f(l1), fmaf(0.03f, exp2f(l3), 0.02f * ph)));
-  }
-  const float a = -0.07400058f + l1;  // log2 0.95
-  const float b = -5.0588937f + l3;   // log2 0.03 (the wide component: sigma * 3)
-  const float c = -5.6438562f + __log2f(ph);  // log2 0.02
-  const float m = fmaxf(a, fmaxf(b, c));
-  if (m == -INFINITY) return INFINITY;
-  return -(m + __log2f(exp2f(a - m) + exp2f(b - m) + exp2f(c - m)));
+  return -l1;
 }
 
 template <int DT>
@@ -246,12 +209,16 @@ __device__ __forceinline__ uint64_t sigma_index(const IdealLaunch &a, uint64_t i
   return (row * (uint64_t)a.geo.ntb + tb) * D + ch;
 }
 
+// Per-warp ring of deferred scalars (power of two).  At most 31 wait between
+// loop iterations and one iteration adds at most 256, so 512 never overflows.
+constexpr uint32_t kIdealRing = 512;
+
 template <int DT, bool O0>
 __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
   __shared__ float s_lo8[256];
   __shared__ double s_part[256];
   __shared__ float s_bits[8 * 256];
-  __shared__ uint16_t s_queue[8 * 256];  // per warp: up to 8 deferred scalars per lane
+  __shared__ uint32_t s_ring[8 * kIdealRing];
   if (DT == 1) {
     // e4m3 bin edges: midpoints of neighbouring values, +-inf at the ends
     for (int r = threadIdx.x; r < 255; r += blockDim.x) {
@@ -263,17 +230,43 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
     }
     __syncthreads();
   }
+  constexpr bool kDefer = DT == 0 && !O0;  // bf16 with a model: the series case first
   const uint64_t TD = (uint64_t)a.geo.T * (uint64_t)a.geo.D;
   const int64_t n8 = a.geo.n / 8;
   const float *sig = a.sigma_chunk ? a.sigma_chunk : a.sigma;
   uint32_t flags = 0;
   double acc = 0.0;
-  // The loop runs the same number of times for every lane of a warp (lanes past
-  // the end are switched off), because the deferred-scalar queue below is
-  // filled and worked off by the whole warp.
   const int lane = threadIdx.x & 31;
-  for (int64_t gw = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); gw < n8;
-       gw += (int64_t)gridDim.x * blockDim.x) {
+  const int64_t gw0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31);
+  const int64_t gstride = (int64_t)gridDim.x * blockDim.x;
+  // Scalars outside the series case (about 1% of a bf16 cache) wait in the
+  // warp's ring as (iteration << 8) | (k << 5) | lane until 32 have gathered;
+  // then the whole warp evaluates them at once, so the long tail code runs once
+  // per 32 of them, not once per loop iteration that holds one.  Iterations fit
+  // in 24 bits: with fewer than 4096 blocks the loop runs once, and with 4096
+  // blocks 2^24 iterations would be 2^47 scalars.
+  uint32_t *ring = s_ring + (threadIdx.x >> 5) * kIdealRing;
+  uint32_t head = 0, tail = 0;  // warp-uniform
+  auto work_off = [&](uint32_t cnt) {  // the oldest cnt <= 32 entries, one per lane
+    if ((uint32_t)lane < cnt) {
+      const uint32_t e = ring[(head + lane) & (kIdealRing - 1)];
+      const int k = (int)((e >> 5) & 7u), owner = (int)(e & 31u);
+      const uint64_t j = (uint64_t)(gw0 + (int64_t)(e >> 8) * gstride + owner) * 8 + k;
+      bool unused = false;
+      const float b = ideal_one<DT, true>((uint32_t)static_cast<const uint16_t *>(a.kv)[j],
+                                          (uint32_t)a.mu[j], __ldg(sig + sigma_index(a, j, TD)),
+                                          a.phat, s_lo8, flags, unused);
+      acc += (double)b;
+      if (a.per_scalar) a.per_scalar[j] = b;  // after the owner's store of 0 (a barrier apart)
+    }
+    head += cnt;
+    __syncwarp();  // the slots just read may be written by the next iteration
+  };
+  // The loop runs the same number of times for every lane of a warp (lanes past
+  // the end are switched off), because the ring is filled and worked off by the
+  // whole warp.
+  uint32_t it = 0;
+  for (int64_t gw = gw0; gw < n8; gw += gstride, ++it) {
     const int64_t g = gw + lane;
     const bool act = g < n8;
     const uint64_t i0 = act ? (uint64_t)g * 8 : 0;
@@ -289,17 +282,12 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
       }
       if (!O0) mu4 = __ldg(reinterpret_cast<const uint4 *>(a.mu + i0));
     }
-    // pass 1: the common case for all 8 scalars.  Scalars that need the tail
-    // evaluation go to a per-warp queue, which the whole warp then works off
-    // 32 at a time, so that no lane idles through the (long) tail code.
-    uint16_t *q = s_queue + (threadIdx.x >> 5) * 256;
-    int qn = 0;
 #pragma unroll 1
     for (int k = 0; k < 8; ++k) {
       bool deferred = false;
       float b = 0.0f;
       // e4m3 bins are wide against sigma, so the tail case is the common one
-      // there: evaluate it in place instead of queueing nearly every scalar
+      // there: it is evaluated in place
       if (act && O0) {
         // order-0 baseline: q = p-hat
         const int32_t r = rank_bf16(sym_at<DT>(kv4, k));
@@ -310,39 +298,36 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
                                    a.phat, s_lo8, flags, deferred);
       }
       s_bits[k * 256 + threadIdx.x] = b;
-      const uint32_t dm = __ballot_sync(0xFFFFFFFFu, deferred);
-      if (deferred) q[qn + __popc(dm & ((1u << lane) - 1u))] = (uint16_t)((k << 5) | lane);
-      qn += __popc(dm);
-    }
-    __syncwarp();
-    for (int base = 0; base < qn; base += 32) {
-      if (base + lane < qn) {
-        const uint32_t e = q[base + lane];
-        const int k = (int)(e >> 5), owner = (int)(e & 31u);
-        const uint64_t j = (uint64_t)(gw + owner) * 8 + k;  // the owner's scalar
-        const uint32_t sym = DT == 0 ? (uint32_t)static_cast<const uint16_t *>(a.kv)[j]
-                                     : (uint32_t)static_cast<const uint8_t *>(a.kv)[j];
-        const uint64_t srow_j = sigma_index(a, j, TD);
-        bool unused = false;
-        s_bits[k * 256 + (threadIdx.x & ~31) + owner] =
-            ideal_one<DT, true>(sym, (uint32_t)a.mu[j], __ldg(sig + srow_j), a.phat, s_lo8,
-                                flags, unused);
+      if (kDefer) {
+        const uint32_t dm = __ballot_sync(0xFFFFFFFFu, deferred);
+        if (deferred)
+          ring[(tail + __popc(dm & ((1u << lane) - 1u))) & (kIdealRing - 1)] =
+              (it << 8) | ((uint32_t)k << 5) | (uint32_t)lane;
+        tail += __popc(dm);
       }
     }
-    __syncwarp();
-    if (!act) continue;
-    float bits[8], part = 0.0f;
+    if (act) {
+      float bits[8], part = 0.0f;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      bits[k] = s_bits[k * 256 + threadIdx.x];
-      part += bits[k];
+      for (int k = 0; k < 8; ++k) {
+        bits[k] = s_bits[k * 256 + threadIdx.x];
+        part += bits[k];
+      }
+      acc += (double)part;
+      if (a.per_scalar) {
+        float4 *o = reinterpret_cast<float4 *>(a.per_scalar + i0);
+        o[0] = make_float4(bits[0], bits[1], bits[2], bits[3]);
+        o[1] = make_float4(bits[4], bits[5], bits[6], bits[7]);
+      }
     }
-    acc += (double)part;
-    if (a.per_scalar) {
-      float4 *o = reinterpret_cast<float4 *>(a.per_scalar + i0);
-      o[0] = make_float4(bits[0], bits[1], bits[2], bits[3]);
-      o[1] = make_float4(bits[4], bits[5], bits[6], bits[7]);
+    if (kDefer) {
+      __syncwarp();  // ring entries and the owners' stores before the work-off
+      while (tail - head >= 32u) work_off(32u);
     }
+  }
+  if (kDefer) {
+    __syncwarp();
+    if (tail != head) work_off(tail - head);
   }
   if (flags) atomicOr(&a.head->flags, flags);
   s_part[threadIdx.x] = acc;
