@@ -127,8 +127,9 @@ __device__ __forceinline__ bool ideal_series_bf16(float lo, float hi, float mu, 
   return true;
 }
 
-// -log2 q of one scalar.  FULL = false (bf16) evaluates only the series case
-// and sets `deferred` when the scalar needs the tail evaluation.
+// -log2 q of one scalar.  FULL = false evaluates only the common cases (bf16:
+// the series; e4m3: all but the deep tails) and sets `deferred` when the
+// scalar needs the rest.
 template <int DT, bool FULL>
 __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float sigma,
                                            const float *phat, const float *lo8, uint32_t &flags,
@@ -162,8 +163,8 @@ __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float
     const float m3 = hi > lo ? gauss_mass(lo, hi, mu, inv_s * (1.0f / 3.0f), far) : 0.0f;
     return -log2f(fmaf(0.95f, fmaxf(m1, 0.0f), fmaf(0.03f, fmaxf(m3, 0.0f), 0.02f * phat[r])));
   }
-  // e4m3 (always the full evaluation): one branch-free difference of tails for
-  // every bin but the deep tails (log domain) and bins under 1e-3 sigma wide
+  // e4m3: one branch-free difference of tails for every bin but the deep tails
+  // (log domain; deferred when FULL = false) and bins under 1e-3 sigma wide
   // (the series, where the difference would cancel); the difference's relative
   // error, about 6e-8 / (a w), is below 1e-4 of the mass from w = 1e-3 on
   const float wz = (hi - lo) * inv_s;
@@ -173,7 +174,14 @@ __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float
   if (!ok) {
     float far;
     const float m = hi > lo ? gauss_mass(lo, hi, mu, inv_s, far) : 0.0f;
-    l1 = (far < 9.0f && m > 0.0f) ? log2f(m) : log2_gauss_tail(lo, hi, mu, inv_s);
+    if (far < 9.0f && m > 0.0f) {
+      l1 = log2f(m);
+    } else if (!FULL) {
+      deferred = true;
+      return 0.0f;
+    } else {
+      l1 = log2_gauss_tail(lo, hi, mu, inv_s);
+    }
   }
   return -l1;
 }
@@ -230,7 +238,7 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
     }
     __syncthreads();
   }
-  constexpr bool kDefer = DT == 0 && !O0;  // bf16 with a model: the series case first
+  constexpr bool kDefer = !O0;  // the order-0 baseline has no rare case
   const uint64_t TD = (uint64_t)a.geo.T * (uint64_t)a.geo.D;
   const int64_t n8 = a.geo.n / 8;
   const float *sig = a.sigma_chunk ? a.sigma_chunk : a.sigma;
@@ -239,7 +247,8 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
   const int lane = threadIdx.x & 31;
   const int64_t gw0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31);
   const int64_t gstride = (int64_t)gridDim.x * blockDim.x;
-  // Scalars outside the series case (about 1% of a bf16 cache) wait in the
+  // Scalars outside the common cases (about 1% of a bf16 cache outside the
+  // series case, about 1% of an e4m3 cache in the deep tails) wait in the
   // warp's ring as (iteration << 8) | (k << 5) | lane until 32 have gathered;
   // then the whole warp evaluates them at once, so the long tail code runs once
   // per 32 of them, not once per loop iteration that holds one.  Iterations fit
@@ -253,8 +262,9 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
       const int k = (int)((e >> 5) & 7u), owner = (int)(e & 31u);
       const uint64_t j = (uint64_t)(gw0 + (int64_t)(e >> 8) * gstride + owner) * 8 + k;
       bool unused = false;
-      const float b = ideal_one<DT, true>((uint32_t)static_cast<const uint16_t *>(a.kv)[j],
-                                          (uint32_t)a.mu[j], __ldg(sig + sigma_index(a, j, TD)),
+      const uint32_t sym = DT == 0 ? (uint32_t)static_cast<const uint16_t *>(a.kv)[j]
+                                   : (uint32_t)static_cast<const uint8_t *>(a.kv)[j];
+      const float b = ideal_one<DT, true>(sym, (uint32_t)a.mu[j], __ldg(sig + sigma_index(a, j, TD)),
                                           a.phat, s_lo8, flags, unused);
       acc += (double)b;
       if (a.per_scalar) a.per_scalar[j] = b;  // after the owner's store of 0 (a barrier apart)
@@ -286,16 +296,14 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
     for (int k = 0; k < 8; ++k) {
       bool deferred = false;
       float b = 0.0f;
-      // e4m3 bins are wide against sigma, so the tail case is the common one
-      // there: it is evaluated in place
       if (act && O0) {
         // order-0 baseline: q = p-hat
         const int32_t r = rank_bf16(sym_at<DT>(kv4, k));
         if (r < 0 || r >= kNsymBf16) flags |= kFlagSymbol;
         else b = -log2f(__ldg(a.phat + r));
       } else if (act) {
-        b = ideal_one<DT, DT == 1>(sym_at<DT>(kv4, k), mu_at(mu4, k), __ldg(sig + srow + k),
-                                   a.phat, s_lo8, flags, deferred);
+        b = ideal_one<DT, false>(sym_at<DT>(kv4, k), mu_at(mu4, k), __ldg(sig + srow + k),
+                                 a.phat, s_lo8, flags, deferred);
       }
       s_bits[k * 256 + threadIdx.x] = b;
       if (kDefer) {
