@@ -132,3 +132,53 @@ def test_repeat_calls_are_deterministic(oracle_mod):
     t1 = codec.ideal_bits(kv_d, mu_d)
     t2 = codec.ideal_bits(kv_d, mu_d)
     assert t1 == t2
+
+
+def _bf16_near_case_edges(rng, T, D):
+    """bf16 scalars whose bins sit on both sides of the ideal-bits kernel's case
+    boundaries (bin width w < 1 and w |z_m| < 2, in sigma units): sigma is a
+    power of two times (1 + delta), the symbol's binade sets w near 2^k_w, and mu
+    is the symbol a few patterns away, so that w |z_m| lands near |steps| w^2."""
+    deltas = np.array([-1e-2, -1e-3, -1e-5, 0.0, 1e-5, 1e-3, 1e-2])
+    j = rng.integers(-8, 9, 2 * D)
+    sig = np.ldexp(1.0 + rng.choice(deltas, 2 * D), j)
+    n = 2 * T * D
+    ch = (np.arange(n) // (T * D)) * D + np.arange(n) % D
+    kw = rng.choice([-2, -1, 0, 0, 1], n)
+    e = 7 + j[ch] + kw
+    x = np.ldexp(1.0 + rng.integers(0, 128, n) / 128.0, e) * rng.choice([-1.0, 1.0], n)
+    kv = (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)  # exact in bf16
+    steps = rng.choice([0, 1, 2, 3, 7, 8, 9, 31, 32, 33], n) * rng.choice([-1, 1], n)
+    mu = (kv.astype(np.int64) + steps).astype(np.uint16)
+    # keep mu finite and on x's side of zero (adjacent patterns are adjacent values there)
+    bad = ((mu & 0x7F80) == 0x7F80) | ((mu ^ kv) & 0x8000 != 0)
+    mu[bad] = kv[bad]
+    return kv, mu, sig
+
+
+def test_ideal_bits_case_edges(oracle_mod):
+    """Per-scalar ideal bits on both sides of every case boundary of the kernel
+    (bf16 series / erfc tails, e4m3 difference of tails / deep tail at 9 sigma)."""
+    rng = np.random.default_rng(11)
+    T, D = 128, 64
+    kv, mu, sig = _bf16_near_case_edges(rng, T, D)
+    counts = rng.integers(0, 50, 65536).astype(np.uint64)
+    w = _custom(synth.BF16, kv, mu, sig, counts, T=T, D=D, Tb=32, G=4)
+    _roundtrip(oracle_mod, w, max_overhead=0.05)
+    # e4m3: mu placed 8.5 to 9.5 sigma beyond the bin edge on its side
+    codes = np.array([u for u in range(256) if u not in (0x7F, 0xFF)], dtype=np.uint8)
+    n = 2 * T * D
+    kv8 = rng.choice(codes, n).astype(np.uint8)
+    r = np.array([oracle_mod.rank(1, int(u)) for u in kv8])
+    lo = np.array([oracle_mod.lo(1, int(q)) for q in r])
+    hi = np.array([oracle_mod.lo(1, int(q) + 1) for q in r])
+    val = np.where(np.isfinite(lo), lo, hi)
+    sig8 = np.exp(rng.uniform(np.log(1e-2), np.log(10.0), 2 * D))
+    ch = (np.arange(n) // (T * D)) * D + np.arange(n) % D
+    a = rng.uniform(8.5, 9.5, n) * sig8[ch]
+    above = rng.random(n) < 0.5  # mu above the bin: the far edge is hi
+    mu_v = np.where(above, np.where(np.isfinite(hi), hi, val) + a, np.where(np.isfinite(lo), lo, val) - a)
+    mu8 = (torch.from_numpy(mu_v.astype(np.float32)).to(torch.bfloat16).view(torch.int16)
+           .numpy().view(np.uint16))
+    _roundtrip(oracle_mod, _custom(synth.E4M3, kv8, mu8, sig8, T=T, D=D, Tb=32, G=4),
+               max_overhead=1.0)
