@@ -29,9 +29,9 @@ __device__ uint2 g_phi[kPhiKnots];
 __device__ float g_lo8[256];
 __device__ float2 g_hinv[2][kHinvN + 1];
 
-// One resident block per SM with 24 warps: a single copy of the tables per SM
-// leaves the rest of the unified L1 / shared memory to the L1 cache (the p-hat
-// prefix table, mu, the streams).
+// At most one resident block per SM, of up to 24 warps: a single copy of the
+// tables per SM leaves the rest of the unified L1 / shared memory to the L1
+// cache (the p-hat prefix table, mu, the streams).  See task_shape.
 constexpr int kCodeThreads = 768;
 constexpr size_t kCodeSmem = sizeof(uint2) * kPhiKnots + sizeof(float) * 256;
 constexpr int kDecThreads = 768;
@@ -429,12 +429,30 @@ __global__ void __launch_bounds__(256) k_compact(EncodeLaunch a) {
   }
 }
 
-static int code_blocks(int64_t ntasks) {
-  // at most one block per SM (see kCodeThreads)
-  const int64_t warps_per_block = kCodeThreads / 32;
-  int64_t want = (ntasks + warps_per_block - 1) / warps_per_block;
-  int64_t cap = (int64_t)device_sm_count();
-  return (int)(want < cap ? want : cap);
+// Grid for ntasks >= 1 warp tasks of a coder kernel (blocks of at most
+// max_threads, at most one block per SM).  A lane's symbols are coded one after
+// another, so a launch takes at least one lane's chain of steps, and a step is
+// several times shorter on an SM running a few warps than on one whose 24
+// warps contend for issue slots (one lane's 2048-symbol chunk: about 1.9 ms
+// alone, 4 ms on a full SM).  A launch too small to fill an eighth of the SMs
+// with full blocks (a chunk range of up to ~900 chunks of 16 lanes, one token
+// block of the adaptive coder) therefore spreads over all SMs with fewer warps
+// per block.  Larger launches keep full blocks on as few SMs as they need, so
+// that launches on other streams (a cache coded as four layer groups side by
+// side: a quarter each) get SMs of their own rather than sharing theirs: a
+// block holds 65-79 KiB of tables, so few fit per SM.
+static void task_shape(int64_t ntasks, int max_threads, int &blocks, int &threads) {
+  const int64_t sms = (int64_t)device_sm_count();
+  const int64_t wmax = max_threads / 32;
+  if (8 * ntasks >= sms * wmax) {
+    const int64_t want = (ntasks + wmax - 1) / wmax;
+    blocks = (int)(want < sms ? want : sms);
+    threads = max_threads;
+    return;
+  }
+  const int64_t wpb = (ntasks + sms - 1) / sms;  // 1 .. wmax / 8
+  threads = (int)(32 * wpb);
+  blocks = (int)((ntasks + wpb - 1) / wpb);
 }
 
 cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s) {
@@ -446,23 +464,24 @@ cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s) {
 cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s) {
   const int64_t ntasks = (a.c_count * a.geo.G + 31) / 32;
   if (ntasks == 0) return cudaSuccess;
-  const int blocks = code_blocks(ntasks);
+  int blocks, threads;
+  task_shape(ntasks, kCodeThreads, blocks, threads);
   cudaError_t e;
   if (a.dtype == 0 && a.order0) {
     e = cudaFuncSetAttribute(k_encode<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kCodeSmem);
     if (e != cudaSuccess) return e;
-    k_encode<0, true><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
+    k_encode<0, true><<<blocks, threads, kCodeSmem, s>>>(a);
   } else if (a.dtype == 0) {
     e = cudaFuncSetAttribute(k_encode<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kCodeSmem);
     if (e != cudaSuccess) return e;
-    k_encode<0, false><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
+    k_encode<0, false><<<blocks, threads, kCodeSmem, s>>>(a);
   } else {
     e = cudaFuncSetAttribute(k_encode<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kCodeSmem);
     if (e != cudaSuccess) return e;
-    k_encode<1, false><<<blocks, kCodeThreads, kCodeSmem, s>>>(a);
+    k_encode<1, false><<<blocks, threads, kCodeSmem, s>>>(a);
   }
   return cudaGetLastError();
 }
@@ -955,11 +974,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
 }
 
 template <int DT, bool BISECT>
-static cudaError_t run_decode(const DecodeLaunch &a, int blocks, cudaStream_t s) {
+static cudaError_t run_decode(const DecodeLaunch &a, int blocks, int threads, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k_decode<DT, BISECT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
   if (e != cudaSuccess) return e;
-  k_decode<DT, BISECT><<<blocks, kDecThreads, kDecSmem, s>>>(a);
+  k_decode<DT, BISECT><<<blocks, threads, kDecSmem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -973,22 +992,21 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s) {
   // the task counter of this launch starts at zero
   e = cudaMemsetAsync(&a.head->next_task, 0, sizeof(unsigned long long), s);
   if (e != cudaSuccess) return e;
-  // at most one block per SM (see kCodeThreads)
   const int64_t ntasks = (((a.c_end - a.c_begin + a.c_step - 1) / a.c_step) * a.geo.G + 31) / 32;
-  const int64_t wpb = kDecThreads / 32;
-  int64_t blocks = (ntasks + wpb - 1) / wpb;
-  const int64_t cap = (int64_t)device_sm_count();
-  if (blocks > cap) blocks = cap;
+  int blocks, threads;
+  task_shape(ntasks, kDecThreads, blocks, threads);
   if (a.order0) {
     constexpr size_t smem = sizeof(int32_t) * (kO0InvN + 1);
     e = cudaFuncSetAttribute(k_decode_o0, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    k_decode_o0<<<(int)blocks, kDecThreads, smem, s>>>(a);
+    k_decode_o0<<<blocks, threads, smem, s>>>(a);
     return cudaGetLastError();
   }
   if (a.dtype == 0)
-    return a.bisect ? run_decode<0, true>(a, (int)blocks, s) : run_decode<0, false>(a, (int)blocks, s);
-  return a.bisect ? run_decode<1, true>(a, (int)blocks, s) : run_decode<1, false>(a, (int)blocks, s);
+    return a.bisect ? run_decode<0, true>(a, blocks, threads, s)
+                    : run_decode<0, false>(a, blocks, threads, s);
+  return a.bisect ? run_decode<1, true>(a, blocks, threads, s)
+                  : run_decode<1, false>(a, blocks, threads, s);
 }
 
 }  // namespace skv
