@@ -711,14 +711,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
           if (has) {
             // (1) guess: invert the CDF's Gaussian part around a reference
             // symbol: slot ~ K F(x) + rank(x) with F = 0.95 Phi(z) + 0.03 Phi(z/3)
-            // + 0.02 E(x), with rank and E taken at mu.  For e4m3 a second pass
-            // takes the rank term at the first guess (for bf16 that pass mainly
+            // + 0.02 E(x), with rank and E taken at mu.  For e4m3, whose rank
+            // term is up to 0.4% of the CDF, one step along the table's slope
+            // then takes it at the first guess (for bf16 a second look mainly
             // helps through E at the guess, whose dependent load costs as much
             // as the Newton steps it saves).
             const float sig = __fdividef(1.0f, inv.s);  // a guess: approximate is enough
             auto guess = [&](int32_t rref) -> int32_t {
               float u, uraw;
-              uraw = (float)(int32_t)(slot - (uint32_t)rref) * kInvK;
+              const int32_t dr = (int32_t)(slot - (uint32_t)rref);
+              uraw = (float)dr * kInvK;
               if (DT == 0) {
                 const float e = (float)__ldg(a.ecdf + rref) * (1.0f / 67108864.0f);
                 u = uraw - 0.02f * e;
@@ -727,14 +729,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
               }
               if (DT == 1) {
                 // beyond both ends of Phi_q's range cum(r) = r (below mu) or
-                // K + r (above): the rank follows from the slot directly
-                if (u <= 0.0f) return min((int32_t)slot, NS - 1);
-                if (u >= 1.0f) return max(min((int32_t)slot - (int32_t)kKE4m3, NS - 1), 0);
+                // K + r (above): the rank follows from the slot directly.  Exact
+                // integer tests: in fp32, K (1/K) rounds below 1.
+                if (dr <= 0) return min((int32_t)slot, NS - 1);
+                if (dr >= (int32_t)kKE4m3) return max(min((int32_t)slot - (int32_t)kKE4m3, NS - 1), 0);
               }
               const float t = fminf(fmaxf(u * kHscale, 0.0f), (float)kHinvN - 0.001f);
               const int kk = (int)t;
               const float2 h = s_hinv[kk];
-              int32_t r = rank_of_value<DT>(fmaf(sig, fmaf(t - (float)kk, h.y, h.x), muf));
+              const float z0 = fmaf(t - (float)kk, h.y, h.x);
+              int32_t r = rank_of_value<DT>(fmaf(sig, z0, muf));
+              if (DT == 1) {
+                // the rank term at the guess: u falls by (r - rref) / K, one step
+                // along the table's slope dz/du = h.y kHscale
+                const float dz = (float)(r - rref) * (kInvK * kHscale);
+                r = rank_of_value<DT>(fmaf(sig, fmaf(-dz, h.y, z0), muf));
+              }
               if (DT == 0 && (u < 0.0f || u > kHinvUmaxBf16)) {
                 // beyond both Gaussian parts only p-hat moves the CDF: invert it
                 const float tgt = (u < 0.0f ? uraw : uraw - kHinvUmaxBf16) * (50.0f * kHinvN);
@@ -745,8 +755,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
               }
               return r;
             };
-            int32_t rg = guess(DT == 0 ? rank_bf16(mub) : rank_of_value<DT>(muf));
-            if (DT == 1) rg = guess(rg);  // e4m3: the rank term is up to 0.4% of the CDF
+            const int32_t rg = guess(DT == 0 ? rank_bf16(mub) : rank_of_value<DT>(muf));
             const uint32_t ca = cum_of<DT>(rg, muf, inv, s_phi, s_lo8, a.ecdf);
             const uint32_t cb = cum_of<DT>(rg + 1, muf, inv, s_phi, s_lo8, a.ecdf);
             bracket_add(br, rg, ca, slot);
