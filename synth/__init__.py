@@ -80,9 +80,10 @@ WORKLOADS = {
     "qwen3-8b-e4m3": Spec("qwen3-8b-e4m3", E4M3, 36, 8, 16384, 128, 0.03, True, 0, 512, False,
                           256, 8),
     # the Qwen3-0.6B shape as an FP8 cache: 234.9M e4m3 scalars, small enough for
-    # a detailed profile of the e4m3 kernels (about 1.5 GB on the device)
+    # a detailed profile of the e4m3 kernels (about 1.5 GB on the device); 16
+    # lanes per chunk fill the GPU as the larger caches do
     "qwen3-0.6b-e4m3": Spec("qwen3-0.6b-e4m3", E4M3, 28, 8, 4096, 128, 0.03, True, 0, 512, False,
-                            256, 8),
+                            256, 16),
     # long-context FP8 stress: 64 x {K,V} x 8 x 32768 x 128 = 2^32 e4m3 scalars
     "long-32k-e4m3": Spec("long-32k-e4m3", E4M3, 64, 8, 32768, 128, 0.03, True, 0, 512, False,
                           128, 4),
