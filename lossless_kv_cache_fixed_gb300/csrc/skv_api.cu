@@ -29,6 +29,7 @@ uint32_t g_phi_host[kPhiKnots];
 float g_lo8_host[256];
 float g_hinv_host[2][kHinvN + 1];
 float g_scale_mult_host[256];
+float g_log2q_host[kTailN];
 std::once_flag g_const_once;
 
 double e4m3_value_host(uint32_t u) {
@@ -73,6 +74,11 @@ void build_constants() {
       g_hinv_host[t][k] = (float)(z < -14.0 ? -14.0 : (z > 14.0 ? 14.0 : z));
     }
   }
+  // log2 Q(z) of the Gaussian upper tail at z = k / kTailPerUnit, in binary64
+  for (int k = 0; k < kTailN; ++k) {
+    const double z = (double)k / kTailPerUnit;
+    g_log2q_host[k] = (float)std::log2(0.5 * std::erfc(z / std::sqrt(2.0)));
+  }
   // per-block scale multipliers m(s) = fp32(2^((s - 128) / 32)); binary64 exp2
   // is within an ulp of 2^(k/32), whose fp32 rounding is never that close to a tie
   for (int k = 0; k < 256; ++k) g_scale_mult_host[k] = (float)std::exp2((k - 128) / 32.0);
@@ -91,6 +97,7 @@ int ensure_device_tables() {
     if (upload_tables(g_phi_host, g_lo8_host, g_hinv_host[0], g_hinv_host[1]) != cudaSuccess)
       return SKV_ERR_CUDA;
     if (upload_scale_mult(g_scale_mult_host) != cudaSuccess) return SKV_ERR_CUDA;
+    if (upload_tail_table(g_log2q_host) != cudaSuccess) return SKV_ERR_CUDA;
     g_dev_ready[dev] = true;
   }
   return SKV_OK;

@@ -15,9 +15,11 @@
 //   * bf16 otherwise (queued per warp): each component's mass as a difference
 //     of complementary error functions on the far side of mu, the mixture in
 //     the linear domain (p-hat's 0.02 floor keeps it a normal float);
-//   * e4m3: the same difference of tails for bins at least 1e-3 sigma wide, the
-//     log-domain tail log Q(z) = log(erfcx(z/sqrt2)/2) - z^2/2 for deep tails,
-//     the series (in log2) for narrower bins.
+//   * e4m3: the difference of tails from a table of log2 Q for bins at least
+//     0.01 sigma wide with the near edge within 9 sigma (about 98.7% of
+//     scalars); for the rest (queued per warp) the difference of erfc tails,
+//     the log-domain tail log Q(z) = log(erfcx(z/sqrt2)/2) - z^2/2 for deep
+//     tails, the series (in log2) for bins under 1e-3 sigma wide.
 // Per-thread sums, then a fixed-order block tree and a fixed-order final sum,
 // all in fp64: the total does not depend on scheduling.
 #include <cuda_runtime.h>
@@ -84,6 +86,36 @@ __device__ __forceinline__ float log2_gauss_series(float lo, float hi, float mu,
 
 __device__ __forceinline__ float lo_e4m3_value(int32_t r);
 
+// (log2 Q(z_k), log2 Q(z_{k+1}) - log2 Q(z_k)) at z_k = k / kTailPerUnit.
+__device__ float2 g_log2q[kTailN];
+
+cudaError_t upload_tail_table(const float *l2q) {
+  float2 pairs[kTailN];
+  for (int k = 0; k < kTailN; ++k)
+    pairs[k] = make_float2(l2q[k], k + 1 < kTailN ? l2q[k + 1] - l2q[k] : 0.0f);
+  return cudaMemcpyToSymbol(g_log2q, pairs, sizeof(pairs));
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Q(z) for z >= 0 from the table, 0 from z = 12 on (Q(12) < 1.8e-33).  log2 Q is
+// linear between knots 1/256 apart; its second derivative, -h (h - z) / ln 2
+// with h = phi / Q, is below 1 / ln 2 in magnitude, so the interpolation error
+// is below 1.45 / (8 256^2) = 2.8e-6 in log2.  With the fp32 rounding of the
+// knots (up to 4e-6 at z = 9, where log2 Q = -63) and of ex2.approx, Q carries
+// at most 5e-6 relative error below z = 9 (2e-6 below z = 3).
+__device__ __forceinline__ float q_tab(float z) {
+  if (!(z < 12.0f)) return 0.0f;
+  const float t = z * (float)kTailPerUnit;
+  const int k = (int)t;
+  const float2 e = __ldg(&g_log2q[k]);
+  return ex2_approx(fmaf(t - (float)k, e.y, e.x));
+}
+
 // N(mu, s^2) mass on [lo, hi) as Q(a) - Q(b), Q(z) = erfc(z / sqrt 2) / 2 the
 // upper tail, with the bin mirrored when it lies below mu so that a < b and a
 // is the edge on the far side of mu (both of a straddling bin's edges: Q(a)
@@ -128,8 +160,8 @@ __device__ __forceinline__ bool ideal_series_bf16(float lo, float hi, float mu, 
 }
 
 // -log2 q of one scalar.  FULL = false evaluates only the common cases (bf16:
-// the series; e4m3: all but the deep tails) and sets `deferred` when the
-// scalar needs the rest.
+// the series; e4m3: the tail table) and sets `deferred` when the scalar needs
+// the rest.
 template <int DT, bool FULL>
 __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float sigma,
                                            const float *phat, const float *lo8, uint32_t &flags,
@@ -163,25 +195,38 @@ __device__ __forceinline__ float ideal_one(uint32_t sym, uint32_t mu_bits, float
     const float m3 = hi > lo ? gauss_mass(lo, hi, mu, inv_s * (1.0f / 3.0f), far) : 0.0f;
     return -log2f(fmaf(0.95f, fmaxf(m1, 0.0f), fmaf(0.03f, fmaxf(m3, 0.0f), 0.02f * phat[r])));
   }
-  // e4m3: one branch-free difference of tails for every bin but the deep tails
-  // (log domain; deferred when FULL = false) and bins under 1e-3 sigma wide
-  // (the series, where the difference would cancel); the difference's relative
-  // error, about 6e-8 / (a w), is below 1e-4 of the mass from w = 1e-3 on
   const float wz = (hi - lo) * inv_s;
+  if (!FULL) {
+    // e4m3 common case, bins at least 0.01 sigma wide whose near edge lies
+    // within 9 sigma (all but about 1.3% of a cache): the mass from the tail
+    // table, Q(a) - Q(b) for a bin on one side of mu (mirrored below it) and
+    // 1 - Q(-a) - Q(b) for a bin around mu, so the error scales with the
+    // tails.  With epsilon <= 5e-6 per tail, a one-sided bin's mass is off by
+    // at most epsilon (Q(a) + Q(b)) / (Q(a) - Q(b)) <= 250 epsilon relative (w =
+    // 0.01 at a = 0, where such a bin costs 8 bits: 2e-3 bits of a 8e-3
+    // tolerance), a bin around mu's by epsilon (1 - m) absolute.  The rest
+    // waits for the full evaluation below.
+    const float za = (lo - mu) * inv_s, zb = (hi - mu) * inv_s;
+    const bool below = zb <= 0.0f;
+    const float a = below ? -zb : za, b = below ? -za : zb;
+    if (!(wz >= 0.01f && a < 9.0f)) {
+      deferred = true;
+      return 0.0f;
+    }
+    const float m = a >= 0.0f ? q_tab(a) - q_tab(b) : 1.0f - q_tab(-a) - q_tab(b);
+    return -__log2f(m);
+  }
+  // e4m3 full evaluation: one branch-free difference of erfc tails for every
+  // bin but the deep tails (log domain) and bins under 1e-3 sigma wide (the
+  // series, where the difference would cancel); the difference's relative
+  // error, about 6e-8 / (a w), is below 1e-4 of the mass from w = 1e-3 on
   bool ok = false;
   float l1 = 0.0f;
   if (wz < 1e-3f) l1 = log2_gauss_series(lo, hi, mu, inv_s, __log2f(sigma), ok);
   if (!ok) {
     float far;
     const float m = hi > lo ? gauss_mass(lo, hi, mu, inv_s, far) : 0.0f;
-    if (far < 9.0f && m > 0.0f) {
-      l1 = log2f(m);
-    } else if (!FULL) {
-      deferred = true;
-      return 0.0f;
-    } else {
-      l1 = log2_gauss_tail(lo, hi, mu, inv_s);
-    }
+    l1 = (far < 9.0f && m > 0.0f) ? log2f(m) : log2_gauss_tail(lo, hi, mu, inv_s);
   }
   return -l1;
 }
@@ -248,8 +293,8 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
   const int64_t gw0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31);
   const int64_t gstride = (int64_t)gridDim.x * blockDim.x;
   // Scalars outside the common cases (about 1% of a bf16 cache outside the
-  // series case, about 1% of an e4m3 cache in the deep tails) wait in the
-  // warp's ring as (iteration << 8) | (k << 5) | lane until 32 have gathered;
+  // series case, about 1.3% of an e4m3 cache in the deep tails or in bins
+  // narrower than 0.01 sigma) wait in the warp's ring as (iteration << 8) | (k << 5) | lane until 32 have gathered;
   // then the whole warp evaluates them at once, so the long tail code runs once
   // per 32 of them, not once per loop iteration that holds one.  Iterations fit
   // in 24 bits: with fewer than 4096 blocks the loop runs once, and with 4096

@@ -125,6 +125,10 @@ constexpr int kHinvN = 1024;
 // Order-0 decode: inverse of the p-hat prefix table at kO0InvN + 1 points.
 constexpr int kO0InvN = 8192;
 constexpr float kHinvUmaxBf16 = 0.98f, kHinvUmaxE4m3 = 1.0f;
+// Ideal bits (e4m3): log2 Q(z), Q(z) = erfc(z / sqrt 2) / 2 the Gaussian upper
+// tail, at z = k / kTailPerUnit for k = 0 .. kTailN - 1 (z from 0 to 12).
+constexpr int kTailPerUnit = 256;
+constexpr int kTailN = 12 * kTailPerUnit + 1;
 
 // Per-block sigma scales.  Estimate mode (kv, mu set): choose each group's
 // scale byte from the residuals; load mode (in set): read them from the
@@ -151,6 +155,7 @@ struct ScaleLaunch {
 cudaError_t upload_tables(const uint32_t *phi_knots, const float *lo8, const float *hinv_bf16,
                           const float *hinv_e4m3);
 cudaError_t upload_scale_mult(const float *mult);
+cudaError_t upload_tail_table(const float *log2_q);  // kTailN values
 cudaError_t launch_scales(const ScaleLaunch &a, cudaStream_t s);
 
 // Model preparation: sigma validation, per-channel reciprocals, E_q checks and
