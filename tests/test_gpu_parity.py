@@ -182,3 +182,28 @@ def test_ideal_bits_case_edges(oracle_mod):
            .numpy().view(np.uint16))
     _roundtrip(oracle_mod, _custom(synth.E4M3, kv8, mu8, sig8, T=T, D=D, Tb=32, G=4),
                max_overhead=1.0)
+
+
+def test_ideal_bits_e4m3_narrow_bins(oracle_mod):
+    """e4m3 bins 0.0095 to 1 sigma wide (both sides of the kernel's 0.01 sigma
+    cut-off between its tail table and the full evaluation), mu within two
+    sigma of the bin's lower edge: one-sided and straddling bins near z = 0,
+    where the table's error bound is tightest.  Per-scalar ideal bits against
+    the oracle."""
+    rng = np.random.default_rng(12)
+    T, D = 64, 64
+    n = 2 * T * D
+    normal = np.array([u for u in range(0x08, 0x7F)] + [u | 0x80 for u in range(0x08, 0x7F)], dtype=np.uint8)
+    codes = rng.choice(normal, 2 * D)
+    r = np.array([oracle_mod.rank(1, int(u)) for u in codes])
+    width = np.array([oracle_mod.lo(1, int(q) + 1) - oracle_mod.lo(1, int(q)) for q in r])
+    lo = np.array([oracle_mod.lo(1, int(q)) for q in r])
+    w_target = rng.choice([0.0095, 0.0099, 0.0101, 0.0105, 0.02, 0.05, 0.2, 1.0], 2 * D)
+    sig = width / w_target
+    ch = (np.arange(n) // (T * D)) * D + np.arange(n) % D
+    kv8 = codes[ch].astype(np.uint8)
+    mu_v = lo[ch] + rng.uniform(-2.0, 2.0, n) * sig[ch]
+    mu8 = (torch.from_numpy(mu_v.astype(np.float32)).to(torch.bfloat16).view(torch.int16)
+           .numpy().view(np.uint16))
+    _roundtrip(oracle_mod, _custom(synth.E4M3, kv8, mu8, sig, T=T, D=D, Tb=32, G=4),
+               max_overhead=1.0)
