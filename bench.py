@@ -144,8 +144,8 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-# Algorithmic work per scalar, in thread-instructions (SURVEY's per-unit
-# figures for this path): one cum evaluation is about 50 (bf16: two Phi_q, one
+# Algorithmic work per scalar, in thread-instructions (the per-unit figures of
+# this path): one cum evaluation is about 50 (bf16: two Phi_q, one
 # E_q load, the integer mix) or 25 (e4m3); encode = 2 evaluations + the 64/32
 # divide + renormalisation = 200 / 130; decode's minimum = the 2 evaluations
 # that verify the symbol + the state update, the stream read and the store =
