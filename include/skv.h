@@ -30,7 +30,9 @@
  * u64 offsets[num_chunks + 1] and the chunk payloads; see skv_encode.
  *
  * Conventions for every call below.
- *   - Pointers are DEVICE pointers unless marked "host".  The caller owns every
+ *   - Pointers are DEVICE pointers unless marked "host": device memory, or
+ *     pinned host memory mapped into the device's address space, which the
+ *     kernels then read or write over the CPU-GPU link.  The caller owns every
  *     buffer; no call allocates memory.
  *   - Tensors are row-major [layers][2][heads][tokens][head_dim]: KV is bf16
  *     bit patterns (uint16) or e4m3 codes (uint8); mu is always bf16.
