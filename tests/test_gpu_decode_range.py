@@ -165,3 +165,27 @@ def test_page_errors_and_corruption_reach_the_status():
     codec.decode_range(buf, nb, 0, nc, mu, out, first=True)
     codec.decode_status()
     assert torch.equal(out, kv)
+
+
+@pytest.mark.parametrize("name,kw", [("qwen3-0.6b-bf16", dict(L=1, H=2, T=600, calib_draws=2)),
+                                     ("qwen3-8b-e4m3", dict(L=2, H=1, T=300, Tb=64, G=4))])
+def test_pinned_host_buffers(name, kw):
+    """Pinned host memory mapped into the device's address space works wherever a
+    device pointer is taken: encode reading KV and mu from host memory gives the
+    same container as from device memory, ideal bits the same total, and the
+    decoder writing straight into a host buffer gives the input back."""
+    spec = synth.WORKLOADS[name].scaled(name="pin-" + name, **kw)
+    w = synth.make(spec)
+    codec = gpu_codec(w)
+    kv_d, mu_d = device_views(w)
+    ref, nref = codec.encode(kv_d, mu_d)
+    ref = ref[:nref].clone()
+    kv_h = kv_d.cpu().pin_memory()
+    mu_h = mu_d.cpu().pin_memory()
+    box, nb = codec.encode(kv_h, mu_h)
+    assert nb == nref and torch.equal(box[:nb], ref)
+    assert codec.ideal_bits(kv_h, mu_h) == codec.ideal_bits(kv_d, mu_d)
+    out_h = torch.empty(kv_d.numel(), dtype=kv_d.dtype).pin_memory()
+    codec.decode(box, nb, mu_d, out=out_h)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, kv_d.cpu())
