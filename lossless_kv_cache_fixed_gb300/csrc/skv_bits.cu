@@ -153,8 +153,13 @@ __device__ __forceinline__ bool ideal_series_bf16(float lo, float hi, float mu, 
                               he2 * (1.0f / 24.0f));
     return w * 0.39894228f * __expf(-0.5f * z2) * (1.0f + y);  // w phi(zm) (1 + y)
   };
-  const float q = fmaf(0.95f, comp(w, zm),
-                       fmaf(0.03f, comp(w * (1.0f / 3.0f), zm * (1.0f / 3.0f)), 0.02f * ph));
+  // the 3 sigma component has w/3 < 1/3 and (w/3) |zm/3| < 2/9, where its He4
+  // and He6 terms stay below 1.9e-5 and 6e-8 relative: He2 alone
+  const float w3 = w * (1.0f / 3.0f), z3 = zm * (1.0f / 3.0f);
+  const float z32 = z3 * z3, w32 = w3 * w3;
+  const float c3 = w3 * 0.39894228f * __expf(-0.5f * z32) *
+                   fmaf(w32 * (1.0f / 24.0f), z32 - 1.0f, 1.0f);
+  const float q = fmaf(0.95f, comp(w, zm), fmaf(0.03f, c3, 0.02f * ph));
   bits = -__log2f(q);
   return true;
 }
