@@ -158,6 +158,12 @@ ALG_OPS = {2: {"encode": 200, "decode": 120, "ideal_bits": 100},
            # decode = the table bracket + ~6 bisection steps + 2 evaluations +
            # the state update = 90; ideal bits = one log2 = 20
            "o0": {"encode": 100, "decode": 90, "ideal_bits": 20}}
+OPS_BASIS = {
+    "encode": "per scalar: 2 cum evaluations, the 64/32 divide, renormalisation",
+    "decode": "per scalar, the algorithmic minimum: the 2 cum evaluations that verify the "
+              "symbol, the state update, the stream read and the store (a 16-step "
+              "bisection would add ~15 evaluations)",
+    "ideal_bits": "per scalar: the Gaussian bin masses, the p-hat term and the logarithm"}
 KERNEL = {"encode": "k_encode", "decode": "k_decode", "ideal_bits": "k_ideal"}
 KERNEL_O0 = {"encode": "k_encode", "decode": "k_decode_o0", "ideal_bits": "k_ideal"}
 
@@ -197,7 +203,7 @@ def roofline(med_ms, n, container_bytes, bps, workload, order0=False):
     roof = {"bound": "alu", "kernel": kname[top], "achieved": round(achieved, 1),
             "peak": round(peak_ops, 1), "unit": "Gop/s", "frac": round(achieved / peak_ops, 4),
             "traffic": load_traffic(kname[top], workload),
-            "ops_per_scalar": ops_tab[top],
+            "ops_per_scalar": ops_tab[top], "ops_basis": OPS_BASIS[top],
             "peak_source": "%d SMs x 128 lanes x %.0f MHz (issue peak)" % (sms, mhz),
             "hbm": {"achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                     "frac": round(gbs / hbm_peak, 4),
