@@ -35,6 +35,12 @@ __device__ float2 g_hinv[2][kHinvN + 1];
 constexpr int kCodeThreads = 768;
 constexpr size_t kCodeSmem = sizeof(uint2) * kPhiKnots + sizeof(float) * 256;
 constexpr int kDecThreads = 768;
+// Decode blocks of launches with several rounds of tasks: as many warps as the
+// registers allow (65,536 per SM; bf16 64 a thread: 28 warps, e4m3 56: 32),
+// which the decoder's latency uses (32B bf16 decode 129 -> 143 GB/s, 8B e4m3
+// 106 -> 125).  bf16 at 32 warps would drop to 62 registers and lost 3%.
+template <int DT>
+constexpr int dec_threads_max() { return DT == 0 ? 896 : 1024; }
 constexpr size_t kDecSmem = kCodeSmem + sizeof(float2) * (kHinvN + 1) + sizeof(int32_t) * (kHinvN + 1);
 
 cudaError_t upload_tables(const uint32_t *T, const float *lo8, const float *hb, const float *he) {
@@ -441,9 +447,16 @@ __global__ void __launch_bounds__(256) k_compact(EncodeLaunch a) {
 // that launches on other streams (a cache coded as four layer groups side by
 // side: a quarter each) get SMs of their own rather than sharing theirs: a
 // block holds 65-79 KiB of tables, so few fit per SM.
-static void task_shape(int64_t ntasks, int max_threads, int &blocks, int &threads) {
+static void task_shape(int64_t ntasks, int max_threads, int &blocks, int &threads,
+                       int multi_round_threads = 0) {
   const int64_t sms = (int64_t)device_sm_count();
   const int64_t wmax = max_threads / 32;
+  if (multi_round_threads > max_threads && ntasks > sms * wmax) {
+    // more tasks than one round of full blocks: larger blocks where they fit
+    blocks = (int)sms;
+    threads = multi_round_threads;
+    return;
+  }
   if (8 * ntasks >= sms * wmax) {
     const int64_t want = (ntasks + wmax - 1) / wmax;
     blocks = (int)(want < sms ? want : sms);
@@ -599,7 +612,7 @@ __device__ __forceinline__ int64_t next_task(WsHead *h, int64_t nwarps) {
 }
 
 template <int DT, bool BISECT>
-__global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
+__global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunch a) {
   extern __shared__ uint2 s_phi[];
   float *s_lo8 = reinterpret_cast<float *>(s_phi + kPhiKnots);
   float2 *s_hinv = reinterpret_cast<float2 *>(s_lo8 + 256);
@@ -880,7 +893,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) k_decode(DecodeLaunch a) {
 //   E_q[r*] < (slot + 1) 2^26 / K       ->  r* < einv[floor((slot + 1) n / K) + 1]
 //   E_q[r* + 1] > (slot - |S|) 2^26 / K ->  r* >= einv[floor((slot - |S|) n / K)] - 1,
 // a bracket of one or two table steps, which bisection finishes.
-__global__ void __launch_bounds__(kDecThreads, 1) k_decode_o0(DecodeLaunch a) {
+__global__ void __launch_bounds__(dec_threads_max<0>(), 1) k_decode_o0(DecodeLaunch a) {
   extern __shared__ int32_t s_einv0[];
   if (!a.einv_row_stride)  // one table for all chunks: stage it once per SM
     for (int i = threadIdx.x; i <= kO0InvN; i += blockDim.x) s_einv0[i] = a.einv[i];
@@ -1003,7 +1016,8 @@ cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int64_t ntasks = (((a.c_end - a.c_begin + a.c_step - 1) / a.c_step) * a.geo.G + 31) / 32;
   int blocks, threads;
-  task_shape(ntasks, kDecThreads, blocks, threads);
+  task_shape(ntasks, kDecThreads, blocks, threads,
+             a.dtype == 0 ? dec_threads_max<0>() : dec_threads_max<1>());
   if (a.order0) {
     constexpr size_t smem = sizeof(int32_t) * (kO0InvN + 1);
     e = cudaFuncSetAttribute(k_decode_o0, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
