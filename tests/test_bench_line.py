@@ -1,0 +1,82 @@
+"""The bench line's assembly on CPU: the roofline arithmetic, the clock record
+and the keys of the JSON line, with the device queries replaced by fixed
+values (no GPU is used)."""
+import argparse
+import types
+
+import pytest
+
+import bench
+import synth
+
+N = 28 * 2 * 8 * 4096 * 128
+MED = {"encode": 2.25, "decode": 4.05, "ideal_bits": 1.38}
+
+
+@pytest.fixture
+def fixed_peaks(monkeypatch):
+    monkeypatch.setattr(bench, "issue_peak_gops", lambda: (152 * 128 * 2070.0 * 1e6 / 1e9, 152, 2070.0))
+    monkeypatch.setattr(bench, "measured_peaks", lambda: (6775.3, "measured"))
+    monkeypatch.setattr(bench, "load_traffic", lambda kernel, workload: 1_076_000_000)
+
+
+def test_roofline_arithmetic(fixed_peaks):
+    nb = 168_754_632
+    roof, kernels = bench.roofline(MED, N, nb, 2, "qwen3-0.6b-bf16")
+    peak = 152 * 128 * 2070.0 * 1e6 / 1e9
+    assert roof["kernel"] == "k_decode" and roof["bound"] == "alu" and roof["unit"] == "Gop/s"
+    achieved = 120 * N / (4.05e-3) / 1e9
+    assert roof["achieved"] == pytest.approx(achieved, rel=1e-4)
+    assert roof["frac"] == pytest.approx(achieved / peak, abs=1e-4)
+    assert roof["ops_per_scalar"] == 120 and "minimum" in roof["ops_basis"]
+    assert roof["traffic"] == 1_076_000_000
+    # HBM view: the container, mu and the decoded cache per scalar
+    assert roof["hbm"]["algorithmic_bytes_per_scalar"] == pytest.approx(nb / N + 2 + 2, abs=1e-4)
+    assert roof["hbm"]["peak"] == 6775.3
+    for op, ms in MED.items():
+        ops = bench.ALG_OPS[2][op] * N / (ms * 1e-3) / 1e9
+        assert kernels[op]["alu_frac"] == pytest.approx(ops / peak, abs=1e-4)
+    # e4m3 and the order-0 baseline take their own per-unit figures
+    roof8, _ = bench.roofline(MED, N, nb // 3, 1, "qwen3-8b-e4m3")
+    assert roof8["ops_per_scalar"] == 70
+    roof0, k0 = bench.roofline(MED, N, nb * 2, 2, "qwen3-0.6b-bf16", order0=True)
+    assert roof0["kernel"] == "k_decode_o0" and roof0["ops_per_scalar"] == 90
+    assert roof0["hbm"]["algorithmic_bytes_per_scalar"] == pytest.approx(2 * nb / N + 2, abs=1e-4)
+
+
+def test_clock_record_median_and_reasons():
+    c = bench.ClockSampler(0)
+    c.lines = ["0, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "0, 2055, 2070, 1100.0, 0x4, Not Active, Not Active, Not Active, Active",
+               "0, 2070, 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "garbage line"]
+    s = c.summary()
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert bench.ClockSampler(0).summary() is None
+
+
+def test_json_line_keys(fixed_peaks):
+    spec = synth.WORKLOADS["qwen3-0.6b-bf16"]
+    args = argparse.Namespace(workload=spec.name, steps=30, warmup=3, no_cpu_baseline=True,
+                              order0=False, adaptive=False, block_scale=False)
+    clk = types.SimpleNamespace(summary=lambda: {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0,
+                                                 "reasons": [], "samples": 2})
+    e2e = {"value": 40.0, "unit": "GB/s", "h2d_bytes_per_step": 2 * N + 2 * N,
+           "d2h_bytes_per_step": 168_754_632 + 2 * N}
+    nb, bits = 168_754_632, 5.722 * N
+    line = bench.finish_line(args, 0, 1, spec, N, nb, bits, 2, 7.68, 2 * N / 7.68e-3 / 1e9,
+                             [MED["encode"]] * 3, [MED["decode"]] * 3, [MED["ideal_bits"]] * 3,
+                             clk, e2e, None)
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
+        assert k in line, k
+    assert line["metric"] == bench.METRIC and line["unit"] == "GB/s" and line["n_gpus"] == 1
+    assert line["higher_is_better"] is True and line["scaling"] == "weak"
+    assert line["config"]["workload"] == spec.name
+    assert line["gpu_launches"] == 12 * 30   # 12 kernels per bf16 step
+    assert line["bits_per_scalar"] == pytest.approx(8.0 * nb / N, abs=1e-5)
+    for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
+        assert k in line["roofline"], k
+    assert bench.finish_line(args, 1, 2, spec, N, nb, bits, 2, 7.68, 1.0, [1.0], [1.0], [1.0],
+                             clk, e2e, None) is None   # only rank 0 prints
