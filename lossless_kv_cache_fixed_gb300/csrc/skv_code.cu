@@ -14,8 +14,10 @@
 // reads mu a symbol at a time (fewer live registers) and writes each group's
 // 8 decoded symbols as one vector.  Warps loop over 32-lane tasks (the decoder
 // hands out tasks after the first round from an atomic counter); the grid has
-// at most one 768-thread block per SM.  The Phi knot table (64 KiB), the e4m3
-// bin edges and the decoder's guess tables sit in shared memory, once per SM.
+// at most one block per SM (768 threads; smaller blocks spread a small launch
+// over all SMs, larger ones carry decode launches with several rounds of tasks:
+// task_shape).  The Phi knot table (64 KiB), the e4m3 bin edges and the
+// decoder's guess tables sit in shared memory, once per SM.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -29,7 +31,7 @@ __device__ uint2 g_phi[kPhiKnots];
 __device__ float g_lo8[256];
 __device__ float2 g_hinv[2][kHinvN + 1];
 
-// At most one resident block per SM, of up to 24 warps: a single copy of the
+// At most one resident block per SM (24 warps as a rule): a single copy of the
 // tables per SM leaves the rest of the unified L1 / shared memory to the L1
 // cache (the p-hat prefix table, mu, the streams).  See task_shape.
 constexpr int kCodeThreads = 768;

@@ -148,14 +148,6 @@ __device__ __forceinline__ int64_t est_div48(int64_t y, float rf) {
   return neg ? -q : q;
 }
 
-// floor(x / f) and x mod f for x < 2^63 and 1 <= f <= 2^28, without the FP64
-// division routine.  For M <= 16 exact integer steps (above); otherwise, starting
-// from y = x with |x/f| < 2^(63 - M), the error bound of the estimates gives:
-//   M = 28: <= 5 * 2^11 + 1, then <= 1.003 after one refinement;
-//   M = 16: <= 5 * 2^23 + 1, then <= 13.3, then <= 1.001 after two.
-// The remainder after the first estimate is below (5 * 2^23 + 1) 2^16 and
-// (5 * 2^11 + 1) 2^28, both < 2^42, so the refinements take two limbs.  The
-// remainder is then within 3f of [0, f), and the loops below fix it.
 // floor(n / f), n mod f for n < 2^32 from m = floor((2^32 - 1) / f): the
 // multiply-high estimate is at most one below the quotient.
 __device__ __forceinline__ uint32_t div32_recip(uint32_t n, uint32_t f, uint32_t m, uint32_t &r) {
@@ -168,6 +160,13 @@ __device__ __forceinline__ uint32_t div32_recip(uint32_t n, uint32_t f, uint32_t
   return q;
 }
 
+// floor(x / f) and x mod f for x < 2^63 and 1 <= f <= 2^M, without the FP64
+// division routine.  M <= 16 (e4m3): exact 32-bit steps.  Otherwise, from
+// y = x with |x/f| < 2^(63 - M), the estimates' error bound gives, for M = 28
+// (bf16), <= 5 * 2^11 + 1 and then <= 1.003 after one refinement (M from 17 to
+// 23 would take two); the remainder after the first estimate is below
+// (5 * 2^11 + 1) 2^28 < 2^42, so the refinement takes two limbs.  The remainder
+// is then within 3f of [0, f), and the loops below fix it.
 template <int M>
 __device__ __forceinline__ uint64_t divmod_u64(uint64_t x, uint32_t f, uint64_t &rem) {
   if (M <= 16) {
