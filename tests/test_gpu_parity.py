@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import container_chunk, device_views, gpu_codec, host_views, oracle_model
+from gpu_helpers import device_views, gpu_codec, host_views, oracle_model
 
 pytestmark = pytest.mark.gpu
 

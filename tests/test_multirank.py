@@ -4,7 +4,6 @@ over ranks and the value sums all ranks' bytes."""
 import os
 import socket
 
-import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp

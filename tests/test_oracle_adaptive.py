@@ -9,7 +9,6 @@ the integer truncation bound); the static prefix table (the first block);
 learning on a stationary 64-symbol source whose entropy is 6 bits; adaptation
 after a switch of source; round trips and model separation.
 """
-import math
 
 import numpy as np
 import pytest

@@ -8,7 +8,6 @@ import json
 import os
 
 import numpy as np
-import pytest
 import torch
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
