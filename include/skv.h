@@ -43,7 +43,10 @@
  *     the workspace and reported at the end of the call; the library never
  *     traps the GPU.
  *   - The first call on a device uploads the model constants to that device
- *     (a synchronous copy), so make one call before any stream capture.
+ *     (a synchronous copy), so make one call before any stream capture.  The
+ *     library remembers per device that this was done (and, for
+ *     skv_ideal_bits_noalloc, where its scratch array lives), so it must not
+ *     be used across a cudaDeviceReset of a device it has already run on.
  *   - Calls on different streams must use different workspaces.
  */
 #ifndef SKV_H
@@ -72,7 +75,12 @@ typedef enum {
   SKV_ERR_CUDA = -6       /* a CUDA runtime error */
 } skv_status;
 
-typedef enum { SKV_OP_ENCODE = 0, SKV_OP_DECODE = 1, SKV_OP_IDEAL_BITS = 2 } skv_op;
+typedef enum {
+  SKV_OP_ENCODE = 0,
+  SKV_OP_DECODE = 1,
+  SKV_OP_IDEAL_BITS = 2,
+  SKV_OP_MODEL_BITS = 3
+} skv_op;
 
 /* Tensor shape.  kv must be 2 (keys and values); head_dim a multiple of 8. */
 typedef struct {
@@ -231,6 +239,27 @@ int skv_decode_status(const void *workspace, skv_stream_t stream);
  * Requires params->phat for bf16.  Errors: SKV_ERR_ARG, SKV_ERR_CAPACITY
  * (workspace), SKV_ERR_SYMBOL, SKV_ERR_PARAM, SKV_ERR_CUDA.  Synchronizes. */
 int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void *kv,
+                   const uint16_t *mu, float *per_scalar, double *total, void *workspace,
+                   size_t workspace_bytes, skv_stream_t stream);
+
+/* Model cost: the code length the coder's own integer frequencies give,
+ * sum over scalars of M - log2(freq), freq = cum(r + 1) - cum(r) exactly as
+ * skv_encode computes it (with per-block scales, under the scales the
+ * encoder would choose).  This is what an ideal arithmetic coder with these
+ * frequencies would write; the rANS payload of a chunk exceeds it by 32 to 64
+ * bits per lane (initial state and flush), the container adds its header and
+ * offsets.  It differs from skv_ideal_bits where the continuous model gives a
+ * scalar less mass than the 1-in-2^M floor of the frequencies (e4m3 outliers
+ * far beyond 9 sigma), and by the rounding of the fixed-point model
+ * elsewhere.  (The pages' section "KV 缓存并非真正随机": the code length of a
+ * symbol is -log2 of its probability.)
+ *   per_scalar    device fp32 [N] output, or NULL.
+ *   total         host; receives the sum in bits (fp64, fixed order).
+ * Per-scalar values are fp32 (within 1e-6 relative + 1e-7 bits of exact).
+ * Workspace: skv_workspace_bytes(..., SKV_OP_MODEL_BITS).  Rejects
+ * SKV_FLAG_ADAPTIVE (SKV_ERR_ARG).  Errors: SKV_ERR_ARG, SKV_ERR_CAPACITY
+ * (workspace), SKV_ERR_SYMBOL, SKV_ERR_PARAM, SKV_ERR_CUDA.  Synchronizes. */
+int skv_model_bits(const skv_params *params, const skv_shape *shape, const void *kv,
                    const uint16_t *mu, float *per_scalar, double *total, void *workspace,
                    size_t workspace_bytes, skv_stream_t stream);
 

@@ -15,7 +15,7 @@ import os
 from .build import LIB, build  # noqa: F401
 
 SKV_BF16, SKV_E4M3 = 0, 1
-SKV_OP_ENCODE, SKV_OP_DECODE, SKV_OP_IDEAL_BITS = 0, 1, 2
+SKV_OP_ENCODE, SKV_OP_DECODE, SKV_OP_IDEAL_BITS, SKV_OP_MODEL_BITS = 0, 1, 2, 3
 SKV_FLAG_DECODE_BISECT = 1
 SKV_FLAG_BLOCK_SCALE = 2
 SKV_FLAG_ORDER0 = 4
@@ -26,7 +26,8 @@ SKV_ERR_PARAM, SKV_ERR_CORRUPT, SKV_ERR_CUDA = -4, -5, -6
 NSYM = {SKV_BF16: 65282, SKV_E4M3: 254}
 
 EXPORTS = ("skv_max_encoded_bytes", "skv_workspace_bytes", "skv_encode", "skv_decode",
-           "skv_decode_range", "skv_decode_status", "skv_ideal_bits", "skv_ideal_bits_noalloc", "skv_ideal_bits_noalloc_max_channels",
+           "skv_decode_range", "skv_decode_status", "skv_ideal_bits", "skv_model_bits",
+           "skv_ideal_bits_noalloc", "skv_ideal_bits_noalloc_max_channels",
            "skv_build_ecdf", "skv_phi_table", "skv_strerror", "skv_version")
 
 
@@ -68,6 +69,7 @@ def lib():
                                            C.c_uint64, C.c_int, vp, sz, vp]),
             "skv_decode_status": (C.c_int, [vp, vp]),
             "skv_ideal_bits": (C.c_int, [P, S, vp, vp, vp, C.POINTER(C.c_double), vp, sz, vp]),
+            "skv_model_bits": (C.c_int, [P, S, vp, vp, vp, C.POINTER(C.c_double), vp, sz, vp]),
             "skv_ideal_bits_noalloc": (C.c_int, [P, S, vp, vp, vp, C.POINTER(C.c_double), vp]),
             "skv_ideal_bits_noalloc_max_channels": (sz, []),
             "skv_build_ecdf": (C.c_int, [vp, vp, vp]),
@@ -121,6 +123,14 @@ def skv_ideal_bits(params, shape, kv_ptr, mu_ptr, per_scalar_ptr, ws_ptr, ws_byt
     """Returns (status, total bits)."""
     tot = C.c_double(0)
     rc = lib().skv_ideal_bits(C.byref(params), C.byref(shape), kv_ptr, mu_ptr, per_scalar_ptr,
+                              C.byref(tot), ws_ptr, ws_bytes, stream)
+    return rc, tot.value
+
+
+def skv_model_bits(params, shape, kv_ptr, mu_ptr, per_scalar_ptr, ws_ptr, ws_bytes, stream):
+    """Returns (status, total bits under the coder's own frequencies)."""
+    tot = C.c_double(0)
+    rc = lib().skv_model_bits(C.byref(params), C.byref(shape), kv_ptr, mu_ptr, per_scalar_ptr,
                               C.byref(tot), ws_ptr, ws_bytes, stream)
     return rc, tot.value
 
@@ -265,4 +275,17 @@ class Codec:
                                  ws.numel(), _stream_handle(stream))
         if rc:
             raise SkvError(rc, "skv_ideal_bits")
+        return (tot, ps) if per_scalar else tot
+
+    def model_bits(self, kv, mu, per_scalar=False, stream=None):
+        """Code length under the coder's own frequencies: total (and per scalar)."""
+        ws = self.workspace(SKV_OP_MODEL_BITS)
+        ps = None
+        if per_scalar:
+            ps = self.torch.empty(self.n, dtype=self.torch.float32, device=self.device)
+        rc, tot = skv_model_bits(self.params, self.shape, kv.data_ptr(), _ptr(mu),
+                                 ps.data_ptr() if ps is not None else None, ws.data_ptr(),
+                                 ws.numel(), _stream_handle(stream))
+        if rc:
+            raise SkvError(rc, "skv_model_bits")
         return (tot, ps) if per_scalar else tot

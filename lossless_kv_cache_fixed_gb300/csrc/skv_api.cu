@@ -22,6 +22,10 @@ namespace {
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+// The workspace head takes the first kAlign-byte slot of every workspace.
+static_assert(sizeof(WsHead) <= kAlign, "the workspace head must fit one aligned slot");
+// Most blocks of the ideal-bits kernel (one fp64 partial sum each).
+constexpr int64_t kMaxBitsBlocks = 4096;
 
 // ---- host-built model constants ----
 
@@ -121,6 +125,7 @@ struct Plan {
   size_t off_enc_cinv, off_enc_words, enc_total;  // encode: per-chunk tables after the stacks
   size_t off_dec_cinv, dec_total;                 // decode: after the inverse p-hat table
   size_t off_bits_csig, bits_total;               // ideal bits: after the partial sums
+  size_t off_mb_cinv, mb_total;                   // model bits: reciprocals per (chunk, channel)
   int64_t stride;  // words per chunk stack
   int bits_blocks;
 };
@@ -190,7 +195,7 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   pl.total = off;
   int64_t n8 = pl.geo.n / 8;
   int64_t nb = (n8 + 255) / 256;
-  pl.bits_blocks = (int)(nb < 4096 ? (nb > 0 ? nb : 1) : 4096);
+  pl.bits_blocks = (int)(nb < kMaxBitsBlocks ? (nb > 0 ? nb : 1) : kMaxBitsBlocks);
   pl.off_bits = align_up(pl.off_inv + sizeof(float2) * (size_t)pl.nsig);
   pl.off_einv = pl.off_bits;  // decode only: the inverse p-hat table follows the reciprocals
   // per-block scales: (chunk, channel) tables appended to each operation's layout
@@ -203,6 +208,8 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   pl.dec_total = align_up(pl.off_dec_cinv + sizeof(float2) * ccells);
   pl.off_bits_csig = align_up(pl.off_bits + sizeof(double) * (size_t)pl.bits_blocks);
   pl.bits_total = align_up(pl.off_bits_csig + sizeof(float) * ccells);
+  pl.off_mb_cinv = pl.off_bits_csig;
+  pl.mb_total = align_up(pl.off_mb_cinv + sizeof(float2) * ccells);
   // adaptive counts: per-row P, C, E (and decode's inverse tables), the token
   // weights and the ideal-bits partial sums, appended to each operation's layout
   pl.ad_bx = (int)std::min<int64_t>(16, (tb_eff * s->head_dim + 2047) / 2048);
@@ -231,6 +238,7 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
 size_t ws_bytes_for(const Plan &pl, int op) {
   if (op == SKV_OP_ENCODE) return pl.enc_total;
   if (op == SKV_OP_DECODE) return pl.dec_total;
+  if (op == SKV_OP_MODEL_BITS) return pl.mb_total;
   return pl.bits_total;
 }
 
@@ -379,6 +387,10 @@ int decode_enqueue(const skv_params *params, const Plan &pl, const void *in, siz
 // the per-channel reciprocal table, then the per-block fp64 partial sums.
 constexpr size_t kNoallocBytes = 2u << 20;  // 2 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
+// sigma entries that fit beside the head and the largest partial-sum array,
+// whatever the token count (bits_blocks never exceeds kMaxBitsBlocks)
+constexpr size_t kNoallocMaxChannels =
+    (kNoallocBytes - 2 * kAlign - sizeof(double) * kMaxBitsBlocks) / sizeof(float2);
 std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[1024];
 
@@ -411,7 +423,7 @@ size_t skv_max_encoded_bytes(const skv_params *params, const skv_shape *shape) {
 size_t skv_workspace_bytes(const skv_params *params, const skv_shape *shape, int op) {
   Plan pl;
   if (make_plan(params, shape, &pl) != SKV_OK) return 0;
-  if (op < SKV_OP_ENCODE || op > SKV_OP_IDEAL_BITS) return 0;
+  if (op < SKV_OP_ENCODE || op > SKV_OP_MODEL_BITS) return 0;
   return ws_bytes_for(pl, op);
 }
 
@@ -614,6 +626,58 @@ int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void 
   return SKV_OK;
 }
 
+int skv_model_bits(const skv_params *params, const skv_shape *shape, const void *kv,
+                   const uint16_t *mu, float *per_scalar, double *total, void *workspace,
+                   size_t workspace_bytes, skv_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  // adaptive tables change from one token block to the next: no single pass
+  if (pl.adaptive) return SKV_ERR_ARG;
+  if ((rc = common_inputs(params, pl, kv, mu))) return rc;
+  if (!total || !workspace || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
+  if (per_scalar && !aligned(per_scalar, 16)) return SKV_ERR_ARG;
+  if (workspace_bytes < ws_bytes_for(pl, SKV_OP_MODEL_BITS)) return SKV_ERR_CAPACITY;
+  if ((rc = ensure_device_tables())) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  WsHead *head = reinterpret_cast<WsHead *>(ws);
+  if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
+  float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
+  const uint32_t *ecdf = pl.dtype == SKV_BF16 ? params->ecdf : nullptr;
+  // the same sigma and E_q checks as encode
+  if (launch_prep(params->sigma, pl.nsig_model, ecdf, inv, head, st) != cudaSuccess)
+    return SKV_ERR_CUDA;
+  ModelBitsLaunch a;
+  std::memset(&a, 0, sizeof(a));
+  a.geo = pl.geo;
+  a.dtype = pl.dtype;
+  a.order0 = pl.order0;
+  a.kv = kv;
+  a.mu = mu;
+  a.inv = inv;
+  if (pl.nsw) {
+    // the encoder's choice of scales, recomputed from the inputs
+    ScaleLaunch sl = scale_launch(pl, params, head);
+    sl.kv = kv;
+    sl.mu = mu;
+    sl.inv = reinterpret_cast<float2 *>(ws + pl.off_mb_cinv);
+    if (launch_scales(sl, st) != cudaSuccess) return SKV_ERR_CUDA;
+    a.inv_chunk = sl.inv;
+  }
+  a.ecdf = ecdf;
+  a.per_scalar = per_scalar;
+  a.partials = reinterpret_cast<double *>(ws + pl.off_bits);
+  a.nblocks = pl.bits_blocks;
+  a.head = head;
+  if (launch_model_bits(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  WsHead h;
+  if ((rc = read_head(head, &h, st))) return rc;
+  if ((rc = status_from_flags(h.flags))) return rc;
+  *total = h.bits;
+  return SKV_OK;
+}
+
 int skv_ideal_bits_noalloc(const skv_params *params, const skv_shape *shape, const void *kv,
                            const uint16_t *mu, float *per_scalar, double *total,
                            skv_stream_t stream) {
@@ -627,7 +691,9 @@ int skv_ideal_bits_noalloc(const skv_params *params, const skv_shape *shape, con
   if (pl.nsw || pl.order0) return SKV_ERR_ARG;
   if (per_scalar && !aligned(per_scalar, 16)) return SKV_ERR_ARG;
   if (pl.dtype == SKV_BF16 && (!params->phat || !aligned(params->phat, 4))) return SKV_ERR_ARG;
-  // the same layout as the workspace of skv_ideal_bits, inside the fixed array
+  // the same layout as the workspace of skv_ideal_bits, inside the fixed array;
+  // the sigma limit is the documented one, the byte check guards the layout
+  if ((size_t)pl.nsig > kNoallocMaxChannels) return SKV_ERR_CAPACITY;
   if (ws_bytes_for(pl, SKV_OP_IDEAL_BITS) > kNoallocBytes) return SKV_ERR_CAPACITY;
   if ((rc = ensure_device_tables())) return rc;
   uint8_t *ws = nullptr;
@@ -660,10 +726,7 @@ int skv_ideal_bits_noalloc(const skv_params *params, const skv_shape *shape, con
   return SKV_OK;
 }
 
-size_t skv_ideal_bits_noalloc_max_channels(void) {
-  // head + reciprocal table + the largest partial-sum array (4096 blocks)
-  return (kNoallocBytes - 2 * kAlign - sizeof(double) * 4096) / sizeof(float2);
-}
+size_t skv_ideal_bits_noalloc_max_channels(void) { return kNoallocMaxChannels; }
 
 int skv_build_ecdf(const uint64_t *counts, uint32_t *ecdf, float *phat) {
   if (!counts || !ecdf) return SKV_ERR_ARG;

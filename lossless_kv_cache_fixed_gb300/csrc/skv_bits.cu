@@ -11,7 +11,8 @@
 //   * bf16, w < 1 and w |zm| < 2 (about 99% of scalars): each Gaussian
 //     component's bin mass by the midpoint rule with Hermite corrections up to
 //     He6 (the first dropped term is below 3e-6 relative there), the mixture in
-//     the linear domain, one logarithm;
+//     the linear domain, one logarithm; narrow bins beyond 64 sigma cost p-hat's
+//     floor -log2(0.02 p-hat) (the Gaussian masses are negligible there);
 //   * bf16 otherwise (queued per warp): each component's mass as a difference
 //     of complementary error functions on the far side of mu, the mixture in
 //     the linear domain (p-hat's 0.02 floor keeps it a normal float);
@@ -130,7 +131,7 @@ __device__ __forceinline__ float gauss_mass(float lo, float hi, float mu, float 
   return 0.5f * (erfcf(a * 0.70710678f) - erfcf(b * 0.70710678f));
 }
 
-// bf16, the series case w < 1 and w |zm| < 2 (then w/3 and zm/3 qualify for
+// bf16, the series case w < 1 and w |zm| < 2, |zm| < 64 (then w/3 and zm/3 qualify for
 // the 3 sigma component too): the mixture in the linear domain, each component
 // w phi(zm) (1 + y) with the Hermite correction y of log2_gauss_series, then
 // one logarithm.  The first dropped term, He8 w^8 / 92897280, is at most
@@ -144,8 +145,17 @@ __device__ __forceinline__ bool ideal_series_bf16(float lo, float hi, float mu, 
   const float width = hi - lo;
   const float w = width * inv_s;
   const float zm = (lo + 0.5f * width - mu) * inv_s;
-  if (!(w < 1.0f && w * fabsf(zm) < 2.0f)) return false;
-  auto comp = [](float w, float zm) {
+  if (!(w < 1.0f)) return false;
+  if (!(fabsf(zm) < 64.0f)) {
+    // a narrow bin beyond 63.5 sigma (or whose centre's distance from mu
+    // overflows fp32): the 3-sigma component's mass is below 1e-98 and the
+    // narrow one's below that, under 1e-85 of p-hat's 0.02 floor (p-hat >=
+    // 2^-37), so q is that floor; the series below would compute 0 * inf there
+    bits = -__log2f(0.02f * ph);
+    return true;
+  }
+  if (!(w * fabsf(zm) < 2.0f)) return false;
+  auto comp =[](float w, float zm) {
     const float z2 = zm * zm, w2 = w * w;
     const float he2 = z2 - 1.0f, he4 = fmaf(z2, z2 - 6.0f, 3.0f);
     const float he6 = fmaf(z2, fmaf(z2, z2 - 15.0f, 45.0f), -15.0f);

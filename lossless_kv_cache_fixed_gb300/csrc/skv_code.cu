@@ -315,6 +315,106 @@ __global__ void __launch_bounds__(kCodeThreads, 1) k_encode(EncodeLaunch a) {
 }
 
 // ------------------------------------------------------------------------
+// Model bits: the code length of the coder's own integer frequencies, the
+// cost the rANS stream approaches (it adds at most 32 to 64 bits per lane for
+// the initial state and the flush).
+// ------------------------------------------------------------------------
+
+// -log2(f / 2^M) of a frequency 1 <= f < 2^M in fp32: above half the range
+// through log1p of the exact complement (a cost below one bit keeps its
+// relative accuracy), else M - log2 f.
+template <int M>
+__device__ __forceinline__ float code_length(uint32_t f) {
+  constexpr uint32_t one = 1u << M;
+  if (f > one / 2) return -1.44269504f * log1pf(-(float)(one - f) * (1.0f / (float)one));
+  return (float)M - log2f((float)f);
+}
+
+template <int DT, bool O0>
+__global__ void __launch_bounds__(256) k_model_bits(ModelBitsLaunch a) {
+  extern __shared__ uint2 s_phi[];
+  float *s_lo8 = reinterpret_cast<float *>(s_phi + kPhiKnots);
+  __shared__ double s_part[256];
+  stage_tables(s_phi, s_lo8);
+  constexpr int M = DT == 0 ? kMBf16 : kME4m3;
+  constexpr int32_t NS = DT == 0 ? kNsymBf16 : kNsymE4m3;
+  const uint64_t D = (uint64_t)a.geo.D, TD = (uint64_t)a.geo.T * D, cw = D * (uint64_t)a.geo.Tb;
+  const int64_t n8 = a.geo.n / 8;
+  double acc = 0.0;
+  uint32_t flags = 0;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < n8;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const uint64_t i0 = 8ull * (uint64_t)g;
+    const uint64_t row = i0 / TD, in_row = i0 - row * TD;
+    uint32_t sym[8], mub[8];
+    ChanInv inv[8];
+    load_syms<DT>(a.kv, i0, sym);
+    if (!O0) {
+      load_mu(a.mu, i0, mub);
+      const float2 *ip = a.inv_chunk ? a.inv_chunk + (row * (uint64_t)a.geo.ntb + in_row / cw) * D
+                                     : a.inv + row * D;
+      load_inv(ip, in_row % D, inv);
+    }
+    float bits[8], part = 0.0f;
+#pragma unroll 1
+    for (int k = 0; k < 8; ++k) {
+      int32_t r = DT == 0 ? rank_bf16(sym[k]) : rank_e4m3(sym[k]);
+      if (r < 0 || r >= NS) {
+        flags |= kFlagSymbol;
+        r = 0;
+      }
+      uint32_t c0, c1;
+      if (O0) {
+        c0 = cum_order0(r, a.ecdf);
+        c1 = cum_order0(r + 1, a.ecdf);
+      } else {
+        if (!mu_valid(mub[k])) {
+          flags |= kFlagParam;
+          mub[k] = 0;
+        }
+        const float muf = bf16_to_f32(mub[k]);
+        c0 = cum_of<DT>(r, muf, inv[k], s_phi, s_lo8, a.ecdf);
+        c1 = cum_of<DT>(r + 1, muf, inv[k], s_phi, s_lo8, a.ecdf);
+      }
+      bits[k] = code_length<M>(c1 - c0);
+      part += bits[k];
+    }
+    acc += (double)part;
+    if (a.per_scalar) {
+      float4 *o = reinterpret_cast<float4 *>(a.per_scalar + i0);
+      o[0] = make_float4(bits[0], bits[1], bits[2], bits[3]);
+      o[1] = make_float4(bits[4], bits[5], bits[6], bits[7]);
+    }
+  }
+  if (flags) atomicOr(&a.head->flags, flags);
+  s_part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int off = 128; off; off >>= 1) {
+    if (threadIdx.x < off) s_part[threadIdx.x] += s_part[threadIdx.x + off];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) a.partials[blockIdx.x] = s_part[0];
+}
+
+template <int DT, bool O0>
+static cudaError_t run_model_bits(const ModelBitsLaunch &a, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k_model_bits<DT, O0>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kCodeSmem);
+  if (e != cudaSuccess) return e;
+  k_model_bits<DT, O0><<<a.nblocks, 256, kCodeSmem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_model_bits(const ModelBitsLaunch &a, cudaStream_t s) {
+  cudaError_t e;
+  if (a.dtype == 0 && a.order0) e = run_model_bits<0, true>(a, s);
+  else if (a.dtype == 0) e = run_model_bits<0, false>(a, s);
+  else e = run_model_bits<1, false>(a, s);
+  if (e != cudaSuccess) return e;
+  return launch_ideal_final(a.partials, a.nblocks, a.head, s);
+}
+
+// ------------------------------------------------------------------------
 // Exclusive scan of chunk sizes: block-local scans, then the block totals.
 // ------------------------------------------------------------------------
 

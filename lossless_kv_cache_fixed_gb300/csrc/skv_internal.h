@@ -118,6 +118,23 @@ struct IdealLaunch {
   uint64_t td_rcp;           // floor((2^64 - 1) / (T * D)): row of a scalar by multiply-high
 };
 
+// Model bits: the code length -log2(freq / 2^M) of every scalar under the
+// coder's own integer frequencies, summed like the ideal bits.
+struct ModelBitsLaunch {
+  Geo geo;
+  int dtype;
+  int32_t order0;           // 1: order-0 baseline (kv only)
+  const void *kv;
+  const uint16_t *mu;
+  const float2 *inv;        // per-channel (1/sigma, 1/(3 sigma)) table in the workspace
+  const float2 *inv_chunk;  // per-block scales: the same per (chunk, channel), else null
+  const uint32_t *ecdf;
+  float *per_scalar;
+  double *partials;
+  int nblocks;
+  WsHead *head;
+};
+
 // Inverse of the model CDF's Gaussian part, G0(z) = 0.95 Phi(z) + 0.03 Phi(z/3)
 // (bf16) or Phi(z) (e4m3), tabulated at kHinvN + 1 equally spaced u in
 // [0, kHinvUmax[dtype]] as (z_k, z_{k+1} - z_k): the decoder's first guess.
@@ -185,6 +202,7 @@ cudaError_t launch_ideal_final(const double *partials, int n, WsHead *head, cuda
 cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, int n, cudaStream_t s);
 cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s);
 cudaError_t launch_ideal(const IdealLaunch &a, cudaStream_t s);
+cudaError_t launch_model_bits(const ModelBitsLaunch &a, cudaStream_t s);
 
 int device_sm_count();
 

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import device_views, gpu_codec
+from gpu_helpers import device_views, gpu_codec, oracle_model
 
 pytestmark = pytest.mark.gpu
 
@@ -96,7 +96,7 @@ def test_header_and_offset_tampering(enc):
     assert _decode_rc(P, codec, t, nb, mu)[0] == P.SKV_ERR_CORRUPT
 
 
-def test_model_mismatch(enc):
+def test_model_mismatch(enc, oracle_mod):
     P, w, codec, kv, mu, buf, nb = enc
     # one sigma one ulp off: the fingerprint in the header no longer matches
     sig = w.sigma.clone()
@@ -110,11 +110,33 @@ def test_model_mismatch(enc):
     w3 = synth.Workload(w.spec, w.kv, w.mu, w.sigma, cnt)
     rc, _ = _decode_rc(P, gpu_codec(w3), buf, nb, mu)
     assert rc == P.SKV_ERR_CORRUPT
-    # mu off by one ulp somewhere: an error or a different cache, never a fault
-    mu2 = mu.clone()
-    mu2[1234] ^= 1
-    rc, out = _decode_rc(P, codec, buf, nb, mu2)
-    assert rc in (P.SKV_OK, P.SKV_ERR_CORRUPT)
+    # mu off by one ulp somewhere: the decoder must do exactly what the oracle
+    # does with the same wrong mu (an error, or the same different cache),
+    # and never fault
+    O = oracle_mod
+    m = oracle_model(O, w)
+    kv_h = kv.cpu().numpy().view(np.uint16)
+    for pos in (1234, 77777):
+        mu2 = mu.clone()
+        mu2[pos] ^= 1
+        rc, out = _decode_rc(P, codec, buf, nb, mu2)
+        rc_o, out_o = O.decode(m, buf.cpu().numpy(), mu2.cpu().numpy().view(np.uint16))
+        assert rc == rc_o and rc in (P.SKV_OK, P.SKV_ERR_CORRUPT)
+        # the model at that scalar's true symbol changed, so a clean decode
+        # cannot return the input
+        sym = int(kv_h[pos])
+        r = O.rank(0, sym)
+        row = pos // (w.spec.T * w.spec.D) * w.spec.D + pos % w.spec.D
+        sg = float(w.sigma.reshape(-1)[row])
+        mu_a = O.bf16_value(int(mu[pos].item()) & 0xFFFF)
+        mu_b = O.bf16_value(int(mu2[pos].item()) & 0xFFFF)
+        changed = (O.cum(m, r, mu_a, sg), O.cum(m, r + 1, mu_a, sg)) != (
+            O.cum(m, r, mu_b, sg), O.cum(m, r + 1, mu_b, sg))
+        if rc == P.SKV_OK:
+            out_h = out.cpu().numpy().view(np.uint16)
+            assert np.array_equal(out_h, out_o)
+            if changed:
+                assert not np.array_equal(out_h, kv_h)
     test_clean_roundtrip_then_library_still_usable(enc)
 
 

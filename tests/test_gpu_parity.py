@@ -41,6 +41,7 @@ def _roundtrip(O, w, Tb=None, G=None, ideal=True, max_overhead=None):
     # the reference bisection search returns the same symbols
     ref = gpu_codec(w, Tb, G, flags=1).decode(buf, nb, mu_d)
     assert torch.equal(ref, kv_d)
+    _check_model_bits(O, codec, m, kv_d, mu_d, kv, mu, got)
     if ideal:
         tot, ps = codec.ideal_bits(kv_d, mu_d, per_scalar=True)
         ref_tot, ref = O.ideal_bits(m, kv, mu, per_scalar=True)
@@ -55,6 +56,35 @@ def _roundtrip(O, w, Tb=None, G=None, ideal=True, max_overhead=None):
             fixed = 512 + 64 * (nc + 1) + 64 * m.s.G * nc
             assert 8.0 * nb <= 1.005 * ref_tot + fixed
     return nb
+
+
+def _check_model_bits(O, codec, m, kv_d, mu_d, kv, mu, container):
+    """skv_model_bits against the oracle chunk by chunk, and the rANS length
+    invariant on the GPU's own container: every chunk's payload exceeds its
+    model bits by 32 to 64 bits per lane (initial state and flush)."""
+    tot, ps = codec.model_bits(kv_d, mu_d, per_scalar=True)
+    ps = ps.double().cpu().numpy()
+    assert abs(tot - ps.sum()) <= 1e-6 * abs(tot) + 1e-3
+    L, _, H, T, D = m.shape
+    Tb, G = m.s.Tb, m.s.G
+    ntb = (T + Tb - 1) // Tb
+    nc = m.num_chunks()
+    head = 64 + 8 * (nc + 1)
+    offs = container[64:head].view(np.uint64)
+    ref_tot = 0.0
+    for c in range(nc):
+        row, tb = divmod(c, ntb)
+        base = row * T * D + tb * Tb * D
+        n_c = min(Tb, T - tb * Tb) * D
+        ref = O.model_bits_chunk(m, kv, mu, c)
+        ref_tot += ref
+        got = ps[base:base + n_c].sum()
+        assert abs(got - ref) <= 1e-5 * ref + 1e-3, c
+        payload_bits = 8.0 * (int(offs[c + 1]) - int(offs[c]))
+        nsw = (D // 8 + 3) // 4 if m.s.block_scale else 0
+        extra = payload_bits - 32 * nsw - ref
+        assert 32 * G - 1e-3 * ref - 1 <= extra <= 64 * G + 1e-3 * ref + 1, c
+    assert abs(tot - ref_tot) <= 1e-6 * ref_tot + 1e-3
 
 
 def test_tiny_bf16_workload(oracle_mod):
@@ -108,7 +138,44 @@ def test_bf16_special_symbols(oracle_mod):
     mu = rng.choice(np.array([0x3F80, 0x0000, 0xC2C8, 0x0001, 0x7F7F, 0xFF7F], np.uint16), n)
     sigma = np.array([1e-30, 1e-8, 1.0, 1e30, 1.17549435e-38, 3.0, 0.5, 1e37] * 2)
     counts = rng.integers(0, 50, 65536).astype(np.uint64)
-    _roundtrip(oracle_mod, _custom(synth.BF16, kv, mu, sigma, counts), ideal=False)
+    # coded size against ideal: a random mix of specials under absurd sigma is
+    # far from the model, so only a loose bound applies
+    _roundtrip(oracle_mod, _custom(synth.BF16, kv, mu, sigma, counts), max_overhead=1.0)
+
+
+# every non-NaN bf16 pattern, in rank order: from -inf (0xFF80) down the
+# negative patterns to -0, then +0 up to +inf (0x7F80)
+_BF16_ALL = np.concatenate([np.arange(0xFF80, 0x7FFF, -1, dtype=np.int64),
+                            np.arange(0x0000, 0x7F81, dtype=np.int64)]).astype(np.uint16)
+
+# (sigma per channel, mu values): tiny to huge sigma, mu at zero, at the
+# smallest subnormals and at the largest finite values of both signs
+_ALPHABET_CASES = [
+    ([1.17549435e-38, 1e-30, 1e-8], [0x0000, 0x0001, 0x8001]),
+    ([1.0, 3.0, 0.01], [0x0000, 0x3F80, 0xC2C8, 0x4120]),
+    ([1e30, 1e37, 1e20], [0x7F7F, 0xFF7F, 0x0000]),
+    ([1e-8, 1.0, 1e37], [0x7F7F, 0x0001, 0xFF7F, 0x8001]),
+]
+
+
+@pytest.mark.parametrize("case", range(len(_ALPHABET_CASES)))
+def test_every_bf16_symbol(oracle_mod, case):
+    """All 65,282 non-NaN bf16 symbols, each twice in a seeded permutation, under
+    extreme sigma and mu: the GPU's cum and ideal bits reach every rank,
+    including the subnormal edges, +-max and +-inf."""
+    assert _BF16_ALL.size == 65282 and len(set(_BF16_ALL.tolist())) == 65282
+    sigmas, mus = _ALPHABET_CASES[case]
+    rng = np.random.default_rng(100 + case)
+    D = 64
+    T = (2 * _BF16_ALL.size + 2 * D - 1) // (2 * D)
+    n = 2 * T * D
+    kv = np.concatenate([rng.permutation(_BF16_ALL), rng.permutation(_BF16_ALL)])
+    kv = np.concatenate([kv, rng.choice(_BF16_ALL, n - kv.size)]).astype(np.uint16)
+    mu = rng.choice(np.array(mus, dtype=np.uint16), n).astype(np.uint16)
+    sigma = np.resize(np.array(sigmas, dtype=np.float64), 2 * D)
+    counts = rng.integers(0, 200, 65536).astype(np.uint64)
+    _roundtrip(oracle_mod, _custom(synth.BF16, kv, mu, sigma, counts, T=T, D=D, Tb=128, G=8),
+               max_overhead=1.0)
 
 
 def test_every_e4m3_symbol(oracle_mod):
