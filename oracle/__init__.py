@@ -86,6 +86,7 @@ def lib():
             "or_max_encoded_bytes": (u64, [P]),
             "or_encode": (C.c_int, [P, vp, vp, vp, u64, C.POINTER(u64)]),
             "or_check_header": (C.c_int, [P, vp, u64]),
+            "or_compare_chunks": (C.c_int, [P, vp, vp, vp, u64, u64, u64, C.POINTER(u64)]),
             "or_decode": (C.c_int, [P, vp, u64, vp, vp]),
             "or_scale_mult": (C.c_float, [i32]),
             "or_adaptive_table": (C.c_int, [P, vp, u64, vp, vp]),
@@ -225,6 +226,38 @@ def decode(model, buf, mu):
 def check_header(model, buf):
     buf = np.ascontiguousarray(buf, dtype=np.uint8)
     return lib().or_check_header(model.ref, _ptr(buf), buf.size)
+
+
+def compare_container(model, kv, mu, buf, threads=None, begin=0, end=None):
+    """Chunks [begin, end) of container `buf` (default: all) against the oracle's
+    encoding of each chunk, spread over the host cores (one slice of chunks per
+    task; each chunk is still coded single-threaded).  The header is checked
+    first.  Returns (status, first differing chunk or -1, threads used)."""
+    kv, mu = _as_sym(model, kv), _as_mu(model, mu)
+    buf = np.ascontiguousarray(buf, dtype=np.uint8)
+    L = lib()
+    rank(model.dtype, 0)          # the oracle's tables, built once before the threads
+    rc = L.or_check_header(model.ref, _ptr(buf), buf.size)
+    if rc:
+        return rc, -1, 1
+    nc = model.num_chunks()
+    end = nc if end is None else end
+    threads = threads or os.cpu_count() or 1
+    nslice = max(1, min(end - begin, 16 * threads))
+    cuts = [begin + (end - begin) * i // nslice for i in range(nslice + 1)]
+
+    def one(i):
+        bad = C.c_uint64(0)
+        r = L.or_compare_chunks(model.ref, _ptr(kv), _ptr(mu), _ptr(buf), buf.size, cuts[i],
+                                cuts[i + 1], C.byref(bad))
+        return r, (int(bad.value) if r else -1)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        res = list(ex.map(one, range(nslice)))
+    for r, bad in res:
+        if r:
+            return r, bad, threads
+    return OK, -1, threads
 
 
 def encode_chunk(model, kv, mu, c):

@@ -736,6 +736,41 @@ int or_encode(const or_model *m, const void *kv, const uint16_t *mu, uint8_t *ou
   return OR_OK;
 }
 
+/* Chunks [c0, c1) of a container (in, in_bytes), each against this oracle's
+ * own encoding of that chunk: OR_OK if every chunk's offsets and payload bytes
+ * are identical, else OR_ERR_CORRUPT with *bad the first chunk that differs.
+ * With c0 = 0 the offset table must start at 0, with c1 = the chunk count it
+ * must end at the payload size.  A loop over or_encode_chunk and a byte
+ * comparison: no arithmetic of its own (the header is or_check_header's). */
+int or_compare_chunks(const or_model *m, const void *kv, const uint16_t *mu, const uint8_t *in,
+                      uint64_t in_bytes, uint64_t c0, uint64_t c1, uint64_t *bad) {
+  int rc = or_model_check(m);
+  if (rc) return rc;
+  uint64_t nc = or_num_chunks(m);
+  uint64_t head = 64 + 8 * (nc + 1);
+  if (in_bytes < head || c1 > nc || c0 > c1) return OR_ERR_ARG;
+  uint64_t payload = in_bytes - head;
+  *bad = c0;
+  if (c0 == 0 && get64(in + 64) != 0) return OR_ERR_CORRUPT;
+  *bad = c1 ? c1 - 1 : 0;
+  if (c1 == nc && get64(in + 64 + 8 * nc) != payload) return OR_ERR_CORRUPT;
+  uint64_t cap = (uint64_t)m->Tb * (uint64_t)m->D + 2 * (uint64_t)m->G + scale_words(m);
+  uint32_t *tmp = (uint32_t *)malloc(sizeof(uint32_t) * cap);
+  if (!tmp) return OR_ERR_ARG;
+  for (uint64_t c = c0; c < c1; ++c) {
+    *bad = c;
+    uint64_t a = get64(in + 64 + 8 * c), b = get64(in + 64 + 8 * (c + 1)), nw = 0;
+    if (b < a || b > payload || (b - a) % 4) { free(tmp); return OR_ERR_CORRUPT; }
+    rc = or_encode_chunk(m, kv, mu, c, tmp, cap, &nw);
+    if (rc) { free(tmp); return rc; }
+    if (nw != (b - a) / 4) { free(tmp); return OR_ERR_CORRUPT; }
+    for (uint64_t i = 0; i < nw; ++i)
+      if (get32(in + head + a + 4 * i) != tmp[i]) { free(tmp); return OR_ERR_CORRUPT; }
+  }
+  free(tmp);
+  return OR_OK;
+}
+
 int or_check_header(const or_model *m, const uint8_t *in, uint64_t in_bytes) {
   if (in_bytes < 64) return OR_ERR_CORRUPT;
   uint8_t want[64];

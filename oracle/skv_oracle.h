@@ -45,6 +45,8 @@ uint64_t or_max_encoded_bytes(const or_model *m);
 int or_encode(const or_model *m, const void *kv, const uint16_t *mu, uint8_t *out, uint64_t cap,
               uint64_t *out_bytes);
 int or_check_header(const or_model *m, const uint8_t *in, uint64_t in_bytes);
+int or_compare_chunks(const or_model *m, const void *kv, const uint16_t *mu, const uint8_t *in,
+                      uint64_t in_bytes, uint64_t c0, uint64_t c1, uint64_t *bad);
 int or_decode(const or_model *m, const uint8_t *in, uint64_t in_bytes, const uint16_t *mu,
               void *kv_out);
 float or_scale_mult(int32_t s);

@@ -1,10 +1,22 @@
 """GPU parity at the full workload sizes, in the launch configuration bench.py
-times: the whole cache round-trips exactly on the device; an evenly spread
-sample of chunks is byte-identical to the oracle's encoding of those chunks;
-ideal bits match the oracle per scalar on the sampled chunks; the coded size is
-at most 1% over the summed ideal (except at 1K-scalar chunks, where the 32-64
-bit rANS flush per lane alone is ~2% of ~2.3 bits/scalar: reported, not a
-failure).
+times.
+
+* The whole cache round-trips exactly on the device (and with the bisection
+  reference search on the smaller caches).
+* Every chunk of the container is byte-identical to the oracle's encoding of
+  that chunk, checked on all host cores (oracle.compare_container), and the
+  header equals the oracle's.
+* Ideal bits match the oracle per scalar, and the coder's model bits
+  (skv_model_bits, sum of M - log2 freq) per chunk, on an evenly spread
+  sample of chunks.
+* Size: the rANS payload is at most 1% over the model bits (it adds 32 to 64
+  bits per lane for the initial state and the flush), except at 1K-scalar
+  chunks with one lane, where that flush alone is 1.5-3% of ~2.1 bits/scalar
+  (reported, not a failure).  bf16 containers are also at most 1% over the
+  summed ideal.  For e4m3 the continuous ideal is no bound: the bin-integrated
+  Gaussian of the pages' FP8 model gives the generator's 2% Laplace outliers
+  hundreds of ideal bits each, while the coder's frequencies stop at 1 in
+  2^16 (16 bits).
 
 Workloads (seeded, synthetic, Qwen3 shapes):
   qwen3-0.6b-bf16  28 x 2 x 8 x 4096 x 128   bf16, 234.9M scalars
@@ -30,6 +42,7 @@ def _cuda():
 
 def _check(O, w, Tb=None, G=None, nsample=32, max_overhead=0.01):
     s = w.spec
+    Tbe, Ge = Tb or s.Tb, G or s.G
     codec = gpu_codec(w, Tb, G)
     kv_d = (w.kv.view(torch.int16) if s.dtype == synth.BF16 else w.kv).reshape(-1)
     mu_d = w.mu.view(torch.int16).reshape(-1)
@@ -43,29 +56,39 @@ def _check(O, w, Tb=None, G=None, nsample=32, max_overhead=0.01):
         del ref
     tot, ps = codec.ideal_bits(kv_d, mu_d, per_scalar=True)
     assert abs(tot - ps.double().sum().item()) <= 1e-6 * tot  # fp32 sums of 8 inside fp64
+    mtot, mps = codec.model_bits(kv_d, mu_d, per_scalar=True)
+    assert abs(mtot - mps.double().sum().item()) <= 1e-6 * mtot
     m = oracle_model(O, w, Tb, G)
     nc = m.num_chunks()
     host = buf[:nb].cpu().numpy()
     del buf
-    assert O.check_header(m, host) == 0
-    chunks = sorted(set(np.linspace(0, nc - 1, nsample).astype(np.int64).tolist()))
     kv_h = kv_d.cpu().numpy()
     kv_h = kv_h.view(np.uint16) if s.dtype == synth.BF16 else kv_h.view(np.uint8)
     mu_h = mu_d.cpu().numpy().view(np.uint16)
-    want = O.encode_chunks(m, kv_h, mu_h, chunks)
-    Tbe = Tb or s.Tb
+    # the whole container, chunk by chunk, on every host core
+    rc, bad, _ = O.compare_container(m, kv_h, mu_h, host)
+    assert rc == 0, "chunk %d differs from the oracle (status %d)" % (bad, rc)
+    chunks = sorted(set(np.linspace(0, nc - 1, nsample).astype(np.int64).tolist()))
     ntb = (s.T + Tbe - 1) // Tbe
-    for c, ww in zip(chunks, want):
-        assert np.array_equal(container_chunk(host, nc, c), ww), c
+    for c in chunks:
         row, tb = divmod(c, ntb)
         base = row * s.T * s.D + tb * Tbe * s.D
         n_c = min(Tbe, s.T - tb * Tbe) * s.D
         ref_tot, ref = O.ideal_bits(m, kv_h, mu_h, base, base + n_c, per_scalar=True)
         got = ps[base: base + n_c].double().cpu().numpy()
         assert np.all(np.abs(got - ref) <= 1e-3 * np.abs(ref) + 1e-6), c
+        mref = O.model_bits_chunk(m, kv_h, mu_h, c)
+        mgot = mps[base: base + n_c].double().sum().item()
+        assert abs(mgot - mref) <= 1e-5 * mref + 1e-3, c
+        # the rANS length invariant on the GPU's own chunk
+        extra = 32.0 * container_chunk(host, nc, c).size - mref
+        assert 32 * Ge - 1e-3 * mref - 1 <= extra <= 64 * Ge + 1e-3 * mref + 1, c
+    payload_bits = 8.0 * (nb - 64 - 8 * (nc + 1))
     if max_overhead is not None:
-        assert 8.0 * nb <= (1.0 + max_overhead) * tot
-    return nb, tot
+        assert payload_bits <= (1.0 + max_overhead) * mtot
+        if s.dtype == synth.BF16:
+            assert 8.0 * nb <= (1.0 + max_overhead) * tot
+    return nb, tot, mtot
 
 
 def test_qwen3_0_6b_bf16(oracle_mod):
@@ -86,6 +109,6 @@ def test_qwen3_8b_e4m3(oracle_mod):
 @pytest.mark.parametrize("tb,G,bound", [(8, 1, None), (32, 1, 0.01), (128, 4, 0.01)])
 def test_long_32k_e4m3_chunk_sweep(oracle_mod, tb, G, bound):
     w = synth.make("long-32k-e4m3", device="cuda")
-    nb, tot = _check(oracle_mod, w, Tb=tb, G=G, nsample=24, max_overhead=bound)
+    _check(oracle_mod, w, Tb=tb, G=G, nsample=24, max_overhead=bound)
     del w
     torch.cuda.empty_cache()

@@ -169,3 +169,35 @@ def test_synthetic_tiny_workload_near_ideal(oracle_mod):
     ideal = O.ideal_bits(m, kv, mu)
     coded = 8.0 * buf.size
     assert ideal <= coded <= 1.01 * ideal
+
+
+@pytest.mark.parametrize("dtype", [0, 1])
+def test_compare_container_accepts_own_and_finds_every_change(oracle_mod, dtype):
+    """The whole-container check (chunk slices on several threads) accepts the
+    oracle's own container and names the chunk of any changed payload byte or
+    offset; a changed header is refused before any chunk is coded."""
+    O = oracle_mod
+    rng = np.random.default_rng(300 + dtype)
+    m = _tiny_model(O, dtype, 2, 2, 70, 16, 16, 4, rng)
+    kv, mu = _random_cache(O, m, rng)
+    rc, buf = O.encode(m, kv, mu)
+    assert rc == 0
+    assert O.compare_container(m, kv, mu, buf, threads=3)[:2] == (0, -1)
+    nc = m.num_chunks()
+    head = 64 + 8 * (nc + 1)
+    offs = buf[64:head].view(np.uint64)
+    for c in rng.choice(nc, 6, replace=False):
+        t = buf.copy()
+        pos = head + int(offs[c]) + int(rng.integers(0, int(offs[c + 1] - offs[c])))
+        t[pos] ^= 1 << int(rng.integers(0, 8))
+        rc, bad, _ = O.compare_container(m, kv, mu, t, threads=3)
+        assert rc == O.ERR_CORRUPT and bad == c
+    t = buf.copy()
+    t[64 + 8 * 5] += 4                # chunk 4 one word longer, chunk 5 one shorter
+    rc, bad, _ = O.compare_container(m, kv, mu, t, threads=2)
+    assert rc == O.ERR_CORRUPT and bad == 4
+    t = buf.copy()
+    t[20] ^= 1                        # the token count in the header
+    assert O.compare_container(m, kv, mu, t)[0] == O.ERR_CORRUPT
+    # a range of chunks alone
+    assert O.compare_container(m, kv, mu, buf, begin=3, end=9)[:2] == (0, -1)
