@@ -64,7 +64,8 @@ def test_json_line_keys(fixed_peaks):
     e2e = {"value": 40.0, "unit": "GB/s", "h2d_bytes_per_step": 2 * N + 2 * N,
            "d2h_bytes_per_step": 168_754_632 + 2 * N}
     nb, bits = 168_754_632, 5.722 * N
-    line = bench.finish_line(args, 0, 1, spec, N, nb, bits, 2, 7.68, 2 * N / 7.68e-3 / 1e9,
+    line = bench.finish_line(args, 0, 1, spec, N, nb, bits, 5.70 * N, 2, 7.68,
+                             2 * N / 7.68e-3 / 1e9,
                              [MED["encode"]] * 3, [MED["decode"]] * 3, [MED["ideal_bits"]] * 3,
                              clk, e2e, None)
     for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
@@ -78,5 +79,51 @@ def test_json_line_keys(fixed_peaks):
     assert line["bits_per_scalar"] == pytest.approx(8.0 * nb / N, abs=1e-5)
     for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
         assert k in line["roofline"], k
-    assert bench.finish_line(args, 1, 2, spec, N, nb, bits, 2, 7.68, 1.0, [1.0], [1.0], [1.0],
+    nch = 28 * 2 * 8 * 16
+    payload = 8.0 * (nb - 64 - 8 * (nch + 1))
+    assert line["model_bits_per_scalar"] == pytest.approx(5.70, abs=1e-5)
+    assert line["overhead_vs_model_pct"] == pytest.approx(100 * (8.0 * nb / (5.70 * N) - 1), abs=1e-3)
+    assert line["payload_overhead_vs_model_pct"] == pytest.approx(
+        100 * (payload / (5.70 * N) - 1), abs=1e-3)
+    assert bench.finish_line(args, 1, 2, spec, N, nb, bits, None, 2, 7.68, 1.0, [1.0], [1.0], [1.0],
                              clk, e2e, None) is None   # only rank 0 prints
+
+
+def test_cpu_baseline_single_and_all_cores(fixed_peaks):
+    """Both oracle legs on the tiny cache: the all-core leg states its cores and
+    the CPU model, and codes the same kind of sample as the one-core leg."""
+    spec = synth.WORKLOADS["tiny-bf16"]
+    w = synth.make(spec)
+    n = spec.n
+    args = argparse.Namespace(workload=spec.name, steps=3, warmup=3, no_cpu_baseline=False,
+                              order0=False, adaptive=False, block_scale=False,
+                              cpu_sample_chunks=4)
+    clk = types.SimpleNamespace(summary=lambda: None)
+    nb, bits = 100_000, 5.2 * n
+    line = bench.finish_line(args, 0, 1, spec, n, nb, bits, 5.1 * n, 2, 1.0, 1.0, [1.0], [1.0],
+                             [1.0], clk, None, w)
+    cpu = line["cpu_baseline"]
+    name, cores = bench.host_cpu()
+    assert cpu["cores"] == cores >= 1 and cpu["cpu_model"] == name and name
+    assert cpu["kind"] == "oracle" and cpu["value"] > 0 and cpu["unit"] == "GB/s"
+    assert cpu["single_core"]["cores"] == 1 and cpu["single_core"]["value"] > 0
+
+
+def test_threaded_oracle_timing_codes_the_same_sample():
+    import oracle as O
+    spec = synth.WORKLOADS["tiny-bf16"]
+    w = synth.make(spec)
+    kv, mu, sig, cnt = synth.to_numpy(w)
+    m = O.Model(spec.dtype, spec.L, spec.H, spec.T, spec.D, spec.Tb, spec.G, sig, counts=cnt)
+    nch = m.num_chunks()
+    a = bench.time_oracle(O, m, kv.reshape(-1), mu.reshape(-1), nch, nch)
+    b = bench.time_oracle(O, m, kv.reshape(-1), mu.reshape(-1), nch, nch, threads=3)
+    assert a[0] == b[0] == spec.n and a[2] == b[2]
+
+
+def test_size_accounting():
+    acc = bench.size_accounting(1000, 1000, 3, 7000.0, 7500.0)
+    assert acc["bits_per_scalar"] == 8.0
+    assert acc["payload_bits_per_scalar"] == pytest.approx(8.0 * (1000 - 64 - 32) / 1000)
+    assert acc["overhead_pct"] == pytest.approx(100 * (8000 / 7000 - 1), abs=1e-3)
+    assert acc["overhead_vs_model_pct"] == pytest.approx(100 * (8000 / 7500 - 1), abs=1e-3)
