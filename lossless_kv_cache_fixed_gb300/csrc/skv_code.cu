@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(256) k_model_bits(ModelBitsLaunch a) {
       load_inv(ip, in_row % D, inv);
     }
     float bits[8], part = 0.0f;
-#pragma unroll 1
+#pragma unroll
     for (int k = 0; k < 8; ++k) {
       int32_t r = DT == 0 ? rank_bf16(sym[k]) : rank_e4m3(sym[k]);
       if (r < 0 || r >= NS) {
@@ -832,16 +832,26 @@ __global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunc
             // helps through E at the guess, whose dependent load costs as much
             // as the Newton steps it saves).
             const float sig = __fdividef(1.0f, inv.s);  // a guess: approximate is enough
+            // bf16: near mu the p-hat term grows about linearly in value,
+            // E(x) ~ E(mu) + rho (x - mu) with rho the p-hat mass of mu's bin
+            // per unit width (the width from mu's exponent: a guess needs no
+            // more), so the guess solves G0(z) + a z = u with a = 0.02 rho sigma.
+            // Without it the p-hat term at mu alone misses where bins are narrow
+            // against sigma (values near zero): about 2 in 3 of the misses.
+            float e_mu = 0.0f, a_rho = 0.0f;
+            const int32_t rmu = DT == 0 ? rank_bf16(mub) : rank_of_value<DT>(muf);
+            if (DT == 0) {
+              const uint32_t ea = __ldg(a.ecdf + rmu), eb = __ldg(a.ecdf + rmu + 1);
+              e_mu = (float)ea * (1.0f / 67108864.0f);
+              const float wmu = __uint_as_float(max(mub & 0x7F80u, 0x0080u) << 16) * (1.0f / 128.0f);
+              a_rho = __fdividef(0.02f * (1.0f / 67108864.0f) * (float)(eb - ea) * sig, wmu);
+              a_rho = a_rho >= 0.0f ? fminf(a_rho, 1e30f) : 0.0f;  // a NaN (0/0) gives 0
+            }
             auto guess = [&](int32_t rref) -> int32_t {
               float u, uraw;
               const int32_t dr = (int32_t)(slot - (uint32_t)rref);
               uraw = (float)dr * kInvK;
-              if (DT == 0) {
-                const float e = (float)__ldg(a.ecdf + rref) * (1.0f / 67108864.0f);
-                u = uraw - 0.02f * e;
-              } else {
-                u = uraw;
-              }
+              u = DT == 0 ? uraw - 0.02f * e_mu : uraw;
               if (DT == 1) {
                 // beyond both ends of Phi_q's range cum(r) = r (below mu) or
                 // K + r (above): the rank follows from the slot directly.  Exact
@@ -852,7 +862,10 @@ __global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunc
               const float t = fminf(fmaxf(u * kHscale, 0.0f), (float)kHinvN - 0.001f);
               const int kk = (int)t;
               const float2 h = s_hinv[kk];
-              const float z0 = fmaf(t - (float)kk, h.y, h.x);
+              float z0 = fmaf(t - (float)kk, h.y, h.x);
+              // the linear p-hat term: z0 / (1 + a dz/du), dz/du = h.y kHscale from
+              // the table; it only moves the guess towards mu, never past it
+              if (DT == 0) z0 = __fdividef(z0, fmaf(a_rho * kHscale, h.y, 1.0f));
               int32_t r = rank_of_value<DT>(fmaf(sig, z0, muf));
               if (DT == 1) {
                 // the rank term at the guess: u falls by (r - rref) / K, one step
@@ -870,7 +883,7 @@ __global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunc
               }
               return r;
             };
-            const int32_t rg = guess(DT == 0 ? rank_bf16(mub) : rank_of_value<DT>(muf));
+            const int32_t rg = guess(rmu);
             const uint32_t ca = cum_of<DT>(rg, muf, inv, s_phi, s_lo8, a.ecdf);
             const uint32_t cb = cum_of<DT>(rg + 1, muf, inv, s_phi, s_lo8, a.ecdf);
             bracket_add(br, rg, ca, slot);
