@@ -229,6 +229,66 @@ int skv_decode_range(const skv_params *params, const skv_shape *shape, const voi
  * SKV_ERR_CORRUPT.  Synchronizes `stream`. */
 int skv_decode_status(const void *workspace, skv_stream_t stream);
 
+/* Encode part of a cache, asynchronously: chunks [chunk_begin, chunk_end) in
+ * container order go into the workspace's per-chunk stacks, and a later
+ * skv_encode_finish turns the stacks into the container.  A caller can so
+ * start encoding the layers that have arrived while the rest of the cache is
+ * still being copied in (the pages' section "该方法的用途": caches move between
+ * tiers over links slower than HBM; section "下一步计划": coding must keep up with
+ * the fast side).  The container is byte for byte the one skv_encode writes.
+ *   kv, mu          device, the whole [L][2][H][T][D] tensors; only the range's
+ *                   chunks are read, so the rest may still be in flight.
+ *   range_flags     SKV_RANGE_FIRST on the first call for a container: clears
+ *                   the status and the chunk count and prepares the model
+ *                   tables.  Later calls must be ordered after it (same stream,
+ *                   or caller-made ordering) and use the same workspace.
+ * Every chunk must be encoded exactly once before skv_encode_finish.  Rejects
+ * SKV_FLAG_ADAPTIVE (its tables depend on a row's earlier blocks).  Argument
+ * errors (SKV_ERR_ARG, SKV_ERR_CAPACITY) return at once; data errors
+ * (SKV_ERR_SYMBOL, SKV_ERR_PARAM) are reported by skv_encode_finish.  Does not
+ * synchronize. */
+int skv_encode_range(const skv_params *params, const skv_shape *shape, const void *kv,
+                     const uint16_t *mu, uint64_t chunk_begin, uint64_t chunk_end,
+                     int range_flags, void *workspace, size_t workspace_bytes,
+                     skv_stream_t stream);
+
+/* Size scan, compaction and header after skv_encode_range calls have coded
+ * every chunk once: writes the container to `out` (device) and its size to
+ * *out_bytes (host).  Checks the number of chunks coded since SKV_RANGE_FIRST
+ * before reading any stack: a different count is SKV_ERR_ARG and nothing is
+ * written.  Other errors as skv_encode.  Synchronizes `stream`. */
+int skv_encode_finish(const skv_params *params, const skv_shape *shape, void *out,
+                      size_t out_capacity, size_t *out_bytes, void *workspace,
+                      size_t workspace_bytes, skv_stream_t stream);
+
+/* The model fingerprint a container of this cache carries in its header (a
+ * sum of SplitMix64 terms over sigma's and E_q's 32-bit words, so a decoder
+ * with a different model refuses the container).  For skv_merge_parts.
+ *   fingerprint   host; receives the value.
+ *   workspace     any operation's workspace for this shape.
+ * Errors: SKV_ERR_ARG, SKV_ERR_CAPACITY, SKV_ERR_PARAM (sigma or E_q
+ * invalid), SKV_ERR_CUDA.  Synchronizes. */
+int skv_model_fingerprint(const skv_params *params, const skv_shape *shape,
+                          uint64_t *fingerprint, void *workspace, size_t workspace_bytes,
+                          skv_stream_t stream);
+
+/* One container from the containers of consecutive layer ranges of a cache,
+ * host memory only (no GPU call): the multi-GPU path, where each GPU codes
+ * its own contiguous layer range -- a contiguous chunk range, since chunks are
+ * independent -- and one exclusive scan of the parts' payload sizes places
+ * them.  parts[i] (host, part_bytes[i] bytes) must be a container written by
+ * skv_encode (or skv_encode_finish) for layers [l_i, l_i + n_i) of the cache
+ * described by params and shape, with sigma's rows of those layers, in layer
+ * order and covering every layer.  The result, written to out (host,
+ * out_capacity bytes; *out_bytes receives its size), is byte for byte the
+ * container skv_encode writes for the whole cache, given the whole cache's
+ * fingerprint (skv_model_fingerprint).  Errors: SKV_ERR_ARG (shape, count of
+ * layers), SKV_ERR_CORRUPT (a part's header does not belong to this cache
+ * or its offsets are malformed), SKV_ERR_CAPACITY. */
+int skv_merge_parts(const skv_params *params, const skv_shape *shape, uint64_t fingerprint,
+                    const void *const *parts, const size_t *part_bytes, int nparts, void *out,
+                    size_t out_capacity, size_t *out_bytes);
+
 /* Ideal code length: the cross-entropy -log2 q(x) of every scalar under the
  * continuous model (bin mass of the mixture, or of N(mu, sigma^2) for e4m3),
  * evaluated in tail-safe fp32 and summed in fp64 in a fixed order.  Every

@@ -25,7 +25,8 @@ SKV_OK, SKV_ERR_ARG, SKV_ERR_CAPACITY, SKV_ERR_SYMBOL = 0, -1, -2, -3
 SKV_ERR_PARAM, SKV_ERR_CORRUPT, SKV_ERR_CUDA = -4, -5, -6
 NSYM = {SKV_BF16: 65282, SKV_E4M3: 254}
 
-EXPORTS = ("skv_max_encoded_bytes", "skv_workspace_bytes", "skv_encode", "skv_decode",
+EXPORTS = ("skv_max_encoded_bytes", "skv_workspace_bytes", "skv_encode", "skv_encode_range",
+           "skv_encode_finish", "skv_model_fingerprint", "skv_merge_parts", "skv_decode",
            "skv_decode_range", "skv_decode_status", "skv_ideal_bits", "skv_model_bits",
            "skv_ideal_bits_noalloc", "skv_ideal_bits_noalloc_max_channels",
            "skv_build_ecdf", "skv_phi_table", "skv_strerror", "skv_version")
@@ -64,6 +65,12 @@ def lib():
             "skv_max_encoded_bytes": (sz, [P, S]),
             "skv_workspace_bytes": (sz, [P, S, C.c_int]),
             "skv_encode": (C.c_int, [P, S, vp, vp, vp, sz, C.POINTER(sz), vp, sz, vp]),
+            "skv_encode_range": (C.c_int, [P, S, vp, vp, C.c_uint64, C.c_uint64, C.c_int, vp, sz,
+                                           vp]),
+            "skv_encode_finish": (C.c_int, [P, S, vp, sz, C.POINTER(sz), vp, sz, vp]),
+            "skv_model_fingerprint": (C.c_int, [P, S, C.POINTER(C.c_uint64), vp, sz, vp]),
+            "skv_merge_parts": (C.c_int, [P, S, C.c_uint64, C.POINTER(vp), C.POINTER(sz), C.c_int,
+                                          vp, sz, C.POINTER(sz)]),
             "skv_decode": (C.c_int, [P, S, vp, sz, vp, vp, vp, sz, vp]),
             "skv_decode_range": (C.c_int, [P, S, vp, sz, C.c_uint64, C.c_uint64, vp, vp, vp,
                                            C.c_uint64, C.c_int, vp, sz, vp]),
@@ -99,6 +106,41 @@ def skv_encode(params, shape, kv_ptr, mu_ptr, out_ptr, out_capacity, ws_ptr, ws_
     nb = C.c_size_t(0)
     rc = lib().skv_encode(C.byref(params), C.byref(shape), kv_ptr, mu_ptr, out_ptr, out_capacity,
                           C.byref(nb), ws_ptr, ws_bytes, stream)
+    return rc, nb.value
+
+
+def skv_encode_range(params, shape, kv_ptr, mu_ptr, chunk_begin, chunk_end, range_flags, ws_ptr,
+                     ws_bytes, stream):
+    """Enqueues the encode of chunks [chunk_begin, chunk_end); returns the argument status."""
+    return lib().skv_encode_range(C.byref(params), C.byref(shape), kv_ptr, mu_ptr, chunk_begin,
+                                  chunk_end, range_flags, ws_ptr, ws_bytes, stream)
+
+
+def skv_encode_finish(params, shape, out_ptr, out_capacity, ws_ptr, ws_bytes, stream):
+    """Returns (status, container bytes)."""
+    nb = C.c_size_t(0)
+    rc = lib().skv_encode_finish(C.byref(params), C.byref(shape), out_ptr, out_capacity,
+                                 C.byref(nb), ws_ptr, ws_bytes, stream)
+    return rc, nb.value
+
+
+def skv_model_fingerprint(params, shape, ws_ptr, ws_bytes, stream):
+    """Returns (status, the model fingerprint of a container's header)."""
+    fp = C.c_uint64(0)
+    rc = lib().skv_model_fingerprint(C.byref(params), C.byref(shape), C.byref(fp), ws_ptr,
+                                     ws_bytes, stream)
+    return rc, fp.value
+
+
+def skv_merge_parts(params, shape, fingerprint, parts, out):
+    """parts: host uint8 numpy arrays (containers of consecutive layer ranges);
+    out: a host uint8 numpy array.  Returns (status, container bytes)."""
+    n = len(parts)
+    ptrs = (C.c_void_p * n)(*[pt.ctypes.data for pt in parts])
+    sizes = (C.c_size_t * n)(*[pt.nbytes for pt in parts])
+    nb = C.c_size_t(0)
+    rc = lib().skv_merge_parts(C.byref(params), C.byref(shape), fingerprint, ptrs, sizes, n,
+                               out.ctypes.data, out.nbytes, C.byref(nb))
     return rc, nb.value
 
 
@@ -236,6 +278,38 @@ class Codec:
         if rc:
             raise SkvError(rc, "skv_encode")
         return out, nb
+
+    def encode_range(self, kv, mu, chunk_begin, chunk_end, first=False, stream=None):
+        """Enqueue the encode of chunks [chunk_begin, chunk_end) (no synchronisation)."""
+        ws = self.workspace(SKV_OP_ENCODE)
+        rc = skv_encode_range(self.params, self.shape, kv.data_ptr(), _ptr(mu), chunk_begin,
+                              chunk_end, SKV_RANGE_FIRST if first else 0, ws.data_ptr(),
+                              ws.numel(), _stream_handle(stream))
+        if rc:
+            raise SkvError(rc, "skv_encode_range")
+
+    def encode_finish(self, out=None, stream=None):
+        """The container from the chunk ranges encoded so far: (tensor, bytes)."""
+        if out is None:
+            out = self.torch.empty(self.max_bytes, dtype=self.torch.uint8, device=self.device)
+        ws = self.workspace(SKV_OP_ENCODE)
+        rc, nb = skv_encode_finish(self.params, self.shape, out.data_ptr(), out.numel(),
+                                   ws.data_ptr(), ws.numel(), _stream_handle(stream))
+        if rc:
+            raise SkvError(rc, "skv_encode_finish")
+        return out, nb
+
+    def fingerprint(self, stream=None):
+        ws = self.workspace(SKV_OP_IDEAL_BITS)
+        rc, fp = skv_model_fingerprint(self.params, self.shape, ws.data_ptr(), ws.numel(),
+                                       _stream_handle(stream))
+        if rc:
+            raise SkvError(rc, "skv_model_fingerprint")
+        return fp
+
+    def num_chunks(self):
+        s, tb = self.shape, self.params.token_block
+        return s.layers * 2 * s.heads * ((s.tokens + tb - 1) // tb)
 
     def decode(self, buf, nbytes, mu, out=None, stream=None):
         if out is None:

@@ -281,7 +281,89 @@ ScaleLaunch scale_launch(const Plan &pl, const skv_params *p, WsHead *head) {
   sl.dtype = pl.dtype;
   sl.sigma = p->sigma;
   sl.head = head;
+  sl.c_begin = 0;
+  sl.c_end = pl.geo.nchunks;
   return sl;
+}
+
+// The encode launch for a plan and its workspace (no chunk range yet).
+EncodeLaunch encode_launch(const skv_params *params, const Plan &pl, uint8_t *ws) {
+  EncodeLaunch a;
+  std::memset(&a, 0, sizeof(a));
+  a.geo = pl.geo;
+  a.dtype = pl.dtype;
+  a.inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
+  a.nsw = pl.nsw;
+  a.order0 = pl.order0;
+  a.adaptive = pl.adaptive;
+  a.ecdf = pl.dtype == SKV_BF16 ? params->ecdf : nullptr;
+  a.scratch = reinterpret_cast<uint32_t *>(ws + pl.off_scratch);
+  a.stride = pl.stride;
+  a.sizes = reinterpret_cast<uint64_t *>(ws + pl.off_sizes);
+  a.starts = reinterpret_cast<uint32_t *>(ws + pl.off_starts);
+  a.partials = reinterpret_cast<uint64_t *>(ws + pl.off_partials);
+  a.head = reinterpret_cast<WsHead *>(ws);
+  a.hash_words = hash_words(pl);
+  a.c_step = 1;
+  if (pl.nsw) {
+    a.inv_chunk = reinterpret_cast<float2 *>(ws + pl.off_enc_cinv);
+    a.scale_words = reinterpret_cast<uint32_t *>(ws + pl.off_enc_words);
+  }
+  return a;
+}
+
+// Encode of chunks [c0, c1) into the workspace's chunk stacks, enqueued on
+// `stream` without a host synchronisation.  `first` clears the status and the
+// chunk count and prepares the model tables (reciprocals, fingerprint).
+int encode_enqueue(const skv_params *params, const Plan &pl, const void *kv, const uint16_t *mu,
+                   uint64_t c0, uint64_t c1, bool first, void *workspace, cudaStream_t st) {
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  EncodeLaunch a = encode_launch(params, pl, ws);
+  if (first) {
+    if (cudaMemsetAsync(a.head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
+    if (launch_prep(params->sigma, pl.nsig_model, a.ecdf, const_cast<float2 *>(a.inv), a.head,
+                    st) != cudaSuccess)
+      return SKV_ERR_CUDA;
+  }
+  if (c1 <= c0) return SKV_OK;
+  a.kv = kv;
+  a.mu = mu;
+  if (pl.nsw) {
+    // the scales of these chunks, from their residuals
+    ScaleLaunch sl = scale_launch(pl, params, a.head);
+    sl.kv = kv;
+    sl.mu = mu;
+    sl.inv = const_cast<float2 *>(a.inv_chunk);
+    sl.words = const_cast<uint32_t *>(a.scale_words);
+    sl.c_begin = (int64_t)c0;
+    sl.c_end = (int64_t)c1;
+    if (launch_scales(sl, st) != cudaSuccess) return SKV_ERR_CUDA;
+  }
+  a.c_first = (int64_t)c0;
+  a.c_count = (int64_t)(c1 - c0);
+  if (launch_encode_chunks(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  return SKV_OK;
+}
+
+// Size scan, compaction and header once every chunk is in its stack; reads the
+// status back (synchronises).  The chunk count is checked first, so a stack
+// that was never written is never copied.
+int encode_finish(const skv_params *params, const Plan &pl, void *out, size_t out_capacity,
+                  size_t *out_bytes, void *workspace, cudaStream_t st) {
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  EncodeLaunch a = encode_launch(params, pl, ws);
+  WsHead h;
+  int rc = read_head(a.head, &h, st);
+  if (rc) return rc;
+  if ((rc = status_from_flags(h.flags))) return rc;
+  if (h.chunks_done != (unsigned long long)pl.geo.nchunks) return SKV_ERR_ARG;
+  a.out = static_cast<uint8_t *>(out);
+  a.capacity = out_capacity;
+  if (launch_encode_finish(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  if ((rc = read_head(a.head, &h, st))) return rc;
+  if ((rc = status_from_flags(h.flags))) return rc;
+  *out_bytes = 64 + 8 * (size_t)(pl.geo.nchunks + 1) + (size_t)h.total;
+  return SKV_OK;
 }
 
 // Decode of chunks [c0, c1) of a container, enqueued on `stream` without a
@@ -439,76 +521,169 @@ int skv_encode(const skv_params *params, const skv_shape *shape, const void *kv,
   if (workspace_bytes < ws_bytes_for(pl, SKV_OP_ENCODE)) return SKV_ERR_CAPACITY;
   if ((rc = ensure_device_tables())) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!pl.adaptive) {
+    if ((rc = encode_enqueue(params, pl, kv, mu, 0, (uint64_t)pl.geo.nchunks, true, workspace, st)))
+      return rc;
+    return encode_finish(params, pl, out, out_capacity, out_bytes, workspace, st);
+  }
+  // adaptive counts: one phase per token block -- the rows' tables, block b of
+  // every row, then the update from that block
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  if ((rc = encode_enqueue(params, pl, kv, mu, 0, 0, true, workspace, st))) return rc;
+  EncodeLaunch a = encode_launch(params, pl, ws);
+  a.kv = kv;
+  a.mu = mu;
+  uint8_t *ad = ws + pl.ad_base_enc;
+  uint64_t *P = reinterpret_cast<uint64_t *>(ad + pl.ad_P);
+  uint64_t *Cn = reinterpret_cast<uint64_t *>(ad + pl.ad_C);
+  uint32_t *Et = reinterpret_cast<uint32_t *>(ad + pl.ad_E);
+  uint64_t *W = reinterpret_cast<uint64_t *>(ad + pl.ad_W);
+  if (launch_ad_init(params->ecdf, P, Cn, pl.nrows, W, pl.geo.Tb, st) != cudaSuccess)
+    return SKV_ERR_CUDA;
+  a.ecdf = Et;
+  a.ecdf_row_stride = kNsymBf16 + 1;
+  a.c_step = pl.geo.ntb;
+  a.c_count = pl.nrows;
+  for (int64_t b = 0; b < pl.geo.ntb; ++b) {
+    if (launch_ad_table(P, Et, nullptr, 0, pl.nrows, st) != cudaSuccess) return SKV_ERR_CUDA;
+    a.c_first = b;
+    if (launch_encode_chunks(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+    if (b + 1 < pl.geo.ntb &&
+        launch_ad_update(pl.geo, static_cast<const uint16_t *>(kv), b, P, Cn, W, a.head, pl.nrows,
+                         st) != cudaSuccess)
+      return SKV_ERR_CUDA;
+  }
+  return encode_finish(params, pl, out, out_capacity, out_bytes, workspace, st);
+}
+
+int skv_encode_range(const skv_params *params, const skv_shape *shape, const void *kv,
+                     const uint16_t *mu, uint64_t chunk_begin, uint64_t chunk_end,
+                     int range_flags, void *workspace, size_t workspace_bytes,
+                     skv_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  if (range_flags & ~SKV_RANGE_FIRST) return SKV_ERR_ARG;
+  // adaptive tables depend on every earlier block of a row: whole caches only
+  if (pl.adaptive) return SKV_ERR_ARG;
+  if (chunk_begin > chunk_end || chunk_end > (uint64_t)pl.geo.nchunks) return SKV_ERR_ARG;
+  if ((rc = common_inputs(params, pl, kv, mu))) return rc;
+  if (!workspace || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
+  if (workspace_bytes < ws_bytes_for(pl, SKV_OP_ENCODE)) return SKV_ERR_CAPACITY;
+  if ((rc = ensure_device_tables())) return rc;
+  return encode_enqueue(params, pl, kv, mu, chunk_begin, chunk_end,
+                        (range_flags & SKV_RANGE_FIRST) != 0, workspace,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+int skv_encode_finish(const skv_params *params, const skv_shape *shape, void *out,
+                      size_t out_capacity, size_t *out_bytes, void *workspace,
+                      size_t workspace_bytes, skv_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  if (pl.adaptive) return SKV_ERR_ARG;
+  if (!out || !out_bytes || !workspace || !aligned(out, 8) || !aligned(workspace, kAlign))
+    return SKV_ERR_ARG;
+  if (workspace_bytes < ws_bytes_for(pl, SKV_OP_ENCODE)) return SKV_ERR_CAPACITY;
+  return encode_finish(params, pl, out, out_capacity, out_bytes, workspace,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int skv_model_fingerprint(const skv_params *params, const skv_shape *shape,
+                          uint64_t *fingerprint, void *workspace, size_t workspace_bytes,
+                          skv_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  if (!fingerprint || !workspace || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
+  if (!pl.order0 && (!params->sigma || !aligned(params->sigma, 4))) return SKV_ERR_ARG;
+  if (pl.dtype == SKV_BF16 && (!params->ecdf || !aligned(params->ecdf, 4))) return SKV_ERR_ARG;
+  // the head and the reciprocal table, which every operation's workspace starts with
+  if (workspace_bytes < pl.off_inv + sizeof(float2) * (size_t)pl.nsig) return SKV_ERR_CAPACITY;
+  if ((rc = ensure_device_tables())) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   WsHead *head = reinterpret_cast<WsHead *>(ws);
   if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
-  float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
-  const uint32_t *ecdf = pl.dtype == SKV_BF16 ? params->ecdf : nullptr;
-  if (launch_prep(params->sigma, pl.nsig_model, ecdf, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
-  EncodeLaunch a;
-  a.geo = pl.geo;
-  a.dtype = pl.dtype;
-  a.kv = kv;
-  a.mu = mu;
-  a.inv = inv;
-  a.inv_chunk = nullptr;
-  a.scale_words = nullptr;
-  a.nsw = pl.nsw;
-  a.order0 = pl.order0;
-  if (pl.nsw) {
-    ScaleLaunch sl = scale_launch(pl, params, head);
-    sl.kv = kv;
-    sl.mu = mu;
-    sl.inv = reinterpret_cast<float2 *>(ws + pl.off_enc_cinv);
-    sl.words = reinterpret_cast<uint32_t *>(ws + pl.off_enc_words);
-    if (launch_scales(sl, st) != cudaSuccess) return SKV_ERR_CUDA;
-    a.inv_chunk = sl.inv;
-    a.scale_words = sl.words;
-  }
-  a.ecdf = ecdf;
-  a.scratch = reinterpret_cast<uint32_t *>(ws + pl.off_scratch);
-  a.stride = pl.stride;
-  a.sizes = reinterpret_cast<uint64_t *>(ws + pl.off_sizes);
-  a.starts = reinterpret_cast<uint32_t *>(ws + pl.off_starts);
-  a.partials = reinterpret_cast<uint64_t *>(ws + pl.off_partials);
-  a.head = head;
-  a.out = static_cast<uint8_t *>(out);
-  a.capacity = out_capacity;
-  a.hash_words = hash_words(pl);
-  a.adaptive = pl.adaptive;
-  a.c_first = 0;
-  a.c_step = 1;
-  a.c_count = pl.geo.nchunks;
-  a.ecdf_row_stride = 0;
-  if (pl.adaptive) {
-    // one phase per token block: the rows' tables, block b of every row, the update
-    uint8_t *ad = ws + pl.ad_base_enc;
-    uint64_t *P = reinterpret_cast<uint64_t *>(ad + pl.ad_P);
-    uint64_t *Cn = reinterpret_cast<uint64_t *>(ad + pl.ad_C);
-    uint32_t *Et = reinterpret_cast<uint32_t *>(ad + pl.ad_E);
-    uint64_t *W = reinterpret_cast<uint64_t *>(ad + pl.ad_W);
-    if (launch_ad_init(ecdf, P, Cn, pl.nrows, W, pl.geo.Tb, st) != cudaSuccess) return SKV_ERR_CUDA;
-    a.ecdf = Et;
-    a.ecdf_row_stride = kNsymBf16 + 1;
-    a.c_step = pl.geo.ntb;
-    a.c_count = pl.nrows;
-    for (int64_t b = 0; b < pl.geo.ntb; ++b) {
-      if (launch_ad_table(P, Et, nullptr, 0, pl.nrows, st) != cudaSuccess) return SKV_ERR_CUDA;
-      a.c_first = b;
-      if (launch_encode_chunks(a, st) != cudaSuccess) return SKV_ERR_CUDA;
-      if (b + 1 < pl.geo.ntb &&
-          launch_ad_update(pl.geo, static_cast<const uint16_t *>(kv), b, P, Cn, W, head, pl.nrows,
-                           st) != cudaSuccess)
-        return SKV_ERR_CUDA;
-    }
-    if (launch_encode_finish(a, st) != cudaSuccess) return SKV_ERR_CUDA;
-  } else if (launch_encode(a, st) != cudaSuccess) {
+  if (launch_prep(params->sigma, pl.nsig_model, pl.dtype == SKV_BF16 ? params->ecdf : nullptr,
+                  reinterpret_cast<float2 *>(ws + pl.off_inv), head, st) != cudaSuccess)
     return SKV_ERR_CUDA;
-  }
   WsHead h;
   if ((rc = read_head(head, &h, st))) return rc;
   if ((rc = status_from_flags(h.flags))) return rc;
-  *out_bytes = 64 + 8 * (size_t)(pl.geo.nchunks + 1) + (size_t)h.total;
+  *fingerprint = mix64(h.hash_acc ^ hash_words(pl));
+  return SKV_OK;
+}
+
+namespace {
+uint64_t get_u64(const uint8_t *p) {
+  uint64_t v = 0;
+  for (int i = 7; i >= 0; --i) v = (v << 8) | p[i];
+  return v;
+}
+}  // namespace
+
+int skv_merge_parts(const skv_params *params, const skv_shape *shape, uint64_t fingerprint,
+                    const void *const *parts, const size_t *part_bytes, int nparts, void *out,
+                    size_t out_capacity, size_t *out_bytes) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  if (!parts || !part_bytes || nparts < 1 || !out || !out_bytes) return SKV_ERR_ARG;
+  const uint32_t features = (pl.nsw ? 1u : 0u) | (pl.order0 ? 2u : 0u) | (pl.adaptive ? 4u : 0u);
+  // every part is a container of a contiguous layer range of this cache, in
+  // order: its header must be this cache's but for the layer count, the chunk
+  // count, the payload size and the fingerprint (which covers its own slice)
+  int64_t layers = 0, chunks = 0;
+  uint64_t payload = 0;
+  for (int i = 0; i < nparts; ++i) {
+    const uint8_t *p = static_cast<const uint8_t *>(parts[i]);
+    if (!p || part_bytes[i] < 64) return SKV_ERR_CORRUPT;
+    const int32_t pl_layers = (int32_t)(p[8] | p[9] << 8 | p[10] << 16 | (uint32_t)p[11] << 24);
+    if (pl_layers <= 0 || pl_layers > pl.geo.L - layers) return SKV_ERR_CORRUPT;
+    Geo g = pl.geo;
+    g.L = pl_layers;
+    g.nchunks = (int64_t)pl_layers * 2 * g.H * g.ntb;
+    const uint64_t hb = 64 + 8 * (uint64_t)(g.nchunks + 1);
+    if (part_bytes[i] < hb) return SKV_ERR_CORRUPT;
+    const uint64_t pp = part_bytes[i] - hb;
+    uint8_t want[64];
+    make_header(want, g, pl.dtype, pp, get_u64(p + 56), features);
+    if (std::memcmp(want, p, 64) != 0) return SKV_ERR_CORRUPT;
+    if (get_u64(p + 64) != 0 || get_u64(p + 64 + 8 * (uint64_t)g.nchunks) != pp)
+      return SKV_ERR_CORRUPT;
+    layers += pl_layers;
+    chunks += g.nchunks;
+    payload += pp;
+  }
+  if (layers != pl.geo.L || chunks != pl.geo.nchunks) return SKV_ERR_ARG;
+  const uint64_t hbytes = 64 + 8 * (uint64_t)(pl.geo.nchunks + 1);
+  if (out_capacity < hbytes + payload) return SKV_ERR_CAPACITY;
+  uint8_t *o = static_cast<uint8_t *>(out);
+  make_header(o, pl.geo, pl.dtype, payload, fingerprint, features);
+  // the offsets: each part's own, shifted by the exclusive scan of the payload
+  // sizes of the parts before it; then the payloads one after another
+  uint64_t base = 0, c = 0;
+  for (int i = 0; i < nparts; ++i) {
+    const uint8_t *p = static_cast<const uint8_t *>(parts[i]);
+    const int64_t nc = ((int64_t)(p[8] | p[9] << 8 | p[10] << 16 | (uint32_t)p[11] << 24)) * 2 *
+                       pl.geo.H * pl.geo.ntb;
+    const uint64_t hb = 64 + 8 * (uint64_t)(nc + 1);
+    const uint64_t pp = part_bytes[i] - hb;
+    uint64_t prev = 0;
+    for (int64_t k = 0; k < nc; ++k) {
+      const uint64_t off = get_u64(p + 64 + 8 * (uint64_t)k);
+      if (off < prev || off > pp || (off & 3)) return SKV_ERR_CORRUPT;
+      prev = off;
+      put_u64(o + 64 + 8 * (c + (uint64_t)k), base + off);
+    }
+    std::memcpy(o + hbytes + base, p + hb, pp);
+    base += pp;
+    c += (uint64_t)nc;
+  }
+  put_u64(o + 64 + 8 * c, base);
+  *out_bytes = hbytes + payload;
   return SKV_OK;
 }
 

@@ -72,15 +72,6 @@ int device_sm_count() {
   return n > 0 ? n : 1;
 }
 
-// SplitMix64 output function (Steele, Lea, Flood, OOPSLA 2014): the model
-// fingerprint is sum_k mix64(k << 32 | word_k) mod 2^64, then mix64(sum ^ nwords).
-__device__ __forceinline__ uint64_t mix64(uint64_t z) {
-  z += 0x9E3779B97F4A7C15ull;
-  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-  return z ^ (z >> 31);
-}
-
 __device__ __forceinline__ void stage_tables(uint2 *s_phi, float *s_lo8) {
   for (int i = threadIdx.x; i < kPhiKnots; i += blockDim.x) s_phi[i] = g_phi[i];
   for (int i = threadIdx.x; i < 256; i += blockDim.x) s_lo8[i] = g_lo8[i];
@@ -308,6 +299,7 @@ __global__ void __launch_bounds__(kCodeThreads, 1) k_encode(EncodeLaunch a) {
         const int64_t start = s0 < 0 ? 0 : s0;
         a.starts[c] = (uint32_t)start;
         a.sizes[c] = 4ull * (uint64_t)(a.stride - start);
+        atomicAdd(&a.head->chunks_done, 1ull);
       }
     }
     if (flags) atomicOr(&a.head->flags, flags);
@@ -470,41 +462,6 @@ __global__ void __launch_bounds__(1024) k_scan_partials(uint64_t *partials, int6
 // ------------------------------------------------------------------------
 // Compaction into the container: header | offsets | payload.
 // ------------------------------------------------------------------------
-
-__device__ __forceinline__ void put_u16(uint8_t *p, uint32_t v) {
-  p[0] = (uint8_t)v;
-  p[1] = (uint8_t)(v >> 8);
-}
-__device__ __forceinline__ void put_u32(uint8_t *p, uint32_t v) {
-  for (int i = 0; i < 4; ++i) p[i] = (uint8_t)(v >> (8 * i));
-}
-__device__ __forceinline__ void put_u64(uint8_t *p, uint64_t v) {
-  for (int i = 0; i < 8; ++i) p[i] = (uint8_t)(v >> (8 * i));
-}
-
-// The 64-byte container header for this geometry (see skv.h).
-__device__ void make_header(uint8_t *h, const Geo &g, int dtype, uint64_t payload,
-                            uint64_t hash, uint32_t features) {
-  for (int i = 0; i < 64; ++i) h[i] = 0;
-  put_u32(h + 0, 0x31564B53u);
-  put_u16(h + 4, 1);
-  h[6] = (uint8_t)dtype;
-  h[7] = (uint8_t)(dtype == 0 ? kMBf16 : kME4m3);
-  put_u32(h + 8, (uint32_t)g.L);
-  put_u32(h + 12, 2);
-  put_u32(h + 16, (uint32_t)g.H);
-  put_u32(h + 20, (uint32_t)g.T);
-  put_u32(h + 24, (uint32_t)g.D);
-  put_u32(h + 28, (uint32_t)g.Tb);
-  put_u16(h + 32, (uint32_t)g.G);
-  h[34] = 8;
-  h[35] = 9;
-  put_u16(h + 36, 8);
-  put_u16(h + 38, features);  // bit 0: per-block scales, bit 1: order-0, bit 2: adaptive
-  put_u64(h + 40, (uint64_t)g.nchunks);
-  put_u64(h + 48, payload);
-  put_u64(h + 56, hash);
-}
 
 __global__ void __launch_bounds__(256) k_compact(EncodeLaunch a) {
   const uint64_t total = a.head->total;

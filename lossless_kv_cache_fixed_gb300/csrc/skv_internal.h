@@ -47,7 +47,55 @@ struct WsHead {
   unsigned long long total;       // encode: payload bytes
   double bits;                    // ideal bits total
   unsigned long long next_task;   // decode: tasks handed out after the first round
+  unsigned long long chunks_done; // encode: chunks coded since the head was cleared
 };
+
+// ---- container header (spec v1), built the same way on the host and the device ----
+
+__host__ __device__ inline void put_u16(uint8_t *p, uint32_t v) {
+  p[0] = (uint8_t)v;
+  p[1] = (uint8_t)(v >> 8);
+}
+__host__ __device__ inline void put_u32(uint8_t *p, uint32_t v) {
+  for (int i = 0; i < 4; ++i) p[i] = (uint8_t)(v >> (8 * i));
+}
+__host__ __device__ inline void put_u64(uint8_t *p, uint64_t v) {
+  for (int i = 0; i < 8; ++i) p[i] = (uint8_t)(v >> (8 * i));
+}
+
+// The 64-byte container header of a cache of geometry g (see skv.h).
+// features: bit 0 per-block scales, bit 1 order-0, bit 2 adaptive counts.
+__host__ __device__ inline void make_header(uint8_t *h, const Geo &g, int dtype, uint64_t payload,
+                                            uint64_t fingerprint, uint32_t features) {
+  for (int i = 0; i < 64; ++i) h[i] = 0;
+  put_u32(h + 0, 0x31564B53u);  // "SKV1"
+  put_u16(h + 4, 1);
+  h[6] = (uint8_t)dtype;
+  h[7] = (uint8_t)(dtype == 0 ? 28 : 16);
+  put_u32(h + 8, (uint32_t)g.L);
+  put_u32(h + 12, 2);
+  put_u32(h + 16, (uint32_t)g.H);
+  put_u32(h + 20, (uint32_t)g.T);
+  put_u32(h + 24, (uint32_t)g.D);
+  put_u32(h + 28, (uint32_t)g.Tb);
+  put_u16(h + 32, (uint32_t)g.G);
+  h[34] = 8;
+  h[35] = 9;
+  put_u16(h + 36, 8);
+  put_u16(h + 38, features);
+  put_u64(h + 40, (uint64_t)g.nchunks);
+  put_u64(h + 48, payload);
+  put_u64(h + 56, fingerprint);
+}
+
+// SplitMix64 output function (Steele, Lea, Flood, OOPSLA 2014): the model
+// fingerprint is sum_k mix64(k << 32 | word_k) mod 2^64, then mix64(sum ^ nwords).
+__host__ __device__ inline uint64_t mix64(uint64_t z) {
+  z += 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
 
 constexpr int kScanBlock = 2048;  // chunks per scan block
 
@@ -164,7 +212,7 @@ struct ScaleLaunch {
   float2 *inv;
   float *sig;
   WsHead *head;
-  int64_t c_begin, c_end;   // load mode: chunks to read
+  int64_t c_begin, c_end;   // chunks to estimate or to read
 };
 
 // Device constants (Phi knot pairs, e4m3 bin edges, the two inverse tables,

@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kScaleThreads) k_scale_est(ScaleLaunch a) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int D = a.geo.D, NG = D / 8, nsw = scale_words(D);
   const int C = DT == 0 ? 18 : 21;
-  for (int64_t c = blockIdx.x; c < a.geo.nchunks; c += gridDim.x) {
+  for (int64_t c = a.c_begin + blockIdx.x; c < a.c_end; c += gridDim.x) {
     const ChunkGeo cg = chunk_geo(a.geo, c);
     const uint32_t tn = cg.ngroup * 8u / (uint32_t)D;  // tokens in the chunk
     const uint32_t need = (tn * 8u + 1u) / 2u;
@@ -222,7 +222,8 @@ cudaError_t launch_scales(const ScaleLaunch &a, cudaStream_t s) {
     k_scale_load<<<(unsigned)(blocks > 0 ? blocks : 1), 256, 0, s>>>(a);
     return cudaGetLastError();
   }
-  int64_t blocks = a.geo.nchunks;
+  int64_t blocks = a.c_end - a.c_begin;
+  if (blocks <= 0) return cudaSuccess;
   if (blocks > cap) blocks = cap;
   if (a.dtype == 0) k_scale_est<0><<<(unsigned)blocks, kScaleThreads, 0, s>>>(a);
   else k_scale_est<1><<<(unsigned)blocks, kScaleThreads, 0, s>>>(a);
