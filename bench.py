@@ -77,9 +77,26 @@ def barrier(world: int):
         dist.barrier()
 
 
-def rank_seed(rank: int) -> int:
-    """Weak scaling: every rank codes its own cache, drawn with its own seed."""
-    return rank
+def layer_range(rank: int, world: int, layers: int):
+    """The contiguous layers [l0, l1) of one cache that `rank` codes: chunks are
+    independent, so a layer range is a contiguous chunk range of the container."""
+    return rank * layers // world, (rank + 1) * layers // world
+
+
+def payload_bases(total: int, world: int, device=None):
+    """Every rank's payload size, gathered (the one collective of the sharded
+    path), and their exclusive scan: (base of each rank's part in the single
+    container's payload, the whole payload size)."""
+    if world <= 1:
+        return [0], int(total)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([int(total)], dtype=torch.int64, device=device)
+    got = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(got, t)
+    sizes = [int(g.item()) for g in got]
+    bases = [sum(sizes[:r]) for r in range(world)]
+    return bases, sum(sizes)
 
 
 class ClockSampler:
@@ -367,9 +384,10 @@ def device_inputs(w, order0=False):
     return kv, mu
 
 
-def time_steps(codec, kv, mu, out, dec, steps, warmup, world, clock_index=None):
+def time_steps(codec, kv, mu, out, dec, steps, warmup, world, clock_index=None, exchange=None):
     """W untimed steps, then K steps (encode, decode, ideal bits) timed with CUDA
-    events on the launching stream between barriers and synchronisations."""
+    events on the launching stream between barriers and synchronisations.
+    exchange(nb), when given, runs after each encode (the ranks' payload sizes)."""
     import torch
     stream = torch.cuda.current_stream()
 
@@ -377,6 +395,8 @@ def time_steps(codec, kv, mu, out, dec, steps, warmup, world, clock_index=None):
         if ev:
             ev[0].record(stream)
         _, nb = codec.encode(kv, mu, out=out)
+        if exchange is not None:
+            exchange(nb)
         if ev:
             ev[1].record(stream)
         codec.decode(out, nb, mu, out=dec)
@@ -439,7 +459,9 @@ def run_gpu(args):
         args.token_block = 128   # the entropy-estimation page's N_update
     if args.lanes or args.token_block:
         spec = spec.scaled(G=args.lanes or spec.G, Tb=args.token_block or spec.Tb)
-    w = synth.make(spec, device=dev, seed=rank_seed(rank))
+    # one cache; under torchrun each rank holds and codes a contiguous layer range of it
+    l0, l1 = layer_range(rank, world, spec.L)
+    w = synth.make(spec, device=dev, seed=0, layers=(l0, l1))
     s = w.spec
     bps = 2 if s.dtype == synth.BF16 else 1
     flags = (P.SKV_FLAG_DECODE_BISECT if args.decode_bisect else 0) | (
@@ -452,18 +474,26 @@ def run_gpu(args):
     out = torch.empty(codec.max_bytes, dtype=torch.uint8, device=dev)
     dec = torch.empty_like(kv)
 
-    r = time_steps(codec, kv, mu, out, dec, args.steps, args.warmup, world, local)
+    nch_part = s.L * 2 * s.H * ((s.T + s.Tb - 1) // s.Tb)
+    exchange = None
+    if world > 1:
+        # the placement of this rank's part in the single container
+        def exchange(nb):
+            return payload_bases(nb - 64 - 8 * (nch_part + 1), world, dev)
+    r = time_steps(codec, kv, mu, out, dec, args.steps, args.warmup, world, local, exchange)
     nb, bits, clk = r["nb"], r["bits"], r["clk"]
     ms = max_over_ranks(r["ms"], world, dev)
     ms_step = ms / args.steps
-    value = world * raw / (ms_step * 1e-3) / 1e9
+    raw_all = spec.n * bps            # the whole cache, over all ranks
+    value = raw_all / (ms_step * 1e-3) / 1e9
     model_bits = None if args.adaptive else codec.model_bits(kv, mu)
     t_enc, t_dec, t_bits = r["t_enc"], r["t_dec"], r["t_bits"]
 
     # ---- end to end through the C ABI with host buffers ----
     e2e = off = None
     if not args.no_e2e:
-        e2e = end_to_end(P, codec, s, w, ecdf, phat, flags, kv, mu, out, raw, world, dev, args)
+        e2e = end_to_end(P, codec, s, w, ecdf, phat, flags, kv, mu, out, raw, world, dev, args,
+                         raw_all)
         # range decode (the offload paths) takes whole containers only for adaptive counts
         if not args.adaptive:
             kv_h = kv.cpu().pin_memory()
@@ -474,7 +504,7 @@ def run_gpu(args):
     # the other full-size workloads, one after another on the freed device
     del codec, kv, mu, out, dec, w, ecdf, phat
     torch.cuda.empty_cache()
-    if not args.no_extra and args.workload == DEFAULT_WORKLOAD and not (
+    if world == 1 and not args.no_extra and args.workload == DEFAULT_WORKLOAD and not (
             args.order0 or args.adaptive or args.block_scale or args.decode_bisect
             or args.lanes or args.token_block):
         extra = extra_workloads(P, dev, args, rank, world, local)
@@ -499,7 +529,7 @@ def extra_workloads(P, dev, args, rank, world, local):
         if have != name:
             w = None
             torch.cuda.empty_cache()
-            w = synth.make(spec, device=dev, seed=rank_seed(rank))
+            w = synth.make(spec, device=dev, seed=0)
             have = name
         s = spec.scaled(Tb=tb or spec.Tb, G=G or spec.G)
         bps = 2 if s.dtype == synth.BF16 else 1
@@ -532,12 +562,14 @@ def extra_workloads(P, dev, args, rank, world, local):
     return res
 
 
-def end_to_end(P, codec, s, w, ecdf, phat, flags, kv, mu, out, raw, world, dev, args):
+def end_to_end(P, codec, s, w, ecdf, phat, flags, kv, mu, out, raw, world, dev, args,
+               raw_all=None):
     """The step through the C ABI with the inputs in pinned host memory and the
     results read back every step.  Modes that produce the product's single
     container lead; the layer-group split (separate containers) rides along."""
     import torch
     n = s.n
+    raw_all = raw_all or raw          # all ranks' raw bytes: the figures are whole-job
     kv_h = kv.cpu().pin_memory()
     mu_h = None if mu is None else mu.cpu().pin_memory()
     box_h = torch.empty(codec.max_bytes, dtype=torch.uint8).pin_memory()
@@ -577,7 +609,7 @@ def end_to_end(P, codec, s, w, ecdf, phat, flags, kv, mu, out, raw, world, dev, 
         raise RuntimeError("end-to-end round trip mismatch")
     # the median step: a single slow step (the host side) does not set the figure
     e2e_s = max_over_ranks(statistics.median(ts), world, dev)
-    staged_e2e = {"value": round(world * raw / e2e_s / 1e9, 3), "unit": "GB/s",
+    staged_e2e = {"value": round(raw_all / e2e_s / 1e9, 3), "unit": "GB/s",
                   "h2d_bytes_per_step": int(raw + mub * n + nb2),
                   "d2h_bytes_per_step": int(nb2 + raw + 8 + 3 * 32),
                   "mode": "one container: staging copies to and from device buffers "
@@ -597,16 +629,20 @@ def end_to_end(P, codec, s, w, ecdf, phat, flags, kv, mu, out, raw, world, dev, 
     if not torch.equal(kv_back, kv_h):
         raise RuntimeError("zero-copy round trip mismatch")
     zc_s = max_over_ranks(statistics.median(ts), world, dev)
-    zc = {"value": round(world * raw / zc_s / 1e9, 3), "unit": "GB/s",
+    zc = {"value": round(raw_all / zc_s / 1e9, 3), "unit": "GB/s",
           "h2d_bytes_per_step": int(2 * raw + mub * n + nb3 + mub * n + raw + mub * n),
           "d2h_bytes_per_step": int(nb3 + raw + 8 + 3 * 32),
           "mode": "one container: kernels read and write pinned host memory over the link",
           "step_s_spread": spread(ts)}
     del box_h
     modes = [zc, staged_e2e]
+    single = e2e_single_pipelined(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all, world,
+                                  dev, args)
+    if single:
+        modes.append(single)
     groups = []
     for to_host in (False, True):
-        g = e2e_pipelined(P, s, w, ecdf, phat, flags, kv_h, mu_h, raw, world, dev, args,
+        g = e2e_pipelined(P, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all, world, dev, args,
                           decode_to_host=to_host)
         if g:
             groups.append(g)
@@ -615,6 +651,94 @@ def end_to_end(P, codec, s, w, ecdf, phat, flags, kv, mu, out, raw, world, dev, 
     e2e = dict(modes[0])
     e2e["other_modes"] = modes[1:] + sorted(groups, key=lambda m: -m["value"])
     return e2e
+
+
+def e2e_single_pipelined(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all, world, dev,
+                         args, groups=4, ranges=4):
+    """The end-to-end step writing one container, pipelined: the layer groups'
+    inputs are copied in on a copy stream while the groups already in are
+    encoded (skv_encode_range) and their ideal bits computed; skv_encode_finish
+    writes the container; its copy out and the copies out of the decoded
+    cache, range by range, overlap the range decodes (skv_decode_range)."""
+    import torch
+    if s.L % groups or mu_h is None or flags & P.SKV_FLAG_ADAPTIVE:
+        return None
+    main = torch.cuda.current_stream()
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    lp = s.L // groups
+    per = kv_h.numel() // groups
+    nc = codec.num_chunks()
+    cpg = nc // groups
+    gcodecs = [P.Codec(s.dtype, lp, s.H, s.T, s.D, s.Tb, s.G,
+                       w.sigma[g * lp:(g + 1) * lp].to(dev).contiguous(), ecdf, phat, flags=flags)
+               for g in range(groups)]
+    kv_d = torch.empty(kv_h.numel(), dtype=kv_h.dtype, device=dev)
+    mu_d = torch.empty(mu_h.numel(), dtype=mu_h.dtype, device=dev)
+    box_d = torch.empty(codec.max_bytes, dtype=torch.uint8, device=dev)
+    back_d = torch.empty_like(kv_d)
+    back_h = torch.empty_like(kv_h).pin_memory()
+    cuts = [nc * i // ranges for i in range(ranges + 1)]
+    per_chunk = s.Tb * s.D       # scalars of a full chunk (token blocks divide T here)
+    state = {"box_h": None}
+
+    def step():
+        evs = []
+        with torch.cuda.stream(cin):
+            for g in range(groups):
+                kv_d[g * per:(g + 1) * per].copy_(kv_h[g * per:(g + 1) * per], non_blocking=True)
+                mu_d[g * per:(g + 1) * per].copy_(mu_h[g * per:(g + 1) * per], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cin)
+                evs.append(ev)
+        bits = 0.0
+        for g in range(groups):
+            main.wait_event(evs[g])
+            codec.encode_range(kv_d, mu_d, g * cpg, (g + 1) * cpg, first=(g == 0), stream=main)
+            bits += gcodecs[g].ideal_bits(kv_d[g * per:(g + 1) * per], mu_d[g * per:(g + 1) * per],
+                                          stream=main)
+        _, nb = codec.encode_finish(out=box_d, stream=main)
+        if state["box_h"] is None or state["box_h"].numel() < nb:
+            state["box_h"] = torch.empty(nb, dtype=torch.uint8).pin_memory()
+        box_h = state["box_h"]
+        cout.wait_stream(main)
+        with torch.cuda.stream(cout):
+            box_h[:nb].copy_(box_d[:nb], non_blocking=True)
+        for r in range(ranges):
+            codec.decode_range(box_d, nb, cuts[r], cuts[r + 1], mu_d, back_d, first=(r == 0),
+                               stream=main)
+            ev = torch.cuda.Event()
+            ev.record(main)
+            cout.wait_event(ev)
+            a, b = cuts[r] * per_chunk, cuts[r + 1] * per_chunk
+            with torch.cuda.stream(cout):
+                back_h[a:b].copy_(back_d[a:b], non_blocking=True)
+        codec.decode_status(stream=main)
+        cout.synchronize()
+        return nb, bits
+
+    if s.T % s.Tb:
+        return None
+    for _ in range(max(1, args.warmup)):
+        step()
+    barrier(world)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        nb, _ = step()
+        ts.append(time.perf_counter() - t0)
+    if not torch.equal(back_h, kv_h):
+        raise RuntimeError("pipelined single-container round trip mismatch")
+    dt = max_over_ranks(statistics.median(ts), world, dev)
+    return {"value": round(raw_all / dt / 1e9, 3), "unit": "GB/s",
+            "h2d_bytes_per_step": int(kv_h.numel() * kv_h.element_size() + 2 * s.n),
+            "d2h_bytes_per_step": int(nb + kv_h.numel() * kv_h.element_size() + 8 * groups
+                                      + 32 * (groups + 2)),
+            "mode": "one container, pipelined: %d layer groups copied in while earlier groups "
+                    "are encoded (skv_encode_range) and their ideal bits computed, then "
+                    "skv_encode_finish; the container and %d decoded chunk ranges "
+                    "(skv_decode_range) copied out while later ranges decode" % (groups, ranges),
+            "container_bytes": int(nb), "step_s_spread": spread(ts)}
 
 
 def spread(ts):
@@ -694,7 +818,7 @@ def e2e_pipelined(P, s, w, ecdf, phat, flags, kv_h, mu_h, raw, world, dev, args,
         if not torch.equal(gr["back_h"], gr["kv_h"]):
             raise RuntimeError("pipelined end-to-end round trip mismatch")
     nbs = sum(gr["nb"] for gr in groups)
-    return {"value": round(world * raw / dt / 1e9, 3), "unit": "GB/s",
+    return {"value": round(raw / dt / 1e9, 3), "unit": "GB/s",
             "h2d_bytes_per_step": int(raw + 2 * s.n),
             "d2h_bytes_per_step": int(nbs + raw + parts * (8 + 3 * 32)),
             "mode": "%d layer groups, each its own container on its own stream and host "
@@ -826,14 +950,17 @@ def finish_line(args, rank, world, s, n, nb, bits, model_bits, bps, ms_step, val
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "int64",
         "data": "synthetic",
         "config": {"workload": args.workload, "symbols": "bf16" if bps == 2 else "e4m3",
-                   "layers": s.L, "heads": s.H, "tokens": s.T, "head_dim": s.D,
+                   "layers": s.L * world if world == 1 else synth.WORKLOADS[args.workload].L,
+                   "heads": s.H, "tokens": s.T, "head_dim": s.D,
                    "scalars_per_gpu": n, "token_block": s.Tb, "lanes": s.G,
                    "block_scale": bool(args.block_scale),
                    "coder": coder_name(args),
-                   "parallelism": "dp%d (independent caches)" % world,
+                   "parallelism": "one GPU" if world == 1 else
+                                  "the cache's layers split over %d ranks: one container, one "
+                                  "all-gather of the parts' payload sizes per step" % world,
                    "l2": "inputs larger than L2: %.0f MB KV + %.0f MB mu per step" % (
                        raw / 1e6, 2 * n / 1e6)},
         "encode_gbs": round(raw / (med["encode"] * 1e-3) / 1e9, 2),

@@ -171,31 +171,40 @@ def _calibrate(spec: Spec, scale: torch.Tensor, device):
     return counts, rms
 
 
-def make(spec: Spec | str, device="cpu", seed: int = 0) -> Workload:
-    """Draw the evaluation cache (seed 0 by default) and its calibration tables."""
+def make(spec: Spec | str, device="cpu", seed: int = 0, layers=None) -> Workload:
+    """Draw the evaluation cache (seed 0 by default) and its calibration tables.
+
+    layers = (l0, l1): only layers l0 .. l1 - 1 of that cache, as a workload of
+    l1 - l0 layers (what one rank holds when a cache is split by layers): the
+    same bytes as those layers of the whole draw, with their rows of the sigma
+    table; the calibration histogram is the whole cache's."""
     if isinstance(spec, str):
         spec = WORKLOADS[spec]
     device = torch.device(device)
     scale = channel_scale(spec, device)
-    shape = (spec.L, 2, spec.H, spec.T, spec.D)
+    l0, l1 = layers if layers is not None else (0, spec.L)
+    if not 0 <= l0 < l1 <= spec.L:
+        raise ValueError("layer range %r outside 0..%d" % (layers, spec.L))
+    part = spec if (l0, l1) == (0, spec.L) else spec.scaled(L=l1 - l0)
+    shape = (l1 - l0, 2, spec.H, spec.T, spec.D)
     x = torch.empty(shape, dtype=torch.bfloat16, device=device)
     mu = torch.empty(shape, dtype=torch.bfloat16, device=device)
-    for l in range(spec.L):
-        x[l], mu[l] = _draw_layer(spec, scale[l], seed, l, spec.T, device)
+    for l in range(l0, l1):
+        x[l - l0], mu[l - l0] = _draw_layer(spec, scale[l], seed, l, spec.T, device)
     sigma_c = (spec.sigma_c * scale).float()
     if spec.dtype == BF16:
         counts, rms = _calibrate(spec, scale, device)
         sigma = rms if spec.calibrated_sigma else sigma_c
-        return Workload(spec, x, mu, sigma.contiguous(), counts)
+        return Workload(part, x, mu, sigma[l0:l1].contiguous(), counts)
     # e4m3: per-(layer, head) absmax / 448 scale shared by K and V
     s = x.float().abs().amax(dim=(1, 3, 4)) / 448.0          # [L, H]
     s = torch.where(s > 0, s, torch.ones_like(s))
     sb = s[:, None, :, None, None]
     x8 = (x.float() / sb).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
     mu8 = (mu.float() / sb).to(torch.bfloat16)
-    sigma = (sigma_c / s[:, None, :, None]).float().contiguous()
+    sigma = (sigma_c[l0:l1] / s[:, None, :, None]).float().contiguous()
     del x, mu
-    return Workload(spec, x8.contiguous(), mu8.contiguous(), sigma, None, s)
+    return Workload(part, x8.contiguous(), mu8.contiguous(), sigma, None, s)
 
 
 def to_numpy(w: Workload):

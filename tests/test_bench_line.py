@@ -73,7 +73,7 @@ def test_json_line_keys(fixed_peaks):
               "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
         assert k in line, k
     assert line["metric"] == bench.METRIC and line["unit"] == "GB/s" and line["n_gpus"] == 1
-    assert line["higher_is_better"] is True and line["scaling"] == "weak"
+    assert line["higher_is_better"] is True and line["scaling"] == "strong"
     assert line["config"]["workload"] == spec.name
     assert line["gpu_launches"] == 12 * 30   # 12 kernels per bf16 step
     assert line["bits_per_scalar"] == pytest.approx(8.0 * nb / N, abs=1e-5)
