@@ -168,26 +168,31 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-# Algorithmic work per scalar, in thread-instructions (the per-unit figures of
-# this path): one cum evaluation is about 50 (bf16: two Phi_q, one
-# E_q load, the integer mix) or 25 (e4m3); encode = 2 evaluations + the 64/32
-# divide + renormalisation = 200 / 130; decode's minimum = the 2 evaluations
-# that verify the symbol + the state update, the stream read and the store =
-# 120 / 70; ideal bits = two Gaussian bin masses, the p-hat term and a 3-term
-# log-sum-exp = 100 (bf16), one bin mass = 50 (e4m3).
-ALG_OPS = {2: {"encode": 200, "decode": 120, "ideal_bits": 100},
-           1: {"encode": 130, "decode": 70, "ideal_bits": 50},
+# Algorithmic work per scalar, in thread-instructions.  The irreducible part
+# of every operation is the pair of exact cum evaluations that gives a symbol's
+# frequency; its cost is measured: k_model_bits does exactly that pair per
+# scalar (with the symbol's loads and rank, and a log2), and ncu counts 170
+# thread-instructions per scalar for bf16 and 105 for e4m3 (profiles/
+# k_model_bits_cum_pair.md).  On top of it: encode's 64/32 divide and
+# renormalisation (~30 bf16, ~25 e4m3), decode's state update, stream read and
+# store (~20), whatever its search costs.  Ideal bits: two Gaussian bin masses,
+# the p-hat term and a logarithm (100 bf16, 50 e4m3: estimates).
+ALG_OPS = {2: {"encode": 200, "decode": 190, "ideal_bits": 100},
+           1: {"encode": 130, "decode": 125, "ideal_bits": 50},
            # order-0 baseline: one cum evaluation is an E_q load, a multiply and
            # a shift (about 8); encode = 2 of them + the divide + renorm = 100;
            # decode = the table bracket + ~6 bisection steps + 2 evaluations +
-           # the state update = 90; ideal bits = one log2 = 20
+           # the state update = 90; ideal bits = one log2 = 20 (estimates)
            "o0": {"encode": 100, "decode": 90, "ideal_bits": 20}}
 OPS_BASIS = {
-    "encode": "per scalar: 2 cum evaluations, the 64/32 divide, renormalisation",
-    "decode": "per scalar, the algorithmic minimum: the 2 cum evaluations that verify the "
-              "symbol, the state update, the stream read and the store (a 16-step "
-              "bisection would add ~15 evaluations)",
-    "ideal_bits": "per scalar: the Gaussian bin masses, the p-hat term and the logarithm"}
+    "encode": "per scalar: the exact cum pair (measured by ncu on k_model_bits: 170 bf16 / "
+              "105 e4m3 thread-instructions) + the 64/32 divide and renormalisation (estimate)",
+    "decode": "per scalar, the minimum any decoder of this model executes: the exact cum pair "
+              "that verifies the symbol (measured by ncu on k_model_bits: 170 bf16 / 105 e4m3 "
+              "thread-instructions) + the state update, stream read and store (estimate, ~20); "
+              "no search",
+    "ideal_bits": "per scalar: the Gaussian bin masses, the p-hat term and the logarithm "
+                  "(estimate)"}
 KERNEL = {"encode": "k_encode", "decode": "k_decode", "ideal_bits": "k_ideal"}
 KERNEL_O0 = {"encode": "k_encode", "decode": "k_decode_o0", "ideal_bits": "k_ideal"}
 
@@ -459,6 +464,8 @@ def run_gpu(args):
         args.token_block = 128   # the entropy-estimation page's N_update
     if args.lanes or args.token_block:
         spec = spec.scaled(G=args.lanes or spec.G, Tb=args.token_block or spec.Tb)
+    if args.layers:
+        spec = spec.scaled(L=args.layers)   # a smaller case of the same recipe (profiling)
     # one cache; under torchrun each rank holds and codes a contiguous layer range of it
     l0, l1 = layer_range(rank, world, spec.L)
     w = synth.make(spec, device=dev, seed=0, layers=(l0, l1))
@@ -506,7 +513,7 @@ def run_gpu(args):
     torch.cuda.empty_cache()
     if world == 1 and not args.no_extra and args.workload == DEFAULT_WORKLOAD and not (
             args.order0 or args.adaptive or args.block_scale or args.decode_bisect
-            or args.lanes or args.token_block):
+            or args.lanes or args.token_block or args.layers):
         extra = extra_workloads(P, dev, args, rank, world, local)
         if line is not None:
             line["workloads"] = extra
@@ -829,7 +836,7 @@ def e2e_pipelined(P, s, w, ecdf, phat, flags, kv_h, mu_h, raw, world, dev, args,
             "container_bytes": int(nbs)}
 
 
-def offload(codec, out, nb, kv, kv_h, mu, s, raw, world, dev, args, pieces=2):
+def offload(codec, out, nb, kv, kv_h, mu, s, raw, world, dev, args, pieces=4):
     """The cache held compressed in pinned host memory and brought back to the
     device where mu is (the pages' section "该方法的用途"): raw KV bytes delivered
     per second by (a) a plain copy of the raw cache over the link, (b) decoding
@@ -953,7 +960,7 @@ def finish_line(args, rank, world, s, n, nb, bits, model_bits, bps, ms_step, val
         "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "int64",
         "data": "synthetic",
         "config": {"workload": args.workload, "symbols": "bf16" if bps == 2 else "e4m3",
-                   "layers": s.L * world if world == 1 else synth.WORKLOADS[args.workload].L,
+                   "layers": s.L if world == 1 else args.layers or synth.WORKLOADS[args.workload].L,
                    "heads": s.H, "tokens": s.T, "head_dim": s.D,
                    "scalars_per_gpu": n, "token_block": s.Tb, "lanes": s.G,
                    "block_scale": bool(args.block_scale),
@@ -1067,6 +1074,8 @@ def main(argv=None):
                     help="measure the named workload only (not the FP8 and long-context caches)")
     ap.add_argument("--lanes", type=int, default=0, help="override the workload's lanes per chunk")
     ap.add_argument("--token-block", type=int, default=0, help="override the token block")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="only the first N layers' shape (a smaller case for profiling)")
     ap.add_argument("--decode-bisect", action="store_true",
                     help="decode with the reference bisection search")
     ap.add_argument("--block-scale", action="store_true",
