@@ -315,7 +315,8 @@ int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void 
  * symbol is -log2 of its probability.)
  *   per_scalar    device fp32 [N] output, or NULL.
  *   total         host; receives the sum in bits (fp64, fixed order).
- * Per-scalar values are fp32 (within 1e-6 relative + 1e-7 bits of exact).
+ * Per-scalar values are fp32: costs below one bit through log1p of the exact
+ * complement, others as M - log2(freq), within 4e-6 bits of exact.
  * Workspace: skv_workspace_bytes(..., SKV_OP_MODEL_BITS).  Rejects
  * SKV_FLAG_ADAPTIVE (SKV_ERR_ARG).  Errors: SKV_ERR_ARG, SKV_ERR_CAPACITY
  * (workspace), SKV_ERR_SYMBOL, SKV_ERR_PARAM, SKV_ERR_CUDA.  Synchronizes. */
