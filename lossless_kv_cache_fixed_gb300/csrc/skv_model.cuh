@@ -111,12 +111,13 @@ __device__ __forceinline__ uint32_t cum_bf16(int32_t r, float mu, ChanInv inv, c
   return (uint32_t)(v / 100u) + (uint32_t)r;
 }
 
-// cum(r) for e4m3: floor(K Phi_q(z1) / 2^26) + r.
+// cum(r) for e4m3: floor(K Phi_q(z1) / 2^26) + r; K Phi_q / 2^26 =
+// (Phi_q K 2^6) / 2^32 exactly, one multiply-high (Phi_q <= 2^26, K 2^6 < 2^23).
 __device__ __forceinline__ uint32_t cum_e4m3(int32_t r, float mu, float inv_s, const uint2 *phi,
                                              const float *lo8) {
   float d = __fsub_rn(lo8[r], mu);
   uint32_t p = phi_q(__fmul_rn(d, inv_s), phi);
-  return (uint32_t)(((uint64_t)kKE4m3 * p) >> 26) + (uint32_t)r;
+  return __umulhi(p, kKE4m3 << 6) + (uint32_t)r;
 }
 
 // Estimate of y / f = y * rf using only 32-bit conversions (64-bit integer
