@@ -642,8 +642,9 @@ __device__ __forceinline__ int32_t rank_of_value(float x) {
 // verified with cum(r), cum(r+1); (2) if it missed, one Newton step in value
 // space with that bin's exact density, verified the same way; (3) lanes still
 // unresolved are finished one at a time by the whole warp, 32 candidates per
-// step.  Every answer is checked by the exact cum bracket, so both searches
-// return the same symbol.
+// step: first 16 stepping inwards from each end of the lane's bracket (its
+// answer is usually close to one of them), then evenly spread.  Every answer
+// is checked by the exact cum bracket, so both searches return the same symbol.
 // First scalar of chunk c in mu and in the output: its place in the
 // [L][2][H][T][D] tensor, or its page in a page pool (then an out-of-range
 // page index is an argument error and the chunk is skipped).
@@ -882,12 +883,24 @@ __global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunc
             int32_t bhi = __shfl_sync(0xFFFFFFFFu, br.hi, l);
             uint32_t bclo = __shfl_sync(0xFFFFFFFFu, br.clo, l);
             uint32_t bchi = __shfl_sync(0xFFFFFFFFu, br.chi, l);
-            for (int it = 0; it < 8 && bhi - blo > 1; ++it) {
+            for (int it = 0; it < 12 && bhi - blo > 1; ++it) {
               const int32_t wdt = bhi - blo;
               const int32_t nact = min(wdt - 1, 32);
-              const int32_t cand = wdt - 1 <= 32
-                                       ? blo + 1 + lane
-                                       : blo + (int32_t)(((int64_t)(lane + 1) * wdt) / 33);
+              int32_t cand;
+              if (wdt - 1 <= 32) {
+                cand = blo + 1 + lane;
+              } else if (it == 0 && wdt > 2 * 256 + 1) {
+                // first round on a wide bracket: the answer lies next to one of
+                // its ends far more often than in its middle (after Newton,
+                // within 256 ranks of an end for ~96% of lanes, within one rank
+                // for ~30%), so 16 candidates step inwards from each end,
+                // 1, 2, 3, 4, 6, 8, 12, ..., 192, 256 ranks away (ascending)
+                const int j = lane < 16 ? lane : 31 - lane;
+                const int32_t g = j < 4 ? j + 1 : (3 + ((j - 4) & 1)) << (((j - 4) >> 1) + 1);
+                cand = lane < 16 ? blo + g : bhi - g;
+              } else {
+                cand = blo + (int32_t)(((int64_t)(lane + 1) * wdt) / 33);
+              }
               const bool act = lane < nact;
               const uint32_t cv = act ? cum_of<DT>(cand, s_mu, s_inv, s_phi, s_lo8, a.ecdf) : 0u;
               const int kle = __popc(__ballot_sync(0xFFFFFFFFu, act && cv <= s_slot));
