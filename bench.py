@@ -661,12 +661,14 @@ def end_to_end(P, codec, s, w, ecdf, phat, flags, kv, mu, out, raw, world, dev, 
 
 
 def e2e_single_pipelined(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all, world, dev,
-                         args, groups=4, ranges=4):
+                         args, groups=8, ranges=4, decode_to_host=False):
     """The end-to-end step writing one container, pipelined: the layer groups'
     inputs are copied in on a copy stream while the groups already in are
     encoded (skv_encode_range) and their ideal bits computed; skv_encode_finish
     writes the container; its copy out and the copies out of the decoded
-    cache, range by range, overlap the range decodes (skv_decode_range)."""
+    cache, range by range, overlap the range decodes (skv_decode_range).
+    decode_to_host: one decode writes the cache straight into the pinned host
+    buffer instead (its stores cross the link while it runs)."""
     import torch
     if s.L % groups or mu_h is None or flags & P.SKV_FLAG_ADAPTIVE:
         return None
@@ -710,15 +712,18 @@ def e2e_single_pipelined(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
         cout.wait_stream(main)
         with torch.cuda.stream(cout):
             box_h[:nb].copy_(box_d[:nb], non_blocking=True)
-        for r in range(ranges):
-            codec.decode_range(box_d, nb, cuts[r], cuts[r + 1], mu_d, back_d, first=(r == 0),
-                               stream=main)
-            ev = torch.cuda.Event()
-            ev.record(main)
-            cout.wait_event(ev)
-            a, b = cuts[r] * per_chunk, cuts[r + 1] * per_chunk
-            with torch.cuda.stream(cout):
-                back_h[a:b].copy_(back_d[a:b], non_blocking=True)
+        if decode_to_host:
+            codec.decode_range(box_d, nb, 0, nc, mu_d, back_h, first=True, stream=main)
+        else:
+            for r in range(ranges):
+                codec.decode_range(box_d, nb, cuts[r], cuts[r + 1], mu_d, back_d, first=(r == 0),
+                                   stream=main)
+                ev = torch.cuda.Event()
+                ev.record(main)
+                cout.wait_event(ev)
+                a, b = cuts[r] * per_chunk, cuts[r + 1] * per_chunk
+                with torch.cuda.stream(cout):
+                    back_h[a:b].copy_(back_d[a:b], non_blocking=True)
         codec.decode_status(stream=main)
         cout.synchronize()
         return nb, bits
@@ -743,8 +748,11 @@ def e2e_single_pipelined(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
                                       + 32 * (groups + 2)),
             "mode": "one container, pipelined: %d layer groups copied in while earlier groups "
                     "are encoded (skv_encode_range) and their ideal bits computed, then "
-                    "skv_encode_finish; the container and %d decoded chunk ranges "
-                    "(skv_decode_range) copied out while later ranges decode" % (groups, ranges),
+                    "skv_encode_finish; %s" % (
+                        groups, "the container copied out while one decode writes the cache "
+                        "straight into pinned host memory" if decode_to_host else
+                        "the container and %d decoded chunk ranges (skv_decode_range) copied "
+                        "out while later ranges decode" % ranges),
             "container_bytes": int(nb), "step_s_spread": spread(ts)}
 
 
