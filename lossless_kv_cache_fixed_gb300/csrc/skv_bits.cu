@@ -285,7 +285,6 @@ template <int DT, bool O0>
 __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
   __shared__ float s_lo8[256];
   __shared__ double s_part[256];
-  __shared__ float s_bits[8 * 256];
   __shared__ uint32_t s_ring[8 * kIdealRing];
   if (DT == 1) {
     // e4m3 bin edges: midpoints of neighbouring values, +-inf at the ends
@@ -352,7 +351,11 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
       }
       if (!O0) mu4 = __ldg(reinterpret_cast<const uint4 *>(a.mu + i0));
     }
-#pragma unroll 1
+    // Unrolled: only the common cases are inlined here (the rare ones wait in
+    // the ring, below), so eight copies stay small, and the symbols, mu and
+    // the results are picked from registers with constant indices.
+    float bits[8];
+#pragma unroll
     for (int k = 0; k < 8; ++k) {
       bool deferred = false;
       float b = 0.0f;
@@ -365,7 +368,7 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
         b = ideal_one<DT, false>(sym_at<DT>(kv4, k), mu_at(mu4, k), __ldg(sig + srow + k),
                                  a.phat, s_lo8, flags, deferred);
       }
-      s_bits[k * 256 + threadIdx.x] = b;
+      bits[k] = b;
       if (kDefer) {
         const uint32_t dm = __ballot_sync(0xFFFFFFFFu, deferred);
         if (deferred)
@@ -375,12 +378,9 @@ __global__ void __launch_bounds__(256) k_ideal(IdealLaunch a) {
       }
     }
     if (act) {
-      float bits[8], part = 0.0f;
+      float part = 0.0f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        bits[k] = s_bits[k * 256 + threadIdx.x];
-        part += bits[k];
-      }
+      for (int k = 0; k < 8; ++k) part += bits[k];
       acc += (double)part;
       if (a.per_scalar) {
         float4 *o = reinterpret_cast<float4 *>(a.per_scalar + i0);
