@@ -196,8 +196,9 @@ cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, int n, cudaStream_t
 // Encode: one thread per lane, rounds descending, lanes descending.
 // ------------------------------------------------------------------------
 
-template <int DT, bool O0>
-__global__ void __launch_bounds__(kCodeThreads, 1) k_encode(EncodeLaunch a) {
+// NT: most threads per block (the register budget follows from it).
+template <int DT, bool O0, int NT = kCodeThreads>
+__global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
   extern __shared__ uint2 s_phi[];
   float *s_lo8 = reinterpret_cast<float *>(s_phi + kPhiKnots);
   stage_tables(s_phi, s_lo8);
@@ -533,29 +534,37 @@ cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s) {
   return launch_encode_finish(a, s);
 }
 
+template <int DT, bool O0, int NT>
+static cudaError_t run_encode(const EncodeLaunch &a, int blocks, int threads, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(k_encode<DT, O0, NT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kCodeSmem);
+  if (e != cudaSuccess) return e;
+  k_encode<DT, O0, NT><<<blocks, threads, kCodeSmem, s>>>(a);
+  return cudaGetLastError();
+}
+
+// bf16 encode launches with more tasks than one round of 768-thread blocks
+// run 896-thread blocks (72 registers instead of 78): 32B shape encode 197 ->
+// 208 GB/s.  Single-round launches (the 0.6B shape: 209 -> 200) and e4m3
+// (8B shape: 157 -> 140) lose with them and keep 768.
+constexpr int kEncMultiRoundThreads = 896;
+
 cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s) {
   const int64_t ntasks = (a.c_count * a.geo.G + 31) / 32;
   if (ntasks == 0) return cudaSuccess;
   int blocks, threads;
-  task_shape(ntasks, kCodeThreads, blocks, threads);
-  cudaError_t e;
   if (a.dtype == 0 && a.order0) {
-    e = cudaFuncSetAttribute(k_encode<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kCodeSmem);
-    if (e != cudaSuccess) return e;
-    k_encode<0, true><<<blocks, threads, kCodeSmem, s>>>(a);
-  } else if (a.dtype == 0) {
-    e = cudaFuncSetAttribute(k_encode<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kCodeSmem);
-    if (e != cudaSuccess) return e;
-    k_encode<0, false><<<blocks, threads, kCodeSmem, s>>>(a);
-  } else {
-    e = cudaFuncSetAttribute(k_encode<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kCodeSmem);
-    if (e != cudaSuccess) return e;
-    k_encode<1, false><<<blocks, threads, kCodeSmem, s>>>(a);
+    task_shape(ntasks, kCodeThreads, blocks, threads);
+    return run_encode<0, true, kCodeThreads>(a, blocks, threads, s);
   }
-  return cudaGetLastError();
+  if (a.dtype == 0) {
+    task_shape(ntasks, kCodeThreads, blocks, threads, kEncMultiRoundThreads);
+    if (threads > kCodeThreads)
+      return run_encode<0, false, kEncMultiRoundThreads>(a, blocks, threads, s);
+    return run_encode<0, false, kCodeThreads>(a, blocks, threads, s);
+  }
+  task_shape(ntasks, kCodeThreads, blocks, threads);
+  return run_encode<1, false, kCodeThreads>(a, blocks, threads, s);
 }
 
 cudaError_t launch_encode_finish(const EncodeLaunch &a, cudaStream_t s) {
