@@ -52,3 +52,32 @@ def container_chunk(buf_host: np.ndarray, nchunks: int, c: int) -> np.ndarray:
     head = 64 + 8 * (nchunks + 1)
     offs = buf_host[64:head].view(np.uint64)
     return buf_host[head + int(offs[c]): head + int(offs[c + 1])].view(np.uint32)
+
+
+def check_model_bits(O, codec, m, kv_d, mu_d, kv, mu, container):
+    """skv_model_bits against the oracle chunk by chunk, and the rANS length
+    invariant on the GPU's own container: every chunk's payload exceeds its
+    model bits by 32 to 64 bits per lane (initial state and flush)."""
+    tot, ps = codec.model_bits(kv_d, mu_d, per_scalar=True)
+    ps = ps.double().cpu().numpy()
+    assert abs(tot - ps.sum()) <= 1e-6 * abs(tot) + 1e-3
+    L, _, H, T, D = m.shape
+    Tb, G = m.s.Tb, m.s.G
+    ntb = (T + Tb - 1) // Tb
+    nc = m.num_chunks()
+    head = 64 + 8 * (nc + 1)
+    offs = container[64:head].view(np.uint64)
+    ref_tot = 0.0
+    for c in range(nc):
+        row, tb = divmod(c, ntb)
+        base = row * T * D + tb * Tb * D
+        n_c = min(Tb, T - tb * Tb) * D
+        ref = O.model_bits_chunk(m, kv, mu, c)
+        ref_tot += ref
+        got = ps[base:base + n_c].sum()
+        assert abs(got - ref) <= 1e-5 * ref + 1e-3, c
+        payload_bits = 8.0 * (int(offs[c + 1]) - int(offs[c]))
+        nsw = (D // 8 + 3) // 4 if m.s.block_scale else 0
+        extra = payload_bits - 32 * nsw - ref
+        assert 32 * G - 1e-3 * ref - 1 <= extra <= 64 * G + 1e-3 * ref + 1, c
+    assert abs(tot - ref_tot) <= 1e-6 * ref_tot + 1e-3

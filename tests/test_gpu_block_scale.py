@@ -4,7 +4,8 @@ prompt and position).
 
 The encoder's scale choice is an exact integer rule, so the CUDA containers
 must equal the oracle's byte for byte; the oracle must decode them; ideal bits
-must match per scalar within 1e-3 relative.  Small cases span several chunks
+must match per scalar within 1e-3 relative, and the coder's model bits per
+chunk within 1e-5.  Small cases span several chunks
 with a ragged last token block, every lane count class, and a head_dim whose
 scale bytes do not fill their last word.  The full-size drift workload is
 checked on an even sample of chunks in the configuration bench.py times.
@@ -14,7 +15,8 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import container_chunk, device_views, gpu_codec, host_views, oracle_model
+from gpu_helpers import (check_model_bits, container_chunk, device_views, gpu_codec, host_views,
+                         oracle_model)
 
 pytestmark = pytest.mark.gpu
 
@@ -56,6 +58,8 @@ def test_block_scale_parity(oracle_mod, name, kw):
     assert rc == 0 and np.array_equal(dec.reshape(-1), kv_h)
     assert torch.equal(codec.decode(buf, nb, mu_d), kv_d)
     assert torch.equal(gpu_codec(w, flags=BS | 1).decode(buf, nb, mu_d), kv_d)  # bisection
+    # model bits under the scales the encoder chose, and the rANS length bound
+    check_model_bits(O, codec, m, kv_d, mu_d, kv_h, mu_h, got)
     tot, ps = codec.ideal_bits(kv_d, mu_d, per_scalar=True)
     ref_tot, ref = O.ideal_bits(m, kv_h, mu_h, 0, kv_h.size, per_scalar=True)
     got_ps = ps.double().cpu().numpy()

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import container_chunk, skv
+from gpu_helpers import check_model_bits, container_chunk, skv
 
 pytestmark = pytest.mark.gpu
 
@@ -63,6 +63,7 @@ def test_order0_parity(oracle_mod, kw):
     rc, dec = O.decode(m, got, None)
     assert rc == 0 and np.array_equal(dec, kv_h)
     assert torch.equal(codec.decode(buf, nb, None), kv_d)
+    check_model_bits(O, codec, m, kv_d, None, kv_h, None, got)
     tot, ps = codec.ideal_bits(kv_d, None, per_scalar=True)
     ref_tot, ref = O.ideal_bits(m, kv_h, None, 0, kv_h.size, per_scalar=True)
     assert np.all(np.abs(ps.double().cpu().numpy() - ref) <= 1e-3 * np.abs(ref) + 1e-6)

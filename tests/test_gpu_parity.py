@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import device_views, gpu_codec, host_views, oracle_model
+from gpu_helpers import check_model_bits, device_views, gpu_codec, host_views, oracle_model
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +41,7 @@ def _roundtrip(O, w, Tb=None, G=None, ideal=True, max_overhead=None):
     # the reference bisection search returns the same symbols
     ref = gpu_codec(w, Tb, G, flags=1).decode(buf, nb, mu_d)
     assert torch.equal(ref, kv_d)
-    _check_model_bits(O, codec, m, kv_d, mu_d, kv, mu, got)
+    check_model_bits(O, codec, m, kv_d, mu_d, kv, mu, got)
     if ideal:
         tot, ps = codec.ideal_bits(kv_d, mu_d, per_scalar=True)
         ref_tot, ref = O.ideal_bits(m, kv, mu, per_scalar=True)
@@ -56,35 +56,6 @@ def _roundtrip(O, w, Tb=None, G=None, ideal=True, max_overhead=None):
             fixed = 512 + 64 * (nc + 1) + 64 * m.s.G * nc
             assert 8.0 * nb <= 1.005 * ref_tot + fixed
     return nb
-
-
-def _check_model_bits(O, codec, m, kv_d, mu_d, kv, mu, container):
-    """skv_model_bits against the oracle chunk by chunk, and the rANS length
-    invariant on the GPU's own container: every chunk's payload exceeds its
-    model bits by 32 to 64 bits per lane (initial state and flush)."""
-    tot, ps = codec.model_bits(kv_d, mu_d, per_scalar=True)
-    ps = ps.double().cpu().numpy()
-    assert abs(tot - ps.sum()) <= 1e-6 * abs(tot) + 1e-3
-    L, _, H, T, D = m.shape
-    Tb, G = m.s.Tb, m.s.G
-    ntb = (T + Tb - 1) // Tb
-    nc = m.num_chunks()
-    head = 64 + 8 * (nc + 1)
-    offs = container[64:head].view(np.uint64)
-    ref_tot = 0.0
-    for c in range(nc):
-        row, tb = divmod(c, ntb)
-        base = row * T * D + tb * Tb * D
-        n_c = min(Tb, T - tb * Tb) * D
-        ref = O.model_bits_chunk(m, kv, mu, c)
-        ref_tot += ref
-        got = ps[base:base + n_c].sum()
-        assert abs(got - ref) <= 1e-5 * ref + 1e-3, c
-        payload_bits = 8.0 * (int(offs[c + 1]) - int(offs[c]))
-        nsw = (D // 8 + 3) // 4 if m.s.block_scale else 0
-        extra = payload_bits - 32 * nsw - ref
-        assert 32 * G - 1e-3 * ref - 1 <= extra <= 64 * G + 1e-3 * ref + 1, c
-    assert abs(tot - ref_tot) <= 1e-6 * ref_tot + 1e-3
 
 
 def test_tiny_bf16_workload(oracle_mod):
