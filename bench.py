@@ -39,11 +39,15 @@ EXTRA_WORKLOADS = (("qwen3-8b-e4m3", 0, 0), ("long-32k-e4m3", 8, 1), ("long-32k-
 # launches of our kernels per step: encode (prep, encode, 2 scans, compact),
 # decode (prep, header check, decode; bf16 adds the inverse p-hat table),
 # ideal bits (prep, bits, final sum); with per-block scales one more in each
-# (scale estimate, scale load, scale estimate)
-def launches_per_step(bf16: bool, block_scale: bool, adaptive_blocks: int = 0) -> int:
+# (scale estimate, scale load, scale estimate).  With the ideal bits inside the
+# encoder (fused_bits) they cost one launch, the final sum, and no scale pass.
+def launches_per_step(bf16: bool, block_scale: bool, adaptive_blocks: int = 0,
+                      fused_bits: bool = False) -> int:
     if adaptive_blocks:   # one phase per token block (tables, chunks, update)
         nb = adaptive_blocks
         return (5 + 3 * nb - 1) + (4 + 2 * nb + nb - 1) + (2 + nb + nb - 1)
+    if fused_bits:
+        return 5 + 1 + (4 if bf16 else 3) + (2 if block_scale else 0)
     return 5 + (4 if bf16 else 3) + 3 + (3 if block_scale else 0)
 
 
@@ -177,13 +181,13 @@ def measured_peaks():
 # renormalisation (~30 bf16, ~25 e4m3), decode's state update, stream read and
 # store (~20), whatever its search costs.  Ideal bits: two Gaussian bin masses,
 # the p-hat term and a logarithm (100 bf16, 50 e4m3: estimates).
-ALG_OPS = {2: {"encode": 200, "decode": 190, "ideal_bits": 100},
-           1: {"encode": 130, "decode": 125, "ideal_bits": 50},
+ALG_OPS = {2: {"encode": 200, "decode": 190, "ideal_bits": 100, "encode_with_bits": 300},
+           1: {"encode": 130, "decode": 125, "ideal_bits": 50, "encode_with_bits": 180},
            # order-0 baseline: one cum evaluation is an E_q load, a multiply and
            # a shift (about 8); encode = 2 of them + the divide + renorm = 100;
            # decode = the table bracket + ~6 bisection steps + 2 evaluations +
            # the state update = 90; ideal bits = one log2 = 20 (estimates)
-           "o0": {"encode": 100, "decode": 90, "ideal_bits": 20}}
+           "o0": {"encode": 100, "decode": 90, "ideal_bits": 20, "encode_with_bits": 120}}
 OPS_BASIS = {
     "encode": "per scalar: the exact cum pair (measured by ncu on k_model_bits: 170 bf16 / "
               "105 e4m3 thread-instructions) + the 64/32 divide and renormalisation (estimate)",
@@ -192,8 +196,10 @@ OPS_BASIS = {
               "thread-instructions) + the state update, stream read and store (estimate, ~20); "
               "no search",
     "ideal_bits": "per scalar: the Gaussian bin masses, the p-hat term and the logarithm "
-                  "(estimate)"}
-KERNEL = {"encode": "k_encode", "decode": "k_decode", "ideal_bits": "k_ideal"}
+                  "(estimate)",
+    "encode_with_bits": "per scalar: encode's figure + ideal bits' figure"}
+KERNEL = {"encode": "k_encode", "decode": "k_decode", "ideal_bits": "k_ideal",
+          "encode_with_bits": "k_encode (ideal bits inside)"}
 KERNEL_O0 = {"encode": "k_encode", "decode": "k_decode_o0", "ideal_bits": "k_ideal"}
 
 
@@ -209,15 +215,20 @@ def issue_peak_gops():
     return sms * 128 * mhz * 1e6 / 1e9, sms, mhz
 
 
-def roofline(med_ms, n, container_bytes, bps, workload, order0=False):
-    """ALU roofline of the dominant kernel (and of each kernel), plus its HBM view."""
+def roofline(med_ms, n, container_bytes, bps, workload, order0=False, fused_bits=True):
+    """ALU roofline of the dominant kernel (and of each kernel), plus its HBM view.
+    encode_with_bits: the encoder with the ideal bits inside (fused_bits) or
+    the encoder and the ideal-bits kernel back to back; its algorithmic bytes
+    are one read of the inputs either way."""
     peak_ops, sms, mhz = issue_peak_gops()
     hbm_peak, peak_kind = measured_peaks()
     cb = container_bytes / n
     mub = 0 if order0 else 2          # the order-0 baseline reads no mu
-    alg_bytes = {"encode": bps + mub + cb, "decode": cb + mub + bps, "ideal_bits": bps + mub}
+    alg_bytes = {"encode": bps + mub + cb, "decode": cb + mub + bps, "ideal_bits": bps + mub,
+                 "encode_with_bits": bps + mub + cb}
     ops_tab = ALG_OPS["o0"] if order0 else ALG_OPS[bps]
-    kname = KERNEL_O0 if order0 else KERNEL
+    kname = dict(KERNEL_O0 if order0 else KERNEL)
+    kname["encode_with_bits"] = KERNEL["encode_with_bits"] if fused_bits else "k_encode + k_ideal"
     kernels = {}
     for op, ms in med_ms.items():
         ops = ops_tab[op] * n / (ms * 1e-3) / 1e9
@@ -389,17 +400,23 @@ def device_inputs(w, order0=False):
     return kv, mu
 
 
-def time_steps(codec, kv, mu, out, dec, steps, warmup, world, clock_index=None, exchange=None):
-    """W untimed steps, then K steps (encode, decode, ideal bits) timed with CUDA
-    events on the launching stream between barriers and synchronisations.
-    exchange(nb), when given, runs after each encode (the ranks' payload sizes)."""
+def time_steps(codec, kv, mu, out, dec, steps, warmup, world, clock_index=None, exchange=None,
+               with_bits=True):
+    """W untimed steps, then K steps timed with CUDA events on the launching
+    stream between barriers and synchronisations.  A step is encode with the
+    ideal bits (skv_encode_with_bits) and decode; with_bits=False (adaptive
+    counts) runs encode, decode and ideal bits apart.  exchange(nb), when
+    given, runs after each encode (the ranks' payload sizes)."""
     import torch
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        _, nb = codec.encode(kv, mu, out=out)
+        if with_bits:
+            _, nb, bits = codec.encode_with_bits(kv, mu, out=out)
+        else:
+            _, nb = codec.encode(kv, mu, out=out)
         if exchange is not None:
             exchange(nb)
         if ev:
@@ -407,7 +424,8 @@ def time_steps(codec, kv, mu, out, dec, steps, warmup, world, clock_index=None, 
         codec.decode(out, nb, mu, out=dec)
         if ev:
             ev[2].record(stream)
-        bits = codec.ideal_bits(kv, mu)
+        if not with_bits:
+            bits = codec.ideal_bits(kv, mu)
         if ev:
             ev[3].record(stream)
         return nb, bits
@@ -428,10 +446,38 @@ def time_steps(codec, kv, mu, out, dec, steps, warmup, world, clock_index=None, 
         stop.record(stream)
         torch.cuda.synchronize()
     barrier(world)
-    return {"ms": start.elapsed_time(stop), "nb": nb, "bits": bits, "clk": clk,
-            "t_enc": [e[0].elapsed_time(e[1]) for e in evs],
-            "t_dec": [e[1].elapsed_time(e[2]) for e in evs],
-            "t_bits": [e[2].elapsed_time(e[3]) for e in evs]}
+    t = {"encode_with_bits" if with_bits else "encode": [e[0].elapsed_time(e[1]) for e in evs],
+         "decode": [e[1].elapsed_time(e[2]) for e in evs]}
+    if not with_bits:
+        t["ideal_bits"] = [e[2].elapsed_time(e[3]) for e in evs]
+    return {"ms": start.elapsed_time(stop), "nb": nb, "bits": bits, "clk": clk, "t": t}
+
+
+def time_alone(codec, kv, mu, out, reps=5):
+    """Median ms of encode and of ideal bits each called on its own (after
+    the timed region, for the per-kernel view when the step runs them as one
+    call)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    res = {}
+    for op, fn in (("encode", lambda: codec.encode(kv, mu, out=out)),
+                   ("ideal_bits", lambda: codec.ideal_bits(kv, mu))):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        res[op] = statistics.median(ts)
+    return res
+
+
+def medians(t):
+    return {op: statistics.median(v) for op, v in t.items()}
 
 
 def size_accounting(n, nb, nchunks, bits, model_bits):
@@ -487,14 +533,18 @@ def run_gpu(args):
         # the placement of this rank's part in the single container
         def exchange(nb):
             return payload_bases(nb - 64 - 8 * (nch_part + 1), world, dev)
-    r = time_steps(codec, kv, mu, out, dec, args.steps, args.warmup, world, local, exchange)
+    with_bits = not args.adaptive     # skv_encode_with_bits takes no adaptive counts
+    r = time_steps(codec, kv, mu, out, dec, args.steps, args.warmup, world, local, exchange,
+                   with_bits=with_bits)
     nb, bits, clk = r["nb"], r["bits"], r["clk"]
     ms = max_over_ranks(r["ms"], world, dev)
     ms_step = ms / args.steps
     raw_all = spec.n * bps            # the whole cache, over all ranks
     value = raw_all / (ms_step * 1e-3) / 1e9
     model_bits = None if args.adaptive else codec.model_bits(kv, mu)
-    t_enc, t_dec, t_bits = r["t_enc"], r["t_dec"], r["t_bits"]
+    med = medians(r["t"])
+    alone = time_alone(codec, kv, mu, out) if with_bits else None
+    fused = codec.encode_with_bits_fused() if with_bits else False
 
     # ---- end to end through the C ABI with host buffers ----
     e2e = off = None
@@ -507,7 +557,7 @@ def run_gpu(args):
             off = offload(codec, out, nb, kv, kv_h, mu, s, raw, world, dev, args)
             del kv_h
     line = finish_line(args, rank, world, s, n, nb, bits, model_bits, bps, ms_step, value,
-                       t_enc, t_dec, t_bits, clk, e2e, w, off)
+                       med, clk, e2e, w, off, alone=alone, fused_bits=fused)
     # the other full-size workloads, one after another on the freed device
     del codec, kv, mu, out, dec, w, ecdf, phat
     torch.cuda.empty_cache()
@@ -549,19 +599,22 @@ def extra_workloads(P, dev, args, rank, world, local):
         ms = max_over_ranks(r["ms"], world, dev) / steps
         raw = s.n * bps
         nch = s.L * 2 * s.H * ((s.T + s.Tb - 1) // s.Tb)
-        med = {"encode": statistics.median(r["t_enc"]), "decode": statistics.median(r["t_dec"]),
-               "ideal_bits": statistics.median(r["t_bits"])}
-        _, kernels = roofline(med, s.n, r["nb"], bps, name)
+        med = medians(r["t"])
+        fused = codec.encode_with_bits_fused()
+        alone = time_alone(codec, kv, mu, out, reps=3)
+        _, kernels = roofline(med, s.n, r["nb"], bps, name, fused_bits=fused)
+        _, k_alone = roofline(alone, s.n, r["nb"], bps, name)
+        med.update(alone)
         key = name if not tb else "%s/%dK" % (name, s.Tb * s.D // 1024)
         ent = {"workload": name, "symbols": "bf16" if bps == 2 else "e4m3",
                "scalars": s.n, "token_block": s.Tb, "lanes": s.G, "chunk_scalars": s.Tb * s.D,
                "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 4),
                "value": round(world * raw / (ms * 1e-3) / 1e9, 3),
-               "encode_gbs": round(raw / (med["encode"] * 1e-3) / 1e9, 2),
-               "decode_gbs": round(raw / (med["decode"] * 1e-3) / 1e9, 2),
-               "ideal_bits_gbs": round(raw / (med["ideal_bits"] * 1e-3) / 1e9, 2)}
+               "fused_bits": fused}
+        ent.update(op_gbs(med, raw))
         ent.update(size_accounting(s.n, r["nb"], nch, r["bits"], mbits))
         ent["kernels"] = kernels
+        ent["kernels_alone"] = k_alone
         ent["clocks"] = r["clk"].summary()
         res[key] = ent
         del codec, kv, mu, out, dec
@@ -919,17 +972,26 @@ def offload(codec, out, nb, kv, kv_h, mu, s, raw, world, dev, args, pieces=4):
             "best_vs_raw_copy": round(max(t_raw / t_dir, t_raw / t_stg), 3)}
 
 
-def finish_line(args, rank, world, s, n, nb, bits, model_bits, bps, ms_step, value, t_enc,
-                t_dec, t_bits, clk, e2e, w, off=None):
+def op_gbs(med, raw):
+    """Raw GB/s of each timed operation: encode_gbs, decode_gbs, ..."""
+    return {op + "_gbs": round(raw / (ms * 1e-3) / 1e9, 2) for op, ms in med.items()}
+
+
+def finish_line(args, rank, world, s, n, nb, bits, model_bits, bps, ms_step, value, med, clk,
+                e2e, w, off=None, alone=None, fused_bits=False):
+    """med: median ms of each operation of the timed step; alone: encode and
+    ideal bits timed on their own after it (when the step runs them as one)."""
     if rank != 0:
         return None
     import synth
     raw = n * bps
 
     # ---- roofline of the dominant kernel ----
-    med = {"encode": statistics.median(t_enc), "decode": statistics.median(t_dec),
-           "ideal_bits": statistics.median(t_bits)}
-    roof, kernels = roofline(med, n, nb, bps, args.workload, order0=args.order0)
+    roof, kernels = roofline(med, n, nb, bps, args.workload, order0=args.order0,
+                             fused_bits=fused_bits)
+    k_alone = None
+    if alone:
+        _, k_alone = roofline(alone, n, nb, bps, args.workload, order0=args.order0)
 
     # ---- oracle on the host cores, bounded sample: one core, then all ----
     cpu = None
@@ -977,11 +1039,15 @@ def finish_line(args, rank, world, s, n, nb, bits, model_bits, bps, ms_step, val
                                   "the cache's layers split over %d ranks: one container, one "
                                   "all-gather of the parts' payload sizes per step" % world,
                    "l2": "inputs larger than L2: %.0f MB KV + %.0f MB mu per step" % (
-                       raw / 1e6, 2 * n / 1e6)},
-        "encode_gbs": round(raw / (med["encode"] * 1e-3) / 1e9, 2),
-        "decode_gbs": round(raw / (med["decode"] * 1e-3) / 1e9, 2),
-        "ideal_bits_gbs": round(raw / (med["ideal_bits"] * 1e-3) / 1e9, 2),
+                       raw / 1e6, 2 * n / 1e6),
+                   "step": ("encode with the ideal bits (skv_encode_with_bits: %s) + decode" % (
+                       "inside the encoder" if fused_bits else "the ideal-bits pass behind the "
+                       "encoder") if "encode_with_bits" in med else
+                       "encode + decode + ideal bits")},
     }
+    line.update(op_gbs(med, raw))
+    if alone:
+        line.update({k.replace("_gbs", "_alone_gbs"): v for k, v in op_gbs(alone, raw).items()})
     nch = s.L * 2 * s.H * ((s.T + s.Tb - 1) // s.Tb)
     if model_bits is not None:
         line.update(size_accounting(n, nb, nch, bits, model_bits))
@@ -992,12 +1058,13 @@ def finish_line(args, rank, world, s, n, nb, bits, model_bits, bps, ms_step, val
     line.update({
         "roofline": roof,
         "kernels": kernels,
+        "kernels_alone": k_alone,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "offload": off,
         "gpu_launches": launches_per_step(bps == 2, args.block_scale,
-                                          s.T // s.Tb + (s.T % s.Tb > 0) if args.adaptive else 0)
-                        * args.steps,
+                                          s.T // s.Tb + (s.T % s.Tb > 0) if args.adaptive else 0,
+                                          fused_bits) * args.steps,
         "clocks": clk.summary(),
     })
     return line

@@ -229,6 +229,34 @@ int skv_decode_range(const skv_params *params, const skv_shape *shape, const voi
  * SKV_ERR_CORRUPT.  Synchronizes `stream`. */
 int skv_decode_status(const void *workspace, skv_stream_t stream);
 
+/* skv_encode and skv_ideal_bits in one call: the container (byte for byte the
+ * one skv_encode writes) and the ideal code length of the cache -- the
+ * per-scalar values and the total skv_ideal_bits gives, within its tolerance
+ * (1e-3 relative + 1e-6 bits per scalar) -- so that a caller gets a coder's
+ * cost and the cross-entropy it should reach side by side (the pages' section
+ * "KV 缓存并非真正随机").  On bf16 mixture caches of more chunk lanes than one
+ * round of the encoder's blocks holds (several tens of millions of scalars and
+ * up), the encoder computes the bits itself from the symbols, mu and
+ * reciprocals in its registers, one read of the inputs for both; elsewhere
+ * the ideal-bits pass runs behind the encoder on the same stream.  The total
+ * is summed in fp64 in a fixed order for a given device and shape.
+ *   per_scalar    device fp32 [N] output, or NULL.
+ *   total         host; receives the ideal bits.
+ * Requires params->phat for bf16; workspace: skv_workspace_bytes(...,
+ * SKV_OP_ENCODE).  Rejects SKV_FLAG_ADAPTIVE (SKV_ERR_ARG).  Other errors as
+ * skv_encode.  Synchronizes. */
+int skv_encode_with_bits(const skv_params *params, const skv_shape *shape, const void *kv,
+                         const uint16_t *mu, void *out, size_t out_capacity, size_t *out_bytes,
+                         float *per_scalar, double *total, void *workspace,
+                         size_t workspace_bytes, skv_stream_t stream);
+
+/* Whether skv_encode_with_bits computes the ideal bits inside the encoder
+ * (*fused = 1: one kernel over the inputs) or runs the ideal-bits pass behind
+ * it (*fused = 0) for this model and shape on the current device (the choice
+ * depends on its SM count).  fused: host.  Errors: SKV_ERR_ARG (NULL fused,
+ * bad params or shape, SKV_FLAG_ADAPTIVE), SKV_ERR_CUDA (no device). */
+int skv_encode_with_bits_fused(const skv_params *params, const skv_shape *shape, int *fused);
+
 /* Encode part of a cache, asynchronously: chunks [chunk_begin, chunk_end) in
  * container order go into the workspace's per-chunk stacks, and a later
  * skv_encode_finish turns the stacks into the container.  A caller can so

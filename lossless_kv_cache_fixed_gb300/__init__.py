@@ -25,8 +25,9 @@ SKV_OK, SKV_ERR_ARG, SKV_ERR_CAPACITY, SKV_ERR_SYMBOL = 0, -1, -2, -3
 SKV_ERR_PARAM, SKV_ERR_CORRUPT, SKV_ERR_CUDA = -4, -5, -6
 NSYM = {SKV_BF16: 65282, SKV_E4M3: 254}
 
-EXPORTS = ("skv_max_encoded_bytes", "skv_workspace_bytes", "skv_encode", "skv_encode_range",
-           "skv_encode_finish", "skv_model_fingerprint", "skv_merge_parts", "skv_decode",
+EXPORTS = ("skv_max_encoded_bytes", "skv_workspace_bytes", "skv_encode", "skv_encode_with_bits",
+           "skv_encode_with_bits_fused", "skv_encode_range", "skv_encode_finish",
+           "skv_model_fingerprint", "skv_merge_parts", "skv_decode",
            "skv_decode_range", "skv_decode_status", "skv_ideal_bits", "skv_model_bits",
            "skv_ideal_bits_noalloc", "skv_ideal_bits_noalloc_max_channels",
            "skv_build_ecdf", "skv_phi_table", "skv_strerror", "skv_version")
@@ -65,6 +66,9 @@ def lib():
             "skv_max_encoded_bytes": (sz, [P, S]),
             "skv_workspace_bytes": (sz, [P, S, C.c_int]),
             "skv_encode": (C.c_int, [P, S, vp, vp, vp, sz, C.POINTER(sz), vp, sz, vp]),
+            "skv_encode_with_bits": (C.c_int, [P, S, vp, vp, vp, sz, C.POINTER(sz), vp,
+                                               C.POINTER(C.c_double), vp, sz, vp]),
+            "skv_encode_with_bits_fused": (C.c_int, [P, S, C.POINTER(C.c_int)]),
             "skv_encode_range": (C.c_int, [P, S, vp, vp, C.c_uint64, C.c_uint64, C.c_int, vp, sz,
                                            vp]),
             "skv_encode_finish": (C.c_int, [P, S, vp, sz, C.POINTER(sz), vp, sz, vp]),
@@ -107,6 +111,24 @@ def skv_encode(params, shape, kv_ptr, mu_ptr, out_ptr, out_capacity, ws_ptr, ws_
     rc = lib().skv_encode(C.byref(params), C.byref(shape), kv_ptr, mu_ptr, out_ptr, out_capacity,
                           C.byref(nb), ws_ptr, ws_bytes, stream)
     return rc, nb.value
+
+
+def skv_encode_with_bits(params, shape, kv_ptr, mu_ptr, out_ptr, out_capacity, per_scalar_ptr,
+                         ws_ptr, ws_bytes, stream):
+    """Returns (status, container bytes, ideal bits)."""
+    nb = C.c_size_t(0)
+    tot = C.c_double(0)
+    rc = lib().skv_encode_with_bits(C.byref(params), C.byref(shape), kv_ptr, mu_ptr, out_ptr,
+                                    out_capacity, C.byref(nb), per_scalar_ptr, C.byref(tot), ws_ptr,
+                                    ws_bytes, stream)
+    return rc, nb.value, tot.value
+
+
+def skv_encode_with_bits_fused(params, shape):
+    """Returns (status, 1 if skv_encode_with_bits computes the bits inside the encoder)."""
+    f = C.c_int(0)
+    rc = lib().skv_encode_with_bits_fused(C.byref(params), C.byref(shape), C.byref(f))
+    return rc, f.value
 
 
 def skv_encode_range(params, shape, kv_ptr, mu_ptr, chunk_begin, chunk_end, range_flags, ws_ptr,
@@ -278,6 +300,30 @@ class Codec:
         if rc:
             raise SkvError(rc, "skv_encode")
         return out, nb
+
+    def encode_with_bits(self, kv, mu, out=None, per_scalar=False, stream=None):
+        """Encode and the ideal code length in one pass: (container, bytes, ideal
+        bits[, per-scalar tensor])."""
+        if out is None:
+            out = self.torch.empty(self.max_bytes, dtype=self.torch.uint8, device=self.device)
+        ps = None
+        if per_scalar:
+            ps = self.torch.empty(self.n, dtype=self.torch.float32, device=self.device)
+        ws = self.workspace(SKV_OP_ENCODE)
+        rc, nb, tot = skv_encode_with_bits(self.params, self.shape, kv.data_ptr(), _ptr(mu),
+                                           out.data_ptr(), out.numel(),
+                                           ps.data_ptr() if ps is not None else None,
+                                           ws.data_ptr(), ws.numel(), _stream_handle(stream))
+        if rc:
+            raise SkvError(rc, "skv_encode_with_bits")
+        return (out, nb, tot, ps) if per_scalar else (out, nb, tot)
+
+    def encode_with_bits_fused(self):
+        """True where encode_with_bits computes the bits inside the encoder."""
+        rc, f = skv_encode_with_bits_fused(self.params, self.shape)
+        if rc:
+            raise SkvError(rc, "skv_encode_with_bits_fused")
+        return bool(f)
 
     def encode_range(self, kv, mu, chunk_begin, chunk_end, first=False, stream=None):
         """Enqueue the encode of chunks [chunk_begin, chunk_end) (no synchronisation)."""

@@ -24,8 +24,6 @@ constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 // The workspace head takes the first kAlign-byte slot of every workspace.
 static_assert(sizeof(WsHead) <= kAlign, "the workspace head must fit one aligned slot");
-// Most blocks of the ideal-bits kernel (one fp64 partial sum each).
-constexpr int64_t kMaxBitsBlocks = 4096;
 
 // ---- host-built model constants ----
 
@@ -122,7 +120,7 @@ struct Plan {
   int64_t nsig_model;  // sigma entries the model reads (0 for the order-0 baseline)
   // workspace layout (byte offsets)
   size_t off_inv, off_sizes, off_starts, off_partials, off_scratch, off_bits, off_einv, total;
-  size_t off_enc_cinv, off_enc_words, enc_total;  // encode: per-chunk tables after the stacks
+  size_t off_enc_cinv, off_enc_words, off_enc_bits, enc_total;  // encode: per-chunk tables after the stacks
   size_t off_dec_cinv, dec_total;                 // decode: after the inverse p-hat table
   size_t off_bits_csig, bits_total;               // ideal bits: after the partial sums
   size_t off_mb_cinv, mb_total;                   // model bits: reciprocals per (chunk, channel)
@@ -202,12 +200,16 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   const size_t ccells = scaled ? (size_t)pl.geo.nchunks * (size_t)s->head_dim : 0;
   pl.off_enc_cinv = pl.total;
   pl.off_enc_words = align_up(pl.off_enc_cinv + sizeof(float2) * ccells);
-  pl.enc_total = align_up(pl.off_enc_words + sizeof(uint32_t) * (size_t)pl.nsw * (size_t)pl.geo.nchunks);
+  pl.off_enc_bits = align_up(pl.off_enc_words + sizeof(uint32_t) * (size_t)pl.nsw * (size_t)pl.geo.nchunks);
+  pl.off_bits_csig = align_up(pl.off_bits + sizeof(double) * (size_t)pl.bits_blocks);
+  pl.bits_total = align_up(pl.off_bits_csig + sizeof(float) * ccells);
+  // skv_encode_with_bits: one fp64 partial sum per encode block when the
+  // encoder computes the bits, else an ideal-bits workspace of its own
+  pl.enc_total = align_up(pl.off_enc_bits +
+                          std::max(sizeof(double) * (size_t)kMaxBitsBlocks, pl.bits_total));
   // the decoder's inverse p-hat table: kHinvN + 1 entries, kO0InvN + 1 for order 0
   pl.off_dec_cinv = align_up(pl.off_einv + sizeof(int32_t) * ((order0 ? kO0InvN : kHinvN) + 1));
   pl.dec_total = align_up(pl.off_dec_cinv + sizeof(float2) * ccells);
-  pl.off_bits_csig = align_up(pl.off_bits + sizeof(double) * (size_t)pl.bits_blocks);
-  pl.bits_total = align_up(pl.off_bits_csig + sizeof(float) * ccells);
   pl.off_mb_cinv = pl.off_bits_csig;
   pl.mb_total = align_up(pl.off_mb_cinv + sizeof(float2) * ccells);
   // adaptive counts: per-row P, C, E (and decode's inverse tables), the token
@@ -316,9 +318,18 @@ EncodeLaunch encode_launch(const skv_params *params, const Plan &pl, uint8_t *ws
 // `stream` without a host synchronisation.  `first` clears the status and the
 // chunk count and prepares the model tables (reciprocals, fingerprint).
 int encode_enqueue(const skv_params *params, const Plan &pl, const void *kv, const uint16_t *mu,
-                   uint64_t c0, uint64_t c1, bool first, void *workspace, cudaStream_t st) {
+                   uint64_t c0, uint64_t c1, bool first, void *workspace, cudaStream_t st,
+                   bool bits = false, float *bits_out = nullptr) {
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   EncodeLaunch a = encode_launch(params, pl, ws);
+  if (bits) {
+    // the ideal code length as it codes: the partial sums start at zero
+    a.bits_partials = reinterpret_cast<double *>(ws + pl.off_enc_bits);
+    a.bits_out = bits_out;
+    a.phat = params->phat;
+    if (cudaMemsetAsync(a.bits_partials, 0, sizeof(double) * kMaxBitsBlocks, st) != cudaSuccess)
+      return SKV_ERR_CUDA;
+  }
   if (first) {
     if (cudaMemsetAsync(a.head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
     if (launch_prep(params->sigma, pl.nsig_model, a.ecdf, const_cast<float2 *>(a.inv), a.head,
@@ -342,6 +353,8 @@ int encode_enqueue(const skv_params *params, const Plan &pl, const void *kv, con
   a.c_first = (int64_t)c0;
   a.c_count = (int64_t)(c1 - c0);
   if (launch_encode_chunks(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  if (bits && launch_ideal_final(a.bits_partials, kMaxBitsBlocks, a.head, st) != cudaSuccess)
+    return SKV_ERR_CUDA;
   return SKV_OK;
 }
 
@@ -349,7 +362,7 @@ int encode_enqueue(const skv_params *params, const Plan &pl, const void *kv, con
 // status back (synchronises).  The chunk count is checked first, so a stack
 // that was never written is never copied.
 int encode_finish(const skv_params *params, const Plan &pl, void *out, size_t out_capacity,
-                  size_t *out_bytes, void *workspace, cudaStream_t st) {
+                  size_t *out_bytes, void *workspace, cudaStream_t st, double *bits = nullptr) {
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   EncodeLaunch a = encode_launch(params, pl, ws);
   WsHead h;
@@ -363,6 +376,7 @@ int encode_finish(const skv_params *params, const Plan &pl, void *out, size_t ou
   if ((rc = read_head(a.head, &h, st))) return rc;
   if ((rc = status_from_flags(h.flags))) return rc;
   *out_bytes = 64 + 8 * (size_t)(pl.geo.nchunks + 1) + (size_t)h.total;
+  if (bits) *bits = h.bits;
   return SKV_OK;
 }
 
@@ -491,6 +505,64 @@ int noalloc_scratch(uint8_t **out) {
   return SKV_OK;
 }
 
+// The ideal-bits pass enqueued on `st` over a workspace of pl.bits_total
+// bytes (its head, reciprocals and partial sums); the total and the status
+// land in that head.
+int ideal_enqueue(const skv_params *params, const Plan &pl, const void *kv, const uint16_t *mu,
+                  float *per_scalar, uint8_t *ws, cudaStream_t st) {
+  WsHead *head = reinterpret_cast<WsHead *>(ws);
+  if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
+  float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
+  // sigma validity only: the p-hat table enters through `phat`
+  if (launch_prep(params->sigma, pl.nsig_model, nullptr, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
+  IdealLaunch a;
+  a.geo = pl.geo;
+  a.dtype = pl.dtype;
+  a.kv = kv;
+  a.mu = mu;
+  a.sigma = params->sigma;
+  a.sigma_chunk = nullptr;
+  a.order0 = pl.order0;
+  if (pl.nsw) {
+    ScaleLaunch sl = scale_launch(pl, params, head);
+    sl.kv = kv;
+    sl.mu = mu;
+    sl.sig = reinterpret_cast<float *>(ws + pl.off_bits_csig);
+    if (launch_scales(sl, st) != cudaSuccess) return SKV_ERR_CUDA;
+    a.sigma_chunk = sl.sig;
+  }
+  a.phat = params->phat;
+  a.per_scalar = per_scalar;
+  a.partials = reinterpret_cast<double *>(ws + pl.off_bits);
+  a.nblocks = pl.bits_blocks;
+  a.td_rcp = ~0ull / ((uint64_t)pl.geo.T * (uint64_t)pl.geo.D);
+  a.head = head;
+  if (pl.adaptive) {
+    // per-row models, one phase per token block, partial sums in a fixed order
+    uint8_t *ad = ws + pl.ad_base_bits;
+    uint64_t *P = reinterpret_cast<uint64_t *>(ad + pl.ad_P);
+    uint64_t *Cn = reinterpret_cast<uint64_t *>(ad + pl.ad_C);
+    uint64_t *W = reinterpret_cast<uint64_t *>(ad + pl.ad_W);
+    double *part = reinterpret_cast<double *>(ad + pl.ad_part);
+    const uint32_t *ecdf = params->ecdf;
+    const uint16_t *kv16 = static_cast<const uint16_t *>(kv);
+    if (launch_ad_init(ecdf, P, Cn, pl.nrows, W, pl.geo.Tb, st) != cudaSuccess) return SKV_ERR_CUDA;
+    for (int64_t b = 0; b < pl.geo.ntb; ++b) {
+      if (launch_ad_ideal(pl.geo, kv16, b, P, per_scalar, part + b * pl.nrows * pl.ad_bx, pl.ad_bx,
+                          head, pl.nrows, st) != cudaSuccess)
+        return SKV_ERR_CUDA;
+      if (b + 1 < pl.geo.ntb &&
+          launch_ad_update(pl.geo, kv16, b, P, Cn, W, head, pl.nrows, st) != cudaSuccess)
+        return SKV_ERR_CUDA;
+    }
+    if (launch_ideal_final(part, (int)(pl.geo.ntb * pl.nrows * pl.ad_bx), head, st) != cudaSuccess)
+      return SKV_ERR_CUDA;
+  } else if (launch_ideal(a, st) != cudaSuccess) {
+    return SKV_ERR_CUDA;
+  }
+  return SKV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -554,6 +626,56 @@ int skv_encode(const skv_params *params, const skv_shape *shape, const void *kv,
       return SKV_ERR_CUDA;
   }
   return encode_finish(params, pl, out, out_capacity, out_bytes, workspace, st);
+}
+
+int skv_encode_with_bits(const skv_params *params, const skv_shape *shape, const void *kv,
+                         const uint16_t *mu, void *out, size_t out_capacity, size_t *out_bytes,
+                         float *per_scalar, double *total, void *workspace,
+                         size_t workspace_bytes, skv_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  // adaptive tables change between token blocks: the two passes apart
+  if (pl.adaptive) return SKV_ERR_ARG;
+  if ((rc = common_inputs(params, pl, kv, mu))) return rc;
+  if (!out || !out_bytes || !total || !workspace || !aligned(out, 8) ||
+      !aligned(workspace, kAlign))
+    return SKV_ERR_ARG;
+  if (per_scalar && !aligned(per_scalar, 16)) return SKV_ERR_ARG;
+  if (pl.dtype == SKV_BF16 && (!params->phat || !aligned(params->phat, 4))) return SKV_ERR_ARG;
+  if (workspace_bytes < ws_bytes_for(pl, SKV_OP_ENCODE)) return SKV_ERR_CAPACITY;
+  if ((rc = ensure_device_tables())) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  if (encode_fuses_bits(pl.dtype == SKV_BF16 ? 0 : 1, pl.order0, pl.geo.nchunks, pl.geo.G)) {
+    if ((rc = encode_enqueue(params, pl, kv, mu, 0, (uint64_t)pl.geo.nchunks, true, workspace, st,
+                             true, per_scalar)))
+      return rc;
+    return encode_finish(params, pl, out, out_capacity, out_bytes, workspace, st, total);
+  }
+  // the encoder, then the ideal-bits pass on a workspace of its own behind it
+  uint8_t *bws = ws + pl.off_enc_bits;
+  if ((rc = encode_enqueue(params, pl, kv, mu, 0, (uint64_t)pl.geo.nchunks, true, workspace, st)))
+    return rc;
+  if ((rc = ideal_enqueue(params, pl, kv, mu, per_scalar, bws, st))) return rc;
+  if ((rc = encode_finish(params, pl, out, out_capacity, out_bytes, workspace, st))) return rc;
+  WsHead h;
+  if ((rc = read_head(reinterpret_cast<WsHead *>(bws), &h, st))) return rc;
+  if ((rc = status_from_flags(h.flags))) return rc;
+  *total = h.bits;
+  return SKV_OK;
+}
+
+int skv_encode_with_bits_fused(const skv_params *params, const skv_shape *shape, int *fused) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  if (!fused || pl.adaptive) return SKV_ERR_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
+  *fused = encode_fuses_bits(pl.dtype == SKV_BF16 ? 0 : 1, pl.order0, pl.geo.nchunks, pl.geo.G)
+               ? 1 : 0;
+  return SKV_OK;
 }
 
 int skv_encode_range(const skv_params *params, const skv_shape *shape, const void *kv,
@@ -744,56 +866,8 @@ int skv_ideal_bits(const skv_params *params, const skv_shape *shape, const void 
   if ((rc = ensure_device_tables())) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
+  if ((rc = ideal_enqueue(params, pl, kv, mu, per_scalar, ws, st))) return rc;
   WsHead *head = reinterpret_cast<WsHead *>(ws);
-  if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
-  float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
-  // sigma validity only: the p-hat table enters through `phat`
-  if (launch_prep(params->sigma, pl.nsig_model, nullptr, inv, head, st) != cudaSuccess) return SKV_ERR_CUDA;
-  IdealLaunch a;
-  a.geo = pl.geo;
-  a.dtype = pl.dtype;
-  a.kv = kv;
-  a.mu = mu;
-  a.sigma = params->sigma;
-  a.sigma_chunk = nullptr;
-  a.order0 = pl.order0;
-  if (pl.nsw) {
-    ScaleLaunch sl = scale_launch(pl, params, head);
-    sl.kv = kv;
-    sl.mu = mu;
-    sl.sig = reinterpret_cast<float *>(ws + pl.off_bits_csig);
-    if (launch_scales(sl, st) != cudaSuccess) return SKV_ERR_CUDA;
-    a.sigma_chunk = sl.sig;
-  }
-  a.phat = params->phat;
-  a.per_scalar = per_scalar;
-  a.partials = reinterpret_cast<double *>(ws + pl.off_bits);
-  a.nblocks = pl.bits_blocks;
-  a.td_rcp = ~0ull / ((uint64_t)pl.geo.T * (uint64_t)pl.geo.D);
-  a.head = head;
-  if (pl.adaptive) {
-    // per-row models, one phase per token block, partial sums in a fixed order
-    uint8_t *ad = ws + pl.ad_base_bits;
-    uint64_t *P = reinterpret_cast<uint64_t *>(ad + pl.ad_P);
-    uint64_t *Cn = reinterpret_cast<uint64_t *>(ad + pl.ad_C);
-    uint64_t *W = reinterpret_cast<uint64_t *>(ad + pl.ad_W);
-    double *part = reinterpret_cast<double *>(ad + pl.ad_part);
-    const uint32_t *ecdf = params->ecdf;
-    const uint16_t *kv16 = static_cast<const uint16_t *>(kv);
-    if (launch_ad_init(ecdf, P, Cn, pl.nrows, W, pl.geo.Tb, st) != cudaSuccess) return SKV_ERR_CUDA;
-    for (int64_t b = 0; b < pl.geo.ntb; ++b) {
-      if (launch_ad_ideal(pl.geo, kv16, b, P, per_scalar, part + b * pl.nrows * pl.ad_bx, pl.ad_bx,
-                          head, pl.nrows, st) != cudaSuccess)
-        return SKV_ERR_CUDA;
-      if (b + 1 < pl.geo.ntb &&
-          launch_ad_update(pl.geo, kv16, b, P, Cn, W, head, pl.nrows, st) != cudaSuccess)
-        return SKV_ERR_CUDA;
-    }
-    if (launch_ideal_final(part, (int)(pl.geo.ntb * pl.nrows * pl.ad_bx), head, st) != cudaSuccess)
-      return SKV_ERR_CUDA;
-  } else if (launch_ideal(a, st) != cudaSuccess) {
-    return SKV_ERR_CUDA;
-  }
   WsHead h;
   if ((rc = read_head(head, &h, st))) return rc;
   if ((rc = status_from_flags(h.flags))) return rc;

@@ -22,6 +22,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include "skv_ideal.cuh"
 #include "skv_internal.h"
 #include "skv_model.cuh"
 
@@ -196,12 +197,21 @@ cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, int n, cudaStream_t
 // Encode: one thread per lane, rounds descending, lanes descending.
 // ------------------------------------------------------------------------
 
-// NT: most threads per block (the register budget follows from it).
-template <int DT, bool O0, int NT = kCodeThreads>
+// NT: most threads per block (the register budget follows from it).  BITS
+// (bf16, multi-round launches only, where it pays): also the ideal code
+// length -log2 q of every scalar (the per-scalar values of skv_ideal_bits),
+// from the symbol's bin edges, mu and reciprocal already in registers.  The
+// rare scalars outside the series' range (about 1%) are evaluated where they
+// are met, out of line; a per-warp ring of them, as in the ideal-bits kernel,
+// cost more in bookkeeping than it saved here.
+template <int DT, bool O0, int NT = kCodeThreads, bool BITS = false>
 __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
+  static_assert(!BITS || (DT == 0 && !O0), "ideal bits fuse into the bf16 mixture coder only");
   extern __shared__ uint2 s_phi[];
   float *s_lo8 = reinterpret_cast<float *>(s_phi + kPhiKnots);
+  __shared__ double s_bpart[BITS ? NT / 32 : 1];
   stage_tables(s_phi, s_lo8);
+  double bacc = 0.0;
 
   constexpr int M = DT == 0 ? kMBf16 : kME4m3;
   constexpr int32_t NS = DT == 0 ? kNsymBf16 : kNsymE4m3;
@@ -229,12 +239,12 @@ __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
     int64_t sp = a.stride;
     uint64_t x = kStateL;
     uint32_t flags = 0;
-
     for (int64_t gi = (int64_t)max_groups - 1; gi >= 0; --gi) {
       const bool has = (uint32_t)gi < my_groups;
       const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * (uint32_t)gi);
       uint32_t sym[8], mub[8];
       ChanInv inv[8];
+      float bk[8];
       if (has) {
         load_syms<DT>(a.kv, cg.base + p0, sym);
         if (!O0) {
@@ -263,8 +273,15 @@ __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
             const float muf = bf16_to_f32(mub[k]);
             cst = cum_of<DT>(r, muf, inv[k], s_phi, s_lo8, a.ecdf);
             f = cum_of<DT>(r + 1, muf, inv[k], s_phi, s_lo8, a.ecdf) - cst;
+            if (BITS) {
+              const float lo = lo_bf16(r), hi = lo_bf16(r + 1), ph = __ldg(a.phat + r);
+              if (!ideal::ideal_series_bf16(lo, hi, muf, inv[k].s, ph, bk[k]))
+                bk[k] = ideal::ideal_full_call<0>(lo, hi, muf, inv[k].s, ph);
+            }
           }
           emit = x >= ((uint64_t)f << (63 - M));
+        } else if (BITS) {
+          bk[k] = 0.0f;
         }
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, emit) & seg;
         const int n = __popc(m);
@@ -279,6 +296,19 @@ __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
           uint64_t rem;
           const uint64_t q = divmod_u64<M>(x, f, rem);
           x = (q << M) + rem + cst;
+        }
+      }
+      if (BITS) {
+        if (has) {
+          float part = 0.0f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) part += bk[k];
+          bacc += (double)part;
+          if (a.bits_out) {
+            float4 *o = reinterpret_cast<float4 *>(a.bits_out + cg.base + p0);
+            o[0] = make_float4(bk[0], bk[1], bk[2], bk[3]);
+            o[1] = make_float4(bk[4], bk[5], bk[6], bk[7]);
+          }
         }
       }
     }
@@ -304,6 +334,17 @@ __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
       }
     }
     if (flags) atomicOr(&a.head->flags, flags);
+  }
+  if (BITS) {
+    // fixed order: a shuffle tree per warp, then the warps in order
+    for (int o = 16; o; o >>= 1) bacc += __shfl_xor_sync(0xFFFFFFFFu, bacc, o);
+    if (lane == 0) s_bpart[threadIdx.x >> 5] = bacc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double t = 0.0;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += s_bpart[w];
+      a.bits_partials[blockIdx.x] = t;
+    }
   }
 }
 
@@ -534,10 +575,19 @@ cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s) {
   return launch_encode_finish(a, s);
 }
 
-template <int DT, bool O0, int NT>
+template <int DT, bool O0, int NT, bool BITS = false>
 static cudaError_t run_encode(const EncodeLaunch &a, int blocks, int threads, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(k_encode<DT, O0, NT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kCodeSmem);
+  cudaError_t e;
+  if (BITS) {
+    if (blocks > kMaxBitsBlocks) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(k_encode<DT, O0, NT, BITS>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kCodeSmem);
+    if (e != cudaSuccess) return e;
+    k_encode<DT, O0, NT, BITS><<<blocks, threads, kCodeSmem, s>>>(a);
+    return cudaGetLastError();
+  }
+  e = cudaFuncSetAttribute(k_encode<DT, O0, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kCodeSmem);
   if (e != cudaSuccess) return e;
   k_encode<DT, O0, NT><<<blocks, threads, kCodeSmem, s>>>(a);
   return cudaGetLastError();
@@ -549,6 +599,20 @@ static cudaError_t run_encode(const EncodeLaunch &a, int blocks, int threads, cu
 // (8B shape: 157 -> 140) lose with them and keep 768.
 constexpr int kEncMultiRoundThreads = 896;
 
+// The ideal bits ride along with the encoder only on bf16 mixture launches of
+// several rounds of tasks (more lanes than one round of full blocks holds).
+// There the encoder is throughput-bound and the series' ~100 extra operations
+// per scalar cost less than a separate pass re-reading kv and mu (32B shape:
+// 14.2 ms fused against 10.4 + 4.8 ms).  A single-round launch is bound by
+// its lanes' serial chains, which the extra work lengthens (0.6B shape: 4.5
+// against 2.3 + 1.1 ms), and e4m3's rare scalars, several per warp step, stall
+// whole warps (8B shape: 32 against 7.7 + 5.6 ms); those run the two kernels.
+bool encode_fuses_bits(int dtype, bool order0, int64_t chunks, int G) {
+  if (dtype != 0 || order0) return false;
+  const int64_t ntasks = (chunks * G + 31) / 32;
+  return ntasks > (int64_t)device_sm_count() * (kCodeThreads / 32);
+}
+
 cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s) {
   const int64_t ntasks = (a.c_count * a.geo.G + 31) / 32;
   if (ntasks == 0) return cudaSuccess;
@@ -559,10 +623,16 @@ cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s) {
   }
   if (a.dtype == 0) {
     task_shape(ntasks, kCodeThreads, blocks, threads, kEncMultiRoundThreads);
+    if (a.bits_partials) {
+      // skv_encode_with_bits fuses only where encode_fuses_bits says so
+      if (a.order0 || threads <= kCodeThreads) return cudaErrorInvalidValue;
+      return run_encode<0, false, kEncMultiRoundThreads, true>(a, blocks, threads, s);
+    }
     if (threads > kCodeThreads)
       return run_encode<0, false, kEncMultiRoundThreads>(a, blocks, threads, s);
     return run_encode<0, false, kCodeThreads>(a, blocks, threads, s);
   }
+  if (a.bits_partials) return cudaErrorInvalidValue;
   task_shape(ntasks, kCodeThreads, blocks, threads);
   return run_encode<1, false, kCodeThreads>(a, blocks, threads, s);
 }

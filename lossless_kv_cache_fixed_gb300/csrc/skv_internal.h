@@ -122,6 +122,12 @@ struct EncodeLaunch {
   uint8_t *out;
   uint64_t capacity;
   uint64_t hash_words;      // number of 32-bit words hashed by the prep kernel
+  // the ideal code length as the encoder codes (bits_partials set; bf16
+  // launches that encode_fuses_bits accepts): the p-hat table, per-scalar
+  // output (or null) and one fp64 partial sum per block
+  const float *phat;
+  float *bits_out;
+  double *bits_partials;
 };
 
 struct DecodeLaunch {
@@ -221,6 +227,8 @@ cudaError_t upload_tables(const uint32_t *phi_knots, const float *lo8, const flo
                           const float *hinv_e4m3);
 cudaError_t upload_scale_mult(const float *mult);
 cudaError_t upload_tail_table(const float *log2_q);  // kTailN values
+// Most blocks of an ideal-bits reduction (one fp64 partial sum each).
+constexpr int kMaxBitsBlocks = 4096;
 cudaError_t launch_scales(const ScaleLaunch &a, cudaStream_t s);
 
 // Model preparation: sigma validation, per-channel reciprocals, E_q checks and
@@ -231,6 +239,9 @@ cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s);
 // The encode kernel alone over a.c_first + a.c_step * i, and the size scan and
 // compaction that follow it (launch_encode = both).
 cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s);
+// Whether a launch of `chunks` chunks computes the ideal bits inside the
+// encoder (skv_encode_with_bits) rather than in a second kernel.
+bool encode_fuses_bits(int dtype, bool order0, int64_t chunks, int G);
 cudaError_t launch_encode_finish(const EncodeLaunch &a, cudaStream_t s);
 
 // Adaptive counts (skv_adapt.cu): per-row probabilities P and counts C (u64,

@@ -81,3 +81,18 @@ def check_model_bits(O, codec, m, kv_d, mu_d, kv, mu, container):
         extra = payload_bits - 32 * nsw - ref
         assert 32 * G - 1e-3 * ref - 1 <= extra <= 64 * G + 1e-3 * ref + 1, c
     assert abs(tot - ref_tot) <= 1e-6 * ref_tot + 1e-3
+
+
+def check_encode_with_bits(codec, kv_d, mu_d, container, ref, ref_tot, rtol=1e-3, atol=1e-6):
+    """skv_encode_with_bits writes the container skv_encode writes, per-scalar
+    ideal bits within the tolerance of the oracle's (ref), a total that agrees
+    with them, and the same total on a second call (fixed summation order)."""
+    import numpy as np
+    buf, nb, tot, ps = codec.encode_with_bits(kv_d, mu_d, per_scalar=True)
+    assert nb == container.size and np.array_equal(buf[:nb].cpu().numpy(), container)
+    got = ps.double().cpu().numpy()
+    assert np.all(np.abs(got - ref) <= rtol * np.abs(ref) + atol)
+    assert abs(tot - got.sum()) <= 1e-6 * abs(tot) + 1e-6
+    assert abs(tot - ref_tot) <= rtol * abs(ref_tot) + 1e-6
+    _, nb2, tot2 = codec.encode_with_bits(kv_d, mu_d)
+    assert nb2 == nb and tot2 == tot

@@ -65,10 +65,11 @@ def test_json_line_keys(fixed_peaks):
     e2e = {"value": 40.0, "unit": "GB/s", "h2d_bytes_per_step": 2 * N + 2 * N,
            "d2h_bytes_per_step": 168_754_632 + 2 * N}
     nb, bits = 168_754_632, 5.722 * N
+    med = {"encode_with_bits": 3.3, "decode": MED["decode"]}
+    alone = {"encode": MED["encode"], "ideal_bits": MED["ideal_bits"]}
     line = bench.finish_line(args, 0, 1, spec, N, nb, bits, 5.70 * N, 2, 7.68,
-                             2 * N / 7.68e-3 / 1e9,
-                             [MED["encode"]] * 3, [MED["decode"]] * 3, [MED["ideal_bits"]] * 3,
-                             clk, e2e, None)
+                             2 * N / 7.68e-3 / 1e9, med, clk, e2e, None, alone=alone,
+                             fused_bits=True)
     for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
               "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
               "roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks"):
@@ -76,7 +77,19 @@ def test_json_line_keys(fixed_peaks):
     assert line["metric"] == bench.METRIC and line["unit"] == "GB/s" and line["n_gpus"] == 1
     assert line["higher_is_better"] is True and line["scaling"] == "strong"
     assert line["config"]["workload"] == spec.name
-    assert line["gpu_launches"] == 12 * 30   # 12 kernels per bf16 step
+    assert "inside the encoder" in line["config"]["step"]
+    # encode (5) + the bits' final sum (1) + bf16 decode (4) per step
+    assert line["gpu_launches"] == 10 * 30
+    assert line["encode_with_bits_gbs"] == pytest.approx(2 * N / 3.3e-3 / 1e9, abs=0.01)
+    assert line["encode_alone_gbs"] == pytest.approx(2 * N / MED["encode"] / 1e6, abs=0.01)
+    assert line["roofline"]["kernel"] == "k_decode"          # 4.05 ms > 3.3 ms
+    assert line["kernels"]["encode_with_bits"]["kernel"] == "k_encode (ideal bits inside)"
+    assert line["kernels_alone"]["ideal_bits"]["kernel"] == "k_ideal"
+    # the two passes apart: encode + ideal bits launches as before
+    two = bench.finish_line(args, 0, 1, spec, N, nb, bits, 5.70 * N, 2, 7.68, 1.0, med, clk, e2e,
+                            None, alone=alone, fused_bits=False)
+    assert two["gpu_launches"] == 12 * 30
+    assert two["kernels"]["encode_with_bits"]["kernel"] == "k_encode + k_ideal"
     assert line["bits_per_scalar"] == pytest.approx(8.0 * nb / N, abs=1e-5)
     for k in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
         assert k in line["roofline"], k
@@ -86,8 +99,8 @@ def test_json_line_keys(fixed_peaks):
     assert line["overhead_vs_model_pct"] == pytest.approx(100 * (8.0 * nb / (5.70 * N) - 1), abs=1e-3)
     assert line["payload_overhead_vs_model_pct"] == pytest.approx(
         100 * (payload / (5.70 * N) - 1), abs=1e-3)
-    assert bench.finish_line(args, 1, 2, spec, N, nb, bits, None, 2, 7.68, 1.0, [1.0], [1.0], [1.0],
-                             clk, e2e, None) is None   # only rank 0 prints
+    assert bench.finish_line(args, 1, 2, spec, N, nb, bits, None, 2, 7.68, 1.0, med, clk, e2e,
+                             None) is None   # only rank 0 prints
 
 
 def test_cpu_baseline_single_and_all_cores(fixed_peaks):
@@ -101,8 +114,8 @@ def test_cpu_baseline_single_and_all_cores(fixed_peaks):
                               cpu_sample_chunks=4)
     clk = types.SimpleNamespace(summary=lambda: None)
     nb, bits = 100_000, 5.2 * n
-    line = bench.finish_line(args, 0, 1, spec, n, nb, bits, 5.1 * n, 2, 1.0, 1.0, [1.0], [1.0],
-                             [1.0], clk, None, w)
+    line = bench.finish_line(args, 0, 1, spec, n, nb, bits, 5.1 * n, 2, 1.0, 1.0,
+                             {"encode": 1.0, "decode": 1.0, "ideal_bits": 1.0}, clk, None, w)
     cpu = line["cpu_baseline"]
     name, cores = bench.host_cpu()
     assert cpu["cores"] == cores >= 1 and cpu["cpu_model"] == name and name

@@ -15,8 +15,8 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import (check_model_bits, container_chunk, device_views, gpu_codec, host_views,
-                         oracle_model)
+from gpu_helpers import (check_encode_with_bits, check_model_bits, container_chunk, device_views,
+                         gpu_codec, host_views, oracle_model)
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +65,7 @@ def test_block_scale_parity(oracle_mod, name, kw):
     got_ps = ps.double().cpu().numpy()
     assert np.all(np.abs(got_ps - ref) <= 1e-3 * np.abs(ref) + 1e-6)
     assert abs(tot - ref_tot) <= 1e-4 * ref_tot
+    check_encode_with_bits(codec, kv_d, mu_d, got, ref, ref_tot)
     # a static-sigma codec refuses the container (feature bit in the header)
     import lossless_kv_cache_fixed_gb300 as P
     with pytest.raises(P.SkvError) as e:

@@ -8,7 +8,8 @@ times.
   header equals the oracle's.
 * Ideal bits match the oracle per scalar, and the coder's model bits
   (skv_model_bits, sum of M - log2 freq) per chunk, on an evenly spread
-  sample of chunks.
+  sample of chunks; skv_encode_with_bits writes the same container and the
+  same bits (inside the encoder on the bf16 caches).
 * Size: the rANS payload is at most 1% over the model bits (it adds 32 to 64
   bits per lane for the initial state and the flush), except at 1K-scalar
   chunks with one lane, where that flush alone is 1.5-3% of ~2.1 bits/scalar
@@ -58,6 +59,12 @@ def _check(O, w, Tb=None, G=None, nsample=32, max_overhead=0.01):
     assert abs(tot - ps.double().sum().item()) <= 1e-6 * tot  # fp32 sums of 8 inside fp64
     mtot, mps = codec.model_bits(kv_d, mu_d, per_scalar=True)
     assert abs(mtot - mps.double().sum().item()) <= 1e-6 * mtot
+    # encode and ideal bits in one call: the same container and bits
+    buf2, nb2, tot2, ps2 = codec.encode_with_bits(kv_d, mu_d, per_scalar=True)
+    assert nb2 == nb and torch.equal(buf2[:nb], buf[:nb])
+    assert abs(tot2 - tot) <= 1e-6 * tot
+    assert torch.allclose(ps2, ps, rtol=1e-3, atol=1e-6)
+    del buf2, ps2
     m = oracle_model(O, w, Tb, G)
     nc = m.num_chunks()
     host = buf[:nb].cpu().numpy()

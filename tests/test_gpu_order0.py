@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import check_model_bits, container_chunk, skv
+from gpu_helpers import check_encode_with_bits, check_model_bits, container_chunk, skv
 
 pytestmark = pytest.mark.gpu
 
@@ -68,6 +68,7 @@ def test_order0_parity(oracle_mod, kw):
     ref_tot, ref = O.ideal_bits(m, kv_h, None, 0, kv_h.size, per_scalar=True)
     assert np.all(np.abs(ps.double().cpu().numpy() - ref) <= 1e-3 * np.abs(ref) + 1e-6)
     assert abs(tot - ref_tot) <= 1e-5 * ref_tot
+    check_encode_with_bits(codec, kv_d, None, got, ref, ref_tot)
     # the predictive codec refuses the order-0 container (feature bit)
     P = skv()
     mu_d = w.mu.view(torch.int16).reshape(-1).cuda()

@@ -10,7 +10,8 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import check_model_bits, device_views, gpu_codec, host_views, oracle_model
+from gpu_helpers import (check_encode_with_bits, check_model_bits, device_views, gpu_codec,
+                         host_views, oracle_model)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,6 +50,8 @@ def _roundtrip(O, w, Tb=None, G=None, ideal=True, max_overhead=None):
         assert np.all(np.abs(ps - ref) <= RTOL * np.abs(ref) + ATOL)
         assert abs(tot - ps.sum()) <= 1e-6 * abs(tot)  # fp32 sums of 8 inside fp64
         assert abs(tot - ref_tot) <= RTOL * ref_tot
+        # encode and ideal bits in one pass: the same container, the same bits
+        check_encode_with_bits(codec, kv_d, mu_d, got, ref, ref_tot)
         nc = m.num_chunks()
         if max_overhead is not None:
             assert 8.0 * nb <= (1.0 + max_overhead) * ref_tot
@@ -245,3 +248,32 @@ def test_ideal_bits_e4m3_narrow_bins(oracle_mod):
            .numpy().view(np.uint16))
     _roundtrip(oracle_mod, _custom(synth.E4M3, kv8, mu8, sig, T=T, D=D, Tb=32, G=4),
                max_overhead=1.0)
+
+
+@pytest.mark.parametrize("flags", [0, 2], ids=["static", "block-scale"])
+def test_encode_with_bits_inside_the_encoder(oracle_mod, flags):
+    """A bf16 cache with more chunk lanes than one round of the encoder's blocks
+    holds: skv_encode_with_bits computes the ideal bits inside the encoder
+    there (smaller caches run the ideal-bits pass behind it).  2 layers x 8
+    heads x 4090 tokens x 64 in 16-token blocks (8,192 chunks, the last token
+    block ragged) x 16 lanes, with the model's sigma or per-block scales."""
+    spec = synth.WORKLOADS["qwen3-0.6b-bf16"].scaled(name="fused-bits", L=2, H=8, T=4090, D=64,
+                                                     Tb=16, G=16, calib_draws=2)
+    w = synth.make(spec)
+    codec = gpu_codec(w, flags=flags)
+    assert codec.encode_with_bits_fused()
+    assert not gpu_codec(synth.make("tiny-bf16")).encode_with_bits_fused()
+    kv_d, mu_d = device_views(w)
+    buf, nb = codec.encode(kv_d, mu_d)
+    got = buf[:nb].cpu().numpy()
+    m = oracle_model(oracle_mod, w, block_scale=bool(flags))
+    kv, mu = host_views(w)
+    rc, want = oracle_mod.encode(m, kv, mu)
+    assert rc == 0 and np.array_equal(got, want)
+    ref_tot, ref = oracle_mod.ideal_bits(m, kv, mu, per_scalar=True)
+    check_encode_with_bits(codec, kv_d, mu_d, got, ref, ref_tot)
+    # the separate pass gives the same per-scalar values within the tolerance
+    tot, ps = codec.ideal_bits(kv_d, mu_d, per_scalar=True)
+    _, _, tot2, ps2 = codec.encode_with_bits(kv_d, mu_d, per_scalar=True)
+    assert torch.allclose(ps2, ps, rtol=RTOL, atol=ATOL)
+    assert abs(tot2 - tot) <= 1e-6 * tot
