@@ -701,6 +701,27 @@ __device__ __forceinline__ float lo_value(int DT, int32_t r, const float *lo8) {
   return DT == 0 ? lo_bf16(r) : lo8[r];
 }
 
+// Position of the n-th (from 0) set bit of m; m has more than n set bits.
+__device__ __forceinline__ int nth_set_bit(uint32_t m, int n) {
+  int pos = 0;
+#pragma unroll
+  for (int w = 16; w; w >>= 1) {
+    const int c = __popc(m & ((1u << w) - 1u));
+    if (n >= c) {
+      n -= c;
+      m >>= w;
+      pos += w;
+    }
+  }
+  return pos;
+}
+
+// The warp search's first-round distances from a bracket end, j = 0 .. 15:
+// 1, 2, 3, 4, 6, 8, 12, 16, ..., 192, 256.
+__device__ __forceinline__ int32_t ladder_step(int j) {
+  return j < 4 ? j + 1 : (3 + ((j - 4) & 1)) << (((j - 4) >> 1) + 1);
+}
+
 // Rank of the symbol an fp32 value rounds to (the decoder's guesses only).
 template <int DT>
 __device__ __forceinline__ int32_t rank_of_value(float x) {
@@ -748,6 +769,142 @@ __device__ __forceinline__ int64_t next_task(WsHead *h, int64_t nwarps) {
   unsigned long long t = 0;
   if ((threadIdx.x & 31) == 0) t = atomicAdd(&h->next_task, 1ull);
   return nwarps + (int64_t)__shfl_sync(0xFFFFFFFFu, t, 0);
+}
+
+// The decoder's warp search for open lane l (all 32 lanes call it): 32
+// candidates per round.  On a wide bracket the first round steps inwards from
+// both ends, 16 candidates each, 1, 2, 3, 4, 6, 8, 12, ..., 192, 256 ranks
+// away: the answer lies next to one of them far more often than in the middle
+// (after Newton within 256 ranks of an end for ~96% of lanes, within one rank
+// for ~30%).  Later rounds spread the candidates evenly (33 subintervals: at
+// most 4 more rounds).  Leaves lane l's bracket in blo .. bchi (all lanes),
+// one rank wide unless cum were not monotone.
+template <int DT>
+__device__ __forceinline__ void search_lane(int l, uint32_t slot, float muf, ChanInv inv,
+                                            const Bracket &br, const uint2 *s_phi,
+                                            const float *s_lo8, const uint32_t *__restrict__ ecdf,
+                                            int32_t &blo, int32_t &bhi, uint32_t &bclo,
+                                            uint32_t &bchi) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t s_slot = __shfl_sync(0xFFFFFFFFu, slot, l);
+  const float s_mu = __shfl_sync(0xFFFFFFFFu, muf, l);
+  ChanInv s_inv;
+  s_inv.s = __shfl_sync(0xFFFFFFFFu, inv.s, l);
+  s_inv.s3 = __shfl_sync(0xFFFFFFFFu, inv.s3, l);
+  blo = __shfl_sync(0xFFFFFFFFu, br.lo, l);
+  bhi = __shfl_sync(0xFFFFFFFFu, br.hi, l);
+  bclo = __shfl_sync(0xFFFFFFFFu, br.clo, l);
+  bchi = __shfl_sync(0xFFFFFFFFu, br.chi, l);
+  for (int it = 0; it < 12 && bhi - blo > 1; ++it) {
+    const int32_t wdt = bhi - blo;
+    const int32_t nact = min(wdt - 1, 32);
+    int32_t cand;
+    if (wdt - 1 <= 32) {
+      cand = blo + 1 + lane;
+    } else if (it == 0 && wdt > 2 * 256 + 1) {
+      cand = lane < 16 ? blo + ladder_step(lane) : bhi - ladder_step(31 - lane);
+    } else {
+      cand = blo + (int32_t)(((int64_t)(lane + 1) * wdt) / 33);
+    }
+    const bool act = lane < nact;
+    const uint32_t cv = act ? cum_of<DT>(cand, s_mu, s_inv, s_phi, s_lo8, ecdf) : 0u;
+    const int kle = __popc(__ballot_sync(0xFFFFFFFFu, act && cv <= s_slot));
+    const int32_t c_lo = __shfl_sync(0xFFFFFFFFu, cand, kle > 0 ? kle - 1 : 0);
+    const uint32_t v_lo = __shfl_sync(0xFFFFFFFFu, cv, kle > 0 ? kle - 1 : 0);
+    const int32_t c_hi = __shfl_sync(0xFFFFFFFFu, cand, kle < nact ? kle : 0);
+    const uint32_t v_hi = __shfl_sync(0xFFFFFFFFu, cv, kle < nact ? kle : 0);
+    if (kle > 0) {
+      blo = c_lo;
+      bclo = v_lo;
+    }
+    if (kle < nact) {
+      bhi = c_hi;
+      bchi = v_hi;
+    }
+  }
+}
+
+// The same for two or more open lanes of a warp step (all 32 lanes call it),
+// side by side: up to kp = 2, 4, 8 or 16 open lanes at a time, each in a
+// segment of S = 32 / kp lanes that tries S candidates per round -- on a wide
+// bracket first every (16 / (S / 2))-th step of the ladder above, then S
+// candidates evenly spread (S + 1 subintervals a round: at most 11 rounds after
+// the first for S = 2).  Each open lane gets back its bracket.  Out of line:
+// it runs in few warp steps except where the model fits badly, and inlined
+// its code slowed every step of the rest.
+template <int DT>
+static __device__ __noinline__ Bracket search_lanes(uint32_t pend, bool mine_open, uint32_t slot,
+                                                    float muf, ChanInv inv, Bracket br,
+                                                    const uint2 *s_phi, const float *s_lo8,
+                                                    const uint32_t *__restrict__ ecdf) {
+  const int lane = threadIdx.x & 31;
+  const int npend = __popc(pend);
+  const int lg_kp = npend <= 2 ? 1 : (npend <= 4 ? 2 : (npend <= 8 ? 3 : 4));
+  const int lg_s = 5 - lg_kp;
+  const int S = 1 << lg_s, half = S >> 1;
+  const int sgi = lane >> lg_s, j = lane & (S - 1);
+  const int sbase = sgi << lg_s;  // first lane of my segment
+  const uint32_t smask = (1u << S) - 1u;
+  const int myord = __popc(pend & ((1u << lane) - 1u));  // my place among the open lanes
+  for (int b0 = 0; b0 < npend; b0 += 1 << lg_kp) {
+    const bool valid = b0 + sgi < npend;
+    const int src = valid ? nth_set_bit(pend, b0 + sgi) : lane;
+    const uint32_t s_slot = __shfl_sync(0xFFFFFFFFu, slot, src);
+    const float s_mu = __shfl_sync(0xFFFFFFFFu, muf, src);
+    ChanInv s_inv;
+    s_inv.s = __shfl_sync(0xFFFFFFFFu, inv.s, src);
+    s_inv.s3 = __shfl_sync(0xFFFFFFFFu, inv.s3, src);
+    int32_t blo = __shfl_sync(0xFFFFFFFFu, br.lo, src);
+    int32_t bhi = __shfl_sync(0xFFFFFFFFu, br.hi, src);
+    uint32_t bclo = __shfl_sync(0xFFFFFFFFu, br.clo, src);
+    uint32_t bchi = __shfl_sync(0xFFFFFFFFu, br.chi, src);
+    for (int it = 0; it < 24; ++it) {
+      const bool open = valid && bhi - blo > 1;
+      if (!__any_sync(0xFFFFFFFFu, open)) break;
+      const int32_t wdt = bhi - blo;
+      const int32_t nact = open ? min(wdt - 1, S) : 0;
+      int32_t cand;
+      if (wdt - 1 <= S) {
+        cand = blo + 1 + j;
+      } else if (it == 0 && wdt > 2 * 256 + 1) {
+        const int jj = j < half ? j : S - 1 - j;
+        const int32_t g = ladder_step(((jj + 1) << (5 - lg_s)) - 1);
+        cand = j < half ? blo + g : bhi - g;
+      } else {
+        cand = blo + (int32_t)(((int64_t)(j + 1) * wdt) / (S + 1));
+      }
+      const bool act = j < nact;
+      const uint32_t cv = act ? cum_of<DT>(cand, s_mu, s_inv, s_phi, s_lo8, ecdf) : 0u;
+      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, act && cv <= s_slot);
+      const int kle = __popc((bal >> sbase) & smask);
+      const int32_t c_lo = __shfl_sync(0xFFFFFFFFu, cand, sbase + (kle > 0 ? kle - 1 : 0));
+      const uint32_t v_lo = __shfl_sync(0xFFFFFFFFu, cv, sbase + (kle > 0 ? kle - 1 : 0));
+      const int32_t c_hi = __shfl_sync(0xFFFFFFFFu, cand, sbase + (kle < nact ? kle : 0));
+      const uint32_t v_hi = __shfl_sync(0xFFFFFFFFu, cv, sbase + (kle < nact ? kle : 0));
+      if (open && kle > 0) {
+        blo = c_lo;
+        bclo = v_lo;
+      }
+      if (open && kle < nact) {
+        bhi = c_hi;
+        bchi = v_hi;
+      }
+    }
+    // each open lane of this batch takes its segment's bracket
+    const bool mine = mine_open && myord >= b0 && myord < b0 + (1 << lg_kp);
+    const int from = mine ? (myord - b0) << lg_s : lane;
+    const int32_t r_lo = __shfl_sync(0xFFFFFFFFu, blo, from);
+    const int32_t r_hi = __shfl_sync(0xFFFFFFFFu, bhi, from);
+    const uint32_t r_clo = __shfl_sync(0xFFFFFFFFu, bclo, from);
+    const uint32_t r_chi = __shfl_sync(0xFFFFFFFFu, bchi, from);
+    if (mine) {
+      br.lo = r_lo;
+      br.hi = r_hi;
+      br.clo = r_clo;
+      br.chi = r_chi;
+    }
+  }
+  return br;
 }
 
 template <int DT, bool BISECT>
@@ -948,60 +1105,47 @@ __global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunc
               done = br.hi - br.lo == 1;
             }
           }
-          // (3) the warp finishes its unresolved lanes, one lane at a time
+          // (3) the warp finishes its unresolved lanes: one lane at a time with
+          // all 32 candidates per round (search_lane), or (bf16) two or more
+          // side by side (search_lanes), so that a warp whose chunks fit the
+          // model badly (many lanes open in one step) does not finish them one
+          // after another
           uint32_t pend = __ballot_sync(0xFFFFFFFFu, !done);
-          while (pend) {
-            const int l = __ffs(pend) - 1;
-            pend &= pend - 1;
-            const uint32_t s_slot = __shfl_sync(0xFFFFFFFFu, slot, l);
-            const float s_mu = __shfl_sync(0xFFFFFFFFu, muf, l);
-            ChanInv s_inv;
-            s_inv.s = __shfl_sync(0xFFFFFFFFu, inv.s, l);
-            s_inv.s3 = __shfl_sync(0xFFFFFFFFu, inv.s3, l);
-            int32_t blo = __shfl_sync(0xFFFFFFFFu, br.lo, l);
-            int32_t bhi = __shfl_sync(0xFFFFFFFFu, br.hi, l);
-            uint32_t bclo = __shfl_sync(0xFFFFFFFFu, br.clo, l);
-            uint32_t bchi = __shfl_sync(0xFFFFFFFFu, br.chi, l);
-            for (int it = 0; it < 12 && bhi - blo > 1; ++it) {
-              const int32_t wdt = bhi - blo;
-              const int32_t nact = min(wdt - 1, 32);
-              int32_t cand;
-              if (wdt - 1 <= 32) {
-                cand = blo + 1 + lane;
-              } else if (it == 0 && wdt > 2 * 256 + 1) {
-                // first round on a wide bracket: the answer lies next to one of
-                // its ends far more often than in its middle (after Newton,
-                // within 256 ranks of an end for ~96% of lanes, within one rank
-                // for ~30%), so 16 candidates step inwards from each end,
-                // 1, 2, 3, 4, 6, 8, 12, ..., 192, 256 ranks away (ascending)
-                const int j = lane < 16 ? lane : 31 - lane;
-                const int32_t g = j < 4 ? j + 1 : (3 + ((j - 4) & 1)) << (((j - 4) >> 1) + 1);
-                cand = lane < 16 ? blo + g : bhi - g;
-              } else {
-                cand = blo + (int32_t)(((int64_t)(lane + 1) * wdt) / 33);
+          if constexpr (DT == 0) {
+            if (__popc(pend) == 1) {
+              const int l = __ffs(pend) - 1;
+              int32_t blo, bhi;
+              uint32_t bclo, bchi;
+              search_lane<DT>(l, slot, muf, inv, br, s_phi, s_lo8, a.ecdf, blo, bhi, bclo, bchi);
+              if (lane == l) {
+                br.lo = blo;
+                br.hi = bhi;
+                br.clo = bclo;
+                br.chi = bchi;
               }
-              const bool act = lane < nact;
-              const uint32_t cv = act ? cum_of<DT>(cand, s_mu, s_inv, s_phi, s_lo8, a.ecdf) : 0u;
-              const int kle = __popc(__ballot_sync(0xFFFFFFFFu, act && cv <= s_slot));
-              const int32_t c_lo = __shfl_sync(0xFFFFFFFFu, cand, kle > 0 ? kle - 1 : 0);
-              const uint32_t v_lo = __shfl_sync(0xFFFFFFFFu, cv, kle > 0 ? kle - 1 : 0);
-              const int32_t c_hi = __shfl_sync(0xFFFFFFFFu, cand, kle < nact ? kle : 0);
-              const uint32_t v_hi = __shfl_sync(0xFFFFFFFFu, cv, kle < nact ? kle : 0);
-              if (kle > 0) {
-                blo = c_lo;
-                bclo = v_lo;
-              }
-              if (kle < nact) {
-                bhi = c_hi;
-                bchi = v_hi;
-              }
+            } else if (pend) {
+              br = search_lanes<DT>(pend, !done, slot, muf, inv, br, s_phi, s_lo8, a.ecdf);
             }
-            if (lane == l) {
-              if (bhi - blo != 1) flags |= kFlagCorrupt;  // only if cum were not monotone
-              br.lo = blo;
-              br.hi = blo + 1;
-              br.clo = bclo;
-              br.chi = bchi;
+            if (!done) {
+              if (br.hi - br.lo != 1) flags |= kFlagCorrupt;  // only if cum were not monotone
+              br.hi = br.lo + 1;
+            }
+          } else {
+            // (e4m3 misses are rarer, and there the out-of-line search's
+            // register cost lost more than it gained)
+            while (pend) {
+              const int l = __ffs(pend) - 1;
+              pend &= pend - 1;
+              int32_t blo, bhi;
+              uint32_t bclo, bchi;
+              search_lane<DT>(l, slot, muf, inv, br, s_phi, s_lo8, a.ecdf, blo, bhi, bclo, bchi);
+              if (lane == l) {
+                if (bhi - blo != 1) flags |= kFlagCorrupt;  // only if cum were not monotone
+                br.lo = blo;
+                br.hi = blo + 1;
+                br.clo = bclo;
+                br.chi = bchi;
+              }
             }
           }
         }

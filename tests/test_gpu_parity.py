@@ -277,3 +277,17 @@ def test_encode_with_bits_inside_the_encoder(oracle_mod, flags):
     _, _, tot2, ps2 = codec.encode_with_bits(kv_d, mu_d, per_scalar=True)
     assert torch.allclose(ps2, ps, rtol=RTOL, atol=ATOL)
     assert abs(tot2 - tot) <= 1e-6 * tot
+
+
+@pytest.mark.parametrize("shrink", [0.2, 0.05, 0.01], ids=["5x", "20x", "100x"])
+def test_model_far_too_narrow(oracle_mod, shrink):
+    """A sigma table 5-100 times narrower than the residuals: most symbols sit
+    in the tails, where the first guess and Newton miss, so warp steps end with
+    many lanes open at once (the warp search then serves 2-16 lanes side by
+    side).  Containers byte-equal to the oracle, both searches decode exactly.
+    2 layers x 2 heads x 600 tokens x 128, 256-token blocks (the last ragged),
+    8 lanes."""
+    w = synth.make(synth.WORKLOADS["qwen3-0.6b-bf16"].scaled(name="narrow", L=2, H=2, T=600,
+                                                             G=8, calib_draws=2))
+    w.sigma.mul_(shrink)
+    _roundtrip(oracle_mod, w, ideal=False)
