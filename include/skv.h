@@ -214,10 +214,18 @@ int skv_decode(const skv_params *params, const skv_shape *shape, const void *in,
  *                   checks the header and the model fingerprint.  Later calls
  *                   for the same container reuse them and must be ordered
  *                   after it (same stream, or caller-made ordering).
+ *                   SKV_RANGE_PARTIAL (with or without FIRST): the container is
+ *                   still being written by skv_encode_commit, so FIRST skips
+ *                   the header check; in_bytes is then the buffer's capacity
+ *                   (every offset read is bounded by it) and only committed
+ *                   chunks may be decoded, after their commit in stream order.
+ *                   The header and model fingerprint are not checked in this
+ *                   mode: it is for a container this process is writing.
  * Argument errors (SKV_ERR_ARG, SKV_ERR_CAPACITY, a container shorter than its
  * offset table: SKV_ERR_CORRUPT) return at once; data errors accumulate in the
  * workspace until skv_decode_status.  Does not synchronize. */
 #define SKV_RANGE_FIRST 1
+#define SKV_RANGE_PARTIAL 2
 int skv_decode_range(const skv_params *params, const skv_shape *shape, const void *in,
                      size_t in_bytes, uint64_t chunk_begin, uint64_t chunk_end,
                      const uint16_t *mu, void *kv_out, const uint32_t *page_of_chunk,
@@ -288,6 +296,34 @@ int skv_encode_range(const skv_params *params, const skv_shape *shape, const voi
 int skv_encode_finish(const skv_params *params, const skv_shape *shape, void *out,
                       size_t out_capacity, size_t *out_bytes, void *workspace,
                       size_t workspace_bytes, skv_stream_t stream);
+
+/* Place encoded chunks in the container while later ones are still being
+ * encoded: chunks [chunk_begin, chunk_end), the next in container order after
+ * those committed before (chunk_begin = 0 on the first call since
+ * SKV_RANGE_FIRST, then the previous chunk_end), whose skv_encode_range calls
+ * were enqueued before this one (same stream, or caller-made ordering), get
+ * their offsets and payload in `out`, right after the committed prefix.  The
+ * chunk after the range gets its offset too, so the range can be decoded
+ * (skv_decode_range with SKV_RANGE_PARTIAL) or its bytes copied out before the
+ * rest of the cache is encoded (the pages' section "该方法的用途": caches move
+ * to a slower tier as they are produced).  skv_encode_finish then writes the
+ * header; it requires every chunk committed, to the same `out`.
+ *   out, out_capacity   device buffer of the container (8-byte aligned), at
+ *                       least skv_max_encoded_bytes for a whole cache.
+ *   end_bytes       optional (NULL: none): receives, when the commit runs (in
+ *                   stream order), the container's size so far -- header,
+ *                   offset table and the committed payload -- so that a caller
+ *                   can copy the new bytes out without a synchronisation.
+ *                   Device memory, or pinned host memory the device can write.
+ * Argument errors return at once (SKV_ERR_ARG; SKV_ERR_CAPACITY for a buffer
+ * without room for the offset table).  A range that does not start where the
+ * committed prefix ends, or with a chunk not encoded since SKV_RANGE_FIRST, is
+ * reported by skv_encode_finish as SKV_ERR_ARG, a container that outgrows
+ * out_capacity as SKV_ERR_CAPACITY; such a range places nothing.  Does not
+ * synchronize. */
+int skv_encode_commit(const skv_params *params, const skv_shape *shape, uint64_t chunk_begin,
+                      uint64_t chunk_end, void *out, size_t out_capacity, uint64_t *end_bytes,
+                      void *workspace, size_t workspace_bytes, skv_stream_t stream);
 
 /* The model fingerprint a container of this cache carries in its header (a
  * sum of SplitMix64 terms over sigma's and E_q's 32-bit words, so a decoder

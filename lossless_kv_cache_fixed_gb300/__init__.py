@@ -21,12 +21,14 @@ SKV_FLAG_BLOCK_SCALE = 2
 SKV_FLAG_ORDER0 = 4
 SKV_FLAG_ADAPTIVE = 8
 SKV_RANGE_FIRST = 1
+SKV_RANGE_PARTIAL = 2
 SKV_OK, SKV_ERR_ARG, SKV_ERR_CAPACITY, SKV_ERR_SYMBOL = 0, -1, -2, -3
 SKV_ERR_PARAM, SKV_ERR_CORRUPT, SKV_ERR_CUDA = -4, -5, -6
 NSYM = {SKV_BF16: 65282, SKV_E4M3: 254}
 
 EXPORTS = ("skv_max_encoded_bytes", "skv_workspace_bytes", "skv_encode", "skv_encode_with_bits",
            "skv_encode_with_bits_fused", "skv_encode_range", "skv_encode_finish",
+           "skv_encode_commit",
            "skv_model_fingerprint", "skv_merge_parts", "skv_decode",
            "skv_decode_range", "skv_decode_status", "skv_ideal_bits", "skv_model_bits",
            "skv_ideal_bits_noalloc", "skv_ideal_bits_noalloc_max_channels",
@@ -72,6 +74,8 @@ def lib():
             "skv_encode_range": (C.c_int, [P, S, vp, vp, C.c_uint64, C.c_uint64, C.c_int, vp, sz,
                                            vp]),
             "skv_encode_finish": (C.c_int, [P, S, vp, sz, C.POINTER(sz), vp, sz, vp]),
+            "skv_encode_commit": (C.c_int, [P, S, C.c_uint64, C.c_uint64, vp, sz, vp, vp, sz,
+                                            vp]),
             "skv_model_fingerprint": (C.c_int, [P, S, C.POINTER(C.c_uint64), vp, sz, vp]),
             "skv_merge_parts": (C.c_int, [P, S, C.c_uint64, C.POINTER(vp), C.POINTER(sz), C.c_int,
                                           vp, sz, C.POINTER(sz)]),
@@ -144,6 +148,13 @@ def skv_encode_finish(params, shape, out_ptr, out_capacity, ws_ptr, ws_bytes, st
     rc = lib().skv_encode_finish(C.byref(params), C.byref(shape), out_ptr, out_capacity,
                                  C.byref(nb), ws_ptr, ws_bytes, stream)
     return rc, nb.value
+
+
+def skv_encode_commit(params, shape, chunk_begin, chunk_end, out_ptr, out_capacity,
+                      end_bytes_ptr, ws_ptr, ws_bytes, stream):
+    """Enqueues the placement of chunks [chunk_begin, chunk_end); returns the argument status."""
+    return lib().skv_encode_commit(C.byref(params), C.byref(shape), chunk_begin, chunk_end,
+                                   out_ptr, out_capacity, end_bytes_ptr, ws_ptr, ws_bytes, stream)
 
 
 def skv_model_fingerprint(params, shape, ws_ptr, ws_bytes, stream):
@@ -345,6 +356,18 @@ class Codec:
             raise SkvError(rc, "skv_encode_finish")
         return out, nb
 
+    def encode_commit(self, chunk_begin, chunk_end, out, end_bytes=None, stream=None):
+        """Place the encoded chunks [chunk_begin, chunk_end) in `out` (no
+        synchronisation); encode_finish(out=out) writes the header.  end_bytes:
+        an int64 tensor element (device or pinned host) that receives the
+        container's size so far."""
+        ws = self.workspace(SKV_OP_ENCODE)
+        rc = skv_encode_commit(self.params, self.shape, chunk_begin, chunk_end, out.data_ptr(),
+                               out.numel(), _ptr(end_bytes), ws.data_ptr(), ws.numel(),
+                               _stream_handle(stream))
+        if rc:
+            raise SkvError(rc, "skv_encode_commit")
+
     def fingerprint(self, stream=None):
         ws = self.workspace(SKV_OP_IDEAL_BITS)
         rc, fp = skv_model_fingerprint(self.params, self.shape, ws.data_ptr(), ws.numel(),
@@ -368,15 +391,16 @@ class Codec:
         return out
 
     def decode_range(self, buf, nbytes, chunk_begin, chunk_end, mu, out, pages=None,
-                     num_pages=0, first=False, stream=None):
+                     num_pages=0, first=False, partial=False, stream=None):
         """Enqueue the decode of chunks [chunk_begin, chunk_end) into `out` (the
         [L,2,H,T,D] tensor, or a page pool when `pages` maps chunks to pages).
+        partial: a container still being committed (nbytes = its capacity).
         No synchronisation; call decode_status() for the accumulated status."""
         ws = self.workspace(SKV_OP_DECODE)
+        flags = (SKV_RANGE_FIRST if first else 0) | (SKV_RANGE_PARTIAL if partial else 0)
         rc = skv_decode_range(self.params, self.shape, buf.data_ptr(), nbytes, chunk_begin,
                               chunk_end, _ptr(mu), out.data_ptr(), _ptr(pages), num_pages,
-                              SKV_RANGE_FIRST if first else 0, ws.data_ptr(), ws.numel(),
-                              _stream_handle(stream))
+                              flags, ws.data_ptr(), ws.numel(), _stream_handle(stream))
         if rc:
             raise SkvError(rc, "skv_decode_range")
 

@@ -332,6 +332,10 @@ int encode_enqueue(const skv_params *params, const Plan &pl, const void *kv, con
   }
   if (first) {
     if (cudaMemsetAsync(a.head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
+    // no chunk coded yet: skv_encode_commit refuses a chunk whose start is the sentinel
+    if (cudaMemsetAsync(a.starts, 0xFF, sizeof(uint32_t) * (size_t)pl.geo.nchunks, st) !=
+        cudaSuccess)
+      return SKV_ERR_CUDA;
     if (launch_prep(params->sigma, pl.nsig_model, a.ecdf, const_cast<float2 *>(a.inv), a.head,
                     st) != cudaSuccess)
       return SKV_ERR_CUDA;
@@ -372,7 +376,13 @@ int encode_finish(const skv_params *params, const Plan &pl, void *out, size_t ou
   if (h.chunks_done != (unsigned long long)pl.geo.nchunks) return SKV_ERR_ARG;
   a.out = static_cast<uint8_t *>(out);
   a.capacity = out_capacity;
-  if (launch_encode_finish(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  if (h.committed) {
+    // placed by skv_encode_commit: every chunk must be, then only the header is left
+    if (h.committed != (unsigned long long)pl.geo.nchunks) return SKV_ERR_ARG;
+    if (launch_commit_header(a, st) != cudaSuccess) return SKV_ERR_CUDA;
+  } else if (launch_encode_finish(a, st) != cudaSuccess) {
+    return SKV_ERR_CUDA;
+  }
   if ((rc = read_head(a.head, &h, st))) return rc;
   if ((rc = status_from_flags(h.flags))) return rc;
   *out_bytes = 64 + 8 * (size_t)(pl.geo.nchunks + 1) + (size_t)h.total;
@@ -388,7 +398,7 @@ int encode_finish(const skv_params *params, const Plan &pl, void *out, size_t ou
 int decode_enqueue(const skv_params *params, const Plan &pl, const void *in, size_t in_bytes,
                    uint64_t c0, uint64_t c1, const uint16_t *mu, void *kv_out,
                    const uint32_t *pages, uint64_t num_pages, bool first, void *workspace,
-                   size_t workspace_bytes, skv_stream_t stream) {
+                   size_t workspace_bytes, skv_stream_t stream, bool check_header = true) {
   int rc = common_inputs(params, pl, kv_out, mu);
   if (rc) return rc;
   if (!in || !aligned(in, 8) || !workspace || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
@@ -425,7 +435,7 @@ int decode_enqueue(const skv_params *params, const Plan &pl, const void *in, siz
   a.ecdf_row_stride = 0;
   a.einv_row_stride = 0;
   a.adaptive = pl.adaptive;
-  a.check_header = first ? 1 : 0;
+  a.check_header = first && check_header ? 1 : 0;
   a.page_of_chunk = pages;
   a.num_pages = num_pages;
   a.page_scalars = (uint64_t)pl.geo.Tb * (uint64_t)pl.geo.D;
@@ -712,6 +722,29 @@ int skv_encode_finish(const skv_params *params, const skv_shape *shape, void *ou
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
+int skv_encode_commit(const skv_params *params, const skv_shape *shape, uint64_t chunk_begin,
+                      uint64_t chunk_end, void *out, size_t out_capacity, uint64_t *end_bytes,
+                      void *workspace, size_t workspace_bytes, skv_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  if (pl.adaptive) return SKV_ERR_ARG;
+  if (chunk_begin > chunk_end || chunk_end > (uint64_t)pl.geo.nchunks) return SKV_ERR_ARG;
+  if (!out || !workspace || !aligned(out, 8) || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
+  if (workspace_bytes < ws_bytes_for(pl, SKV_OP_ENCODE)) return SKV_ERR_CAPACITY;
+  if (out_capacity < 64 + 8 * (size_t)(pl.geo.nchunks + 1)) return SKV_ERR_CAPACITY;
+  if (end_bytes && !aligned(end_bytes, 8)) return SKV_ERR_ARG;
+  if (chunk_begin == chunk_end && !end_bytes) return SKV_OK;
+  EncodeLaunch a = encode_launch(params, pl, static_cast<uint8_t *>(workspace));
+  a.out = static_cast<uint8_t *>(out);
+  a.capacity = out_capacity;
+  a.c_first = (int64_t)chunk_begin;
+  a.c_count = (int64_t)(chunk_end - chunk_begin);
+  if (launch_encode_commit(a, end_bytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SKV_ERR_CUDA;
+  return SKV_OK;
+}
+
 int skv_model_fingerprint(const skv_params *params, const skv_shape *shape,
                           uint64_t *fingerprint, void *workspace, size_t workspace_bytes,
                           skv_stream_t stream) {
@@ -833,14 +866,14 @@ int skv_decode_range(const skv_params *params, const skv_shape *shape, const voi
   Plan pl;
   int rc = make_plan(params, shape, &pl);
   if (rc) return rc;
-  if (range_flags & ~SKV_RANGE_FIRST) return SKV_ERR_ARG;
+  if (range_flags & ~(SKV_RANGE_FIRST | SKV_RANGE_PARTIAL)) return SKV_ERR_ARG;
   // adaptive tables depend on every earlier block of a row: whole containers only
   if (pl.adaptive) return SKV_ERR_ARG;
   if (chunk_begin > chunk_end || chunk_end > (uint64_t)pl.geo.nchunks) return SKV_ERR_ARG;
   if (page_of_chunk && (!aligned(page_of_chunk, 4) || num_pages == 0)) return SKV_ERR_ARG;
   return decode_enqueue(params, pl, in, in_bytes, chunk_begin, chunk_end, mu, kv_out,
                         page_of_chunk, num_pages, (range_flags & SKV_RANGE_FIRST) != 0, workspace,
-                        workspace_bytes, stream);
+                        workspace_bytes, stream, (range_flags & SKV_RANGE_PARTIAL) == 0);
 }
 
 int skv_decode_status(const void *workspace, skv_stream_t stream) {

@@ -536,6 +536,97 @@ __global__ void __launch_bounds__(256) k_compact(EncodeLaunch a) {
   }
 }
 
+// Incremental compaction (skv_encode_commit).  The sizes of the range's chunks
+// are scanned in place by k_scan_local (block-local offsets, block sums in
+// partials[0 ..]); k_commit_partials turns the block sums into offsets after
+// the payload committed before and records the new prefix; k_commit_compact
+// copies the chunks' stacks.  A range that does not start where the committed
+// prefix ends is an argument error and nothing is placed.  The chunk after the
+// range gets its offset now (the range's end), so the range can be decoded
+// before the next commit; that commit writes the same value again.
+__global__ void __launch_bounds__(1024) k_commit_partials(EncodeLaunch a, int64_t nb,
+                                                           uint64_t *end_bytes) {
+  __shared__ uint64_t s[1024];
+  const bool in_order = a.head->committed == (unsigned long long)a.c_first;
+  uint64_t carry = a.head->commit_total;
+  for (int64_t b0 = 0; b0 < nb; b0 += 1024) {
+    const int64_t i = b0 + threadIdx.x;
+    const uint64_t v = i < nb ? a.partials[i] : 0;
+    s[threadIdx.x] = v;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+      uint64_t t = threadIdx.x >= off ? s[threadIdx.x - off] : 0;
+      __syncthreads();
+      s[threadIdx.x] += t;
+      __syncthreads();
+    }
+    if (i < nb) a.partials[i] = carry + s[threadIdx.x] - v;
+    carry += s[1023];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const int64_t c_end = a.c_first + a.c_count;
+    const uint64_t hbytes = 64 + 8 * (uint64_t)(a.geo.nchunks + 1);
+    if (!in_order) {
+      atomicOr(&a.head->flags, kFlagArg);
+    } else if (hbytes + carry > a.capacity) {
+      atomicOr(&a.head->flags, kFlagCapacity);
+    } else {
+      reinterpret_cast<uint64_t *>(a.out + 64)[c_end] = carry;
+      a.head->commit_total = carry;
+      a.head->committed = (unsigned long long)c_end;
+    }
+    if (end_bytes) *end_bytes = hbytes + a.head->commit_total;
+  }
+}
+
+__global__ void __launch_bounds__(256) k_commit_compact(EncodeLaunch a) {
+  // an out-of-order range or a full container: k_commit_partials has flagged it
+  if (a.head->committed != (unsigned long long)(a.c_first + a.c_count)) return;
+  const uint64_t hbytes = 64 + 8 * (uint64_t)(a.geo.nchunks + 1);
+  uint64_t *offs = reinterpret_cast<uint64_t *>(a.out + 64);
+  uint32_t *payload = reinterpret_cast<uint32_t *>(a.out + hbytes);
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); i < a.c_count;
+       i += nwarps) {
+    const int64_t c = a.c_first + i;
+    const uint64_t off = a.sizes[c] + a.partials[i / kScanBlock];
+    const uint32_t start = a.starts[c];
+    // a chunk not encoded since SKV_RANGE_FIRST still holds the sentinel start
+    if (start > a.stride) {
+      if (lane == 0) atomicOr(&a.head->flags, kFlagArg);
+      continue;
+    }
+    const int64_t nw = a.stride - start;
+    if (hbytes + off + 4 * (uint64_t)nw > a.capacity) {  // only if sizes and starts disagree
+      if (lane == 0) atomicOr(&a.head->flags, kFlagArg);
+      continue;
+    }
+    const uint32_t *src = a.scratch + c * a.stride + start;
+    uint32_t *dst = payload + off / 4;
+    for (int64_t k = lane; k < nw; k += 32) dst[k] = src[k];
+    if (lane == 0) offs[c] = off;
+  }
+}
+
+// The header of a container placed by commits, once every chunk is committed.
+__global__ void k_commit_header(EncodeLaunch a) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const int64_t nc = a.geo.nchunks;
+  if (a.head->committed != (unsigned long long)nc) {
+    atomicOr(&a.head->flags, kFlagArg);
+    return;
+  }
+  const uint64_t total = a.head->commit_total;
+  a.head->total = total;
+  uint8_t h[64];
+  make_header(h, a.geo, a.dtype, total, mix64(a.head->hash_acc ^ a.hash_words),
+              (a.nsw > 0 ? 1u : 0u) | (a.order0 ? 2u : 0u) | (a.adaptive ? 4u : 0u));
+  for (int i = 0; i < 64; ++i) a.out[i] = h[i];
+  reinterpret_cast<uint64_t *>(a.out + 64)[0] = 0;
+}
+
 // Grid for ntasks >= 1 warp tasks of a coder kernel (blocks of at most
 // max_threads, at most one block per SM).  A lane's symbols are coded one after
 // another, so a launch takes at least one lane's chain of steps, and a step is
@@ -635,6 +726,27 @@ cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s) {
   if (a.bits_partials) return cudaErrorInvalidValue;
   task_shape(ntasks, kCodeThreads, blocks, threads);
   return run_encode<1, false, kCodeThreads>(a, blocks, threads, s);
+}
+
+cudaError_t launch_encode_commit(const EncodeLaunch &a, uint64_t *end_bytes, cudaStream_t s) {
+  cudaError_t e;
+  const int64_t nb = (a.c_count + kScanBlock - 1) / kScanBlock;
+  if (nb > 0) {
+    k_scan_local<<<(unsigned)nb, 256, 0, s>>>(a.sizes + a.c_first, a.c_count, a.partials);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  k_commit_partials<<<1, 1024, 0, s>>>(a, nb, end_bytes);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.c_count <= 0) return cudaSuccess;
+  int64_t cblocks = (a.c_count + 7) / 8;
+  if (cblocks > (int64_t)device_sm_count() * 16) cblocks = (int64_t)device_sm_count() * 16;
+  k_commit_compact<<<(unsigned)cblocks, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_commit_header(const EncodeLaunch &a, cudaStream_t s) {
+  k_commit_header<<<1, 32, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_encode_finish(const EncodeLaunch &a, cudaStream_t s) {

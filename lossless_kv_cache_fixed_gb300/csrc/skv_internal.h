@@ -48,6 +48,8 @@ struct WsHead {
   double bits;                    // ideal bits total
   unsigned long long next_task;   // decode: tasks handed out after the first round
   unsigned long long chunks_done; // encode: chunks coded since the head was cleared
+  unsigned long long committed;   // encode: chunks placed by skv_encode_commit (a prefix)
+  unsigned long long commit_total;  // encode: payload bytes of those chunks
 };
 
 // ---- container header (spec v1), built the same way on the host and the device ----
@@ -243,6 +245,12 @@ cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s);
 // encoder (skv_encode_with_bits) rather than in a second kernel.
 bool encode_fuses_bits(int dtype, bool order0, int64_t chunks, int G);
 cudaError_t launch_encode_finish(const EncodeLaunch &a, cudaStream_t s);
+// skv_encode_commit: chunks [a.c_first, a.c_first + a.c_count), the next after
+// those committed before, placed in the container a.out (offsets and payload),
+// and the container's size so far in *end_bytes (if not null);
+// launch_commit_header then writes the header once every chunk is committed.
+cudaError_t launch_encode_commit(const EncodeLaunch &a, uint64_t *end_bytes, cudaStream_t s);
+cudaError_t launch_commit_header(const EncodeLaunch &a, cudaStream_t s);
 
 // Adaptive counts (skv_adapt.cu): per-row probabilities P and counts C (u64,
 // kNsymBf16 per row), per-row tables E (kNsymBf16 + 1) and, for decode, their

@@ -119,12 +119,25 @@ def test_argument_errors_without_gpu(skv):
                             1 << 20, 1 << 30, None)
     assert rc == P.SKV_ERR_ARG
     # range decode: range, flags and page-table arguments are checked on the host
-    for c0, c1, fl, pages, npg in ((5, 4, 1, None, 0), (0, 9, 1, None, 0), (0, 8, 2, None, 0),
+    for c0, c1, fl, pages, npg in ((5, 4, 1, None, 0), (0, 9, 1, None, 0), (0, 8, 4, None, 0),
                                    (0, 8, 1, 1 << 20, 0), (0, 8, 1, (1 << 20) + 2, 8)):
         rc = P.skv_decode_range(good, shape, 1 << 20, 1 << 20, c0, c1, 1 << 20, 1 << 20, pages,
                                 npg, fl, 1 << 20, 1 << 30, None)
         assert rc == P.SKV_ERR_ARG, (c0, c1, fl, pages, npg)
     assert P.skv_decode_status(None, None) == P.SKV_ERR_ARG
+    # commits: range, buffer alignment and room for the offset table, on the host
+    for c0, c1, out, cap in ((5, 4, 1 << 20, 1 << 30), (0, 9, 1 << 20, 1 << 30),
+                             (0, 8, (1 << 20) + 4, 1 << 30)):
+        assert P.skv_encode_commit(good, shape, c0, c1, out, cap, None, 1 << 20, 1 << 30,
+                                   None) == P.SKV_ERR_ARG, (c0, c1, out, cap)
+    assert P.skv_encode_commit(good, shape, 0, 8, 1 << 20, 64 + 8 * 8, None, 1 << 20, 1 << 30,
+                               None) == P.SKV_ERR_CAPACITY
+    assert P.skv_encode_commit(good, shape, 0, 8, 1 << 20, 1 << 30, (1 << 20) + 4, 1 << 20,
+                               1 << 30, None) == P.SKV_ERR_ARG   # end_bytes misaligned
+    assert P.skv_encode_commit(good, shape, 3, 3, 1 << 20, 1 << 30, None, 1 << 20, 1 << 30,
+                               None) == P.SKV_OK           # an empty range places nothing
+    assert P.skv_encode_commit(ad, shape, 0, 8, 1 << 20, 1 << 30, None, 1 << 20, 1 << 30,
+                               None) == P.SKV_ERR_ARG      # adaptive counts: whole caches
     # NULL and misaligned pointers
     rc, _ = P.skv_encode(good, shape, None, 1 << 20, 1 << 20, 1 << 30, 1 << 20, 1 << 30, None)
     assert rc == P.SKV_ERR_ARG

@@ -8,7 +8,11 @@ through the C ABI.
   stack is read, and a bad symbol in one range is reported there;
 * skv_model_fingerprint equals the oracle's model fingerprint;
 * containers of consecutive layer ranges, each encoded on the GPU with its
-  rows of sigma, merge (skv_merge_parts, host) into the whole container.
+  rows of sigma, merge (skv_merge_parts, host) into the whole container;
+* ranges committed as they are encoded (skv_encode_commit) build the same
+  container, and each committed range decodes before the rest is encoded;
+  commits out of order, of chunks not yet encoded, of a prefix only, or past
+  the buffer's capacity are reported by skv_encode_finish.
 """
 import numpy as np
 import pytest
@@ -141,3 +145,82 @@ def test_gpu_parts_merge_into_the_whole_container(kind):
     out = np.zeros(nb, dtype=np.uint8)
     rc, nb2 = P.skv_merge_parts(codec.params, codec.shape, codec.fingerprint(), parts, out)
     assert rc == P.SKV_OK and nb2 == nb and np.array_equal(out, want)
+
+
+@pytest.mark.parametrize("kind", ["bf16", "e4m3"])
+@pytest.mark.parametrize("flags", [0, 2], ids=["static", "block-scale"])
+def test_commits_build_the_container_and_decode_early(kind, flags):
+    """Chunk ranges encoded in order, each committed right after (or several at
+    once), give the container skv_encode writes; every committed range decodes
+    (SKV_RANGE_PARTIAL) before the later ones are encoded."""
+    w = synth.make(CASES[kind])
+    codec = gpu_codec(w, flags=flags)
+    kv_d, mu_d = device_views(w)
+    whole, nb = codec.encode(kv_d, mu_d)
+    whole = whole[:nb].clone()
+    nc = codec.num_chunks()
+    rng = np.random.default_rng(11 + flags)
+    for pieces, batch in ((1, 1), (3, 1), (7, 2), (nc, 5)):
+        cuts = sorted(set([0, nc] + rng.choice(np.arange(1, nc), pieces - 1, replace=False).tolist()))
+        out = torch.zeros(codec.max_bytes, dtype=torch.uint8, device="cuda")
+        dec = torch.zeros_like(kv_d)
+        ends = torch.zeros(nc + 1, dtype=torch.int64).pin_memory()  # written by the device
+        done, ncommit = 0, 0
+        for i, (a, b) in enumerate(zip(cuts[:-1], cuts[1:])):
+            codec.encode_range(kv_d, mu_d, a, b, first=(i == 0))
+            if (i + 1) % batch == 0 or b == nc:
+                codec.encode_commit(done, b, out, end_bytes=ends[ncommit:ncommit + 1])
+                codec.decode_range(out, out.numel(), done, b, mu_d, dec, first=(done == 0),
+                                   partial=True)
+                done, ncommit = b, ncommit + 1
+        codec.decode_status()
+        assert torch.equal(dec, kv_d)
+        out2, nb2 = codec.encode_finish(out=out)
+        assert nb2 == nb and torch.equal(out2[:nb2], whole)
+        # the sizes so far: increasing, the last one the container's
+        e = ends[:ncommit].tolist()
+        assert e == sorted(e) and e[-1] == nb
+        # the finished container passes the full header check
+        assert torch.equal(codec.decode(out2, nb2, mu_d), kv_d)
+
+
+def test_commit_errors_are_reported_by_finish():
+    import lossless_kv_cache_fixed_gb300 as P
+    w = synth.make(CASES["bf16"])
+    codec = gpu_codec(w)
+    kv_d, mu_d = device_views(w)
+    nc = codec.num_chunks()
+    h = nc // 2
+    out = torch.zeros(codec.max_bytes, dtype=torch.uint8, device="cuda")
+
+    def finish_rc(buf=out):
+        ws = codec.workspace(P.SKV_OP_ENCODE)
+        rc, _ = P.skv_encode_finish(codec.params, codec.shape, buf.data_ptr(), buf.numel(),
+                                    ws.data_ptr(), ws.numel(), P._stream_handle())
+        return rc
+
+    # a range that does not start where the committed prefix ends
+    codec.encode_range(kv_d, mu_d, 0, nc, first=True)
+    codec.encode_commit(h, nc, out)
+    assert finish_rc() == P.SKV_ERR_ARG
+    # a chunk committed before it was encoded (its start is still the sentinel)
+    codec.encode_range(kv_d, mu_d, 0, h, first=True)
+    codec.encode_commit(0, h + 1, out)
+    codec.encode_range(kv_d, mu_d, h, nc)
+    assert finish_rc() == P.SKV_ERR_ARG
+    # only a prefix committed
+    codec.encode_range(kv_d, mu_d, 0, nc, first=True)
+    codec.encode_commit(0, h, out)
+    assert finish_rc() == P.SKV_ERR_ARG
+    # a buffer with room for the offset table but not for the payload
+    small = torch.zeros(64 + 8 * (nc + 1) + 4096, dtype=torch.uint8, device="cuda")
+    codec.encode_range(kv_d, mu_d, 0, nc, first=True)
+    codec.encode_commit(0, nc, small)
+    assert finish_rc(small) == P.SKV_ERR_CAPACITY
+    # and a clean run afterwards
+    codec.encode_range(kv_d, mu_d, 0, nc, first=True)
+    codec.encode_commit(0, h, out)
+    codec.encode_commit(h, nc, out)
+    o2, nb = codec.encode_finish(out=out)
+    ref, nb_ref = codec.encode(kv_d, mu_d)
+    assert nb == nb_ref and torch.equal(o2[:nb], ref[:nb_ref])
