@@ -814,7 +814,7 @@ def e2e_single_pipelined(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
 
 
 def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all, world, dev,
-                         args, groups=4):
+                         args, groups=4, layer_cuts=None):
     """The end-to-end step writing one container, committed as it is encoded:
     the layer groups' inputs are copied in on a copy stream; each group, once
     in, is encoded (skv_encode_range), its ideal bits computed and placed in the
@@ -826,17 +826,24 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
     4 groups of the Qwen3-32B-shaped cache: 58.1 GB/s (8: 47.4, 16: 40.7;
     smaller groups pay a lane chain per launch more often)."""
     import torch
-    if s.L % groups or mu_h is None or flags & P.SKV_FLAG_ADAPTIVE or s.T % s.Tb:
+    if layer_cuts is None:
+        if s.L % groups:
+            return None
+        layer_cuts = [s.L * g // groups for g in range(groups + 1)]
+    groups = len(layer_cuts) - 1
+    if mu_h is None or flags & P.SKV_FLAG_ADAPTIVE or s.T % s.Tb:
         return None
     main = torch.cuda.current_stream()
     cin, cout, dst = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    lp = s.L // groups
-    per = kv_h.numel() // groups
     nc = codec.num_chunks()
-    cpg = nc // groups
+    per_layer = kv_h.numel() // s.L           # scalars of one layer (K and V)
+    cpl = nc // s.L                           # chunks of one layer
+    sc = [l * per_layer for l in layer_cuts]  # scalar cuts
+    cc = [l * cpl for l in layer_cuts]        # chunk cuts
     hb = 64 + 8 * (nc + 1)        # header and offset table
-    gcodecs = [P.Codec(s.dtype, lp, s.H, s.T, s.D, s.Tb, s.G,
-                       w.sigma[g * lp:(g + 1) * lp].to(dev).contiguous(), ecdf, phat, flags=flags)
+    gcodecs = [P.Codec(s.dtype, layer_cuts[g + 1] - layer_cuts[g], s.H, s.T, s.D, s.Tb, s.G,
+                       w.sigma[layer_cuts[g]:layer_cuts[g + 1]].to(dev).contiguous(), ecdf, phat,
+                       flags=flags)
                for g in range(groups)]
     kv_d = torch.empty(kv_h.numel(), dtype=kv_h.dtype, device=dev)
     mu_d = torch.empty(mu_h.numel(), dtype=mu_h.dtype, device=dev)
@@ -850,8 +857,9 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
         evs = []
         with torch.cuda.stream(cin):
             for g in range(groups):
-                kv_d[g * per:(g + 1) * per].copy_(kv_h[g * per:(g + 1) * per], non_blocking=True)
-                mu_d[g * per:(g + 1) * per].copy_(mu_h[g * per:(g + 1) * per], non_blocking=True)
+                a, b = sc[g], sc[g + 1]
+                kv_d[a:b].copy_(kv_h[a:b], non_blocking=True)
+                mu_d[a:b].copy_(mu_h[a:b], non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(cin)
                 evs.append(ev)
@@ -859,12 +867,12 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
         sent = hb
         for g in range(groups):
             main.wait_event(evs[g])
-            c0, c1 = g * cpg, (g + 1) * cpg
+            c0, c1 = cc[g], cc[g + 1]
+            a, b = sc[g], sc[g + 1]
             codec.encode_range(kv_d, mu_d, c0, c1, first=(g == 0), stream=main)
             codec.encode_commit(c0, c1, box_d, end_bytes=ends[g:g + 1], stream=main)
             # synchronises main: the commit has run and ends[g] holds its size
-            bits += gcodecs[g].ideal_bits(kv_d[g * per:(g + 1) * per],
-                                          mu_d[g * per:(g + 1) * per], stream=main)
+            bits += gcodecs[g].ideal_bits(kv_d[a:b], mu_d[a:b], stream=main)
             end = int(ends[g])
             # the group decodes on its own stream, beside the next group's encode
             dst.wait_stream(main)
@@ -874,8 +882,7 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
                 cout.wait_stream(main)
                 box_h[sent:end].copy_(box_d[sent:end], non_blocking=True)
                 cout.wait_stream(dst)
-                back_h[g * per:(g + 1) * per].copy_(back_d[g * per:(g + 1) * per],
-                                                    non_blocking=True)
+                back_h[a:b].copy_(back_d[a:b], non_blocking=True)
             sent = end
         _, nb = codec.encode_finish(out=box_d, stream=main)
         cout.wait_stream(main)

@@ -242,11 +242,12 @@ int skv_decode_status(const void *workspace, skv_stream_t stream);
  * per-scalar values and the total skv_ideal_bits gives, within its tolerance
  * (1e-3 relative + 1e-6 bits per scalar) -- so that a caller gets a coder's
  * cost and the cross-entropy it should reach side by side (the pages' section
- * "KV 缓存并非真正随机").  On bf16 mixture caches of more chunk lanes than one
- * round of the encoder's blocks holds (several tens of millions of scalars and
- * up), the encoder computes the bits itself from the symbols, mu and
- * reciprocals in its registers, one read of the inputs for both; elsewhere
- * the ideal-bits pass runs behind the encoder on the same stream.  The total
+ * "KV 缓存并非真正随机").  On bf16 mixture caches without per-block scales and
+ * of more chunk lanes than one round of the encoder's blocks holds (several
+ * tens of millions of scalars and up), the encoder computes the bits itself
+ * from the symbols, mu and reciprocals in its registers, one read of the
+ * inputs for both; elsewhere the ideal-bits pass runs behind the encoder on
+ * the same stream.  The total
  * is summed in fp64 in a fixed order for a given device and shape.
  *   per_scalar    device fp32 [N] output, or NULL.
  *   total         host; receives the ideal bits.

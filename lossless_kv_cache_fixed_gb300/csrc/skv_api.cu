@@ -657,7 +657,8 @@ int skv_encode_with_bits(const skv_params *params, const skv_shape *shape, const
   if ((rc = ensure_device_tables())) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t *ws = static_cast<uint8_t *>(workspace);
-  if (encode_fuses_bits(pl.dtype == SKV_BF16 ? 0 : 1, pl.order0, pl.geo.nchunks, pl.geo.G)) {
+  if (encode_fuses_bits(pl.dtype == SKV_BF16 ? 0 : 1, pl.order0, pl.nsw > 0, pl.geo.nchunks,
+                        pl.geo.G)) {
     if ((rc = encode_enqueue(params, pl, kv, mu, 0, (uint64_t)pl.geo.nchunks, true, workspace, st,
                              true, per_scalar)))
       return rc;
@@ -683,7 +684,8 @@ int skv_encode_with_bits_fused(const skv_params *params, const skv_shape *shape,
   if (!fused || pl.adaptive) return SKV_ERR_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
-  *fused = encode_fuses_bits(pl.dtype == SKV_BF16 ? 0 : 1, pl.order0, pl.geo.nchunks, pl.geo.G)
+  *fused = encode_fuses_bits(pl.dtype == SKV_BF16 ? 0 : 1, pl.order0, pl.nsw > 0,
+                             pl.geo.nchunks, pl.geo.G)
                ? 1 : 0;
   return SKV_OK;
 }

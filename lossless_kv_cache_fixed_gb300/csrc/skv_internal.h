@@ -243,7 +243,7 @@ cudaError_t launch_encode(const EncodeLaunch &a, cudaStream_t s);
 cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s);
 // Whether a launch of `chunks` chunks computes the ideal bits inside the
 // encoder (skv_encode_with_bits) rather than in a second kernel.
-bool encode_fuses_bits(int dtype, bool order0, int64_t chunks, int G);
+bool encode_fuses_bits(int dtype, bool order0, bool scaled, int64_t chunks, int G);
 cudaError_t launch_encode_finish(const EncodeLaunch &a, cudaStream_t s);
 // skv_encode_commit: chunks [a.c_first, a.c_first + a.c_count), the next after
 // those committed before, placed in the container a.out (offsets and payload),

@@ -254,14 +254,15 @@ def test_ideal_bits_e4m3_narrow_bins(oracle_mod):
 def test_encode_with_bits_inside_the_encoder(oracle_mod, flags):
     """A bf16 cache with more chunk lanes than one round of the encoder's blocks
     holds: skv_encode_with_bits computes the ideal bits inside the encoder
-    there (smaller caches run the ideal-bits pass behind it).  2 layers x 8
-    heads x 4090 tokens x 64 in 16-token blocks (8,192 chunks, the last token
-    block ragged) x 16 lanes, with the model's sigma or per-block scales."""
+    there (smaller caches, and caches with per-block scales, run the ideal-bits
+    pass behind it).  2 layers x 8 heads x 4090 tokens x 64 in 16-token blocks
+    (8,192 chunks, the last token block ragged) x 16 lanes, with the model's
+    sigma or per-block scales."""
     spec = synth.WORKLOADS["qwen3-0.6b-bf16"].scaled(name="fused-bits", L=2, H=8, T=4090, D=64,
                                                      Tb=16, G=16, calib_draws=2)
     w = synth.make(spec)
     codec = gpu_codec(w, flags=flags)
-    assert codec.encode_with_bits_fused()
+    assert codec.encode_with_bits_fused() == (flags == 0)
     assert not gpu_codec(synth.make("tiny-bf16")).encode_with_bits_fused()
     kv_d, mu_d = device_views(w)
     buf, nb = codec.encode(kv_d, mu_d)
