@@ -817,14 +817,17 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
                          args, groups=4, layer_cuts=None):
     """The end-to-end step writing one container, committed as it is encoded:
     the layer groups' inputs are copied in on a copy stream; each group, once
-    in, is encoded (skv_encode_range), its ideal bits computed and placed in the
-    container (skv_encode_commit), then decoded from it (skv_decode_range with
-    SKV_RANGE_PARTIAL) on a stream of its own, beside the next group's encode;
-    a second copy stream takes the decoded scalars and the container bytes
+    in, is encoded (skv_encode_range) and placed in the container
+    (skv_encode_commit) while its ideal bits are computed on a stream of their
+    own, then decoded from the container (skv_decode_range with
+    SKV_RANGE_PARTIAL) on a third stream, beside the next group's encode; a
+    second copy stream takes the decoded scalars and the container bytes
     committed so far back to host memory while later groups are still being
     copied in and coded.  skv_encode_finish writes the header at the end.
-    4 groups of the Qwen3-32B-shaped cache: 58.1 GB/s (8: 47.4, 16: 40.7;
-    smaller groups pay a lane chain per launch more often)."""
+    4 groups of the Qwen3-32B-shaped cache: 59.8 GB/s (58.2 with the ideal
+    bits on the encode stream; 8 groups 47.4, 16 groups 40.7: smaller groups
+    pay a lane chain per launch more often; smaller first or last groups lose
+    too)."""
     import torch
     if layer_cuts is None:
         if s.L % groups:
@@ -835,6 +838,7 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
         return None
     main = torch.cuda.current_stream()
     cin, cout, dst = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    bst = torch.cuda.Stream()
     nc = codec.num_chunks()
     per_layer = kv_h.numel() // s.L           # scalars of one layer (K and V)
     cpl = nc // s.L                           # chunks of one layer
@@ -871,8 +875,12 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
             a, b = sc[g], sc[g + 1]
             codec.encode_range(kv_d, mu_d, c0, c1, first=(g == 0), stream=main)
             codec.encode_commit(c0, c1, box_d, end_bytes=ends[g:g + 1], stream=main)
-            # synchronises main: the commit has run and ends[g] holds its size
-            bits += gcodecs[g].ideal_bits(kv_d[a:b], mu_d[a:b], stream=main)
+            committed = torch.cuda.Event()
+            committed.record(main)
+            # the group's ideal bits beside its encode (the call synchronises bst)
+            bst.wait_event(evs[g])
+            bits += gcodecs[g].ideal_bits(kv_d[a:b], mu_d[a:b], stream=bst)
+            committed.synchronize()          # the commit has run: ends[g] holds its size
             end = int(ends[g])
             # the group decodes on its own stream, beside the next group's encode
             dst.wait_stream(main)
@@ -913,11 +921,12 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
             "d2h_bytes_per_step": int(nb + kv_h.numel() * kv_h.element_size() + 8 * groups
                                       + 8 * groups + 32 * (groups + 2)),
             "mode": "one container, committed as it is encoded: %d layer groups copied in "
-                    "while earlier groups are encoded (skv_encode_range), committed "
-                    "(skv_encode_commit) and decoded from the container being written "
-                    "(skv_decode_range, SKV_RANGE_PARTIAL, beside the next group's encode); "
-                    "their decoded scalars and the container's committed bytes copied out "
-                    "as they are ready; skv_encode_finish writes the header" % groups,
+                    "while earlier groups are encoded (skv_encode_range) and committed "
+                    "(skv_encode_commit), their ideal bits computed alongside, and decoded "
+                    "from the container being written (skv_decode_range, SKV_RANGE_PARTIAL, "
+                    "beside the next group's encode); their decoded scalars and the "
+                    "container's committed bytes copied out as they are ready; "
+                    "skv_encode_finish writes the header" % groups,
             "container_bytes": int(nb), "step_s_spread": spread(ts)}
 
 
@@ -1232,7 +1241,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * dt / args.steps, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+        "scaling": "strong", "vs_baseline": None, "dtype": "int64", "data": "synthetic",
         "config": {"workload": args.workload, "scalars_per_gpu": s.n, "token_block": s.Tb,
                    "lanes": s.G, "block_scale": bool(args.block_scale),
                    "coder": coder_name(args)},
