@@ -149,15 +149,21 @@ def test_gpu_parts_merge_into_the_whole_container(kind):
 
 @pytest.mark.parametrize("kind", ["bf16", "e4m3"])
 @pytest.mark.parametrize("flags", [0, 2], ids=["static", "block-scale"])
-def test_commits_build_the_container_and_decode_early(kind, flags):
+def test_commits_build_the_container_and_decode_early(oracle_mod, kind, flags):
     """Chunk ranges encoded in order, each committed right after (or several at
-    once), give the container skv_encode writes; every committed range decodes
-    (SKV_RANGE_PARTIAL) before the later ones are encoded."""
+    once), give the oracle's container (the one skv_encode writes); every
+    committed range decodes (SKV_RANGE_PARTIAL) before the later ones are
+    encoded."""
+    import lossless_kv_cache_fixed_gb300 as P
     w = synth.make(CASES[kind])
     codec = gpu_codec(w, flags=flags)
     kv_d, mu_d = device_views(w)
     whole, nb = codec.encode(kv_d, mu_d)
     whole = whole[:nb].clone()
+    m = oracle_model(oracle_mod, w, block_scale=bool(flags & P.SKV_FLAG_BLOCK_SCALE))
+    kv_h, mu_h = host_views(w)
+    rc, want = oracle_mod.encode(m, kv_h, mu_h)
+    assert rc == 0 and np.array_equal(whole.cpu().numpy(), want)
     nc = codec.num_chunks()
     rng = np.random.default_rng(11 + flags)
     for pieces, batch in ((1, 1), (3, 1), (7, 2), (nc, 5)):
