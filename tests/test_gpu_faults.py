@@ -175,3 +175,37 @@ def test_invalid_inputs(enc):
         c3.encode(kv, mu)
     assert e.value.status == P.SKV_ERR_PARAM
     test_clean_roundtrip_then_library_still_usable(enc)
+
+
+def test_encode_with_bits_reports_data_errors(enc):
+    """skv_encode_with_bits on the two-pass path (this small cache) and inside
+    the encoder (a cache of several rounds of tasks) reports a NaN symbol, an
+    infinite mu and a short output buffer like skv_encode, and the library
+    stays usable."""
+    P, w, codec, kv, mu, buf, nb = enc
+    big_spec = synth.WORKLOADS["qwen3-0.6b-bf16"].scaled(name="fused-faults", L=2, H=8, T=4096,
+                                                         D=64, Tb=16, G=16, calib_draws=2)
+    big = synth.make(big_spec)
+    bcodec = gpu_codec(big)
+    bkv = big.kv.view(torch.int16).reshape(-1).cuda()
+    bmu = big.mu.view(torch.int16).reshape(-1).cuda()
+    assert not codec.encode_with_bits_fused() and bcodec.encode_with_bits_fused()
+    for c, k, m in ((codec, kv, mu), (bcodec, bkv, bmu)):
+        bad = k.clone()
+        bad[77] = 0x7FC1                          # a NaN pattern
+        with pytest.raises(P.SkvError) as e:
+            c.encode_with_bits(bad, m)
+        assert e.value.status == P.SKV_ERR_SYMBOL
+        badmu = m.clone()
+        badmu[5] = 0x7F80                         # mu = +inf
+        with pytest.raises(P.SkvError) as e:
+            c.encode_with_bits(k, badmu)
+        assert e.value.status == P.SKV_ERR_PARAM
+        _, n_ok = c.encode(k, m)
+        small = torch.empty(n_ok - 100, dtype=torch.uint8, device="cuda")
+        with pytest.raises(P.SkvError) as e:
+            c.encode_with_bits(k, m, out=small)
+        assert e.value.status == P.SKV_ERR_CAPACITY
+        out, n2, tot = c.encode_with_bits(k, m)
+        assert n2 == n_ok and tot > 0
+    test_clean_roundtrip_then_library_still_usable(enc)
