@@ -32,6 +32,11 @@ if ROOT not in sys.path:
 
 METRIC = "raw-KV encode & decode GB/s on 1 GB300 (% of roofline); bits/scalar vs ideal"
 DEFAULT_WORKLOAD = "qwen3-32b-bf16"
+# bytes one status read copies back to the host: the 64-byte workspace head
+# (skv_encode and skv_encode_finish read it twice, skv_decode, skv_ideal_bits
+# and skv_decode_status once; skv_encode_with_bits twice, three times when its
+# ideal-bits pass runs apart)
+HEAD_BYTES = 64
 # the other full-size workloads measured in the same run: (workload, token
 # block, lanes) -- the long-context cache at 1K, 4K and 16K scalars per chunk
 EXTRA_WORKLOADS = (("qwen3-8b-e4m3", 0, 0), ("long-32k-e4m3", 8, 1), ("long-32k-e4m3", 32, 1),
@@ -638,17 +643,30 @@ def end_to_end(P, codec, s, w, ecdf, phat, flags, kv, mu, out, raw, world, dev, 
     mu_d = None if mu is None else torch.empty_like(mu)
     box_d = out
     mub = 0 if mu is None else 2      # mu bytes per scalar moved
+    # the step's calls, as in the device-timed step: encode with the ideal bits
+    # and decode (adaptive counts: encode, decode and ideal bits)
+    with_bits = not flags & P.SKV_FLAG_ADAPTIVE
+    fused = with_bits and codec.encode_with_bits_fused()
+    heads = 1 + (2 if fused else 3)   # status reads per step (decode + encode's)
+
+    def encode_and_bits(kv_in, mu_in, box):
+        if with_bits:
+            _, nbx, tot = codec.encode_with_bits(kv_in, mu_in, out=box)
+            return nbx, tot
+        _, nbx = codec.encode(kv_in, mu_in, out=box)
+        return nbx, None
 
     def e2e_step():
         kv_d.copy_(kv_h, non_blocking=True)
         if mu_d is not None:
             mu_d.copy_(mu_h, non_blocking=True)
-        _, nb2 = codec.encode(kv_d, mu_d, out=box_d)
+        nb2, tot = encode_and_bits(kv_d, mu_d, box_d)
         box_h[:nb2].copy_(box_d[:nb2], non_blocking=True)
         box_d[:nb2].copy_(box_h[:nb2], non_blocking=True)
         codec.decode(box_d, nb2, mu_d, out=kv_d)
         kv_back.copy_(kv_d, non_blocking=True)
-        tot = codec.ideal_bits(kv_d, mu_d)
+        if tot is None:
+            tot = codec.ideal_bits(kv_d, mu_d)
         torch.cuda.synchronize()
         return nb2, tot
 
@@ -671,7 +689,7 @@ def end_to_end(P, codec, s, w, ecdf, phat, flags, kv, mu, out, raw, world, dev, 
     e2e_s = max_over_ranks(statistics.median(ts), world, dev)
     staged_e2e = {"value": round(raw_all / e2e_s / 1e9, 3), "unit": "GB/s",
                   "h2d_bytes_per_step": int(raw + mub * n + nb2),
-                  "d2h_bytes_per_step": int(nb2 + raw + 8 + 3 * 32),
+                  "d2h_bytes_per_step": int(nb2 + raw + heads * HEAD_BYTES),
                   "mode": "one container: staging copies to and from device buffers "
                           "(the container makes a round trip through host memory)",
                   "step_s_spread": spread(ts)}
@@ -679,9 +697,10 @@ def end_to_end(P, codec, s, w, ecdf, phat, flags, kv, mu, out, raw, world, dev, 
     # the same step with the kernels reading and writing the pinned host buffers
     # directly (mapped memory over the CPU-GPU link): no staging copies
     def e2e_zero_copy():
-        _, nb3 = codec.encode(kv_h, mu_h, out=box_h)
+        nb3, tot = encode_and_bits(kv_h, mu_h, box_h)
         codec.decode(box_h, nb3, mu_h, out=kv_back)
-        tot = codec.ideal_bits(kv_h, mu_h)
+        if tot is None:
+            tot = codec.ideal_bits(kv_h, mu_h)
         return nb3, tot
 
     kv_back.zero_()
@@ -690,8 +709,11 @@ def end_to_end(P, codec, s, w, ecdf, phat, flags, kv, mu, out, raw, world, dev, 
         raise RuntimeError("zero-copy round trip mismatch")
     zc_s = max_over_ranks(statistics.median(ts), world, dev)
     zc = {"value": round(raw_all / zc_s / 1e9, 3), "unit": "GB/s",
-          "h2d_bytes_per_step": int(2 * raw + mub * n + nb3 + mub * n + raw + mub * n),
-          "d2h_bytes_per_step": int(nb3 + raw + 8 + 3 * 32),
+          # encode reads kv and mu, decode the container and mu, and the
+          # ideal bits, unless inside the encoder, kv and mu again
+          "h2d_bytes_per_step": int(raw + mub * n + nb3 + mub * n
+                                    + (0 if fused else raw + mub * n)),
+          "d2h_bytes_per_step": int(nb3 + raw + heads * HEAD_BYTES),
           "mode": "one container: kernels read and write pinned host memory over the link",
           "step_s_spread": spread(ts)}
     del box_h
@@ -801,8 +823,8 @@ def e2e_single_pipelined(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
     dt = max_over_ranks(statistics.median(ts), world, dev)
     return {"value": round(raw_all / dt / 1e9, 3), "unit": "GB/s",
             "h2d_bytes_per_step": int(kv_h.numel() * kv_h.element_size() + 2 * s.n),
-            "d2h_bytes_per_step": int(nb + kv_h.numel() * kv_h.element_size() + 8 * groups
-                                      + 32 * (groups + 2)),
+            "d2h_bytes_per_step": int(nb + kv_h.numel() * kv_h.element_size()
+                                      + (groups + 3) * HEAD_BYTES),
             "mode": "one container, pipelined: %d layer groups copied in while earlier groups "
                     "are encoded (skv_encode_range) and their ideal bits computed, then "
                     "skv_encode_finish; %s" % (
@@ -919,7 +941,7 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
     return {"value": round(raw_all / dt / 1e9, 3), "unit": "GB/s",
             "h2d_bytes_per_step": int(kv_h.numel() * kv_h.element_size() + 2 * s.n),
             "d2h_bytes_per_step": int(nb + kv_h.numel() * kv_h.element_size() + 8 * groups
-                                      + 8 * groups + 32 * (groups + 2)),
+                                      + (groups + 3) * HEAD_BYTES),
             "mode": "one container, committed as it is encoded: %d layer groups copied in "
                     "while earlier groups are encoded (skv_encode_range) and committed "
                     "(skv_encode_commit), their ideal bits computed alongside, and decoded "
@@ -1009,7 +1031,7 @@ def e2e_pipelined(P, s, w, ecdf, phat, flags, kv_h, mu_h, raw, world, dev, args,
     nbs = sum(gr["nb"] for gr in groups)
     return {"value": round(raw / dt / 1e9, 3), "unit": "GB/s",
             "h2d_bytes_per_step": int(raw + 2 * s.n),
-            "d2h_bytes_per_step": int(nbs + raw + parts * (8 + 3 * 32)),
+            "d2h_bytes_per_step": int(nbs + raw + parts * 4 * HEAD_BYTES),
             "mode": "%d layer groups, each its own container on its own stream and host "
                     "thread (separate containers, not the product's single one): copies "
                     "overlap other groups' kernels%s" % (
