@@ -3,8 +3,9 @@
 back over the slow link and are decoded where they are used).
 
 Decoding a container range by range -- from device memory, from pinned host
-memory, or from a device buffer whose chunk ranges are copied in just before
-they are decoded -- and into a paged layout must give exactly the cache the
+memory, from a device buffer whose chunk ranges are copied in just before
+they are decoded, or from a container still being committed range by range
+as it is encoded -- and into a paged layout must give exactly the cache the
 whole-container decode gives (which the parity tests tie to the oracle).
 Page-index and corruption errors surface through skv_decode_status.
 """
@@ -121,6 +122,23 @@ def test_ranges_paged_hostmem_and_staged(name, flags, kw):
         codec.decode_range(dev, nb, c0, c1, mu, out)
     codec.decode_status()
     assert torch.equal(out, kv)
+
+    # 5. committed as it is encoded: each range placed in a container still
+    #    being written (skv_encode_commit) and decoded from it into the page
+    #    pool (SKV_RANGE_PARTIAL) before the next range is encoded
+    cont = torch.zeros(codec.max_bytes, dtype=torch.uint8, device="cuda")
+    pool = torch.zeros(npages * P_, dtype=kv.dtype, device="cuda")
+    cover = ranges[:-1]
+    for i, (c0, c1) in enumerate(cover):
+        codec.encode_range(kv, mu, c0, c1, first=(i == 0))
+        codec.encode_commit(c0, c1, cont)
+        codec.decode_range(cont, cont.numel(), c0, c1, mu_pool, pool, pages, npages,
+                           first=(i == 0), partial=True)
+    codec.decode_status()
+    for c, (b, n) in enumerate(chunks):
+        assert torch.equal(pool[int(perm[c]) * P_: int(perm[c]) * P_ + n], kv[b: b + n]), c
+    done, nb5 = codec.encode_finish(out=cont)
+    assert nb5 == nb and torch.equal(done[:nb], buf)
 
 
 def test_page_errors_and_corruption_reach_the_status():
