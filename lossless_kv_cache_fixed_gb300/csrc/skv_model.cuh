@@ -100,6 +100,13 @@ __device__ __forceinline__ ChanInv chan_inv(float sigma) {
 
 // cum(r) for bf16: floor(K (95 Phi_q(z1) + 3 Phi_q(z3) + 2 E_q[r]) / (100 2^26)) + r,
 // z1 = (lo - mu) / sigma, z3 = (lo - mu) / (3 sigma), each product rounded.
+// The quotient is the high word of F M with M = ceil(K 2^38 / 100): F M / 2^64
+// exceeds K F / (100 2^26) by F (M - K 2^38 / 100) / 2^64 <= 0.44 F / 2^64 <=
+// 1.6e-10 (F <= 100 2^26), less than the 2 / (100 2^26) = 3.0e-10 spacing of
+// that quotient's fractional parts (gcd(K, 100 2^26) = 2), so the floor is the
+// same for every F: one 64-bit multiply-high in place of the multiply by K,
+// the shift and the division by 100.
+constexpr uint64_t kCumMagicBf16 = 737690317153170883ull;  // ceil(K 2^38 / 100)
 __device__ __forceinline__ uint32_t cum_bf16(int32_t r, float mu, ChanInv inv, const uint2 *phi,
                                              const uint32_t *__restrict__ ecdf) {
   float d = __fsub_rn(lo_bf16(r), mu);
@@ -107,8 +114,7 @@ __device__ __forceinline__ uint32_t cum_bf16(int32_t r, float mu, ChanInv inv, c
   uint32_t p3 = phi_q(__fmul_rn(d, inv.s3), phi);
   uint32_t e = __ldg(ecdf + r);
   uint64_t F = 95ull * p1 + 3ull * p3 + 2ull * e;
-  uint64_t v = ((uint64_t)kKBf16 * F) >> 26;
-  return (uint32_t)(v / 100u) + (uint32_t)r;
+  return (uint32_t)__umul64hi(F, kCumMagicBf16) + (uint32_t)r;
 }
 
 // cum(r) for e4m3: floor(K Phi_q(z1) / 2^26) + r; K Phi_q / 2^26 =
