@@ -239,7 +239,12 @@ __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
     int64_t sp = a.stride;
     uint64_t x = kStateL;
     uint32_t flags = 0;
-    for (int64_t gi = (int64_t)max_groups - 1; gi >= 0; --gi) {
+    // p0 % D (the group's first channel), stepped down by 8 G mod D a group
+    const uint32_t dstep = (8u * (uint32_t)G) % D;
+    uint32_t pmod = max_groups
+                        ? (8u * ((uint32_t)ell + (uint32_t)G * (max_groups - 1u))) % D : 0u;
+    for (int64_t gi = (int64_t)max_groups - 1; gi >= 0;
+         --gi, pmod = pmod >= dstep ? pmod - dstep : pmod + D - dstep) {
       const bool has = (uint32_t)gi < my_groups;
       const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * (uint32_t)gi);
       uint32_t sym[8], mub[8];
@@ -249,7 +254,9 @@ __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
         load_syms<DT>(a.kv, cg.base + p0, sym);
         if (!O0) {
           load_mu(a.mu, cg.base + p0, mub);
-          load_inv(invrow, p0 % D, inv);
+          // (the encoder with the ideal bits inside keeps the modulo: the
+          // stepped index cost it registers)
+          load_inv(invrow, BITS ? p0 % D : pmod, inv);
         }
       }
 #pragma unroll
@@ -1082,11 +1089,15 @@ __global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunc
     const float2 *invrow = a.inv_chunk ? a.inv_chunk + (uint64_t)(live ? c : 0) * D
                                        : a.inv + cg.srow;
 
-    for (uint32_t gi = 0; gi < max_groups; ++gi) {
+    // p0 % D (the group's first channel), stepped up by 8 G mod D a group
+    const uint32_t dstep = (8u * (uint32_t)G) % D;
+    uint32_t pmod = (8u * (uint32_t)ell) % D;
+    for (uint32_t gi = 0; gi < max_groups;
+         ++gi, pmod = pmod + dstep >= D ? pmod + dstep - D : pmod + dstep) {
       const bool has = gi < my_groups;
       const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * gi);
       const uint16_t *mup = a.mu + obase + p0;
-      const float2 *ivp2 = invrow + p0 % D;
+      const float2 *ivp2 = invrow + pmod;
       uint64_t out_lo = 0, out_hi = 0;  // the group's 8 symbols, shifted in from the top
 #pragma unroll 1
       for (int k = 0; k < 8; ++k) {
