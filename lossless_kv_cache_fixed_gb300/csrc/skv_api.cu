@@ -121,7 +121,7 @@ struct Plan {
   // workspace layout (byte offsets)
   size_t off_inv, off_sizes, off_starts, off_partials, off_scratch, off_bits, off_einv, total;
   size_t off_enc_cinv, off_enc_words, off_enc_bits, enc_total;  // encode: per-chunk tables after the stacks
-  size_t off_dec_cinv, dec_total;                 // decode: after the inverse p-hat table
+  size_t off_dec_gmu, off_dec_cinv, dec_total;    // decode: after the inverse p-hat table
   size_t off_bits_csig, bits_total;               // ideal bits: after the partial sums
   size_t off_mb_cinv, mb_total;                   // model bits: reciprocals per (chunk, channel)
   int64_t stride;  // words per chunk stack
@@ -207,8 +207,11 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   // encoder computes the bits, else an ideal-bits workspace of its own
   pl.enc_total = align_up(pl.off_enc_bits +
                           std::max(sizeof(double) * (size_t)kMaxBitsBlocks, pl.bits_total));
-  // the decoder's inverse p-hat table: kHinvN + 1 entries, kO0InvN + 1 for order 0
-  pl.off_dec_cinv = align_up(pl.off_einv + sizeof(int32_t) * ((order0 ? kO0InvN : kHinvN) + 1));
+  // the decoder's inverse p-hat table: kHinvN + 1 entries, kO0InvN + 1 for order 0;
+  // then (bf16 mixture) its per-rank guess terms for mu
+  pl.off_dec_gmu = align_up(pl.off_einv + sizeof(int32_t) * ((order0 ? kO0InvN : kHinvN) + 1));
+  const bool gmu = p->dtype == SKV_BF16 && !order0;
+  pl.off_dec_cinv = align_up(pl.off_dec_gmu + (gmu ? sizeof(float2) * (size_t)kNsymBf16 : 0));
   pl.dec_total = align_up(pl.off_dec_cinv + sizeof(float2) * ccells);
   pl.off_mb_cinv = pl.off_bits_csig;
   pl.mb_total = align_up(pl.off_mb_cinv + sizeof(float2) * ccells);
@@ -411,11 +414,13 @@ int decode_enqueue(const skv_params *params, const Plan &pl, const void *in, siz
   float2 *inv = reinterpret_cast<float2 *>(ws + pl.off_inv);
   const uint32_t *ecdf = pl.dtype == SKV_BF16 ? params->ecdf : nullptr;
   int32_t *einv = pl.dtype == SKV_BF16 ? reinterpret_cast<int32_t *>(ws + pl.off_einv) : nullptr;
+  float2 *gmu = pl.dtype == SKV_BF16 && !pl.order0 ? reinterpret_cast<float2 *>(ws + pl.off_dec_gmu)
+                                                   : nullptr;
   if (first) {
     if (cudaMemsetAsync(head, 0, sizeof(WsHead), st) != cudaSuccess) return SKV_ERR_CUDA;
     if (launch_prep(params->sigma, pl.nsig_model, ecdf, inv, head, st) != cudaSuccess)
       return SKV_ERR_CUDA;
-    if (einv && launch_einv(ecdf, einv, pl.order0 ? kO0InvN : kHinvN, st) != cudaSuccess)
+    if (einv && launch_einv(ecdf, einv, pl.order0 ? kO0InvN : kHinvN, gmu, st) != cudaSuccess)
       return SKV_ERR_CUDA;
   }
   DecodeLaunch a;
@@ -455,6 +460,7 @@ int decode_enqueue(const skv_params *params, const Plan &pl, const void *in, siz
   a.hash_words = hash_words(pl);
   a.bisect = (params->flags & SKV_FLAG_DECODE_BISECT) ? 1 : 0;
   a.einv = einv;
+  a.gmu = gmu;
   if (pl.adaptive) {
     // the whole container, one phase per token block: each block's tables come
     // from the blocks decoded before it

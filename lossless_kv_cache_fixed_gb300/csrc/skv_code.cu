@@ -173,23 +173,43 @@ cudaError_t launch_prep(const float *sigma, int64_t nsig, const uint32_t *ecdf, 
   return cudaGetLastError();
 }
 
+// The bound on the guess's p-hat slope term a (below): large enough that the
+// guess sits at mu's symbol, small enough that 1 + a dz/du stays finite.
+constexpr float kGuessSlopeMax = 1e30f * kHscaleBf16;
+
 // Inverse of the p-hat prefix table for the decoder's guess in the tails that
-// only the p-hat component reaches (a guess only: any error costs search steps).
-__global__ void k_einv(const uint32_t *__restrict__ ecdf, int32_t *__restrict__ einv, int n) {
+// only the p-hat component reaches, and (gmu) the guess's p-hat terms for each
+// rank r of mu: 0.02 E(mu) as a fraction of the CDF, and the slope
+// 0.02 rho / (knot step of u), with rho the p-hat mass of mu's bin per unit
+// width (the width from mu's exponent: the bin of a mantissa step), so that
+// the decoder's slope term is one multiply by sigma.  A guess only: any error
+// costs search steps, never a wrong symbol.
+__global__ void k_einv(const uint32_t *__restrict__ ecdf, int32_t *__restrict__ einv, int n,
+                       float2 *__restrict__ gmu) {
   const int k = blockIdx.x * blockDim.x + threadIdx.x;
-  if (k > n) return;
-  const uint32_t target = (uint32_t)(((uint64_t)k << 26) / (uint64_t)n);
-  int32_t lo = 0, hi = kNsymBf16;  // smallest r in [0, 65282] with ecdf[r] >= target
-  while (lo < hi) {
-    const int32_t mid = (lo + hi) >> 1;
-    if (ecdf[mid] >= target) hi = mid;
-    else lo = mid + 1;
+  if (k <= n) {
+    const uint32_t target = (uint32_t)(((uint64_t)k << 26) / (uint64_t)n);
+    int32_t lo = 0, hi = kNsymBf16;  // smallest r in [0, 65282] with ecdf[r] >= target
+    while (lo < hi) {
+      const int32_t mid = (lo + hi) >> 1;
+      if (ecdf[mid] >= target) hi = mid;
+      else lo = mid + 1;
+    }
+    einv[k] = lo;
   }
-  einv[k] = lo;
+  if (gmu && k < kNsymBf16) {
+    const uint32_t ea = ecdf[k], eb = ecdf[k + 1];
+    const uint32_t mub = bits_bf16(k);
+    const float w = __uint_as_float(max(mub & 0x7F80u, 0x0080u) << 16) * (1.0f / 128.0f);
+    float slope = 0.02f * (1.0f / 67108864.0f) * (float)(eb - ea) / w * kHscaleBf16;
+    slope = slope >= 0.0f ? fminf(slope, kGuessSlopeMax) : 0.0f;  // a NaN (0 inf) gives 0
+    gmu[k] = make_float2(0.02f * ((float)ea * (1.0f / 67108864.0f)), slope);
+  }
 }
 
-cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, int n, cudaStream_t s) {
-  k_einv<<<(n + 1 + 255) / 256, 256, 0, s>>>(ecdf, einv, n);
+cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, int n, float2 *gmu, cudaStream_t s) {
+  const int m = gmu && kNsymBf16 > n + 1 ? kNsymBf16 : n + 1;
+  k_einv<<<(m + 255) / 256, 256, 0, s>>>(ecdf, einv, n, gmu);
   return cudaGetLastError();
 }
 
@@ -1072,20 +1092,21 @@ __global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunc
       off_a = offs[c];
       off_b = offs[c + 1];
     }
-    // both ends word-aligned (a misaligned word read would fault), inside the payload
+    // both ends word-aligned (a misaligned word read would fault), inside the
+    // payload; a chunk's words fit 32 bits (a full chunk holds below 2^31)
     bool ok = live && off_a <= off_b && off_b <= payload_bytes && ((off_a | off_b) & 3) == 0 &&
-              (off_b - off_a) / 4 >= 2ull * G + (uint64_t)a.nsw;
+              (off_b - off_a) / 4 >= 2ull * G + (uint64_t)a.nsw && (off_b - off_a) / 4 < (1ull << 32);
     if (live && !ok) flags |= kFlagCorrupt;
     const uint64_t obase = chunk_out_base(a, c, ok, flags);  // mu and output
     const uint32_t *w = reinterpret_cast<const uint32_t *>(payload + (ok ? off_a : 0));
-    const uint64_t nw = ok ? (off_b - off_a) / 4 : 0;
+    const uint32_t nw = ok ? (uint32_t)((off_b - off_a) / 4) : 0u;
     ChunkGeo cg = chunk_geo(a.geo, live ? c : 0);
     const uint32_t my_groups =
         (ok && (uint32_t)ell < cg.ngroup) ? (cg.ngroup - ell + G - 1) / G : 0u;
     const uint32_t max_groups = __reduce_max_sync(0xFFFFFFFFu, my_groups);
     const uint32_t *ws0 = w + a.nsw;  // the lane states follow the scale words
     uint64_t x = ok ? ((uint64_t)ws0[2 * ell] | ((uint64_t)ws0[2 * ell + 1] << 32)) : kStateL;
-    uint64_t cur = 2ull * G + (uint64_t)a.nsw;
+    uint32_t cur = 2u * (uint32_t)G + (uint32_t)a.nsw;
     const float2 *invrow = a.inv_chunk ? a.inv_chunk + (uint64_t)(live ? c : 0) * D
                                        : a.inv + cg.srow;
 
@@ -1158,20 +1179,20 @@ __global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunc
             // more), so the guess solves G0(z) + a z = u with a = 0.02 rho sigma.
             // Without it the p-hat term at mu alone misses where bins are narrow
             // against sigma (values near zero): about 2 in 3 of the misses.
-            float e_mu = 0.0f, a_rho = 0.0f;
+            // Both terms come from one per-rank entry (k_einv): 0.02 E(mu), and
+            // 0.02 rho in the table's knot units, taken times sigma here.
+            float e_mu2 = 0.0f, a_knot = 0.0f;
             const int32_t rmu = DT == 0 ? rank_bf16(mub) : rank_of_value<DT>(muf);
             if (DT == 0) {
-              const uint32_t ea = __ldg(a.ecdf + rmu), eb = __ldg(a.ecdf + rmu + 1);
-              e_mu = (float)ea * (1.0f / 67108864.0f);
-              const float wmu = __uint_as_float(max(mub & 0x7F80u, 0x0080u) << 16) * (1.0f / 128.0f);
-              a_rho = __fdividef(0.02f * (1.0f / 67108864.0f) * (float)(eb - ea) * sig, wmu);
-              a_rho = a_rho >= 0.0f ? fminf(a_rho, 1e30f) : 0.0f;  // a NaN (0/0) gives 0
+              const float2 g = __ldg(a.gmu + rmu);
+              e_mu2 = g.x;
+              a_knot = fminf(g.y * sig, kGuessSlopeMax);  // NaN (sigma NaN) gives the bound
             }
             auto guess = [&](int32_t rref) -> int32_t {
               float u, uraw;
               const int32_t dr = (int32_t)(slot - (uint32_t)rref);
               uraw = (float)dr * kInvK;
-              u = DT == 0 ? uraw - 0.02f * e_mu : uraw;
+              u = DT == 0 ? uraw - e_mu2 : uraw;
               if (DT == 1) {
                 // beyond both ends of Phi_q's range cum(r) = r (below mu) or
                 // K + r (above): the rank follows from the slot directly.  Exact
@@ -1185,7 +1206,7 @@ __global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunc
               float z0 = fmaf(t - (float)kk, h.y, h.x);
               // the linear p-hat term: z0 / (1 + a dz/du), dz/du = h.y kHscale from
               // the table; it only moves the guess towards mu, never past it
-              if (DT == 0) z0 = __fdividef(z0, fmaf(a_rho * kHscale, h.y, 1.0f));
+              if (DT == 0) z0 = __fdividef(z0, fmaf(a_knot, h.y, 1.0f));
               int32_t r = rank_of_value<DT>(fmaf(sig, z0, muf));
               if (DT == 1) {
                 // the rank term at the guess: u falls by (r - rref) / K, one step
@@ -1206,9 +1227,14 @@ __global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunc
             const int32_t rg = guess(rmu);
             const uint32_t ca = cum_of<DT>(rg, muf, inv, s_phi, s_lo8, a.ecdf);
             const uint32_t cb = cum_of<DT>(rg + 1, muf, inv, s_phi, s_lo8, a.ecdf);
-            bracket_add(br, rg, ca, slot);
-            bracket_add(br, rg + 1, cb, slot);
-            done = br.hi - br.lo == 1;
+            // the bracket from the full one and these two points (cum(0) = 0,
+            // cum(|S|) = 2^M): below rg, [rg, rg + 1) itself, or above rg + 1
+            const bool at_lo = ca <= slot, at_hi = slot < cb;
+            br.lo = at_lo ? (at_hi ? rg : rg + 1) : 0;
+            br.clo = at_lo ? (at_hi ? ca : cb) : 0u;
+            br.hi = at_hi ? (at_lo ? rg + 1 : rg) : NS;
+            br.chi = at_hi ? (at_lo ? cb : ca) : (1u << M);
+            done = at_lo && at_hi;
             if (!done) {
               // (2) Newton in value space with the density of bin rg
               const float blo = lo_value(DT, rg, s_lo8), bhi = lo_value(DT, rg + 1, s_lo8);
@@ -1289,7 +1315,7 @@ __global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunc
         }
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, need) & seg;
         if (need) {
-          const uint64_t pos = cur + __popc(m & lt);
+          const uint32_t pos = cur + __popc(m & lt);  // pos < nw keeps the read in the chunk
           if (pos < nw) {
             x = (x << 32) | w[pos];
           } else {
@@ -1406,7 +1432,7 @@ __global__ void __launch_bounds__(dec_threads_max<0>(), 1) k_decode_o0(DecodeLau
         }
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, need) & seg;
         if (need) {
-          const uint64_t pos = cur + __popc(m & lt);
+          const uint32_t pos = cur + __popc(m & lt);  // pos < nw keeps the read in the chunk
           if (pos < nw) {
             x = (x << 32) | w[pos];
           } else {

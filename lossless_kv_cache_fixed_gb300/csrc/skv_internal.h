@@ -137,6 +137,7 @@ struct DecodeLaunch {
   int dtype;
   int bisect;               // 1: plain bisection search (reference path)
   const int32_t *einv;      // bf16: inverse of the p-hat prefix table (kHinvN + 1 ranks)
+  const float2 *gmu;        // bf16 mixture: per rank of mu, the guess's p-hat terms (k_einv)
   const uint8_t *in;
   uint64_t in_bytes;
   const uint16_t *mu;
@@ -198,6 +199,8 @@ constexpr int kHinvN = 1024;
 // Order-0 decode: inverse of the p-hat prefix table at kO0InvN + 1 points.
 constexpr int kO0InvN = 8192;
 constexpr float kHinvUmaxBf16 = 0.98f, kHinvUmaxE4m3 = 1.0f;
+// The guess table's knots per unit of u (bf16).
+constexpr float kHscaleBf16 = (float)kHinvN / kHinvUmaxBf16;
 // Ideal bits (e4m3): log2 Q(z), Q(z) = erfc(z / sqrt 2) / 2 the Gaussian upper
 // tail, at z = k / kTailPerUnit for k = 0 .. kTailN - 1 (z from 0 to 12).
 constexpr int kTailPerUnit = 256;
@@ -265,8 +268,9 @@ cudaError_t launch_ad_ideal(const Geo &g, const uint16_t *kv, int64_t b, const u
                             float *per_scalar, double *partials, int bx, WsHead *head,
                             int64_t nrows, cudaStream_t s);
 cudaError_t launch_ideal_final(const double *partials, int n, WsHead *head, cudaStream_t s);
-// einv[k] = the smallest rank r with E_q[r] >= k 2^26 / n, k = 0..n (n divides 2^26).
-cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, int n, cudaStream_t s);
+// einv[k] = the smallest rank r with E_q[r] >= k 2^26 / n, k = 0..n (n divides 2^26);
+// with gmu, also the decoder's per-rank guess terms (kNsymBf16 entries).
+cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, int n, float2 *gmu, cudaStream_t s);
 cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s);
 cudaError_t launch_ideal(const IdealLaunch &a, cudaStream_t s);
 cudaError_t launch_model_bits(const ModelBitsLaunch &a, cudaStream_t s);
