@@ -1049,8 +1049,8 @@ static __device__ __noinline__ Bracket search_lanes(uint32_t pend, bool mine_ope
   return br;
 }
 
-template <int DT, bool BISECT>
-__global__ void __launch_bounds__(dec_threads_max<DT>(), 1) k_decode(DecodeLaunch a) {
+template <int DT, bool BISECT, int NT = dec_threads_max<DT>()>
+__global__ void __launch_bounds__(NT, 1) k_decode(DecodeLaunch a) {
   extern __shared__ uint2 s_phi[];
   float *s_lo8 = reinterpret_cast<float *>(s_phi + kPhiKnots);
   float2 *s_hinv = reinterpret_cast<float2 *>(s_lo8 + 256);
@@ -1457,6 +1457,17 @@ __global__ void __launch_bounds__(dec_threads_max<0>(), 1) k_decode_o0(DecodeLau
 
 template <int DT, bool BISECT>
 static cudaError_t run_decode(const DecodeLaunch &a, int blocks, int threads, cudaStream_t s) {
+  // bf16 launches of one round of tasks at most: blocks of up to 768 threads,
+  // whose launch bound leaves 80 registers a thread instead of 72
+  if constexpr (DT == 0 && !BISECT) {
+    if (threads <= kDecThreads) {
+      cudaError_t e = cudaFuncSetAttribute(k_decode<DT, BISECT, kDecThreads>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+      if (e != cudaSuccess) return e;
+      k_decode<DT, BISECT, kDecThreads><<<blocks, threads, kDecSmem, s>>>(a);
+      return cudaGetLastError();
+    }
+  }
   cudaError_t e = cudaFuncSetAttribute(k_decode<DT, BISECT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
   if (e != cudaSuccess) return e;
