@@ -126,35 +126,6 @@ __device__ __forceinline__ uint32_t cum_e4m3(int32_t r, float mu, float inv_s, c
   return __umulhi(p, kKE4m3 << 6) + (uint32_t)r;
 }
 
-// Estimate of y / f = y * rf using only 32-bit conversions (64-bit integer
-// <-> float conversions run on the slow FP64 unit of this part).  |y| is split
-// into exact 24-bit limbs, so the float value carries only relative error; the
-// quotient (< 2^48 here) comes back as floor(qf / 2^24) plus an exactly
-// representable 24-bit rest.  With the roundings of the FMAs, of 1/f (and of f
-// itself above 2^24), of the product and of the rest, the estimate is within
-// 5 * 2^-24 |y/f| + 1.  est_div_pos takes x >= 0 (three limbs, no sign);
-// est_div48 a signed |y| < 2^48 (two limbs: y >> 24 < 2^24 is exact in fp32).
-__device__ __forceinline__ int64_t est_div_pos(uint64_t a, float rf) {
-  const float af = fmaf((float)(uint32_t)(a >> 48), 281474976710656.0f,
-                        fmaf((float)(uint32_t)((a >> 24) & 0xFFFFFFu), 16777216.0f,
-                             (float)(uint32_t)(a & 0xFFFFFFu)));
-  const float qf = af * rf;
-  const uint32_t qh = __float2uint_rd(qf * (1.0f / 16777216.0f));
-  const uint32_t ql = __float2uint_rn(fmaf(-(float)qh, 16777216.0f, qf));
-  return (int64_t)qh * 16777216 + ql;
-}
-
-__device__ __forceinline__ int64_t est_div48(int64_t y, float rf) {
-  const bool neg = y < 0;
-  const uint64_t a = neg ? (uint64_t)(-y) : (uint64_t)y;
-  const float af = fmaf((float)(uint32_t)(a >> 24), 16777216.0f, (float)(uint32_t)(a & 0xFFFFFFu));
-  const float qf = af * rf;
-  const uint32_t qh = __float2uint_rd(qf * (1.0f / 16777216.0f));
-  const uint32_t ql = __float2uint_rn(fmaf(-(float)qh, 16777216.0f, qf));
-  const int64_t q = (int64_t)qh * 16777216 + ql;
-  return neg ? -q : q;
-}
-
 // floor(n / f), n mod f for n < 2^32 from m = floor((2^32 - 1) / f): the
 // multiply-high estimate is at most one below the quotient.
 __device__ __forceinline__ uint32_t div32_recip(uint32_t n, uint32_t f, uint32_t m, uint32_t &r) {
@@ -167,13 +138,22 @@ __device__ __forceinline__ uint32_t div32_recip(uint32_t n, uint32_t f, uint32_t
   return q;
 }
 
-// floor(x / f) and x mod f for x < 2^63 and 1 <= f <= 2^M, without the FP64
-// division routine.  M <= 16 (e4m3): exact 32-bit steps.  Otherwise, from
-// y = x with |x/f| < 2^(63 - M), the estimates' error bound gives, for M = 28
-// (bf16), <= 5 * 2^11 + 1 and then <= 1.003 after one refinement (M from 17 to
-// 23 would take two); the remainder after the first estimate is below
-// (5 * 2^11 + 1) 2^28 < 2^42, so the refinement takes two limbs.  The remainder
-// is then within 3f of [0, f), and the loops below fix it.
+// floor(x / f) and x mod f for x < 2^63, 1 <= f <= 2^M and x / f < 2^(63 - M)
+// (the encoder renormalises to x < f 2^(63 - M) first), without the FP64
+// division routine or 64-bit integer <-> float conversions (both run on the
+// slow FP64 unit of this part).  M <= 16 (e4m3): exact 32-bit steps.  M = 28
+// (bf16), in fp32 with an approximate reciprocal rf of f (1 ulp, PTX
+// rcp.approx), so rf carries at most 3 2^-24 relative error with the rounding
+// of f itself:
+//  1. q0 = 8 floor(fl(x) rf / 8), x converted as two 32-bit halves (2 2^-24
+//     relative with their sum) and the product rounded: 6 2^-24 relative in
+//     all, so |x / f - q0| < 6 2^-24 2^35 + 8 < 2^14 (the conversion to u32
+//     saturates only within that bound);
+//  2. r0 = x - q0 f (exact, |r0| < 2^14 f <= 2^42) splits into exact 24-bit
+//     limbs, so fl(r0) rf is within 5 2^-24 2^14 < 0.005 of r0 / f and its
+//     nearest integer d within 0.505;
+//  3. q1 = q0 + d leaves r1 = x - q1 f in (-0.505 f, 0.505 f): the quotient
+//     is q1 or q1 - 1.  The bounded fix-up loops below take that step.
 template <int M>
 __device__ __forceinline__ uint64_t divmod_u64(uint64_t x, uint32_t f, uint64_t &rem) {
   if (M <= 16) {
@@ -189,15 +169,17 @@ __device__ __forceinline__ uint64_t divmod_u64(uint64_t x, uint32_t f, uint64_t 
     rem = r3;
     return ((uint64_t)q1 << 32) + ((uint64_t)q2 << 16) + q3;
   }
-  const float rf = __frcp_rn((float)f);
-  int64_t q = est_div_pos(x, rf);
+  static_assert(M <= 16 || M == 28, "the error bounds above are for M = 28");
+  float rf;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rf) : "f"((float)f));
+  const float xf = fmaf((float)(uint32_t)(x >> 32), 4294967296.0f, (float)(uint32_t)x);
+  const float qf = xf * rf;
+  int64_t q = (int64_t)__float2uint_rz(qf * 0.125f) << 3;
   int64_t r = (int64_t)x - q * (int64_t)f;
-#pragma unroll
-  for (int i = 0; i < (M >= 24 ? 1 : 2); ++i) {
-    const int64_t d = est_div48(r, rf);
-    q += d;
-    r -= d * (int64_t)f;
-  }
+  const float rl = fmaf((float)(int32_t)(r >> 24), 16777216.0f, (float)(uint32_t)(r & 0xFFFFFF));
+  const int32_t d = __float2int_rn(rl * rf);
+  q += d;
+  r -= (int64_t)d * (int64_t)f;
   for (int i = 0; i < 4 && r < 0; ++i) {
     q -= 1;
     r += f;
