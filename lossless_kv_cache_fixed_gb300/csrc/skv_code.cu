@@ -946,7 +946,8 @@ __device__ __forceinline__ void search_lane(int l, uint32_t slot, float muf, Cha
     } else if (it == 0 && wdt > 2 * 256 + 1) {
       cand = lane < 16 ? blo + ladder_step(lane) : bhi - ladder_step(31 - lane);
     } else {
-      cand = blo + (int32_t)(((int64_t)(lane + 1) * wdt) / 33);
+      // (lane + 1) wdt < 32 * 65283: 32-bit
+      cand = blo + (int32_t)(((uint32_t)(lane + 1) * (uint32_t)wdt) / 33u);
     }
     const bool act = lane < nact;
     const uint32_t cv = act ? cum_of<DT>(cand, s_mu, s_inv, s_phi, s_lo8, ecdf) : 0u;
@@ -988,6 +989,10 @@ static __device__ __noinline__ Bracket search_lanes(uint32_t pend, bool mine_ope
   const int sbase = sgi << lg_s;  // first lane of my segment
   const uint32_t smask = (1u << S) - 1u;
   const int myord = __popc(pend & ((1u << lane) - 1u));  // my place among the open lanes
+  // floor(n / (S + 1)) = umulhi(n, ceil(2^32 / (S + 1))) for n < 2^27 (the
+  // error n (m (S + 1) - 2^32) / 2^32 stays below 1 / (S + 1)); here n =
+  // (j + 1) wdt < 16 * 65283
+  const uint32_t inv_s1 = 0xFFFFFFFFu / (uint32_t)(S + 1) + 1u;
   for (int b0 = 0; b0 < npend; b0 += 1 << lg_kp) {
     const bool valid = b0 + sgi < npend;
     const int src = valid ? nth_set_bit(pend, b0 + sgi) : lane;
@@ -1013,7 +1018,7 @@ static __device__ __noinline__ Bracket search_lanes(uint32_t pend, bool mine_ope
         const int32_t g = ladder_step(((jj + 1) << (5 - lg_s)) - 1);
         cand = j < half ? blo + g : bhi - g;
       } else {
-        cand = blo + (int32_t)(((int64_t)(j + 1) * wdt) / (S + 1));
+        cand = blo + (int32_t)__umulhi((uint32_t)(j + 1) * (uint32_t)wdt, inv_s1);
       }
       const bool act = j < nact;
       const uint32_t cv = act ? cum_of<DT>(cand, s_mu, s_inv, s_phi, s_lo8, ecdf) : 0u;
