@@ -179,6 +179,7 @@ int make_plan(const skv_params *p, const skv_shape *s, Plan *out) {
   if (wl > nlane) wl = nlane;
   pl.nsw = scaled ? scale_words(s->head_dim) : 0;
   pl.stride = ((G * (wl + 2)) + pl.nsw + 3) / 4 * 4;
+  if (pl.stride >= (1ll << 31)) return SKV_ERR_ARG;  // the encoder's stack index is 32-bit
   size_t off = align_up(sizeof(WsHead));
   pl.off_inv = off;
   off = align_up(off + sizeof(float2) * (size_t)pl.nsig);

@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
     const uint32_t max_groups = __reduce_max_sync(0xFFFFFFFFu, my_groups);
     uint32_t *region = a.scratch + c * a.stride;
     const float2 *invrow = a.inv_chunk ? a.inv_chunk + (uint64_t)c * D : a.inv + cg.srow;
-    int64_t sp = a.stride;
+    int32_t sp = (int32_t)a.stride;  // a chunk's stack holds below 2^31 words (make_plan)
     uint64_t x = kStateL;
     uint32_t flags = 0;
     // p0 % D (the group's first channel), stepped down by 8 G mod D a group
@@ -306,14 +306,15 @@ __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
                 bk[k] = ideal::ideal_full_call<0>(lo, hi, muf, inv[k].s, ph);
             }
           }
-          emit = x >= ((uint64_t)f << (63 - M));
+          // x >= f 2^(63 - M), a multiple of 2^32: a test of x's high word
+          emit = (uint32_t)(x >> 32) >= (f << (31 - M));
         } else if (BITS) {
           bk[k] = 0.0f;
         }
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, emit) & seg;
         const int n = __popc(m);
         if (emit) {
-          const int64_t idx = sp - n + __popc(m & lt);
+          const int32_t idx = sp - n + __popc(m & lt);
           if (idx >= 0) region[idx] = (uint32_t)x;
           else flags |= kFlagOverflow;
           x >>= 32;
