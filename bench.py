@@ -181,26 +181,31 @@ def measured_peaks():
 # of every operation is the pair of exact cum evaluations that gives a symbol's
 # frequency; its cost is measured: k_model_bits does exactly that pair per
 # scalar (with the symbol's loads and rank, and a log2), and ncu counts 160
-# thread-instructions per scalar for bf16 and 105 for e4m3.  On top of it: encode's 64/32 divide and
-# renormalisation (~30 bf16, ~25 e4m3), decode's state update, stream read and
-# store (~20), whatever its search costs.  Ideal bits: two Gaussian bin masses,
-# the p-hat term and a logarithm (100 bf16, 50 e4m3: estimates).
-ALG_OPS = {2: {"encode": 190, "decode": 180, "ideal_bits": 100, "encode_with_bits": 290},
-           1: {"encode": 130, "decode": 125, "ideal_bits": 50, "encode_with_bits": 180},
+# thread-instructions per scalar for bf16 and 105 for e4m3.  On top of it:
+# encode's rANS division, renormalisation and word store (at least ~10 bf16,
+# ~15 e4m3: the bf16 encoder executes 185 in all, measured), decode's state
+# update, stream read and store (~20), whatever its search costs.  Ideal bits:
+# two Gaussian bin masses, the p-hat term and one logarithm (70 bf16, 50 e4m3:
+# estimates; inside the bf16 encoder they add 86 thread-instructions per
+# scalar, measured).  Each figure stays below what the kernels execute.
+ALG_OPS = {2: {"encode": 170, "decode": 180, "ideal_bits": 70, "encode_with_bits": 240},
+           1: {"encode": 120, "decode": 125, "ideal_bits": 50, "encode_with_bits": 170},
            # order-0 baseline: one cum evaluation is an E_q load, a multiply and
-           # a shift (about 8); encode = 2 of them + the divide + renorm = 100;
-           # decode = the table bracket + ~6 bisection steps + 2 evaluations +
-           # the state update = 90; ideal bits = one log2 = 20 (estimates)
-           "o0": {"encode": 100, "decode": 90, "ideal_bits": 20, "encode_with_bits": 120}}
+           # a shift (about 8); encode = 2 of them + the divide, renormalisation,
+           # rank and loads = 70; decode = the table bracket + ~6 bisection
+           # steps + 2 evaluations + the state update = 90; ideal bits = one
+           # log2 = 20 (estimates)
+           "o0": {"encode": 70, "decode": 90, "ideal_bits": 20, "encode_with_bits": 90}}
 OPS_BASIS = {
     "encode": "per scalar: the exact cum pair (measured by ncu on k_model_bits: 160 bf16 / "
-              "105 e4m3 thread-instructions) + the 64/32 divide and renormalisation (estimate)",
+              "105 e4m3 thread-instructions) + the rANS division, renormalisation and word "
+              "store (estimate, >= 10 bf16 / 15 e4m3)",
     "decode": "per scalar, the minimum any decoder of this model executes: the exact cum pair "
               "that verifies the symbol (measured by ncu on k_model_bits: 160 bf16 / 105 e4m3 "
               "thread-instructions) + the state update, stream read and store (estimate, ~20); "
               "no search",
     "ideal_bits": "per scalar: the Gaussian bin masses, the p-hat term and the logarithm "
-                  "(estimate)",
+                  "(estimate: 70 bf16, 50 e4m3)",
     "encode_with_bits": "per scalar: encode's figure + ideal bits' figure"}
 KERNEL = {"encode": "k_encode", "decode": "k_decode", "ideal_bits": "k_ideal",
           "encode_with_bits": "k_encode (ideal bits inside)"}
