@@ -95,6 +95,41 @@ __device__ __forceinline__ void load_syms(const void *kv, uint64_t at, uint32_t 
   }
 }
 
+// The first 4 of them (the encoder with the ideal bits inside codes a group in
+// two halves: its unrolled body stays half as long)
+template <int DT>
+__device__ __forceinline__ void load_syms(const void *kv, uint64_t at, uint32_t (&s)[4]) {
+  if (DT == 0) {
+    uint2 v = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(kv) + at));
+    uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s[k] = (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+  } else {
+    const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(kv) + at));
+#pragma unroll
+    for (int k = 0; k < 4; ++k) s[k] = (v >> (8 * k)) & 0xFFu;
+  }
+}
+
+__device__ __forceinline__ void load_mu(const uint16_t *mu, uint64_t at, uint32_t (&m)[4]) {
+  uint2 v = __ldg(reinterpret_cast<const uint2 *>(mu + at));
+  uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) m[k] = (w[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+}
+
+__device__ __forceinline__ void load_inv(const float2 *inv, uint64_t at, ChanInv (&c)[4]) {
+  const float4 *p = reinterpret_cast<const float4 *>(inv + at);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    float4 v = __ldg(p + k);
+    c[2 * k].s = v.x;
+    c[2 * k].s3 = v.y;
+    c[2 * k + 1].s = v.z;
+    c[2 * k + 1].s3 = v.w;
+  }
+}
+
 __device__ __forceinline__ void load_mu(const uint16_t *mu, uint64_t at, uint32_t (&m)[8]) {
   uint4 v = __ldg(reinterpret_cast<const uint4 *>(mu + at));
   uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -263,79 +298,88 @@ __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
     const uint32_t dstep = (8u * (uint32_t)G) % D;
     uint32_t pmod = max_groups
                         ? (8u * ((uint32_t)ell + (uint32_t)G * (max_groups - 1u))) % D : 0u;
+    // symbols per pass over a group: the encoder with the ideal bits inside
+    // codes each group in two halves, so that its unrolled body, twice the
+    // plain encoder's, stays in the instruction cache
+    constexpr int KH = BITS ? 4 : 8;
     for (int64_t gi = (int64_t)max_groups - 1; gi >= 0;
          --gi, pmod = pmod >= dstep ? pmod - dstep : pmod + D - dstep) {
       const bool has = (uint32_t)gi < my_groups;
-      const uint32_t p0 = 8u * ((uint32_t)ell + (uint32_t)G * (uint32_t)gi);
-      uint32_t sym[8], mub[8];
-      ChanInv inv[8];
-      float bk[8];
-      if (has) {
-        load_syms<DT>(a.kv, cg.base + p0, sym);
-        if (!O0) {
-          load_mu(a.mu, cg.base + p0, mub);
-          // (the encoder with the ideal bits inside keeps the modulo: the
-          // stepped index cost it registers)
-          load_inv(invrow, BITS ? p0 % D : pmod, inv);
-        }
-      }
-#pragma unroll
-      for (int k = 7; k >= 0; --k) {
-        uint32_t cst = 0, f = 1;
-        bool emit = false;
+      const uint32_t p0g = 8u * ((uint32_t)ell + (uint32_t)G * (uint32_t)gi);
+      // (the encoder with the ideal bits inside keeps the modulo: the stepped
+      // index cost it registers)
+      const uint32_t ch0 = BITS ? p0g % D : pmod;
+#pragma unroll 1
+      for (int hh = 8 / KH - 1; hh >= 0; --hh) {
+        const uint32_t p0 = p0g + (uint32_t)(KH * hh);  // a group never crosses a row of D
+        uint32_t sym[KH], mub[KH];
+        ChanInv inv[KH];
+        float bk[KH];
         if (has) {
-          int32_t r = DT == 0 ? rank_bf16(sym[k]) : rank_e4m3(sym[k]);
-          if (r < 0 || r >= NS) {
-            flags |= kFlagSymbol;
-            r = 0;
+          load_syms<DT>(a.kv, cg.base + p0, sym);
+          if (!O0) {
+            load_mu(a.mu, cg.base + p0, mub);
+            load_inv(invrow, ch0 + (uint32_t)(KH * hh), inv);
           }
-          if (O0) {
-            cst = cum_order0(r, ecdf);
-            f = cum_order0(r + 1, ecdf) - cst;
-          } else {
-            if (!mu_valid(mub[k])) {
-              flags |= kFlagParam;
-              mub[k] = 0;
-            }
-            const float muf = bf16_to_f32(mub[k]);
-            cst = cum_of<DT>(r, muf, inv[k], s_phi, s_lo8, a.ecdf);
-            f = cum_of<DT>(r + 1, muf, inv[k], s_phi, s_lo8, a.ecdf) - cst;
-            if (BITS) {
-              const float lo = lo_bf16(r), hi = lo_bf16(r + 1), ph = __ldg(a.phat + r);
-              if (!ideal::ideal_series_bf16(lo, hi, muf, inv[k].s, ph, bk[k]))
-                bk[k] = ideal::ideal_full_call<0>(lo, hi, muf, inv[k].s, ph);
-            }
-          }
-          // x >= f 2^(63 - M), a multiple of 2^32: a test of x's high word
-          emit = (uint32_t)(x >> 32) >= (f << (31 - M));
-        } else if (BITS) {
-          bk[k] = 0.0f;
         }
-        const uint32_t m = __ballot_sync(0xFFFFFFFFu, emit) & seg;
-        const int n = __popc(m);
-        if (emit) {
-          const int32_t idx = sp - n + __popc(m & lt);
-          if (idx >= 0) region[idx] = (uint32_t)x;
-          else flags |= kFlagOverflow;
-          x >>= 32;
-        }
-        sp -= n;
-        if (has) {
-          uint64_t rem;
-          const uint64_t q = divmod_u64<M>(x, f, rem);
-          x = (q << M) + rem + cst;
-        }
-      }
-      if (BITS) {
-        if (has) {
-          float part = 0.0f;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) part += bk[k];
-          bacc += (double)part;
-          if (a.bits_out) {
-            float4 *o = reinterpret_cast<float4 *>(a.bits_out + cg.base + p0);
-            o[0] = make_float4(bk[0], bk[1], bk[2], bk[3]);
-            o[1] = make_float4(bk[4], bk[5], bk[6], bk[7]);
+        for (int k = KH - 1; k >= 0; --k) {
+          uint32_t cst = 0, f = 1;
+          bool emit = false;
+          if (has) {
+            int32_t r = DT == 0 ? rank_bf16(sym[k]) : rank_e4m3(sym[k]);
+            if (r < 0 || r >= NS) {
+              flags |= kFlagSymbol;
+              r = 0;
+            }
+            if (O0) {
+              cst = cum_order0(r, ecdf);
+              f = cum_order0(r + 1, ecdf) - cst;
+            } else {
+              if (!mu_valid(mub[k])) {
+                flags |= kFlagParam;
+                mub[k] = 0;
+              }
+              const float muf = bf16_to_f32(mub[k]);
+              cst = cum_of<DT>(r, muf, inv[k], s_phi, s_lo8, a.ecdf);
+              f = cum_of<DT>(r + 1, muf, inv[k], s_phi, s_lo8, a.ecdf) - cst;
+              if (BITS) {
+                const float lo = lo_bf16(r), hi = lo_bf16(r + 1), ph = __ldg(a.phat + r);
+                if (!ideal::ideal_series_bf16(lo, hi, muf, inv[k].s, ph, bk[k]))
+                  bk[k] = ideal::ideal_full_call<0>(lo, hi, muf, inv[k].s, ph);
+              }
+            }
+            // x >= f 2^(63 - M), a multiple of 2^32: a test of x's high word
+            emit = (uint32_t)(x >> 32) >= (f << (31 - M));
+          } else if (BITS) {
+            bk[k] = 0.0f;
+          }
+          const uint32_t m = __ballot_sync(0xFFFFFFFFu, emit) & seg;
+          const int n = __popc(m);
+          if (emit) {
+            const int32_t idx = sp - n + __popc(m & lt);
+            if (idx >= 0) region[idx] = (uint32_t)x;
+            else flags |= kFlagOverflow;
+            x >>= 32;
+          }
+          sp -= n;
+          if (has) {
+            uint64_t rem;
+            const uint64_t q = divmod_u64<M>(x, f, rem);
+            x = (q << M) + rem + cst;
+          }
+        }
+        if (BITS) {
+          if (has) {
+            float part = 0.0f;
+#pragma unroll
+            for (int k = 0; k < KH; ++k) part += bk[k];
+            bacc += (double)part;
+            if (a.bits_out) {
+              float4 *o = reinterpret_cast<float4 *>(a.bits_out + cg.base + p0);
+#pragma unroll
+              for (int k = 0; k < KH; k += 4) o[k / 4] = make_float4(bk[k], bk[k + 1], bk[k + 2], bk[k + 3]);
+            }
           }
         }
       }
