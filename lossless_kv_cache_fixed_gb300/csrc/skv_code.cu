@@ -300,8 +300,11 @@ __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
                         ? (8u * ((uint32_t)ell + (uint32_t)G * (max_groups - 1u))) % D : 0u;
     // symbols per pass over a group: the encoder with the ideal bits inside
     // codes each group in two halves, so that its unrolled body, twice the
-    // plain encoder's, stays in the instruction cache
-    constexpr int KH = BITS ? 4 : 8;
+    // plain encoder's, stays in the instruction cache (193.9 against 177.7
+    // GB/s on the Qwen3-32B shape); the multi-round bf16 encoder gains a
+    // little from them too (260.6 against 258.4), the 768-thread ones lose
+    // (Qwen3-0.6B 247.8 against 252.4, Qwen3-8B e4m3 155.5 against 161.4)
+    constexpr int KH = BITS || NT > kCodeThreads ? 4 : 8;
     for (int64_t gi = (int64_t)max_groups - 1; gi >= 0;
          --gi, pmod = pmod >= dstep ? pmod - dstep : pmod + D - dstep) {
       const bool has = (uint32_t)gi < my_groups;
