@@ -843,17 +843,16 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
                          args, groups=4, layer_cuts=None):
     """The end-to-end step writing one container, committed as it is encoded:
     the layer groups' inputs are copied in on a copy stream; each group, once
-    in, is encoded (skv_encode_range) and placed in the container
-    (skv_encode_commit) while its ideal bits are computed on a stream of their
-    own, then decoded from the container (skv_decode_range with
+    in, is encoded (skv_encode_range, with SKV_RANGE_BITS: its ideal bits inside
+    the encoder, where the encoder fuses them for a group of its size; else an
+    ideal-bits pass on a stream of its own) and placed in the container
+    (skv_encode_commit), then decoded from the container (skv_decode_range with
     SKV_RANGE_PARTIAL) on a third stream, beside the next group's encode; a
     second copy stream takes the decoded scalars and the container bytes
     committed so far back to host memory while later groups are still being
     copied in and coded.  skv_encode_finish writes the header at the end.
-    4 groups of the Qwen3-32B-shaped cache: 59.8 GB/s (58.2 with the ideal
-    bits on the encode stream; 8 groups 47.4, 16 groups 40.7: smaller groups
-    pay a lane chain per launch more often; smaller first or last groups lose
-    too)."""
+    4 groups of the Qwen3-32B-shaped cache: 68.2 GB/s (65.0 with the ideal-bits
+    pass beside the encodes)."""
     import torch
     if layer_cuts is None:
         if s.L % groups:
@@ -875,6 +874,9 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
                        w.sigma[layer_cuts[g]:layer_cuts[g + 1]].to(dev).contiguous(), ecdf, phat,
                        flags=flags)
                for g in range(groups)]
+    # the groups' ideal bits inside their encodes (SKV_RANGE_BITS) where the
+    # encoder fuses them for a group of this size, else a pass beside them
+    fused = all(gc.encode_with_bits_fused() for gc in gcodecs)
     kv_d = torch.empty(kv_h.numel(), dtype=kv_h.dtype, device=dev)
     mu_d = torch.empty(mu_h.numel(), dtype=mu_h.dtype, device=dev)
     box_d = torch.empty(codec.max_bytes, dtype=torch.uint8, device=dev)
@@ -899,13 +901,14 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
             main.wait_event(evs[g])
             c0, c1 = cc[g], cc[g + 1]
             a, b = sc[g], sc[g + 1]
-            codec.encode_range(kv_d, mu_d, c0, c1, first=(g == 0), stream=main)
+            codec.encode_range(kv_d, mu_d, c0, c1, first=(g == 0), bits=fused, stream=main)
             codec.encode_commit(c0, c1, box_d, end_bytes=ends[g:g + 1], stream=main)
             committed = torch.cuda.Event()
             committed.record(main)
-            # the group's ideal bits beside its encode (the call synchronises bst)
-            bst.wait_event(evs[g])
-            bits += gcodecs[g].ideal_bits(kv_d[a:b], mu_d[a:b], stream=bst)
+            if not fused:
+                # the group's ideal bits beside its encode (the call synchronises bst)
+                bst.wait_event(evs[g])
+                bits += gcodecs[g].ideal_bits(kv_d[a:b], mu_d[a:b], stream=bst)
             committed.synchronize()          # the commit has run: ends[g] holds its size
             end = int(ends[g])
             # the group decodes on its own stream, beside the next group's encode
@@ -919,6 +922,8 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
                 back_h[a:b].copy_(back_d[a:b], non_blocking=True)
             sent = end
         _, nb = codec.encode_finish(out=box_d, stream=main)
+        if fused:
+            bits = codec.encode_range_bits(stream=main)
         cout.wait_stream(main)
         with torch.cuda.stream(cout):
             box_h[:hb].copy_(box_d[:hb], non_blocking=True)
@@ -945,14 +950,15 @@ def e2e_single_committed(P, codec, s, w, ecdf, phat, flags, kv_h, mu_h, raw_all,
     return {"value": round(raw_all / dt / 1e9, 3), "unit": "GB/s",
             "h2d_bytes_per_step": int(kv_h.numel() * kv_h.element_size() + 2 * s.n),
             "d2h_bytes_per_step": int(nb + kv_h.numel() * kv_h.element_size() + 8 * groups
-                                      + (groups + 3) * HEAD_BYTES),
+                                      + ((4 if fused else groups + 3) * HEAD_BYTES)),
             "mode": "one container, committed as it is encoded: %d layer groups copied in "
-                    "while earlier groups are encoded (skv_encode_range) and committed "
-                    "(skv_encode_commit), their ideal bits computed alongside, and decoded "
-                    "from the container being written (skv_decode_range, SKV_RANGE_PARTIAL, "
-                    "beside the next group's encode); their decoded scalars and the "
-                    "container's committed bytes copied out as they are ready; "
-                    "skv_encode_finish writes the header" % groups,
+                    "while earlier groups are encoded (skv_encode_range%s) and committed "
+                    "(skv_encode_commit), and decoded from the container being written "
+                    "(skv_decode_range, SKV_RANGE_PARTIAL, beside the next group's encode); "
+                    "their decoded scalars and the container's committed bytes copied out as "
+                    "they are ready; skv_encode_finish writes the header"
+                    % (groups, " with SKV_RANGE_BITS: the ideal bits inside the encoder" if fused
+                       else "; their ideal bits computed alongside"),
             "container_bytes": int(nb), "step_s_spread": spread(ts)}
 
 

@@ -226,6 +226,7 @@ int skv_decode(const skv_params *params, const skv_shape *shape, const void *in,
  * workspace until skv_decode_status.  Does not synchronize. */
 #define SKV_RANGE_FIRST 1
 #define SKV_RANGE_PARTIAL 2
+#define SKV_RANGE_BITS 4   /* skv_encode_range only: see there */
 int skv_decode_range(const skv_params *params, const skv_shape *shape, const void *in,
                      size_t in_bytes, uint64_t chunk_begin, uint64_t chunk_end,
                      const uint16_t *mu, void *kv_out, const uint32_t *page_of_chunk,
@@ -276,9 +277,21 @@ int skv_encode_with_bits_fused(const skv_params *params, const skv_shape *shape,
  *   kv, mu          device, the whole [L][2][H][T][D] tensors; only the range's
  *                   chunks are read, so the rest may still be in flight.
  *   range_flags     SKV_RANGE_FIRST on the first call for a container: clears
- *                   the status and the chunk count and prepares the model
- *                   tables.  Later calls must be ordered after it (same stream,
- *                   or caller-made ordering) and use the same workspace.
+ *                   the status, the chunk count and the ideal-bits total and
+ *                   prepares the model tables.  Later calls must be ordered
+ *                   after it (same stream, or caller-made ordering) and use the
+ *                   same workspace.
+ *                   SKV_RANGE_BITS: the encoder also evaluates the ideal code
+ *                   length of the range's scalars (the per-scalar values of
+ *                   skv_ideal_bits) as it codes them, and adds their sum to the
+ *                   workspace's total, in call order; skv_encode_range_bits
+ *                   reads it.  bf16 mixture model only (not e4m3, not
+ *                   SKV_FLAG_ORDER0 or SKV_FLAG_BLOCK_SCALE: SKV_ERR_ARG), with
+ *                   params->phat.  It pays on ranges of more chunk lanes than
+ *                   one round of the encoder's blocks holds, as with
+ *                   skv_encode_with_bits_fused.  Calls with this flag share
+ *                   the workspace's partial sums: order them one after the
+ *                   other (same stream, or caller-made ordering).
  * Every chunk must be encoded exactly once before skv_encode_finish.  Rejects
  * SKV_FLAG_ADAPTIVE (its tables depend on a row's earlier blocks).  Argument
  * errors (SKV_ERR_ARG, SKV_ERR_CAPACITY) return at once; data errors
@@ -297,6 +310,14 @@ int skv_encode_range(const skv_params *params, const skv_shape *shape, const voi
 int skv_encode_finish(const skv_params *params, const skv_shape *shape, void *out,
                       size_t out_capacity, size_t *out_bytes, void *workspace,
                       size_t workspace_bytes, skv_stream_t stream);
+
+/* The ideal bits of the chunks encoded with SKV_RANGE_BITS since the last
+ * SKV_RANGE_FIRST on this workspace (each range's fixed-order sum, added in
+ * call order) into *total (host); 0 if none.  Reads the workspace's status
+ * first: a data error of the ranges encoded so far (SKV_ERR_SYMBOL,
+ * SKV_ERR_PARAM) is returned instead.  Synchronizes `stream`. */
+int skv_encode_range_bits(const skv_params *params, const skv_shape *shape, double *total,
+                          void *workspace, size_t workspace_bytes, skv_stream_t stream);
 
 /* Place encoded chunks in the container while later ones are still being
  * encoded: chunks [chunk_begin, chunk_end), the next in container order after

@@ -22,13 +22,14 @@ SKV_FLAG_ORDER0 = 4
 SKV_FLAG_ADAPTIVE = 8
 SKV_RANGE_FIRST = 1
 SKV_RANGE_PARTIAL = 2
+SKV_RANGE_BITS = 4
 SKV_OK, SKV_ERR_ARG, SKV_ERR_CAPACITY, SKV_ERR_SYMBOL = 0, -1, -2, -3
 SKV_ERR_PARAM, SKV_ERR_CORRUPT, SKV_ERR_CUDA = -4, -5, -6
 NSYM = {SKV_BF16: 65282, SKV_E4M3: 254}
 
 EXPORTS = ("skv_max_encoded_bytes", "skv_workspace_bytes", "skv_encode", "skv_encode_with_bits",
            "skv_encode_with_bits_fused", "skv_encode_range", "skv_encode_finish",
-           "skv_encode_commit",
+           "skv_encode_range_bits", "skv_encode_commit",
            "skv_model_fingerprint", "skv_merge_parts", "skv_decode",
            "skv_decode_range", "skv_decode_status", "skv_ideal_bits", "skv_model_bits",
            "skv_ideal_bits_noalloc", "skv_ideal_bits_noalloc_max_channels",
@@ -74,6 +75,7 @@ def lib():
             "skv_encode_range": (C.c_int, [P, S, vp, vp, C.c_uint64, C.c_uint64, C.c_int, vp, sz,
                                            vp]),
             "skv_encode_finish": (C.c_int, [P, S, vp, sz, C.POINTER(sz), vp, sz, vp]),
+            "skv_encode_range_bits": (C.c_int, [P, S, C.POINTER(C.c_double), vp, sz, vp]),
             "skv_encode_commit": (C.c_int, [P, S, C.c_uint64, C.c_uint64, vp, sz, vp, vp, sz,
                                             vp]),
             "skv_model_fingerprint": (C.c_int, [P, S, C.POINTER(C.c_uint64), vp, sz, vp]),
@@ -140,6 +142,14 @@ def skv_encode_range(params, shape, kv_ptr, mu_ptr, chunk_begin, chunk_end, rang
     """Enqueues the encode of chunks [chunk_begin, chunk_end); returns the argument status."""
     return lib().skv_encode_range(C.byref(params), C.byref(shape), kv_ptr, mu_ptr, chunk_begin,
                                   chunk_end, range_flags, ws_ptr, ws_bytes, stream)
+
+
+def skv_encode_range_bits(params, shape, ws_ptr, ws_bytes, stream):
+    """Returns (status, ideal bits of the ranges encoded with SKV_RANGE_BITS)."""
+    tot = C.c_double(0.0)
+    rc = lib().skv_encode_range_bits(C.byref(params), C.byref(shape), C.byref(tot), ws_ptr,
+                                     ws_bytes, stream)
+    return rc, tot.value
 
 
 def skv_encode_finish(params, shape, out_ptr, out_capacity, ws_ptr, ws_bytes, stream):
@@ -336,14 +346,25 @@ class Codec:
             raise SkvError(rc, "skv_encode_with_bits_fused")
         return bool(f)
 
-    def encode_range(self, kv, mu, chunk_begin, chunk_end, first=False, stream=None):
-        """Enqueue the encode of chunks [chunk_begin, chunk_end) (no synchronisation)."""
+    def encode_range(self, kv, mu, chunk_begin, chunk_end, first=False, bits=False,
+                     stream=None):
+        """Enqueue the encode of chunks [chunk_begin, chunk_end) (no synchronisation);
+        bits: their ideal bits too, added to the total encode_range_bits reads."""
         ws = self.workspace(SKV_OP_ENCODE)
+        flags = (SKV_RANGE_FIRST if first else 0) | (SKV_RANGE_BITS if bits else 0)
         rc = skv_encode_range(self.params, self.shape, kv.data_ptr(), _ptr(mu), chunk_begin,
-                              chunk_end, SKV_RANGE_FIRST if first else 0, ws.data_ptr(),
-                              ws.numel(), _stream_handle(stream))
+                              chunk_end, flags, ws.data_ptr(), ws.numel(), _stream_handle(stream))
         if rc:
             raise SkvError(rc, "skv_encode_range")
+
+    def encode_range_bits(self, stream=None):
+        """Ideal bits of the ranges encoded with bits=True since the first one."""
+        ws = self.workspace(SKV_OP_ENCODE)
+        rc, tot = skv_encode_range_bits(self.params, self.shape, ws.data_ptr(), ws.numel(),
+                                        _stream_handle(stream))
+        if rc:
+            raise SkvError(rc, "skv_encode_range_bits")
+        return tot
 
     def encode_finish(self, out=None, stream=None):
         """The container from the chunk ranges encoded so far: (tensor, bytes)."""

@@ -704,17 +704,38 @@ int skv_encode_range(const skv_params *params, const skv_shape *shape, const voi
   Plan pl;
   int rc = make_plan(params, shape, &pl);
   if (rc) return rc;
-  if (range_flags & ~SKV_RANGE_FIRST) return SKV_ERR_ARG;
+  if (range_flags & ~(SKV_RANGE_FIRST | SKV_RANGE_BITS)) return SKV_ERR_ARG;
   // adaptive tables depend on every earlier block of a row: whole caches only
   if (pl.adaptive) return SKV_ERR_ARG;
   if (chunk_begin > chunk_end || chunk_end > (uint64_t)pl.geo.nchunks) return SKV_ERR_ARG;
   if ((rc = common_inputs(params, pl, kv, mu))) return rc;
   if (!workspace || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
+  const bool bits = (range_flags & SKV_RANGE_BITS) != 0;
+  // the bits ride along with the bf16 mixture coder only (the fused encoder)
+  if (bits && (pl.dtype != SKV_BF16 || pl.order0 || pl.nsw || !params->phat ||
+               !aligned(params->phat, 4)))
+    return SKV_ERR_ARG;
   if (workspace_bytes < ws_bytes_for(pl, SKV_OP_ENCODE)) return SKV_ERR_CAPACITY;
   if ((rc = ensure_device_tables())) return rc;
   return encode_enqueue(params, pl, kv, mu, chunk_begin, chunk_end,
                         (range_flags & SKV_RANGE_FIRST) != 0, workspace,
-                        reinterpret_cast<cudaStream_t>(stream));
+                        reinterpret_cast<cudaStream_t>(stream), bits && chunk_end > chunk_begin);
+}
+
+int skv_encode_range_bits(const skv_params *params, const skv_shape *shape, double *total,
+                          void *workspace, size_t workspace_bytes, skv_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(params, shape, &pl);
+  if (rc) return rc;
+  if (pl.adaptive || !total || !workspace || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
+  if (workspace_bytes < ws_bytes_for(pl, SKV_OP_ENCODE)) return SKV_ERR_CAPACITY;
+  WsHead h;
+  if ((rc = read_head(reinterpret_cast<WsHead *>(workspace), &h,
+                      reinterpret_cast<cudaStream_t>(stream))))
+    return rc;
+  if ((rc = status_from_flags(h.flags))) return rc;
+  *total = h.bits;
+  return SKV_OK;
 }
 
 int skv_encode_finish(const skv_params *params, const skv_shape *shape, void *out,

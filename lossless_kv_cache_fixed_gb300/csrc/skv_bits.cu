@@ -218,7 +218,8 @@ __device__ __forceinline__ float lo_e4m3_value(int32_t r) {
 }
 
 // Sum of the block partials, in a fixed order: a strided pass per thread,
-// then a tree.
+// then a tree; added to the head's total (zeroed with the head, so that
+// encoded chunk ranges add up their bits in call order).
 __global__ void __launch_bounds__(1024) k_ideal_final(const double *partials, int nb, WsHead *head) {
   __shared__ double s_sum[1024];
   double v = 0.0;
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(1024) k_ideal_final(const double *partials, in
     if (threadIdx.x < off) s_sum[threadIdx.x] += s_sum[threadIdx.x + off];
     __syncthreads();
   }
-  if (threadIdx.x == 0) head->bits = s_sum[0];
+  if (threadIdx.x == 0) head->bits += s_sum[0];
 }
 
 cudaError_t launch_ideal_final(const double *partials, int n, WsHead *head, cudaStream_t s) {

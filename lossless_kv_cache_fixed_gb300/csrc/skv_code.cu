@@ -793,8 +793,10 @@ cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s) {
   if (a.dtype == 0) {
     task_shape(ntasks, kCodeThreads, blocks, threads, kEncMultiRoundThreads);
     if (a.bits_partials) {
-      // skv_encode_with_bits fuses only where encode_fuses_bits says so
-      if (a.order0 || threads <= kCodeThreads) return cudaErrorInvalidValue;
+      // skv_encode_with_bits fuses where encode_fuses_bits says so, chunk
+      // ranges encoded with their bits whatever their size (the 896-thread
+      // instantiation runs the smaller blocks of a single-round launch too)
+      if (a.order0) return cudaErrorInvalidValue;
       return run_encode<0, false, kEncMultiRoundThreads, true>(a, blocks, threads, s);
     }
     if (threads > kCodeThreads)

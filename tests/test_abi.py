@@ -138,6 +138,21 @@ def test_argument_errors_without_gpu(skv):
                                None) == P.SKV_OK           # an empty range places nothing
     assert P.skv_encode_commit(ad, shape, 0, 8, 1 << 20, 1 << 30, None, 1 << 20, 1 << 30,
                                None) == P.SKV_ERR_ARG      # adaptive counts: whole caches
+    # ranges with their ideal bits: the bf16 mixture coder with p-hat only
+    with_phat = P.SkvParams(P.SKV_BF16, 256, 8, 0, 1 << 20, 1 << 21, 1 << 22)
+    for prm in (P.SkvParams(P.SKV_E4M3, 256, 8, 0, 1 << 20, None, None), good,
+                P.SkvParams(P.SKV_BF16, 256, 8, P.SKV_FLAG_BLOCK_SCALE, 1 << 20, 1 << 21, 1 << 22),
+                P.SkvParams(P.SKV_BF16, 256, 8, P.SKV_FLAG_ORDER0, None, 1 << 21, 1 << 22)):
+        assert P.skv_encode_range(prm, shape, 1 << 20, 1 << 20, 0, 8,
+                                  P.SKV_RANGE_FIRST | P.SKV_RANGE_BITS, 1 << 20, 1 << 30,
+                                  None) == P.SKV_ERR_ARG
+    assert P.skv_encode_range(with_phat, shape, 1 << 20, 1 << 20, 0, 8, 8, 1 << 20, 1 << 30,
+                              None) == P.SKV_ERR_ARG     # an unknown flag
+    assert P.skv_encode_range(with_phat, shape, 1 << 20, 1 << 20, 0, 8, P.SKV_RANGE_BITS,
+                              1 << 20, 16, None) == P.SKV_ERR_CAPACITY
+    assert P.skv_encode_range_bits(with_phat, shape, 1 << 20, 16, None)[0] == P.SKV_ERR_CAPACITY
+    assert P.skv_encode_range_bits(with_phat, shape, (1 << 20) + 8, 1 << 30,
+                                   None)[0] == P.SKV_ERR_ARG   # workspace misaligned
     # NULL and misaligned pointers
     rc, _ = P.skv_encode(good, shape, None, 1 << 20, 1 << 20, 1 << 30, 1 << 20, 1 << 30, None)
     assert rc == P.SKV_ERR_ARG

@@ -230,3 +230,60 @@ def test_commit_errors_are_reported_by_finish():
     o2, nb = codec.encode_finish(out=out)
     ref, nb_ref = codec.encode(kv_d, mu_d)
     assert nb == nb_ref and torch.equal(o2[:nb], ref[:nb_ref])
+
+
+def _scalar_base(spec, c):
+    """First scalar of chunk c in the [L][2][H][T][D] tensor (chunks of
+    consecutive indices are consecutive in memory: the last chunk's end is n)."""
+    ntb = (spec.T + spec.Tb - 1) // spec.Tb
+    row, tb = divmod(c, ntb)
+    return row * spec.T * spec.D + min(tb * spec.Tb, spec.T) * spec.D
+
+
+@pytest.mark.parametrize("size", ["small", "multi-round"])
+def test_ranges_with_their_ideal_bits(oracle_mod, size):
+    """SKV_RANGE_BITS: a cover of the cache in pieces, all but one encoded with
+    their ideal bits inside the encoder, gives skv_encode's container, and the
+    running total equals the oracle's ideal bits over the flagged pieces'
+    scalars (the per-scalar tolerance of the ideal bits) and the GPU's own
+    ideal-bits pass over them; the same sequence gives the same total again.
+    'small': ranges of one round of tasks or less; 'multi-round': 8,192 chunks
+    of 16 lanes (2 layers x 8 heads x 4090 tokens x 64, 16-token blocks, the
+    last ragged), where the pieces run several rounds."""
+    if size == "small":
+        spec = CASES["bf16"]
+    else:
+        spec = synth.WORKLOADS["qwen3-0.6b-bf16"].scaled(name="range-bits", L=2, H=8, T=4090,
+                                                         D=64, Tb=16, G=16, calib_draws=2)
+    w = synth.make(spec)
+    codec = gpu_codec(w)
+    kv_d, mu_d = device_views(w)
+    whole, nb = codec.encode(kv_d, mu_d)
+    whole = whole[:nb].clone()
+    m = oracle_model(oracle_mod, w)
+    kv_h, mu_h = host_views(w)
+    _, ref = oracle_mod.ideal_bits(m, kv_h, mu_h, per_scalar=True)
+    _, gps = codec.ideal_bits(kv_d, mu_d, per_scalar=True)
+    gps = gps.double().cpu().numpy()
+    nc = codec.num_chunks()
+    rng = np.random.default_rng(17)
+    ranges = _cover(nc, rng, 5)
+    skip = 2                                   # this piece is encoded without its bits
+    totals = []
+    for _ in range(2):
+        for i, (a, b) in enumerate(ranges):
+            codec.encode_range(kv_d, mu_d, a, b, first=(i == 0), bits=(i != skip))
+        totals.append(codec.encode_range_bits())
+        out, nb2 = codec.encode_finish()
+        assert nb2 == nb and torch.equal(out[:nb2], whole)
+    assert totals[0] == totals[1]
+    sel = np.zeros(spec.n, dtype=bool)
+    for i, (a, b) in enumerate(ranges):
+        if i != skip:
+            sel[_scalar_base(spec, a):_scalar_base(spec, b)] = True
+    want = ref[sel].sum()
+    assert abs(totals[0] - want) <= 1e-3 * abs(want) + 1e-6
+    assert abs(totals[0] - gps[sel].sum()) <= 1e-5 * abs(want) + 1e-6
+    # a fresh FIRST range clears the total
+    codec.encode_range(kv_d, mu_d, 0, nc, first=True)
+    assert codec.encode_range_bits() == 0.0
