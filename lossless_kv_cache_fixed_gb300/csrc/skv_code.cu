@@ -214,8 +214,8 @@ constexpr float kGuessSlopeMax = 1e30f * kHscaleBf16;
 
 // Inverse of the p-hat prefix table for the decoder's guess in the tails that
 // only the p-hat component reaches, and (gmu) the guess's p-hat terms for each
-// rank r of mu: 0.02 E(mu) as a fraction of the CDF, and the slope
-// 0.02 rho / (knot step of u), with rho the p-hat mass of mu's bin per unit
+// rank r of mu, in knots of the guess table (u times kHscaleBf16): 0.02 E(mu),
+// and the slope 0.02 rho, with rho the p-hat mass of mu's bin per unit
 // width (the width from mu's exponent: the bin of a mantissa step), so that
 // the decoder's slope term is one multiply by sigma.  A guess only: any error
 // costs search steps, never a wrong symbol.
@@ -238,7 +238,7 @@ __global__ void k_einv(const uint32_t *__restrict__ ecdf, int32_t *__restrict__ 
     const float w = __uint_as_float(max(mub & 0x7F80u, 0x0080u) << 16) * (1.0f / 128.0f);
     float slope = 0.02f * (1.0f / 67108864.0f) * (float)(eb - ea) / w * kHscaleBf16;
     slope = slope >= 0.0f ? fminf(slope, kGuessSlopeMax) : 0.0f;  // a NaN (0 inf) gives 0
-    gmu[k] = make_float2(0.02f * ((float)ea * (1.0f / 67108864.0f)), slope);
+    gmu[k] = make_float2(0.02f * ((float)ea * (1.0f / 67108864.0f)) * kHscaleBf16, slope);
   }
 }
 
@@ -919,8 +919,9 @@ template <int DT>
 __device__ __forceinline__ int32_t rank_of_value(float x) {
   if (DT == 0) {
     const uint32_t u = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
-    const int32_t r = rank_bf16(u);
-    return r < 0 ? 0 : (r >= kNsymBf16 ? kNsymBf16 - 1 : r);
+    // a NaN rounds to a NaN pattern, whose key lies outside [0, |S|): the
+    // unsigned clamp sends both signs to the last rank (a guess, still in range)
+    return (int32_t)min((uint32_t)rank_bf16(u), (uint32_t)(kNsymBf16 - 1));
   }
   const uint32_t u = (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
   const int32_t r = rank_e4m3(u);
@@ -1234,8 +1235,8 @@ __global__ void __launch_bounds__(NT, 1) k_decode(DecodeLaunch a) {
             // more), so the guess solves G0(z) + a z = u with a = 0.02 rho sigma.
             // Without it the p-hat term at mu alone misses where bins are narrow
             // against sigma (values near zero): about 2 in 3 of the misses.
-            // Both terms come from one per-rank entry (k_einv): 0.02 E(mu), and
-            // 0.02 rho in the table's knot units, taken times sigma here.
+            // Both terms come from one per-rank entry (k_einv), in the guess
+            // table's knot units: 0.02 E(mu), and 0.02 rho, taken times sigma here.
             float e_mu2 = 0.0f, a_knot = 0.0f;
             const int32_t rmu = DT == 0 ? rank_bf16(mub) : rank_of_value<DT>(muf);
             if (DT == 0) {
@@ -1244,10 +1245,10 @@ __global__ void __launch_bounds__(NT, 1) k_decode(DecodeLaunch a) {
               a_knot = fminf(g.y * sig, kGuessSlopeMax);  // NaN (sigma NaN) gives the bound
             }
             auto guess = [&](int32_t rref) -> int32_t {
-              float u, uraw;
               const int32_t dr = (int32_t)(slot - (uint32_t)rref);
-              uraw = (float)dr * kInvK;
-              u = DT == 0 ? uraw - e_mu2 : uraw;
+              // u = dr / K (bf16: less 0.02 E(mu)) in the table's knot units
+              const float tu = DT == 0 ? fmaf((float)dr, kInvK * kHscale, -e_mu2)
+                                       : (float)dr * (kInvK * kHscale);
               if (DT == 1) {
                 // beyond both ends of Phi_q's range cum(r) = r (below mu) or
                 // K + r (above): the rank follows from the slot directly.  Exact
@@ -1255,7 +1256,7 @@ __global__ void __launch_bounds__(NT, 1) k_decode(DecodeLaunch a) {
                 if (dr <= 0) return min((int32_t)slot, NS - 1);
                 if (dr >= (int32_t)kKE4m3) return max(min((int32_t)slot - (int32_t)kKE4m3, NS - 1), 0);
               }
-              const float t = fminf(fmaxf(u * kHscale, 0.0f), (float)kHinvN - 0.001f);
+              const float t = fminf(fmaxf(tu, 0.0f), (float)kHinvN - 0.001f);
               const int kk = (int)t;
               const float2 h = s_hinv[kk];
               float z0 = fmaf(t - (float)kk, h.y, h.x);
@@ -1269,9 +1270,10 @@ __global__ void __launch_bounds__(NT, 1) k_decode(DecodeLaunch a) {
                 const float dz = (float)(r - rref) * (kInvK * kHscale);
                 r = rank_of_value<DT>(fmaf(sig, fmaf(-dz, h.y, z0), muf));
               }
-              if (DT == 0 && (u < 0.0f || u > kHinvUmaxBf16)) {
+              if (DT == 0 && (tu < 0.0f || tu > (float)kHinvN)) {
                 // beyond both Gaussian parts only p-hat moves the CDF: invert it
-                const float tgt = (u < 0.0f ? uraw : uraw - kHinvUmaxBf16) * (50.0f * kHinvN);
+                const float uraw = (float)dr * kInvK;
+                const float tgt = (tu < 0.0f ? uraw : uraw - kHinvUmaxBf16) * (50.0f * kHinvN);
                 const float te = fminf(fmaxf(tgt, 0.0f), (float)kHinvN - 0.001f);
                 const int ke = (int)te;
                 const int32_t r0 = s_einv[ke], r1 = s_einv[ke + 1];
