@@ -1284,15 +1284,27 @@ __global__ void __launch_bounds__(NT, 1) k_decode(DecodeLaunch a) {
             const int32_t rg = guess(rmu);
             const uint32_t ca = cum_of<DT>(rg, muf, inv, s_phi, s_lo8, a.ecdf);
             const uint32_t cb = cum_of<DT>(rg + 1, muf, inv, s_phi, s_lo8, a.ecdf);
-            // the bracket from the full one and these two points (cum(0) = 0,
-            // cum(|S|) = 2^M): below rg, [rg, rg + 1) itself, or above rg + 1
-            const bool at_lo = ca <= slot, at_hi = slot < cb;
-            br.lo = at_lo ? (at_hi ? rg : rg + 1) : 0;
-            br.clo = at_lo ? (at_hi ? ca : cb) : 0u;
-            br.hi = at_hi ? (at_lo ? rg + 1 : rg) : NS;
-            br.chi = at_hi ? (at_lo ? cb : ca) : (1u << M);
-            done = at_lo && at_hi;
+            // the guess's bracket [rg, rg + 1); on a miss, the full one cut by
+            // these two points (cum(0) = 0, cum(|S|) = 2^M): below rg or above
+            // rg + 1
+            const bool at_lo = ca <= slot;
+            br.lo = rg;
+            br.hi = rg + 1;
+            br.clo = ca;
+            br.chi = cb;
+            done = at_lo && slot < cb;
             if (!done) {
+              if (!at_lo) {
+                br.lo = 0;
+                br.clo = 0u;
+                br.hi = rg;
+                br.chi = ca;
+              } else {
+                br.lo = rg + 1;
+                br.clo = cb;
+                br.hi = NS;
+                br.chi = 1u << M;
+              }
               // (2) Newton in value space with the density of bin rg
               const float blo = lo_value(DT, rg, s_lo8), bhi = lo_value(DT, rg + 1, s_lo8);
               const float dens_inv = __fdividef(bhi - blo, (float)(cb - ca));
