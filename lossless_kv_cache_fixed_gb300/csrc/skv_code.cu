@@ -1501,7 +1501,7 @@ __global__ void __launch_bounds__(dec_threads_max<0>(), 1) k_decode_o0(DecodeLau
         }
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, need) & seg;
         if (need) {
-          const uint32_t pos = cur + __popc(m & lt);  // pos < nw keeps the read in the chunk
+          const uint64_t pos = cur + __popc(m & lt);
           if (pos < nw) {
             x = (x << 32) | w[pos];
           } else {
