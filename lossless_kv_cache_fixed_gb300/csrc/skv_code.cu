@@ -309,9 +309,7 @@ __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
          --gi, pmod = pmod >= dstep ? pmod - dstep : pmod + D - dstep) {
       const bool has = (uint32_t)gi < my_groups;
       const uint32_t p0g = 8u * ((uint32_t)ell + (uint32_t)G * (uint32_t)gi);
-      // (the encoder with the ideal bits inside keeps the modulo: the stepped
-      // index cost it registers)
-      const uint32_t ch0 = BITS ? p0g % D : pmod;
+      const uint32_t ch0 = pmod;
 #pragma unroll 1
       for (int hh = 8 / KH - 1; hh >= 0; --hh) {
         const uint32_t p0 = p0g + (uint32_t)(KH * hh);  // a group never crosses a row of D
