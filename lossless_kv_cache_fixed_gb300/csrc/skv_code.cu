@@ -578,6 +578,22 @@ __global__ void __launch_bounds__(1024) k_scan_partials(uint64_t *partials, int6
 // Compaction into the container: header | offsets | payload.
 // ------------------------------------------------------------------------
 
+// Copies nw words from a chunk's stack to its place in the container with the
+// lanes of a warp, four loads in flight per lane before their stores (a
+// chunk's offsets are only word-aligned, so the copy moves words).
+__device__ __forceinline__ void warp_copy_words(uint32_t *dst, const uint32_t *src, int64_t nw,
+                                                int lane) {
+  int64_t k = lane;
+  for (; k + 96 < nw; k += 128) {
+    const uint32_t v0 = src[k], v1 = src[k + 32], v2 = src[k + 64], v3 = src[k + 96];
+    dst[k] = v0;
+    dst[k + 32] = v1;
+    dst[k + 64] = v2;
+    dst[k + 96] = v3;
+  }
+  for (; k < nw; k += 32) dst[k] = src[k];
+}
+
 __global__ void __launch_bounds__(256) k_compact(EncodeLaunch a) {
   const uint64_t total = a.head->total;
   const int64_t nc = a.geo.nchunks;
@@ -596,8 +612,7 @@ __global__ void __launch_bounds__(256) k_compact(EncodeLaunch a) {
     const int64_t start = a.starts[c];
     const int64_t nw = a.stride - start;
     const uint32_t *src = a.scratch + c * a.stride + start;
-    uint32_t *dst = payload + off / 4;
-    for (int64_t i = lane; i < nw; i += 32) dst[i] = src[i];
+    warp_copy_words(payload + off / 4, src, nw, lane);
     if (lane == 0) offs[c] = off;
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -677,8 +692,7 @@ __global__ void __launch_bounds__(256) k_commit_compact(EncodeLaunch a) {
       continue;
     }
     const uint32_t *src = a.scratch + c * a.stride + start;
-    uint32_t *dst = payload + off / 4;
-    for (int64_t k = lane; k < nw; k += 32) dst[k] = src[k];
+    warp_copy_words(payload + off / 4, src, nw, lane);
     if (lane == 0) offs[c] = off;
   }
 }
