@@ -773,9 +773,11 @@ static cudaError_t run_encode(const EncodeLaunch &a, int blocks, int threads, cu
 
 // bf16 encode launches with more tasks than one round of 768-thread blocks
 // run 896-thread blocks (72 registers instead of 78): 32B shape encode 197 ->
-// 208 GB/s.  Single-round launches (the 0.6B shape: 209 -> 200) and e4m3
-// (8B shape: 157 -> 140) lose with them and keep 768.
+// 208 GB/s.  Single-round launches (the 0.6B shape: 209 -> 200) lose with
+// them and keep 768.  e4m3 multi-round launches run 1024-thread blocks with
+// their groups coded in halves (58 registers; see launch_encode_chunks).
 constexpr int kEncMultiRoundThreads = 896;
+constexpr int kEncMultiRoundThreadsE4m3 = 1024;
 
 // The ideal bits ride along with the encoder only on bf16 mixture launches of
 // several rounds of tasks (more lanes than one round of full blocks holds).
@@ -816,7 +818,12 @@ cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s) {
     return run_encode<0, false, kCodeThreads>(a, blocks, threads, s);
   }
   if (a.bits_partials) return cudaErrorInvalidValue;
-  task_shape(ntasks, kCodeThreads, blocks, threads);
+  // e4m3 launches of several rounds: 1024-thread blocks, groups coded in
+  // halves (58 registers): Qwen3-8B shape encode 162.3 -> 191.9 GB/s (whole
+  // groups in 896-thread blocks had lost, 157 -> 140)
+  task_shape(ntasks, kCodeThreads, blocks, threads, kEncMultiRoundThreadsE4m3);
+  if (threads > kCodeThreads)
+    return run_encode<1, false, kEncMultiRoundThreadsE4m3>(a, blocks, threads, s);
   return run_encode<1, false, kCodeThreads>(a, blocks, threads, s);
 }
 
