@@ -282,8 +282,9 @@ int skv_encode_with_bits_fused(const skv_params *params, const skv_shape *shape,
  *                   after it (same stream, or caller-made ordering) and use the
  *                   same workspace.
  *                   SKV_RANGE_BITS: the encoder also evaluates the ideal code
- *                   length of the range's scalars (the per-scalar values of
- *                   skv_ideal_bits) as it codes them, and adds their sum to the
+ *                   length of the range's scalars (the per-scalar values
+ *                   skv_ideal_bits gives, within its tolerance) as it codes
+ *                   them, and adds their sum to the
  *                   workspace's total, in call order; skv_encode_range_bits
  *                   reads it.  bf16 mixture model only (not e4m3, not
  *                   SKV_FLAG_ORDER0 or SKV_FLAG_BLOCK_SCALE: SKV_ERR_ARG), with
