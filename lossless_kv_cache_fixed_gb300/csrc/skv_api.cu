@@ -331,6 +331,7 @@ int encode_enqueue(const skv_params *params, const Plan &pl, const void *kv, con
     a.bits_partials = reinterpret_cast<double *>(ws + pl.off_enc_bits);
     a.bits_out = bits_out;
     a.phat = params->phat;
+    if (!(a.log2q = tail_table())) return SKV_ERR_CUDA;
     if (cudaMemsetAsync(a.bits_partials, 0, sizeof(double) * kMaxBitsBlocks, st) != cudaSuccess)
       return SKV_ERR_CUDA;
   }

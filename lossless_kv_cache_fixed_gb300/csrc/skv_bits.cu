@@ -38,6 +38,12 @@ __device__ __forceinline__ float lo_e4m3_value(int32_t r);
 // (log2 Q(z_k), log2 Q(z_{k+1}) - log2 Q(z_k)) at z_k = k / kTailPerUnit.
 __device__ float2 g_log2q[kTailN];
 
+const float2 *tail_table() {
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_log2q) != cudaSuccess) return nullptr;
+  return static_cast<const float2 *>(p);
+}
+
 cudaError_t upload_tail_table(const float *l2q) {
   float2 pairs[kTailN];
   for (int k = 0; k < kTailN; ++k)

@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(NT, 1) k_encode(EncodeLaunch a) {
               if (BITS) {
                 const float lo = lo_bf16(r), hi = lo_bf16(r + 1), ph = __ldg(a.phat + r);
                 if (!ideal::ideal_series_bf16(lo, hi, muf, inv[k].s, ph, bk[k]))
-                  bk[k] = ideal::ideal_full_call<0>(lo, hi, muf, inv[k].s, ph);
+                  bk[k] = ideal::ideal_rare_bf16(lo, hi, muf, inv[k].s, ph, a.log2q);
               }
             }
             // x >= f 2^(63 - M), a multiple of 2^32: a test of x's high word

@@ -204,12 +204,31 @@ __device__ __forceinline__ float ideal_full(float lo, float hi, float mu, float 
   return -l1;
 }
 
-// The same, out of line: for a caller that evaluates its rare scalars where
-// it meets them, so that its unrolled loop keeps one copy of this code.
-template <int DT>
-static __device__ __noinline__ float ideal_full_call(float lo, float hi, float mu, float inv_s,
-                                                    float ph) {
-  return ideal_full<DT>(lo, hi, mu, inv_s, ph);
+// bf16 bins outside the series case, from the tail table: each component's
+// mass Q(a) - Q(b) on one side of mu (mirrored below it), 1 - Q(-a) - Q(b)
+// around it.  Such a bin has w >= 1 or w |zm| >= 2, so on one side Q(a) / Q(b)
+// >= e^0.5 for the sigma component, and the 3-sigma one has w |zm| / 9 >=
+// 2 / 9: with epsilon <= 5e-6 per tail below z = 9 the masses keep about
+// 10 epsilon relative error; a bin around mu is at least 1 sigma wide, its
+// mass at least 0.38.  Beyond z = 9 a Gaussian mass is below 1.2e-19, under
+// 1e-6 of p-hat's 0.02 floor (p-hat >= 2^-37), so the table's coarser values
+// there (0 from z = 12) do not matter.
+__device__ __forceinline__ float mass_tab(float lo, float hi, float mu, float inv_s,
+                                          const float2 *__restrict__ log2q) {
+  const float za = (lo - mu) * inv_s, zb = (hi - mu) * inv_s;
+  if (za >= 0.0f) return q_tab(za, log2q) - q_tab(zb, log2q);
+  if (zb <= 0.0f) return q_tab(-zb, log2q) - q_tab(-za, log2q);
+  return 1.0f - q_tab(-za, log2q) - q_tab(zb, log2q);
+}
+
+__device__ __forceinline__ float ideal_rare_bf16(float lo, float hi, float mu, float inv_s,
+                                                 float ph, const float2 *__restrict__ log2q) {
+  float m1 = 0.0f, m3 = 0.0f;
+  if (hi > lo) {
+    m1 = fmaxf(mass_tab(lo, hi, mu, inv_s, log2q), 0.0f);
+    m3 = fmaxf(mass_tab(lo, hi, mu, inv_s * (1.0f / 3.0f), log2q), 0.0f);
+  }
+  return -__log2f(fmaf(0.95f, m1, fmaf(0.03f, m3, 0.02f * ph)));
 }
 
 // -log2 q of one scalar (its symbol and mu's bf16 bits), inv_s = 1 / sigma

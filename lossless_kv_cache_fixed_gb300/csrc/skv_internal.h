@@ -130,6 +130,7 @@ struct EncodeLaunch {
   const float *phat;
   float *bits_out;
   double *bits_partials;
+  const float2 *log2q;      // the Gaussian tail table (tail_table()) for the rare scalars
 };
 
 struct DecodeLaunch {
@@ -271,6 +272,8 @@ cudaError_t launch_ideal_final(const double *partials, int n, WsHead *head, cuda
 // einv[k] = the smallest rank r with E_q[r] >= k 2^26 / n, k = 0..n (n divides 2^26);
 // with gmu, also the decoder's per-rank guess terms (kNsymBf16 entries).
 cudaError_t launch_einv(const uint32_t *ecdf, int32_t *einv, int n, float2 *gmu, cudaStream_t s);
+// Device address of the Gaussian tail table (log2 Q at kTailN points), or null.
+const float2 *tail_table();
 cudaError_t launch_decode(const DecodeLaunch &a, cudaStream_t s);
 cudaError_t launch_ideal(const IdealLaunch &a, cudaStream_t s);
 cudaError_t launch_model_bits(const ModelBitsLaunch &a, cudaStream_t s);
