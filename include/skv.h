@@ -243,12 +243,11 @@ int skv_decode_status(const void *workspace, skv_stream_t stream);
  * per-scalar values and the total skv_ideal_bits gives, within its tolerance
  * (1e-3 relative + 1e-6 bits per scalar) -- so that a caller gets a coder's
  * cost and the cross-entropy it should reach side by side (the pages' section
- * "KV 缓存并非真正随机").  On bf16 mixture caches without per-block scales and
- * of more chunk lanes than one round of the encoder's blocks holds (several
- * tens of millions of scalars and up), the encoder computes the bits itself
- * from the symbols, mu and reciprocals in its registers, one read of the
- * inputs for both; elsewhere the ideal-bits pass runs behind the encoder on
- * the same stream.  The total
+ * "KV 缓存并非真正随机").  On bf16 mixture caches (with or without per-block
+ * scales) the encoder computes the bits itself from the symbols, mu and
+ * reciprocals in its registers, one read of the inputs for both; on e4m3 and
+ * with SKV_FLAG_ORDER0 the ideal-bits pass runs behind the encoder on the
+ * same stream.  The total
  * is summed in fp64 in a fixed order for a given device and shape.
  *   per_scalar    device fp32 [N] output, or NULL.
  *   total         host; receives the ideal bits.
@@ -262,9 +261,9 @@ int skv_encode_with_bits(const skv_params *params, const skv_shape *shape, const
 
 /* Whether skv_encode_with_bits computes the ideal bits inside the encoder
  * (*fused = 1: one kernel over the inputs) or runs the ideal-bits pass behind
- * it (*fused = 0) for this model and shape on the current device (the choice
- * depends on its SM count).  fused: host.  Errors: SKV_ERR_ARG (NULL fused,
- * bad params or shape, SKV_FLAG_ADAPTIVE), SKV_ERR_CUDA (no device). */
+ * it (*fused = 0) for this model and shape on the current device.  fused:
+ * host.  Errors: SKV_ERR_ARG (NULL fused, bad params or shape,
+ * SKV_FLAG_ADAPTIVE), SKV_ERR_CUDA (no device). */
 int skv_encode_with_bits_fused(const skv_params *params, const skv_shape *shape, int *fused);
 
 /* Encode part of a cache, asynchronously: chunks [chunk_begin, chunk_end) in
@@ -286,11 +285,9 @@ int skv_encode_with_bits_fused(const skv_params *params, const skv_shape *shape,
  *                   skv_ideal_bits gives, within its tolerance) as it codes
  *                   them, and adds their sum to the
  *                   workspace's total, in call order; skv_encode_range_bits
- *                   reads it.  bf16 mixture model only (not e4m3, not
- *                   SKV_FLAG_ORDER0 or SKV_FLAG_BLOCK_SCALE: SKV_ERR_ARG), with
- *                   params->phat.  It pays on ranges of more chunk lanes than
- *                   one round of the encoder's blocks holds, as with
- *                   skv_encode_with_bits_fused.  Calls with this flag share
+ *                   reads it.  bf16 mixture model only, with or without
+ *                   per-block scales (not e4m3, not SKV_FLAG_ORDER0:
+ *                   SKV_ERR_ARG), with params->phat.  Calls with this flag share
  *                   the workspace's partial sums: order them one after the
  *                   other (same stream, or caller-made ordering).
  * Every chunk must be encoded exactly once before skv_encode_finish.  Rejects

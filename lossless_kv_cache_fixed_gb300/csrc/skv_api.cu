@@ -713,8 +713,7 @@ int skv_encode_range(const skv_params *params, const skv_shape *shape, const voi
   if (!workspace || !aligned(workspace, kAlign)) return SKV_ERR_ARG;
   const bool bits = (range_flags & SKV_RANGE_BITS) != 0;
   // the bits ride along with the bf16 mixture coder only (the fused encoder)
-  if (bits && (pl.dtype != SKV_BF16 || pl.order0 || pl.nsw || !params->phat ||
-               !aligned(params->phat, 4)))
+  if (bits && (pl.dtype != SKV_BF16 || pl.order0 || !params->phat || !aligned(params->phat, 4)))
     return SKV_ERR_ARG;
   if (workspace_bytes < ws_bytes_for(pl, SKV_OP_ENCODE)) return SKV_ERR_CAPACITY;
   if ((rc = ensure_device_tables())) return rc;

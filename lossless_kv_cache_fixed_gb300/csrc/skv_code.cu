@@ -779,21 +779,21 @@ static cudaError_t run_encode(const EncodeLaunch &a, int blocks, int threads, cu
 constexpr int kEncMultiRoundThreads = 896;
 constexpr int kEncMultiRoundThreadsE4m3 = 1024;
 
-// The ideal bits ride along with the encoder only on bf16 mixture launches of
-// several rounds of tasks (more lanes than one round of full blocks holds).
-// There the encoder is throughput-bound and the series' ~100 extra operations
-// per scalar cost less than a separate pass re-reading kv and mu (32B shape:
-// 14.2 ms fused against 10.4 + 4.8 ms).  A single-round launch is bound by
-// its lanes' serial chains, which the extra work lengthens (0.6B shape: 4.5
-// against 2.3 + 1.1 ms), and e4m3's rare scalars, several per warp step, stall
-// whole warps (8B shape: 32 against 7.7 + 5.6 ms); those run the two kernels.
-// So do caches with per-block scales: their sigma fits tighter, more scalars
-// fall outside the series' range, and each takes its warp through the full
-// evaluation (32B shape: 29 ms fused against 11.5 + 6.6 ms).
+// The ideal bits ride along with the bf16 mixture encoder, whatever the
+// launch's size and with or without per-block scales: the series' extra work
+// per scalar costs less than a separate pass re-reading kv and mu (Qwen3-32B
+// shape: 10.9 ms fused against 8.1 + 4.8 ms; Qwen3-0.6B shape, one round of
+// tasks, where it fills issue slots the lanes' serial chains leave idle: step
+// +5.4%; with per-block scales +6.5% and +9.7%), now that the scalars
+// outside the series take the tail table and each group is coded in halves.
+// It costs caches whose model fits badly, where most warp steps hold such
+// scalars (the drift workload: step -4.5% with the static sigma, -4.6% with
+// per-block scales).  e4m3's rare scalars, several per warp step, stall whole
+// warps (8B shape: 32 against 7.7 + 5.6 ms), and the order-0 coder has no
+// series: those run the two kernels.
 bool encode_fuses_bits(int dtype, bool order0, bool scaled, int64_t chunks, int G) {
-  if (dtype != 0 || order0 || scaled) return false;
-  const int64_t ntasks = (chunks * G + 31) / 32;
-  return ntasks > (int64_t)device_sm_count() * (kCodeThreads / 32);
+  (void)scaled;
+  return dtype == 0 && !order0 && chunks > 0 && G > 0;
 }
 
 cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s) {

@@ -141,7 +141,6 @@ def test_argument_errors_without_gpu(skv):
     # ranges with their ideal bits: the bf16 mixture coder with p-hat only
     with_phat = P.SkvParams(P.SKV_BF16, 256, 8, 0, 1 << 20, 1 << 21, 1 << 22)
     for prm in (P.SkvParams(P.SKV_E4M3, 256, 8, 0, 1 << 20, None, None), good,
-                P.SkvParams(P.SKV_BF16, 256, 8, P.SKV_FLAG_BLOCK_SCALE, 1 << 20, 1 << 21, 1 << 22),
                 P.SkvParams(P.SKV_BF16, 256, 8, P.SKV_FLAG_ORDER0, None, 1 << 21, 1 << 22)):
         assert P.skv_encode_range(prm, shape, 1 << 20, 1 << 20, 0, 8,
                                   P.SKV_RANGE_FIRST | P.SKV_RANGE_BITS, 1 << 20, 1 << 30,

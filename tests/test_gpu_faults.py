@@ -178,10 +178,10 @@ def test_invalid_inputs(enc):
 
 
 def test_encode_with_bits_reports_data_errors(enc):
-    """skv_encode_with_bits on the two-pass path (this small cache) and inside
-    the encoder (a cache of several rounds of tasks) reports a NaN symbol, an
-    infinite mu and a short output buffer like skv_encode, and the library
-    stays usable."""
+    """skv_encode_with_bits inside the encoder (bf16: this small cache, one
+    round of tasks, and one of several rounds) and on the two-pass path
+    (e4m3) reports a NaN symbol, an infinite mu and a short output buffer
+    like skv_encode, and the library stays usable."""
     P, w, codec, kv, mu, buf, nb = enc
     big_spec = synth.WORKLOADS["qwen3-0.6b-bf16"].scaled(name="fused-faults", L=2, H=8, T=4096,
                                                          D=64, Tb=16, G=16, calib_draws=2)
@@ -189,10 +189,15 @@ def test_encode_with_bits_reports_data_errors(enc):
     bcodec = gpu_codec(big)
     bkv = big.kv.view(torch.int16).reshape(-1).cuda()
     bmu = big.mu.view(torch.int16).reshape(-1).cuda()
-    assert not codec.encode_with_bits_fused() and bcodec.encode_with_bits_fused()
-    for c, k, m in ((codec, kv, mu), (bcodec, bkv, bmu)):
+    e8 = synth.make(synth.WORKLOADS["qwen3-8b-e4m3"].scaled(name="faults-e4m3", L=1, H=2, T=512))
+    ecodec = gpu_codec(e8)
+    ekv, emu = device_views(e8)
+    assert codec.encode_with_bits_fused() and bcodec.encode_with_bits_fused()
+    assert not ecodec.encode_with_bits_fused()
+    for c, k, m, nan in ((codec, kv, mu, 0x7FC1), (bcodec, bkv, bmu, 0x7FC1),
+                         (ecodec, ekv, emu, 0x7F)):
         bad = k.clone()
-        bad[77] = 0x7FC1                          # a NaN pattern
+        bad[77] = nan                             # a NaN pattern
         with pytest.raises(P.SkvError) as e:
             c.encode_with_bits(bad, m)
         assert e.value.status == P.SKV_ERR_SYMBOL

@@ -252,18 +252,21 @@ def test_ideal_bits_e4m3_narrow_bins(oracle_mod):
 
 @pytest.mark.parametrize("flags", [0, 2], ids=["static", "block-scale"])
 def test_encode_with_bits_inside_the_encoder(oracle_mod, flags):
-    """A bf16 cache with more chunk lanes than one round of the encoder's blocks
-    holds: skv_encode_with_bits computes the ideal bits inside the encoder
-    there (smaller caches, and caches with per-block scales, run the ideal-bits
-    pass behind it).  2 layers x 8 heads x 4090 tokens x 64 in 16-token blocks
-    (8,192 chunks, the last token block ragged) x 16 lanes, with the model's
-    sigma or per-block scales."""
+    """skv_encode_with_bits computes the ideal bits inside the encoder on bf16
+    mixture caches of any size, with or without per-block scales (e4m3 and the
+    order-0 coder run the ideal-bits pass behind it): here a cache with more
+    chunk lanes than one round of the encoder's blocks holds, 2 layers x 8
+    heads x 4090 tokens x 64 in 16-token blocks (8,192 chunks, the last token
+    block ragged) x 16 lanes, with the model's sigma or per-block scales."""
     spec = synth.WORKLOADS["qwen3-0.6b-bf16"].scaled(name="fused-bits", L=2, H=8, T=4090, D=64,
                                                      Tb=16, G=16, calib_draws=2)
     w = synth.make(spec)
     codec = gpu_codec(w, flags=flags)
-    assert codec.encode_with_bits_fused() == (flags == 0)
-    assert not gpu_codec(synth.make("tiny-bf16")).encode_with_bits_fused()
+    assert codec.encode_with_bits_fused()
+    assert gpu_codec(synth.make("tiny-bf16")).encode_with_bits_fused()
+    tiny8 = synth.WORKLOADS["qwen3-8b-e4m3"].scaled(name="tiny-e4m3", L=1, H=2, T=300, D=64,
+                                                    Tb=128, G=4)
+    assert not gpu_codec(synth.make(tiny8)).encode_with_bits_fused()
     kv_d, mu_d = device_views(w)
     buf, nb = codec.encode(kv_d, mu_d)
     got = buf[:nb].cpu().numpy()

@@ -240,8 +240,9 @@ def _scalar_base(spec, c):
     return row * spec.T * spec.D + min(tb * spec.Tb, spec.T) * spec.D
 
 
+@pytest.mark.parametrize("flags", [0, 2], ids=["static", "block-scale"])
 @pytest.mark.parametrize("size", ["small", "multi-round"])
-def test_ranges_with_their_ideal_bits(oracle_mod, size):
+def test_ranges_with_their_ideal_bits(oracle_mod, size, flags):
     """SKV_RANGE_BITS: a cover of the cache in pieces, all but one encoded with
     their ideal bits inside the encoder, gives skv_encode's container, and the
     running total equals the oracle's ideal bits over the flagged pieces'
@@ -249,18 +250,19 @@ def test_ranges_with_their_ideal_bits(oracle_mod, size):
     ideal-bits pass over them; the same sequence gives the same total again.
     'small': ranges of one round of tasks or less; 'multi-round': 8,192 chunks
     of 16 lanes (2 layers x 8 heads x 4090 tokens x 64, 16-token blocks, the
-    last ragged), where the pieces run several rounds."""
+    last ragged), where the pieces run several rounds; with the model's sigma
+    or per-block scales."""
     if size == "small":
         spec = CASES["bf16"]
     else:
         spec = synth.WORKLOADS["qwen3-0.6b-bf16"].scaled(name="range-bits", L=2, H=8, T=4090,
                                                          D=64, Tb=16, G=16, calib_draws=2)
     w = synth.make(spec)
-    codec = gpu_codec(w)
+    codec = gpu_codec(w, flags=flags)
     kv_d, mu_d = device_views(w)
     whole, nb = codec.encode(kv_d, mu_d)
     whole = whole[:nb].clone()
-    m = oracle_model(oracle_mod, w)
+    m = oracle_model(oracle_mod, w, block_scale=bool(flags))
     kv_h, mu_h = host_views(w)
     _, ref = oracle_mod.ideal_bits(m, kv_h, mu_h, per_scalar=True)
     _, gps = codec.ideal_bits(kv_d, mu_d, per_scalar=True)
