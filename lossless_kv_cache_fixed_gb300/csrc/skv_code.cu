@@ -807,10 +807,12 @@ cudaError_t launch_encode_chunks(const EncodeLaunch &a, cudaStream_t s) {
   if (a.dtype == 0) {
     task_shape(ntasks, kCodeThreads, blocks, threads, kEncMultiRoundThreads);
     if (a.bits_partials) {
-      // skv_encode_with_bits fuses where encode_fuses_bits says so, chunk
-      // ranges encoded with their bits whatever their size (the 896-thread
-      // instantiation runs the smaller blocks of a single-round launch too)
+      // skv_encode_with_bits and chunk ranges with their bits; launches of one
+      // round of tasks run a 768-bound instantiation (77 registers against
+      // 71: Qwen3-0.6B shape encode with bits 179.5 -> 181.0 GB/s)
       if (a.order0) return cudaErrorInvalidValue;
+      if (threads <= kCodeThreads)
+        return run_encode<0, false, kCodeThreads, true>(a, blocks, threads, s);
       return run_encode<0, false, kEncMultiRoundThreads, true>(a, blocks, threads, s);
     }
     if (threads > kCodeThreads)
