@@ -58,17 +58,22 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
             raise RuntimeError("nvcc failed on %s" % src)
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + ".tmp" + tag
-    cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("nvcc link failed")
-    os.replace(tmp, LIB)
-    for o in objs:
-        os.remove(o)
+    leftovers = [os.path.join(OUT, src.replace(".cu", ".%s.o" % tag)) for src in SOURCES] + [tmp]
+    try:
+        with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+            objs = list(ex.map(compile_one, SOURCES))
+        cmd = [nvcc(), "-shared", "-o", tmp] + objs + ARCH + ["-Xcompiler", "-fPIC"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            sys.stderr.write(r.stdout + r.stderr)
+            raise RuntimeError("nvcc link failed")
+        os.replace(tmp, LIB)
+    finally:
+        # this build's objects and temporary library go, whether it succeeded or not
+        for f in leftovers:
+            if os.path.exists(f):
+                os.remove(f)
     return LIB
 
 
